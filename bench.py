@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the KIVI 2-bit KV cache on GB300.
+
+Workload: Llama-2-7B-shaped MHA decode (batch 8, 32 heads, head dim 128, context
+4096 + 17 tokens, key groups of G = 32, 2-bit codes), seeded synthetic fp16 K/V
+with fixed outlier key channels.  The cache is quantized once (untimed); one step
+is the whole hot path for one new token per sequence: kivi_append_token (value
+quantization, residual write, group flush every 32 steps) + kivi_decode_attention
+(fused 2-bit decode attention + split combine).  The metric is decode tokens/s
+(batch / step time) with the attention kernel's achieved HBM GB/s against the
+measured copy bandwidth.  L2 is flushed (256 MiB write) before every step, outside
+the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
+
+--impl reference times the CPU oracle (plain C, the host's cores) on a bounded
+sample of the same workload.  Under torchrun every rank runs an independent
+replica (the path has no cross-GPU step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attention tokens/s and achieved HBM GB/s (fraction of peak) on 2-bit KV"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int) -> int:
+    """Bytes one decode-attention launch must move at context n (D = 128):
+    per (batch, KV head) nq*(32 + 512/G) + r*256 + n*36, plus q and out."""
+    nq = (n // G) * G
+    r = n - nq
+    per_head = nq * 32 + (nq // G) * 512 + r * 256 + n * 36
+    return B * Hkv * per_head + 2 * B * Hq * 128 * 2
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def profiled_traffic(kernel_sha: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_attention_llama2-7b-mha.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    fields = {}
+    for ln in lines:
+        if ln.startswith("- ") and ":" in ln:
+            k, v = ln[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_sha256") != kernel_sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_asymmetric_kv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in (self.out or "").splitlines():
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for name, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"], p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and --impl reference)
+# ----------------------------------------------------------------------------------------
+def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float):
+    """Time the oracle's decode step (append + fp64 attention over the dequantized
+    cache) on `sample_heads` of the workload's KV heads; scale to the whole batch."""
+    import oracle
+    from bit_asymmetric_kv_gb300 import synth
+
+    heads = [(i % wl.B, (i * 7) % wl.Hkv) for i in range(sample_heads)]
+    T = wl.capacity(extra=steps + 64)
+    k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
+    v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
+    c = oracle.prefill(k, v, wl.G, T)  # untimed, like the GPU's prefill
+    R = wl.Hq // wl.Hkv
+    t_total, done = 0.0, 0
+    for step in range(steps):
+        k_new, v_new, q = synth.make_step(wl, pre, step)
+        kn = np.stack([k_new[b, h].numpy() for b, h in heads])[None]
+        vn = np.stack([v_new[b, h].numpy() for b, h in heads])[None]
+        qs = np.stack([q[b, h * R + j].numpy() for b, h in heads for j in range(R)])[None]
+        t0 = time.perf_counter()
+        oracle.append(c, kn, vn)
+        oracle.attention(c, qs, 1.0)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total > budget_s:
+            break
+    per_step = t_total / done * (wl.B * wl.Hkv / sample_heads)
+    return {"value": wl.B / per_step, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{sample_heads} of {wl.B * wl.Hkv} KV heads x {done} decode steps (append + fp64 attention), "
+                      f"scaled to the full batch", "seconds": round(t_total, 3)}
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from bit_asymmetric_kv_gb300 import synth
+
+    pre = synth.make_prefill(wl)
+    for w in range(args.warmup):  # untimed warm-up: the first call builds the oracle
+        oracle_timing(wl, pre, 1, 4, 0.0)
+    cb = oracle_timing(wl, pre, args.steps, 16, 60.0)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B / cb["value"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u2 codes, f16 inputs, f64 attention (CPU oracle)", "data": "synthetic",
+            "config": workload_config(wl), "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
+            "context_tokens": wl.n, "step": "append_token + decode_attention (one new token per sequence)",
+            "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
+            "parallelism": "replicas (one independent cache per GPU)"}
+
+
+# ----------------------------------------------------------------------------------------
+# GPU benchmark
+# ----------------------------------------------------------------------------------------
+def run_kivi(args, wl):
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi, synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    kivi.lib()
+    pre = synth.make_prefill(wl)
+    total = args.warmup + args.steps
+    T = wl.capacity(extra=total + 2 * args.warmup + 64)
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
+    kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
+    steps_in = [synth.make_step(wl, pre, s) for s in range(total)]
+    # inputs resident in HBM before timing
+    dev_in = [(k.to(dev), v.to(dev), q.to(dev)) for k, v, q in steps_in]
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
+    ws = kivi.workspace(cache, wl.Hq, n_tokens=T, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_events(i, rec):
+        k, v, q = dev_in[i]
+        flush.fill_(i & 0xFF)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        kivi.kivi_append_token(cache, k, v, stream=stream)
+        e1.record(stream)
+        kivi.kivi_decode_attention(cache, q, 1.0, out=out, ws=ws, stream=stream)
+        e2.record(stream)
+        rec.append((e0, e1, e2, cache.n_tokens))
+
+    warm = []
+    for i in range(args.warmup):
+        step_events(i, warm)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    rec = []
+    launches = 0
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(args.warmup, total):
+            n_before = cache.n_tokens
+            step_events(i, rec)
+            launches += 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier()
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2, _ in rec]
+    attn_ms = [e1.elapsed_time(e2) for _, e1, e2, _ in rec]
+    app_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in rec]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = wl.B * world / (ms_per_step / 1e3)
+    bytes_per = [algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n) for *_, n in rec]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+    achieved = (sum(bytes_per) / len(bytes_per)) / (attn_avg_ms / 1e3) / 1e9
+    peak, peak_src = measured_peak()
+    sha = kernel_source_sha()
+    traffic = profiled_traffic(sha)
+
+    # ---- end to end through the public API: host buffers, copies inside the timing
+    e2e = e2e_run(args, wl, pre, steps_in, dev, stream, flush)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return 0
+    cb = oracle_timing(wl, pre, 8, 16, 15.0) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u2 codes, f16 q/out, f32 accumulate", "data": "synthetic (seeded, fixed outlier key channels)",
+        "config": workload_config(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "kivi_decode_attention (decode_kernel + combine_kernel)",
+                     "peak_source": peak_src, "attention_ms": attn_avg_ms,
+                     "algorithmic_bytes_per_launch": sum(bytes_per) / len(bytes_per),
+                     "kernel_source_sha256": sha},
+        "append_ms": sum(app_ms) / len(app_ms),
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_loop": t_wall,
+        "cpu_baseline": cb,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
+    """Same metric through the public API with host inputs: every step copies its
+    new k, v, q from pinned host memory, runs append + decode attention and copies
+    the output back; the copies are inside the timed events."""
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi
+
+    total = args.warmup + args.steps
+    T = wl.capacity(extra=total + 64)
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
+    kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
+    host = [(k.pin_memory(), v.pin_memory(), q.pin_memory()) for k, v, q in steps_in]
+    dk = torch.empty_like(steps_in[0][0], device=dev)
+    dv = torch.empty_like(steps_in[0][1], device=dev)
+    dq = torch.empty_like(steps_in[0][2], device=dev)
+    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    ws = kivi.workspace(cache, wl.Hq, n_tokens=T, device=dev)
+    times = []
+    for i in range(total):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hk, hv, hq = host[i]
+        e0.record(stream)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dq.copy_(hq, non_blocking=True)
+        kivi.kivi_append_token(cache, dk, dv, stream=stream)
+        kivi.kivi_decode_attention(cache, dq, 1.0, out=out, ws=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        e1.record(stream)
+        if i >= args.warmup:
+            times.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    h2d = sum(t.numel() * t.element_size() for t in steps_in[0])
+    d2h = out.numel() * out.element_size()
+    return {"value": wl.B * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kivi", "reference"], default="kivi")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from bit_asymmetric_kv_gb300 import synth
+
+    wl = synth.LLAMA2_7B_MHA
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_kivi(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,186 @@
+// kivi_api.cu -- the C ABI (include/kivi.h): argument checks, then kernel launches.
+// Nothing here allocates device memory, synchronises with the host or keeps state.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kivi.h"
+#include "kivi_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_dims(const kivi_dims *d) {
+  if (!d) return KIVI_ERR_ARG;
+  if (d->B <= 0 || d->Hkv <= 0 || d->max_tokens <= 0) return KIVI_ERR_ARG;
+  if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
+  if (d->max_tokens % d->G != 0) return KIVI_ERR_ARG;
+  return KIVI_OK;
+}
+
+int check_cache(const kivi_cache *c) {
+  if (!c || !c->k_codes || !c->k_meta || !c->k_res || !c->v_codes || !c->v_meta) return KIVI_ERR_ARG;
+  if (!aligned16(c->k_codes) || !aligned16(c->k_meta) || !aligned16(c->k_res) || !aligned16(c->v_codes) ||
+      !aligned16(c->v_meta))
+    return KIVI_ERR_ALIGN;
+  return KIVI_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
+
+int num_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+int check_heads(const kivi_dims *d, int32_t Hq) {
+  if (Hq <= 0) return KIVI_ERR_ARG;
+  if (Hq % d->Hkv != 0) return KIVI_ERR_UNSUPPORTED;
+  const int R = Hq / d->Hkv;
+  if (R != 1 && R != 2 && R != 4) return KIVI_ERR_UNSUPPORTED;
+  if ((int64_t)d->B * d->Hkv > 65535) return KIVI_ERR_UNSUPPORTED;  // grid.y of the decode launch
+  return KIVI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kivi_status_string(int s) {
+  switch (s) {
+    case KIVI_OK: return "KIVI_OK";
+    case KIVI_ERR_ARG: return "KIVI_ERR_ARG";
+    case KIVI_ERR_ALIGN: return "KIVI_ERR_ALIGN";
+    case KIVI_ERR_UNSUPPORTED: return "KIVI_ERR_UNSUPPORTED";
+    case KIVI_ERR_CAPACITY: return "KIVI_ERR_CAPACITY";
+    case KIVI_ERR_WORKSPACE: return "KIVI_ERR_WORKSPACE";
+    case KIVI_ERR_CUDA: return "KIVI_ERR_CUDA";
+    default: return "KIVI_ERR_UNKNOWN";
+  }
+}
+
+int kivi_buffer_bytes(const kivi_dims *d, size_t out[5]) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if (!out) return KIVI_ERR_ARG;
+  const size_t heads = (size_t)d->B * (size_t)d->Hkv;
+  const size_t T = (size_t)d->max_tokens;
+  out[0] = heads * T * (d->D / 16) * sizeof(uint32_t);
+  out[1] = heads * (T / d->G) * d->D * sizeof(uint32_t);
+  out[2] = heads * (size_t)d->G * d->D * sizeof(uint16_t);
+  out[3] = heads * T * (d->D / 16) * sizeof(uint32_t);
+  out[4] = heads * T * sizeof(uint32_t);
+  return KIVI_OK;
+}
+
+int kivi_quantize_prefill(const kivi_dims *d, kivi_cache *c, const uint16_t *k, const uint16_t *v, int64_t n,
+                          cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if (n < 0) return KIVI_ERR_ARG;
+  if (n > d->max_tokens) return KIVI_ERR_CAPACITY;
+  if (n > 0) {
+    if (!k || !v) return KIVI_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v)) return KIVI_ERR_ALIGN;
+    const int64_t heads = (int64_t)d->B * d->Hkv;
+    const int64_t groups = n / d->G, nq = groups * d->G;
+    cudaError_t e = kivi::launch_key_groups(k, n * 128, heads, groups, 0, d->G, c->k_codes, c->k_meta,
+                                            d->max_tokens, st);
+    if (e == cudaSuccess) e = kivi::launch_residual_copy(k, heads, n, nq, d->G, c->k_res, st);
+    if (e == cudaSuccess)
+      e = kivi::launch_value_rows(v, heads, n, 0, c->v_codes, c->v_meta, d->max_tokens, st);
+    if ((s = cuda_status(e)) != KIVI_OK) return s;
+  }
+  c->n_tokens = n;
+  return KIVI_OK;
+}
+
+int kivi_append_token(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, const uint16_t *v_new,
+                      cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if (!k_new || !v_new) return KIVI_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_ERR_ALIGN;
+  const int64_t n = c->n_tokens;
+  if (n < 0) return KIVI_ERR_ARG;
+  if (n >= d->max_tokens) return KIVI_ERR_CAPACITY;
+  const int64_t heads = (int64_t)d->B * d->Hkv;
+  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
+                                      d->max_tokens, st);
+  if (e == cudaSuccess && (n % d->G) + 1 == d->G)  // the residual is full: flush it as group n / G
+    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
+                                d->max_tokens, st);
+  if ((s = cuda_status(e)) != KIVI_OK) return s;
+  c->n_tokens = n + 1;
+  return KIVI_OK;
+}
+
+int kivi_decode_splits(const kivi_dims *d, int32_t Hq, int64_t n) {
+  if (check_dims(d) != KIVI_OK || check_heads(d, Hq) != KIVI_OK || n <= 0) return 0;
+  const int sms = num_sms();
+  if (sms <= 0) return 0;
+  int splits = 0, gps = 0;
+  kivi::decode_plan(d->B, d->Hkv, d->G, n, sms, &splits, &gps);
+  return splits;
+}
+
+size_t kivi_decode_workspace_bytes(const kivi_dims *d, int32_t Hq, int64_t n) {
+  const int splits = kivi_decode_splits(d, Hq, n);
+  if (splits <= 0) return 0;
+  return (size_t)d->B * (size_t)Hq * (size_t)splits * (size_t)(d->D + 2) * sizeof(float);
+}
+
+int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_t *q, int32_t Hq,
+                          float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_heads(d, Hq)) != KIVI_OK) return s;
+  if (!q || !out) return KIVI_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  if (c->n_tokens <= 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
+  const int sms = num_sms();
+  if (sms <= 0) return KIVI_ERR_CUDA;
+  int splits = 0, gps = 0;
+  kivi::decode_plan(d->B, d->Hkv, d->G, c->n_tokens, sms, &splits, &gps);
+  const size_t need = (size_t)d->B * (size_t)Hq * (size_t)splits * (size_t)(d->D + 2) * sizeof(float);
+  if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KIVI_ERR_ALIGN;
+  kivi::DecodeArgs a;
+  a.k_codes = c->k_codes;
+  a.k_meta = c->k_meta;
+  a.k_res = c->k_res;
+  a.v_codes = c->v_codes;
+  a.v_meta = c->v_meta;
+  a.q = q;
+  a.out = out;
+  a.ws = static_cast<float *>(ws);
+  a.max_tokens = d->max_tokens;
+  a.n = c->n_tokens;
+  a.B = d->B;
+  a.Hkv = d->Hkv;
+  a.Hq = Hq;
+  a.G = d->G;
+  a.splits = splits;
+  a.groups_per_split = gps;
+  a.softmax_scale = softmax_scale;
+  return cuda_status(kivi::launch_decode(a, st));
+}
+
+int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out, float *v_out, cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if (!k_out || !v_out) return KIVI_ERR_ARG;
+  if (!aligned16(k_out) || !aligned16(v_out)) return KIVI_ERR_ALIGN;
+  if (c->n_tokens < 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
+  return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta,
+                                          (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->max_tokens, k_out, v_out,
+                                          st));
+}
+
+}  // extern "C"

@@ -1,0 +1,124 @@
+// kivi_device.cuh -- device helpers shared by the KIVI kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kivi {
+
+constexpr int kD = 128;          // head dim
+constexpr int kWordsPerRow = 8;  // 128 channels x 2 bits / 32
+
+// ---- fp16 bit-pattern helpers ----------------------------------------------------
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ uint16_t f2h(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+// ---- the 2-bit quantizer ------------------------------------------------------------
+// Per-group parameters.  The rounding rule
+//     code = clamp(round_half_even(fl32(fl32(x - mn) / s)), 0, 3)
+// is evaluated in its comparison form: with d = fl32(x - mn) and an fp16 scale s > 0,
+//     code = [d > s/2] + [d >= 3s/2] + [d > 5s/2].
+// Why the two agree: s has an 11-bit significand, so s/2, 3s/2 and 5s/2 are exact
+// in fp32.  fl32(d/s) > 1/2 holds exactly when d/s > 1/2 + 2^-25 (above the midpoint
+// to the next float; the midpoint itself rounds to the even 1/2), and s * 2^-25 is
+// smaller than one ulp of s/2, so for an fp32 d this is d > s/2.  Likewise
+// fl32(d/s) >= 3/2 iff d/s >= 3/2 - 2^-24 iff d >= 3s/2 (the gap s * 2^-24 is below
+// one ulp of 3s/2), and fl32(d/s) > 5/2 iff d > 5s/2.  round_half_even then gives
+// code >= 1, >= 2, >= 3 exactly at these three events, and d <= max - min keeps the
+// code at most 3.  When the fp16 scale is 0 all codes are 0 (thresholds = +inf).
+struct QParams {
+  float mn, t1, t2, t3;
+  uint32_t meta;  // fp16 s | fp16 z << 16
+};
+
+__device__ __forceinline__ QParams make_qparams(float mn, float mx) {
+  QParams p;
+  float range = __fsub_rn(mx, mn);
+  float s32 = __fdiv_rn(range, 3.0f);
+  uint16_t s16 = f2h(s32);
+  float s = h2f(s16);
+  uint16_t z16 = f2h(mn);  // exact: mn is an fp16 value
+  if (z16 == 0x8000u) z16 = 0;  // -0 is stored as +0
+  p.mn = mn;
+  if (s16 == 0) {
+    p.t1 = p.t2 = p.t3 = __int_as_float(0x7f800000);  // +inf: every code is 0
+  } else {
+    p.t1 = __fmul_rn(0.5f, s);
+    p.t2 = __fmul_rn(1.5f, s);
+    p.t3 = __fmul_rn(2.5f, s);
+  }
+  p.meta = (uint32_t)s16 | ((uint32_t)z16 << 16);
+  return p;
+}
+
+__device__ __forceinline__ uint32_t quant_code(float x, const QParams &p) {
+  float d = __fsub_rn(x, p.mn);
+  return (uint32_t)(d > p.t1) + (uint32_t)(d >= p.t2) + (uint32_t)(d > p.t3);
+}
+
+// Codes of the 8 channels held in one 16-byte chunk (4 half2), packed 2 bits each
+// into the low 16 bits: channel j of the chunk at bits [2j, 2j+1].
+__device__ __forceinline__ uint32_t quant_chunk8(const uint4 &c, const QParams &p) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float lo = h2f((uint16_t)(w[k] & 0xffffu));
+    float hi = h2f((uint16_t)(w[k] >> 16));
+    bits |= quant_code(lo, p) << (4 * k);
+    bits |= quant_code(hi, p) << (4 * k + 2);
+  }
+  return bits;
+}
+
+// ---- packed half2 min / max of a 16-byte chunk ---------------------------------------
+__device__ __forceinline__ __half2 u2h2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
+__device__ __forceinline__ uint32_t h22u(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+
+// ---- cp.async (16-byte global -> shared copies, completion tracked per thread) ----
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// ---- warp-level tensor-core MMA: D(16x8,f32) += A(16x16,f16) * B(16x8,f16) ---------
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- 2-bit code unpack into fp16 MMA operands ------------------------------------------
+// A 32-bit word w holds 16 codes, code i at bits [2i, 2i+1].  Masking with
+// 0x00030003 << 2m leaves codes i and i+8 in the two 16-bit halves at bit 2m; as
+// fp16 bit patterns these are the subnormals code * 4^m * 2^-24, exact.  Shifting w
+// by 0, 4, 8, 12 and using m in {0, 1} gives:
+//   r[k] = {code_k, code_{k+8}} * f_k * 2^-24,   f_k = 1 for even k, 4 for odd k.
+// The 2^-24 and f_k are undone on the other MMA operand or after accumulation.
+__device__ __forceinline__ void unpack16(uint32_t w, uint32_t r[8]) {
+  const uint32_t m0 = 0x00030003u, m1 = 0x000C000Cu;
+  r[0] = w & m0;
+  r[1] = w & m1;
+  uint32_t x1 = w >> 4;
+  r[2] = x1 & m0;
+  r[3] = x1 & m1;
+  uint32_t x2 = w >> 8;
+  r[4] = x2 & m0;
+  r[5] = x2 & m1;
+  uint32_t x3 = w >> 12;
+  r[6] = x3 & m0;
+  r[7] = x3 & m1;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
+
+}  // namespace kivi

@@ -1,0 +1,262 @@
+// kivi_quant.cu -- quantize / pack kernels of the KIVI 2-bit KV cache (sm_103a).
+//
+// KIVI page ("Makale Bulteni -- KIVI", cmlonder.com radar / paper-to-prod,
+// 2026-11-01): headline paragraph (keys per channel, values per token, asymmetric
+// 2-bit) and section "Iddia ve Gerceklik", paragraphs 2-3 (G-token key groups, a
+// full-precision residual for the unfilled group).  All kernels here stream fp16
+// inputs once from HBM and write 1/8 of that in codes: they are bandwidth-bound.
+#include "kivi_device.cuh"
+#include "kivi_internal.h"
+
+namespace kivi {
+
+// -------------------------------------------------------------------------------------
+// Key groups: one CTA (4 warps) quantizes one G-token group of one (batch, KV head).
+// Warp w owns channels 32w .. 32w+31.  Lane = 4 * t8 + c4: the lane loads the
+// 16-byte chunk c4 (8 channels) of tokens t8, t8 + 8, ... so one warp instruction
+// reads 8 token rows x 64 contiguous bytes.
+// -------------------------------------------------------------------------------------
+template <int G>
+__global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
+                                                        int64_t groups_per_head, int64_t g0,
+                                                        uint32_t *__restrict__ k_codes,
+                                                        uint32_t *__restrict__ k_meta, int64_t max_tokens) {
+  constexpr int TPL = G / 8;  // tokens per lane
+  __shared__ __align__(16) uint32_t s_codes[G * kWordsPerRow];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t8 = lane >> 2, c4 = lane & 3;
+  const int64_t bh = blockIdx.x / groups_per_head;
+  const int64_t gi = blockIdx.x % groups_per_head;
+  const int64_t g = g0 + gi;
+  const uint16_t *src = in + bh * in_head_stride + gi * (int64_t)G * kD + 32 * warp + 8 * c4;
+
+  uint4 x[TPL];
+#pragma unroll
+  for (int k = 0; k < TPL; ++k) x[k] = __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)(t8 + 8 * k) * kD));
+
+  // per-channel min and max over the G tokens: local, then across the 8 token lanes
+  __half2 mn[4], mx[4];
+  {
+    const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&x[0]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mn[j] = mx[j] = u2h2(w0[j]);
+  }
+#pragma unroll
+  for (int k = 1; k < TPL; ++k) {
+    const uint32_t *wk = reinterpret_cast<const uint32_t *>(&x[k]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mn[j] = __hmin2(mn[j], u2h2(wk[j]));
+      mx[j] = __hmax2(mx[j], u2h2(wk[j]));
+    }
+  }
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      mn[j] = __hmin2(mn[j], u2h2(__shfl_xor_sync(0xffffffffu, h22u(mn[j]), off)));
+      mx[j] = __hmax2(mx[j], u2h2(__shfl_xor_sync(0xffffffffu, h22u(mx[j]), off)));
+    }
+  }
+  // lane (t8, c4) derives the parameters of channel t8 of its chunk, then they are
+  // broadcast to the 8 lanes that hold the chunk
+  const uint32_t mn_bits = h22u(mn[t8 >> 1]), mx_bits = h22u(mx[t8 >> 1]);
+  const float my_mn = h2f((uint16_t)((t8 & 1) ? (mn_bits >> 16) : (mn_bits & 0xffffu)));
+  const float my_mx = h2f((uint16_t)((t8 & 1) ? (mx_bits >> 16) : (mx_bits & 0xffffu)));
+  const QParams mine = make_qparams(my_mn, my_mx);
+  k_meta[(bh * (max_tokens / G) + g) * kD + 32 * warp + 8 * c4 + t8] = mine.meta;
+
+  QParams p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int src_lane = 4 * j + c4;
+    p[j].mn = __shfl_sync(0xffffffffu, mine.mn, src_lane);
+    p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
+    p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
+    p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
+  }
+#pragma unroll
+  for (int k = 0; k < TPL; ++k) {
+    const uint32_t *wk = reinterpret_cast<const uint32_t *>(&x[k]);
+    uint32_t bits = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      bits |= quant_code(h2f((uint16_t)(wk[j] & 0xffffu)), p[2 * j]) << (4 * j);
+      bits |= quant_code(h2f((uint16_t)(wk[j] >> 16)), p[2 * j + 1]) << (4 * j + 2);
+    }
+    // chunks 2m and 2m+1 form word 2*warp + m of the token row
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+    if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * kWordsPerRow + 2 * warp + (c4 >> 1)] = bits | (other << 16);
+  }
+  __syncthreads();
+  // coalesced write of the G packed token rows
+  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + (bh * max_tokens + g * G) * kWordsPerRow);
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(s_codes);
+  for (int i = threadIdx.x; i < G * kWordsPerRow / 4; i += blockDim.x) dst[i] = s4[i];
+}
+
+// -------------------------------------------------------------------------------------
+// Value tokens: 16 lanes per token row (one 16-byte chunk of 8 channels each).
+// quantize_value_row works on one half-warp; `lane16` is the lane within it.
+// -------------------------------------------------------------------------------------
+__device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, uint32_t half_mask,
+                                                   uint32_t *codes_row, uint32_t *meta_out) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  __half2 mn = __hmin2(__hmin2(u2h2(w[0]), u2h2(w[1])), __hmin2(u2h2(w[2]), u2h2(w[3])));
+  __half2 mx = __hmax2(__hmax2(u2h2(w[0]), u2h2(w[1])), __hmax2(u2h2(w[2]), u2h2(w[3])));
+  // pack (min, -max) so one __hmin2 reduces both
+  __half2 red = __halves2half2(__hmin(__low2half(mn), __high2half(mn)),
+                               __hneg(__hmax(__low2half(mx), __high2half(mx))));
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) red = __hmin2(red, u2h2(__shfl_xor_sync(half_mask, h22u(red), off)));
+  const float fmn = __low2float(red);
+  const float fmx = -__high2float(red);
+  const QParams p = make_qparams(fmn, fmx);
+  const uint32_t bits = quant_chunk8(x, p);
+  const uint32_t other = __shfl_xor_sync(half_mask, bits, 1);
+  if ((lane16 & 1) == 0) codes_row[lane16 >> 1] = bits | (other << 16);
+  if (lane16 == 0) *meta_out = p.meta;
+}
+
+// rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head
+__global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restrict__ v, int64_t rows,
+                                                         int64_t tokens_per_head, int64_t t0,
+                                                         uint32_t *__restrict__ v_codes,
+                                                         uint32_t *__restrict__ v_meta, int64_t max_tokens) {
+  const int lane = threadIdx.x & 31;
+  const int lane16 = lane & 15;
+  const uint32_t half_mask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;
+  const int64_t half_warps = (int64_t)gridDim.x * (blockDim.x >> 4);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4); row < rows; row += half_warps) {
+    const int64_t bh = row / tokens_per_head;
+    const int64_t t = t0 + row % tokens_per_head;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + row * kD) + lane16);
+    quantize_value_row(x, lane16, half_mask, v_codes + (bh * max_tokens + t) * kWordsPerRow,
+                       v_meta + bh * max_tokens + t);
+  }
+}
+
+// Append: one warp per (batch, KV head).  Lanes 0-15 quantize the new value row;
+// lanes 16-31 copy the new key (256 bytes) into residual slot r.
+__global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict__ k_new,
+                                                     const uint16_t *__restrict__ v_new, int64_t heads,
+                                                     int64_t n, int G, uint16_t *__restrict__ k_res,
+                                                     uint32_t *__restrict__ v_codes,
+                                                     uint32_t *__restrict__ v_meta, int64_t max_tokens) {
+  const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (bh >= heads) return;
+  const int lane = threadIdx.x & 31;
+  const int lane16 = lane & 15;
+  if (lane < 16) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v_new + bh * kD) + lane16);
+    quantize_value_row(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * kWordsPerRow,
+                       v_meta + bh * max_tokens + n);
+  } else {
+    const int64_t r = n % G;
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(k_new + bh * kD) + lane16);
+    reinterpret_cast<uint4 *>(k_res + (bh * G + r) * kD)[lane16] = x;
+  }
+}
+
+// Residual copy at prefill: tokens nq .. n-1 of every head into slots 0 .. r-1.
+__global__ void __launch_bounds__(128) residual_copy_kernel(const uint16_t *__restrict__ k, int64_t n, int64_t nq,
+                                                            int G, uint16_t *__restrict__ k_res) {
+  const int64_t bh = blockIdx.x;
+  const int64_t chunks = (n - nq) * (kD / 8);
+  const uint4 *src = reinterpret_cast<const uint4 *>(k + (bh * n + nq) * kD);
+  uint4 *dst = reinterpret_cast<uint4 *>(k_res + bh * G * kD);
+  for (int64_t i = threadIdx.x; i < chunks; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+// Dequantize (test aid): thread per (head, token, 8-channel chunk).
+__global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict__ k_codes,
+                                                      const uint32_t *__restrict__ k_meta,
+                                                      const uint16_t *__restrict__ k_res,
+                                                      const uint32_t *__restrict__ v_codes,
+                                                      const uint32_t *__restrict__ v_meta, int64_t heads, int64_t n,
+                                                      int G, int64_t max_tokens, float *__restrict__ k_out,
+                                                      float *__restrict__ v_out) {
+  const int64_t total = heads * n * (kD / 8);
+  const int64_t nq = (n / G) * G;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int chunk = (int)(i % (kD / 8));
+    const int64_t t = (i / (kD / 8)) % n;
+    const int64_t bh = i / ((kD / 8) * n);
+    const int c0 = chunk * 8;
+    float *ko = k_out + (bh * n + t) * kD + c0;
+    float *vo = v_out + (bh * n + t) * kD + c0;
+    if (t < nq) {
+      const uint32_t word = k_codes[(bh * max_tokens + t) * kWordsPerRow + (c0 >> 4)] >> (2 * (c0 & 15));
+      const uint32_t *meta = k_meta + (bh * (max_tokens / G) + t / G) * kD + c0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float s = h2f((uint16_t)(meta[j] & 0xffffu)), z = h2f((uint16_t)(meta[j] >> 16));
+        ko[j] = __fadd_rn(z, __fmul_rn((float)((word >> (2 * j)) & 3u), s));
+      }
+    } else {
+      const uint16_t *res = k_res + (bh * G + (t - nq)) * kD + c0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ko[j] = h2f(res[j]);
+    }
+    const uint32_t vm = v_meta[bh * max_tokens + t];
+    const float s = h2f((uint16_t)(vm & 0xffffu)), z = h2f((uint16_t)(vm >> 16));
+    const uint32_t word = v_codes[(bh * max_tokens + t) * kWordsPerRow + (c0 >> 4)] >> (2 * (c0 & 15));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) vo[j] = __fadd_rn(z, __fmul_rn((float)((word >> (2 * j)) & 3u), s));
+  }
+}
+
+// ------------------------------------------------------------------ host launchers
+static int grid_cap(int64_t want) {
+  const int64_t cap = 152LL * 32;
+  return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_t heads, int64_t groups_per_head,
+                              int64_t g0, int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
+                              cudaStream_t st) {
+  const int64_t blocks = heads * groups_per_head;
+  if (blocks == 0) return cudaSuccess;
+  if (G == 32)
+    key_group_kernel<32><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes, k_meta,
+                                                           max_tokens);
+  else
+    key_group_kernel<64><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes, k_meta,
+                                                           max_tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t t0,
+                              uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
+  const int64_t rows = heads * tokens_per_head;
+  if (rows == 0) return cudaSuccess;
+  value_rows_kernel<<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, t0, v_codes, v_meta,
+                                                                max_tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G,
+                          uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
+  append_kernel<<<(unsigned)((heads + 3) / 4), 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta,
+                                                             max_tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, int64_t nq, int G, uint16_t *k_res,
+                                 cudaStream_t st) {
+  if (n == nq) return cudaSuccess;
+  residual_copy_kernel<<<(unsigned)heads, 128, 0, st>>>(k, n, nq, G, k_res);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
+                           const uint32_t *v_codes, const uint32_t *v_meta, int64_t heads, int64_t n, int G,
+                           int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st) {
+  const int64_t total = heads * n * (kD / 8);
+  if (total == 0) return cudaSuccess;
+  dequant_kernel<<<grid_cap((total + 255) / 256), 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G,
+                                                                max_tokens, k_out, v_out);
+  return cudaGetLastError();
+}
+
+}  // namespace kivi

@@ -1,0 +1,158 @@
+/*
+ * kivi.h -- C ABI of the GB300 (sm_103a) KIVI asymmetric 2-bit KV-cache library.
+ *
+ * The method is KIVI ("KIVI: A Tuning-Free Asymmetric 2bit Quantization for KV
+ * Cache", ICML 2024) as summarised on the page "Makale Bulteni -- KIVI"
+ * (cmlonder.com, radar / paper-to-prod, 2026-11-01):
+ *   - headline paragraph: keys are quantized per channel and values per token, in
+ *     an asymmetric 2-bit format;
+ *   - section "Iddia ve Gerceklik", paragraph 2: key outlier channels stay fixed
+ *     over the sequence (so keys are grouped along the channel axis); values are
+ *     kept per token because the attention output is a weighted sum of values;
+ *   - same section, paragraph 3: keys are split into groups of G = 32 or 64 tokens;
+ *     the tokens of a group that has not filled yet stay in a full-precision
+ *     residual buffer; unpacking 2-bit codes for 16-bit tensor cores is done with
+ *     bit shifts and masks on the GPU.
+ * The page gives no formulas, so these readings apply throughout:
+ *   - zero = min, scale = (max - min) / 3, both stored as fp16;
+ *   - code = clamp(round_half_even(fp32((x - min) / scale)), 0, 3), all fp32
+ *     operations IEEE round-to-nearest-even, computed with the stored fp16 scale;
+ *     a group whose fp16 scale is 0 gets all-zero codes; a zero of -0 is stored +0;
+ *   - one (scale, zero) pair per value token per KV head over all D channels;
+ *   - only keys have a residual; a key group is quantized ("flushed") as soon as it
+ *     holds G tokens, so the residual holds n mod G tokens;
+ *   - query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
+ *
+ * Supported shapes: D = 128, bits = 2, G in {32, 64}, Hq / Hkv in {1, 2, 4}.
+ * Inputs must be finite; codes for non-finite inputs are unspecified.
+ *
+ * Memory: every buffer is device memory owned by the caller (nothing is allocated
+ * inside the library, nothing is freed), 16-byte aligned, in these layouts:
+ *   k_codes  uint32 [B][Hkv][max_tokens][D/16]  token rows of packed key codes
+ *   k_meta   uint32 [B][Hkv][max_tokens/G][D]   per (group, channel) {s, z}
+ *   k_res    fp16   [B][Hkv][G][D]              residual keys, slot j = token nq + j
+ *   v_codes  uint32 [B][Hkv][max_tokens][D/16]  token rows of packed value codes
+ *   v_meta   uint32 [B][Hkv][max_tokens]        per token {s, z}
+ * A {s, z} word holds the fp16 scale in bits 0-15 and the fp16 zero in bits 16-31.
+ * Packing: word w of a token row holds channels 16w .. 16w+15; channel 16w+i sits
+ * in bits [2i, 2i+1].  fp16 buffers are IEEE binary16 bit patterns (uint16_t).
+ * nq = floor(n / G) * G tokens are quantized keys; rows at or beyond nq of k_codes,
+ * groups at or beyond n / G of k_meta, residual slots at or beyond n mod G and
+ * value rows at or beyond n are not read.
+ *
+ * Streams and state: every compute call is asynchronous on the given stream and
+ * never synchronises with the host.  The only state is the caller's kivi_cache;
+ * its n_tokens field is host memory, updated by the library when a call succeeds
+ * and left unchanged when it fails.  Concurrent calls on the same cache race.
+ * No call throws across the ABI; every call returns a kivi_status.
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KIVI_API __attribute__((visibility("default")))
+#else
+#define KIVI_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KIVI_OK = 0,
+  KIVI_ERR_ARG = 1,          /* null pointer, non-positive size, n > max_tokens ... */
+  KIVI_ERR_ALIGN = 2,        /* a buffer is not 16-byte aligned */
+  KIVI_ERR_UNSUPPORTED = 3,  /* D != 128, bits != 2, G not in {32, 64}, Hq/Hkv not in {1,2,4} */
+  KIVI_ERR_CAPACITY = 4,     /* append on a full cache, prefill longer than max_tokens */
+  KIVI_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
+  KIVI_ERR_CUDA = 6          /* a CUDA runtime call or launch failed */
+} kivi_status;
+
+/* Cache geometry.  max_tokens must be a positive multiple of G. */
+typedef struct {
+  int32_t B;         /* batch */
+  int32_t Hkv;       /* KV heads */
+  int32_t D;         /* head dim, 128 */
+  int32_t G;         /* key group size, 32 or 64 */
+  int32_t bits;      /* code width, 2 */
+  int64_t max_tokens;
+} kivi_dims;
+
+/* Caller-owned device buffers (layouts above) plus the host-side token count. */
+typedef struct {
+  uint32_t *k_codes;
+  uint32_t *k_meta;
+  uint16_t *k_res;
+  uint32_t *v_codes;
+  uint32_t *v_meta;
+  int64_t n_tokens;
+} kivi_cache;
+
+/* Bytes of the five cache buffers, in the order k_codes, k_meta, k_res, v_codes,
+ * v_meta.  Pure host arithmetic. */
+KIVI_API int kivi_buffer_bytes(const kivi_dims *dims, size_t out_bytes[5]);
+
+/*
+ * Quantize a prompt of n tokens into an empty cache (headline paragraph; section
+ * "Iddia ve Gerceklik", paragraphs 2-3).  k, v: fp16 [B][Hkv][n][D] device.
+ * Keys of the floor(n/G) full groups are quantized per channel; the last n mod G
+ * keys are copied to k_res; all n values are quantized per token.  Sets
+ * cache->n_tokens = n.  n == 0 launches nothing.  n > max_tokens: KIVI_ERR_CAPACITY.
+ */
+KIVI_API int kivi_quantize_prefill(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k,
+                          const uint16_t *v, int64_t n, cudaStream_t stream);
+
+/*
+ * Append one token per (batch, KV head) (section "Iddia ve Gerceklik", paragraph 3).
+ * k_new, v_new: fp16 [B][Hkv][D] device.  The key goes to residual slot
+ * n_tokens mod G; the value is quantized at once; when the residual fills, its G
+ * keys are quantized as one group in the same call.  Increments cache->n_tokens.
+ * A full cache returns KIVI_ERR_CAPACITY.
+ */
+KIVI_API int kivi_append_token(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k_new,
+                      const uint16_t *v_new, cudaStream_t stream);
+
+/* Number of context splits kivi_decode_attention uses for these sizes on the
+ * current device (>= 1; 0 on bad arguments). */
+KIVI_API int kivi_decode_splits(const kivi_dims *dims, int32_t Hq, int64_t n_tokens);
+
+/* Workspace bytes kivi_decode_attention needs for these sizes on the current
+ * device: B * Hq * splits * (D + 2) floats.  0 on bad arguments. */
+KIVI_API size_t kivi_decode_workspace_bytes(const kivi_dims *dims, int32_t Hq, int64_t n_tokens);
+
+/*
+ * One decode step of attention over the quantized cache (section "Iddia ve
+ * Gerceklik", paragraphs 2-3): for every batch b and query head h,
+ *   score_t = softmax_scale * q[b][h] . K'_t  over the cache's n_tokens tokens,
+ *   out[b][h] = sum_t softmax(score)_t V'_t,
+ * where K'_t = z + code * s for quantized keys, the fp16 residual key itself for
+ * the last n mod G tokens, and V'_t = z_t + code * s_t.  q, out: fp16 [B][Hq][D]
+ * device.  ws: device workspace of at least kivi_decode_workspace_bytes() bytes,
+ * caller-owned, contents overwritten.  n_tokens == 0 returns KIVI_ERR_ARG.
+ */
+KIVI_API int kivi_decode_attention(const kivi_dims *dims, const kivi_cache *cache, const uint16_t *q,
+                          int32_t Hq, float softmax_scale, uint16_t *out, void *ws,
+                          size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Test aid: write the dequantized cache as fp32 [B][Hkv][n_tokens][D] to k_out and
+ * v_out (device, caller-owned).  Quantized entries are fp32(z) + code * fp32(s)
+ * (exact product, one rounding); residual keys are copied exactly.
+ */
+KIVI_API int kivi_dequantize_debug(const kivi_dims *dims, const kivi_cache *cache, float *k_out,
+                          float *v_out, cudaStream_t stream);
+
+/* Human-readable name of a kivi_status. */
+KIVI_API const char *kivi_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIVI_H */

@@ -1,0 +1,121 @@
+"""The C-ABI library: it loads on a machine without a GPU, exports every entry point
+include/kivi.h declares, and rejects bad arguments on the host, before any launch.
+No test here touches device memory: every call fails validation first.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_asymmetric_kv_gb300 import build as kbuild
+from bit_asymmetric_kv_gb300 import kivi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    kbuild.build()
+    return kivi.lib()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "kivi.h")).read()
+    return re.findall(r"KIVI_API\s+[\w\s\*]+?\b(kivi_\w+)\s*\(", src)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    for n in ("kivi_quantize_prefill", "kivi_append_token", "kivi_decode_attention", "kivi_dequantize_debug",
+              "kivi_buffer_bytes", "kivi_decode_workspace_bytes", "kivi_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code, name in kivi.STATUS.items():
+        assert kivi.kivi_status_string(code) == name
+
+
+def _dims(**kw):
+    d = dict(B=2, Hkv=4, D=128, G=32, bits=2, max_tokens=256)
+    d.update(kw)
+    return kivi.kivi_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["max_tokens"])
+
+
+FAKE = 1 << 20  # an aligned, never dereferenced address
+
+
+def _cache(n=0, align=0):
+    return kivi.kivi_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, n)
+
+
+def test_buffer_bytes(L):
+    out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640))
+    heads = 15
+    assert out == [heads * 640 * 32, heads * 10 * 128 * 4, heads * 64 * 128 * 2, heads * 640 * 32, heads * 640 * 4]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(bits=4), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(G=16), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(B=0), kivi.KIVI_ERR_ARG),
+    (dict(max_tokens=100), kivi.KIVI_ERR_ARG),   # not a multiple of G
+])
+def test_bad_dims(L, kw, status):
+    d = _dims(**kw)
+    out = (ctypes.c_size_t * 5)()
+    assert L.kivi_buffer_bytes(ctypes.byref(d), out) == status
+    c = _cache()
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, 10, None) == status
+    assert c.n_tokens == 0
+
+
+def test_prefill_checks(L):
+    d = _dims()
+    c = _cache()
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), None, FAKE, 10, None) == kivi.KIVI_ERR_ARG
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE + 2, FAKE, 10, None) == kivi.KIVI_ERR_ALIGN
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, 257, None) == kivi.KIVI_ERR_CAPACITY
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, -1, None) == kivi.KIVI_ERR_ARG
+    bad = _cache(align=4)
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(bad), FAKE, FAKE, 10, None) == kivi.KIVI_ERR_ALIGN
+    null = kivi.kivi_cache(FAKE, 0, FAKE, FAKE, FAKE, 0)
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(null), FAKE, FAKE, 10, None) == kivi.KIVI_ERR_ARG
+    # n == 0 launches nothing and succeeds
+    c.n_tokens = 7
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), None, None, 0, None) == kivi.KIVI_OK
+    assert c.n_tokens == 0
+
+
+def test_append_capacity_leaves_state(L):
+    d = _dims()
+    c = _cache(n=256)
+    assert L.kivi_append_token(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, None) == kivi.KIVI_ERR_CAPACITY
+    assert c.n_tokens == 256
+    c = _cache(n=3)
+    assert L.kivi_append_token(ctypes.byref(d), ctypes.byref(c), FAKE + 8, FAKE, None) == kivi.KIVI_ERR_ALIGN
+    assert c.n_tokens == 3
+
+
+def test_decode_argument_checks(L):
+    d = _dims()
+    c = _cache(n=0)
+    call = lambda c, Hq=8, q=FAKE, out=FAKE: L.kivi_decode_attention(  # noqa: E731
+        ctypes.byref(d), ctypes.byref(c), q, Hq, 1.0, out, FAKE, 1 << 30, None)
+    assert call(c) == kivi.KIVI_ERR_ARG                       # empty cache
+    c = _cache(n=10)
+    assert call(c, Hq=6) == kivi.KIVI_ERR_UNSUPPORTED         # Hq % Hkv != 0
+    assert call(c, Hq=32) == kivi.KIVI_ERR_UNSUPPORTED        # Hq / Hkv = 8
+    assert call(c, q=None) == kivi.KIVI_ERR_ARG
+    assert call(c, out=FAKE + 6) == kivi.KIVI_ERR_ALIGN
+    c = _cache(n=300)                                         # more tokens than capacity
+    assert call(c) == kivi.KIVI_ERR_ARG
+    assert L.kivi_decode_splits(ctypes.byref(d), 6, 10) == 0
+    assert L.kivi_decode_workspace_bytes(ctypes.byref(d), 8, 0) == 0
