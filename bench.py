@@ -9,7 +9,9 @@ quantization, residual write, group flush every 32 steps) + kivi_decode_attentio
 (fused 2-bit decode attention + split combine).  The metric is decode tokens/s
 (batch / step time) with the attention kernel's achieved HBM GB/s against the
 measured copy bandwidth.  L2 is flushed (256 MiB write) before every step, outside
-the timed events.
+the timed events.  Every 64 steps the cache is rolled back to the prompt (token
+count reset, residual keys restored; outside the timed events), so the context
+stays within 4113 .. 4176 tokens however many steps run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
 
@@ -37,6 +39,7 @@ METRIC = "decode-attention tokens/s and achieved HBM GB/s (fraction of peak) on 
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+CYCLE = 64  # steps between cache rollbacks
 
 
 def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int) -> int:
@@ -103,7 +106,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                                          "-i", str(self.gpu), "-lms", "50"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -190,7 +193,7 @@ def run_reference(args, wl):
     pre = synth.make_prefill(wl)
     for w in range(args.warmup):  # untimed warm-up: the first call builds the oracle
         oracle_timing(wl, pre, 1, 4, 0.0)
-    cb = oracle_timing(wl, pre, args.steps, 16, 60.0)
+    cb = oracle_timing(wl, pre, args.steps, 32, 60.0)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B / cb["value"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -203,7 +206,7 @@ def run_reference(args, wl):
 
 def workload_config(wl):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
-            "context_tokens": wl.n, "step": "append_token + decode_attention (one new token per sequence)",
+            "context_tokens": f"{wl.n}..{wl.n + CYCLE} (cache rolled back every {CYCLE} steps)", "step": "append_token + decode_attention (one new token per sequence)",
             "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
             "parallelism": "replicas (one independent cache per GPU)"}
 
@@ -233,27 +236,35 @@ def run_kivi(args, wl):
     kivi.lib()
     pre = synth.make_prefill(wl)
     total = args.warmup + args.steps
-    T = wl.capacity(extra=total + 2 * args.warmup + 64)
+    T = wl.capacity(extra=CYCLE + 64)
     cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
     kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
-    steps_in = [synth.make_step(wl, pre, s) for s in range(total)]
-    # inputs resident in HBM before timing
-    dev_in = [(k.to(dev), v.to(dev), q.to(dev)) for k, v, q in steps_in]
+    n0 = cache.n_tokens
+    res0 = cache.k_res.clone()
+    # the inputs of one rollback cycle, resident in HBM before timing
+    dev_in = [tuple(t.to(dev) for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
-    ws = kivi.workspace(cache, wl.Hq, n_tokens=T, device=dev)
+    ws = kivi.workspace(cache, wl.Hq, n_tokens=n0 + CYCLE, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def rollback():
+        cache.k_res.copy_(res0)
+        cache.c.n_tokens = n0
+
     def step_events(i, rec):
-        k, v, q = dev_in[i]
+        if i % CYCLE == 0:
+            rollback()
+        k, v, q = dev_in[i % CYCLE]
         flush.fill_(i & 0xFF)
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        n_before = cache.n_tokens
         e0.record(stream)
         kivi.kivi_append_token(cache, k, v, stream=stream)
         e1.record(stream)
         kivi.kivi_decode_attention(cache, q, 1.0, out=out, ws=ws, stream=stream)
         e2.record(stream)
-        rec.append((e0, e1, e2, cache.n_tokens))
+        rec.append((e0, e1, e2, cache.n_tokens, 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2))
 
     warm = []
     for i in range(args.warmup):
@@ -262,19 +273,17 @@ def run_kivi(args, wl):
     barrier()
     torch.cuda.synchronize()
     rec = []
-    launches = 0
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for i in range(args.warmup, total):
-            n_before = cache.n_tokens
             step_events(i, rec)
-            launches += 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier()
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2, _ in rec]
-    attn_ms = [e1.elapsed_time(e2) for _, e1, e2, _ in rec]
-    app_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in rec]
+    launches = sum(x[4] for x in rec)
+    step_ms = [e0.elapsed_time(e2) for e0, _, e2, _, _ in rec]
+    attn_ms = [e1.elapsed_time(e2) for _, e1, e2, _, _ in rec]
+    app_ms = [e0.elapsed_time(e1) for e0, e1, _, _, _ in rec]
     ms_per_step = sum(step_ms) / len(step_ms)
     if world > 1:
         import torch.distributed as dist
@@ -283,7 +292,7 @@ def run_kivi(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
     value = wl.B * world / (ms_per_step / 1e3)
-    bytes_per = [algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n) for *_, n in rec]
+    bytes_per = [algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n) for _, _, _, n, _ in rec]
     attn_avg_ms = sum(attn_ms) / len(attn_ms)
     achieved = (sum(bytes_per) / len(bytes_per)) / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
@@ -291,7 +300,7 @@ def run_kivi(args, wl):
     traffic = profiled_traffic(sha)
 
     # ---- end to end through the public API: host buffers, copies inside the timing
-    e2e = e2e_run(args, wl, pre, steps_in, dev, stream, flush)
+    e2e = e2e_run(args, wl, pre, dev, stream, flush)
 
     if rank != 0:
         if world > 1:
@@ -299,7 +308,7 @@ def run_kivi(args, wl):
 
             dist.destroy_process_group()
         return 0
-    cb = oracle_timing(wl, pre, 8, 16, 15.0) if world == 1 else None
+    cb = oracle_timing(wl, pre, 64, 32, 2.0) if world == 1 else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -325,30 +334,35 @@ def run_kivi(args, wl):
     return 0
 
 
-def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
+def e2e_run(args, wl, pre, dev, stream, flush):
     """Same metric through the public API with host inputs: every step copies its
     new k, v, q from pinned host memory, runs append + decode attention and copies
     the output back; the copies are inside the timed events."""
     import torch
 
-    from bit_asymmetric_kv_gb300 import kivi
+    from bit_asymmetric_kv_gb300 import kivi, synth
 
     total = args.warmup + args.steps
-    T = wl.capacity(extra=total + 64)
+    T = wl.capacity(extra=CYCLE + 64)
     cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
     kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
-    host = [(k.pin_memory(), v.pin_memory(), q.pin_memory()) for k, v, q in steps_in]
-    dk = torch.empty_like(steps_in[0][0], device=dev)
-    dv = torch.empty_like(steps_in[0][1], device=dev)
-    dq = torch.empty_like(steps_in[0][2], device=dev)
+    n0 = cache.n_tokens
+    res0 = cache.k_res.clone()
+    host = [tuple(t.pin_memory() for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
+    dk = torch.empty_like(host[0][0], device=dev)
+    dv = torch.empty_like(host[0][1], device=dev)
+    dq = torch.empty_like(host[0][2], device=dev)
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     out_h = torch.empty_like(out, device="cpu").pin_memory()
-    ws = kivi.workspace(cache, wl.Hq, n_tokens=T, device=dev)
+    ws = kivi.workspace(cache, wl.Hq, n_tokens=n0 + CYCLE, device=dev)
     times = []
     for i in range(total):
+        if i % CYCLE == 0:
+            cache.k_res.copy_(res0)
+            cache.c.n_tokens = n0
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        hk, hv, hq = host[i]
+        hk, hv, hq = host[i % CYCLE]
         e0.record(stream)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
@@ -362,7 +376,7 @@ def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    h2d = sum(t.numel() * t.element_size() for t in steps_in[0])
+    h2d = sum(t.numel() * t.element_size() for t in host[0])
     d2h = out.numel() * out.element_size()
     return {"value": wl.B * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
@@ -371,8 +385,8 @@ def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["kivi", "reference"], default="kivi")
     args = ap.parse_args(argv)
     if args.warmup < 3:

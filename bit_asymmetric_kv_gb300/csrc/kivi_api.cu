@@ -28,19 +28,11 @@ int check_cache(const kivi_cache *c) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
 
-int num_sms() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return sms;
-}
-
 int check_heads(const kivi_dims *d, int32_t Hq) {
   if (Hq <= 0) return KIVI_ERR_ARG;
   if (Hq % d->Hkv != 0) return KIVI_ERR_UNSUPPORTED;
   const int R = Hq / d->Hkv;
   if (R != 1 && R != 2 && R != 4) return KIVI_ERR_UNSUPPORTED;
-  if ((int64_t)d->B * d->Hkv > 65535) return KIVI_ERR_UNSUPPORTED;  // grid.y of the decode launch
   return KIVI_OK;
 }
 
@@ -121,17 +113,15 @@ int kivi_append_token(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, 
 
 int kivi_decode_splits(const kivi_dims *d, int32_t Hq, int64_t n) {
   if (check_dims(d) != KIVI_OK || check_heads(d, Hq) != KIVI_OK || n <= 0) return 0;
-  const int sms = num_sms();
-  if (sms <= 0) return 0;
-  int splits = 0, gps = 0;
-  kivi::decode_plan(d->B, d->Hkv, d->G, n, sms, &splits, &gps);
-  return splits;
+  kivi::DecodeGeom g;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, n, &g) != cudaSuccess) return 0;
+  return g.pmax;
 }
 
 size_t kivi_decode_workspace_bytes(const kivi_dims *d, int32_t Hq, int64_t n) {
-  const int splits = kivi_decode_splits(d, Hq, n);
-  if (splits <= 0) return 0;
-  return (size_t)d->B * (size_t)Hq * (size_t)splits * (size_t)(d->D + 2) * sizeof(float);
+  const int slots = kivi_decode_splits(d, Hq, n);
+  if (slots <= 0) return 0;
+  return (size_t)d->B * (size_t)Hq * (size_t)slots * (size_t)(d->D + 2) * sizeof(float);
 }
 
 int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_t *q, int32_t Hq,
@@ -143,11 +133,9 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   if (!q || !out) return KIVI_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
   if (c->n_tokens <= 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
-  const int sms = num_sms();
-  if (sms <= 0) return KIVI_ERR_CUDA;
-  int splits = 0, gps = 0;
-  kivi::decode_plan(d->B, d->Hkv, d->G, c->n_tokens, sms, &splits, &gps);
-  const size_t need = (size_t)d->B * (size_t)Hq * (size_t)splits * (size_t)(d->D + 2) * sizeof(float);
+  kivi::DecodeGeom g;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, c->n_tokens, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
   kivi::DecodeArgs a;
@@ -165,8 +153,11 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.Hkv = d->Hkv;
   a.Hq = Hq;
   a.G = d->G;
-  a.splits = splits;
-  a.groups_per_split = gps;
+  a.units_per_head = g.units_per_head;
+  a.total_units = g.total_units;
+  a.n_warps = g.n_warps;
+  a.grid = g.grid;
+  a.pmax = g.pmax;
   a.softmax_scale = softmax_scale;
   return cuda_status(kivi::launch_decode(a, st));
 }

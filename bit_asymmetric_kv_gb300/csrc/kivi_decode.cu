@@ -14,17 +14,35 @@
 //   * the codes enter as fp16 subnormals (exact, see unpack16);
 //   * the fp32 factors qs and p*s enter as an fp16 pair hi + lo (hi = fp16(x),
 //     lo = fp16(x - hi)), one per MMA column, which keeps ~22 significant bits;
-//   * the 8 MMA columns are (query head r, hi/lo part) = 2r + part.
+//     qs is first scaled by a power of two chosen per group so that its largest
+//     entry sits just below 2^14 (no fp16 overflow, full precision for any range).
 // Tokens are tiled by 16 (the MMA M dimension for q.K, the K dimension for P.V).
-// Each CTA covers one context split of one (batch, KV head); its 4 warps take the
-// split's key groups round-robin, staging each group (codes, scales, zeros) into
-// shared memory with cp.async three groups ahead.  The last split also covers the
-// fp16 residual keys.  Partial (max, sum, output) per split go to the workspace and
-// a combine kernel merges the splits (flash-decoding).
+// The 4 column pairs of an MMA carry (tile slot, query head): a softmax step covers
+// T = 4/R tiles at once, so that for every R each lane owns the scores of one
+// (tile, head) pair: lane (g, tig) holds tokens g and g+8 of tile slot tig/R for
+// head tig%R.  For q.K the per-head factors are replicated over the slots and each
+// tile accumulates separately; for P.V each tile's weights sit in its own column
+// pairs and all tiles accumulate together (the slots are summed at the end).
+//
+// Work decomposition (persistent, balanced): a "unit" is 64 tokens of one (batch, KV
+// head) -- one or two key groups -- plus one unit for the fp16 residual keys when
+// n mod G > 0.  The grid holds exactly as many warps as fit on the GPU at once; warp
+// w takes the contiguous unit range [w*W/NW, (w+1)*W/NW), staging each unit (codes,
+// scales, zeros) in its shared memory with cp.async one unit ahead, and runs an
+// online softmax over it.  At every head boundary the warp writes a partial (max,
+// sum, unnormalised output) to the workspace; the combine kernel merges a head's
+// partials (flash-decoding) and is launched as a programmatic dependent.
 #include <math.h>
+
+#include <type_traits>
 
 #include "kivi_device.cuh"
 #include "kivi_internal.h"
+
+// Resident CTAs per SM the register allocation is sized for (3: up to 168 registers).
+#ifndef KIVI_DECODE_MIN_CTAS
+#define KIVI_DECODE_MIN_CTAS 3
+#endif
 
 namespace kivi {
 
@@ -33,18 +51,20 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
+constexpr int kUnit = 64;                            // tokens per unit
 constexpr int kFragRowWords = 20;                    // 16 B-fragment words + 4 pad (bank spread)
-constexpr int kFragBytes = 32 * kFragRowWords * 4;   // per warp
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int G>
-struct Stage {
-  static constexpr int kKCodes = 0;                  // G rows x 32 B
-  static constexpr int kVCodes = G * 32;             // G rows x 32 B
-  static constexpr int kVMeta = 2 * G * 32;          // G x 4 B
-  static constexpr int kKMeta = 2 * G * 32 + G * 4;  // 128 x 4 B
-  static constexpr int kBytes = kKMeta + kD * 4;
-  static constexpr int kWarpBytes = kStages * kBytes + kFragBytes;
+template <int R, int G>
+struct Layout {
+  static constexpr int kGroups = kUnit / G;          // key groups per unit
+  static constexpr int kKCodes = 0;                  // 64 rows x 32 B
+  static constexpr int kVCodes = kUnit * 32;         // 64 rows x 32 B
+  static constexpr int kVMeta = 2 * kUnit * 32;      // 64 x 4 B
+  static constexpr int kKMeta = kVMeta + kUnit * 4;  // kGroups x 128 x 4 B
+  static constexpr int kStageBytes = kKMeta + kGroups * kD * 4;
+  static constexpr int kFragGroupBytes = 8 * R * kFragRowWords * 4;  // rows 4*(2h+p)+tig
+  static constexpr int kWarpBytes = kStages * kStageBytes + kGroups * kFragGroupBytes;
   static constexpr int kSmem = kWarps * kWarpBytes;
 };
 
@@ -54,424 +74,675 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
+
 __device__ __forceinline__ uint2 lds64(const unsigned char *p) { return *reinterpret_cast<const uint2 *>(p); }
 __device__ __forceinline__ uint32_t lds32(const unsigned char *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
-// Per-warp running softmax state and P.V accumulators.  Lane (g, tig) owns query
-// head tig: acc[j] = O[channel 16g+j | 16g+8+j][head tig, hi | lo].
-struct WarpState {
-  float acc[8][4];
-  float m;     // running max, log2 domain
-  float l;     // this lane's share of sum_t p_t
-  float zs;    // this lane's share of sum_t p_t z_t
-};
-
-// Online softmax over one 16-token tile, then P.V on the tensor cores.
-//   sa, sb   : log2-domain scores of tokens g and g+8 for head tig (-inf if masked)
-//   vma, vmb : {s, z} words of those tokens (ignored where masked)
-//   v[4]     : word g of the value rows of tokens tig, tig+4, tig+8, tig+12
-__device__ __forceinline__ void softmax_pv(WarpState &st, float sa, float sb, bool va, bool vb, uint32_t vma,
-                                           uint32_t vmb, const uint32_t v[4], int lane) {
-  const int g = lane >> 2, tig = lane & 3;
-  float tmax = fmaxf(sa, sb);
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 4));
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
-  tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-  const float m_new = fmaxf(st.m, tmax);
-  if (__any_sync(0xffffffffu, m_new > st.m)) {
-    const float alpha = ex2(st.m - m_new);  // st.m = -inf at the start: alpha = 0
+__device__ __forceinline__ void load_frag(const unsigned char *row, uint32_t bf[16]) {
+  const uint4 *p = reinterpret_cast<const uint4 *>(row);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) st.acc[j][k] *= alpha;
-    st.l *= alpha;
-    st.zs *= alpha;
-    st.m = m_new;
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = p[k];
+    bf[4 * k] = u.x;
+    bf[4 * k + 1] = u.y;
+    bf[4 * k + 2] = u.z;
+    bf[4 * k + 3] = u.w;
   }
-  const float pa = va ? ex2(sa - st.m) : 0.f;
-  const float pb = vb ? ex2(sb - st.m) : 0.f;
-  const float sva = va ? h2f((uint16_t)(vma & 0xffffu)) : 0.f, zva = va ? h2f((uint16_t)(vma >> 16)) : 0.f;
-  const float svb = vb ? h2f((uint16_t)(vmb & 0xffffu)) : 0.f, zvb = vb ? h2f((uint16_t)(vmb >> 16)) : 0.f;
-  st.l += pa + pb;
-  st.zs = fmaf(pa, zva, fmaf(pb, zvb, st.zs));
-  const float wa = pa * sva, wb = pb * svb;
-  const uint16_t ha = f2h(wa), hb = f2h(wb);
-  const uint16_t la = f2h(wa - h2f(ha)), lb = f2h(wb - h2f(hb));
-  const uint32_t q1 = (uint32_t)ha | ((uint32_t)la << 16);
-  const uint32_t q2 = (uint32_t)hb | ((uint32_t)lb << 16);
-  // B operand of P.V: column g = (head g/2, part g%2); K slots 2tig, 2tig+1,
-  // 2tig+8, 2tig+9 hold tokens tig, tig+4, tig+8, tig+12.  Token u's weight for
-  // head h lives in lane 4*(u%8) + h (first token if u < 8, second otherwise).
-  const int src_a = 4 * tig + (g >> 1);
-  const int src_b = src_a + 16;
-  const uint32_t a1 = __shfl_sync(0xffffffffu, q1, src_a);
-  const uint32_t b1 = __shfl_sync(0xffffffffu, q1, src_b);
-  const uint32_t a2 = __shfl_sync(0xffffffffu, q2, src_a);
-  const uint32_t b2 = __shfl_sync(0xffffffffu, q2, src_b);
-  const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
-  const uint32_t bw0 = prmt(a1, b1, sel), bw1 = prmt(a2, b2, sel);
-  // A operand of P.V: rows = channels 16g + j (from the low 16 bits of word g) and
-  // 16g + 8 + j (high 16 bits), columns = the four tokens paired as above.
+}
+
+// q.K of one 16-token tile: A from the unpacked codes (or fp16 keys) of token g
+// (ra*) and g+8 (rb*), words 2tig (..0) and 2tig+1 (..1); accumulates into sc.
+__device__ __forceinline__ void qk_tile(const uint32_t ra0[8], const uint32_t ra1[8], const uint32_t rb0[8],
+                                        const uint32_t rb1[8], const uint32_t bf[16], float sc[4]) {
+  float s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    mma16816(sc, ra0[2 * j], rb0[2 * j], ra0[2 * j + 1], rb0[2 * j + 1], bf[2 * j], bf[2 * j + 1]);
+    mma16816(s1, ra1[2 * j], rb1[2 * j], ra1[2 * j + 1], rb1[2 * j + 1], bf[8 + 2 * j], bf[8 + 2 * j + 1]);
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) sc[k] += s1[k];
+}
+
+// P.V of one 16-token tile: A = value codes of word g of tokens tig, tig+4, tig+8,
+// tig+12 (v[0..3]), B = (bw0, bw1).
+__device__ __forceinline__ void pv_tile(float acc[8][4], const uint32_t v[4], uint32_t bw0, uint32_t bw1) {
   uint32_t x01[8], y01[8], x23[8], y23[8];
   unpack16(prmt(v[0], v[1], 0x5410u), x01);
   unpack16(prmt(v[0], v[1], 0x7632u), y01);
   unpack16(prmt(v[2], v[3], 0x5410u), x23);
   unpack16(prmt(v[2], v[3], 0x7632u), y23);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) mma16816(st.acc[j], x01[j], y01[j], x23[j], y23[j], bw0, bw1);
+  for (int j = 0; j < 8; ++j) mma16816(acc[j], x01[j], y01[j], x23[j], y23[j], bw0, bw1);
 }
 
-// q.K of one 16-token tile from unpacked A registers: ra* for token g, rb* for
-// token g+8, words 2tig (…0) and 2tig+1 (…1).  Returns the 4 accumulator values.
-__device__ __forceinline__ void qk_tile(const uint32_t ra0[8], const uint32_t ra1[8], const uint32_t rb0[8],
-                                        const uint32_t rb1[8], const uint32_t bf[16], float sc[4]) {
-  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    mma16816(s0, ra0[2 * j], rb0[2 * j], ra0[2 * j + 1], rb0[2 * j + 1], bf[2 * j], bf[2 * j + 1]);
-    mma16816(s1, ra1[2 * j], rb1[2 * j], ra1[2 * j + 1], rb1[2 * j + 1], bf[8 + 2 * j], bf[8 + 2 * j + 1]);
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) sc[k] = s0[k] + s1[k];
-}
-
-// Channel c's place in the q.K B fragment: lane row 4*col + tig, word 2j + (c odd),
-// half (c mod 16 >= 8).  Word w of a token row feeds MMA steps 4*(w&1) .. +3 of the
-// lanes with tig = w >> 1.
-__device__ __forceinline__ int frag_half_index(int c, int col) {
-  const int W = c >> 4, i = c & 15, i8 = i & 7;
-  const int tig = W >> 1;
-  const int j = 4 * (W & 1) + (i8 >> 1);
-  const int word = 2 * j + (i8 & 1);
-  return (4 * col + tig) * (kFragRowWords * 2) + word * 2 + (i >= 8 ? 1 : 0);
-}
-
-template <int R>
-__device__ __forceinline__ void load_frag(const unsigned char *frag, int lane, uint32_t bf[16]) {
-  const int g = lane >> 2;
-  if (g < 2 * R) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(frag + lane * kFragRowWords * 4);
+// 32 fp16 keys (channels 32tig .. 32tig+31) of one residual token, paired (m, m+8)
+// like the unpacked codes.
+__device__ __forceinline__ void residual_pairs(const uint16_t *row, bool valid, int tig, uint32_t r0[8],
+                                               uint32_t r1[8]) {
+  uint32_t p[16];
+  if (valid) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + 32 * tig);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 u = p[k];
-      bf[4 * k] = u.x;
-      bf[4 * k + 1] = u.y;
-      bf[4 * k + 2] = u.z;
-      bf[4 * k + 3] = u.w;
+      const uint4 uu = __ldg(src + k);
+      p[4 * k] = uu.x;
+      p[4 * k + 1] = uu.y;
+      p[4 * k + 2] = uu.z;
+      p[4 * k + 3] = uu.w;
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) bf[k] = 0u;
+    for (int k = 0; k < 16; ++k) p[k] = 0u;
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const uint32_t sel = (m & 1) ? 0x7632u : 0x5410u;
+    r0[m] = prmt(p[m >> 1], p[(m >> 1) + 4], sel);
+    r1[m] = prmt(p[8 + (m >> 1)], p[8 + (m >> 1) + 4], sel);
+  }
+}
+
+// Index of the first warp whose unit range contains unit u.
+__device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t NW) { return ((u + 1) * NW - 1) / W; }
+
+// Per-lane constants of the fragment bookkeeping.
+struct LaneInfo {
+  int g, tig, slot_mine, pv_slot, src_a, src_b;
+  uint32_t pv_sel;
+};
+
+// Softmax state of the q.K side: running max (log2 domain, per head) and this
+// lane's shares of sum_t p_t and sum_t p_t z_t.
+struct SoftState {
+  float m, l, zs;
+};
+
+// Max over the lanes that share this lane's query head.
+template <int R>
+__device__ __forceinline__ float head_max(float x) {
+  if (R == 1) {
+    // one head per warp: an order-preserving integer key and one warp reduction
+    const int k = __float_as_int(x);
+    const int key = k ^ ((k >> 31) & 0x7fffffff);
+    const int mk = __reduce_max_sync(0xffffffffu, key);
+    return __int_as_float(mk ^ ((mk >> 31) & 0x7fffffff));
+  }
+#pragma unroll
+  for (int off = R; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+// q.K side of one softmax step over T = 4/R tiles of 16 tokens.
+//   kfill(i, sc)  accumulates tile slot i's q.K MMA into sc[4];
+//   cq, beta      this lane's score scale and offset (log2 domain);
+//   n_valid       tokens of the step that exist (FULL: all 16*T);
+//   vmeta(tok)    {s, z} of step token tok.
+// Returns the P.V B operand of this lane (bw0, bw1) and the rescale factor alpha
+// that the P.V accumulators need before this step's contribution is added.
+template <int R, bool FULL, class KF, class VM>
+__device__ __forceinline__ void qk_step(SoftState &st, const LaneInfo &li, KF &&kfill, float cq, float beta,
+                                        int n_valid, VM &&vmeta, uint32_t &bw0, uint32_t &bw1, float &alpha) {
+  constexpr int T = 4 / R;
+  float S[T][4];
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) S[i][k] = 0.f;
+    if (FULL || 16 * i < n_valid) kfill(i, S[i]);
+  }
+  float d[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) d[k] = S[0][k];
+#pragma unroll
+  for (int i = 1; i < T; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) d[k] = (li.slot_mine == i) ? S[i][k] : d[k];
+  const int ta = 16 * li.slot_mine + li.g, tb = ta + 8;  // this lane's tokens in the step
+  const bool va = FULL || ta < n_valid, vb = FULL || tb < n_valid;
+  const float sa = va ? fmaf(cq, d[0] + d[1], beta) : -INFINITY;
+  const float sb = vb ? fmaf(cq, d[2] + d[3], beta) : -INFINITY;
+  const float m_new = fmaxf(st.m, head_max<R>(fmaxf(sa, sb)));
+  alpha = ex2(st.m - m_new);  // st.m = -inf at the start of a head: alpha = 0
+  st.m = m_new;
+  const uint32_t vma = vmeta(va ? ta : 0), vmb = vmeta(vb ? tb : 0);
+  const float pa = va ? ex2(sa - m_new) : 0.f;
+  const float pb = vb ? ex2(sb - m_new) : 0.f;
+  const float2 fa = __half22float2(u2h2(vma)), fb = __half22float2(u2h2(vmb));  // {s, z}
+  const float sva = va ? fa.x : 0.f, zva = va ? fa.y : 0.f;
+  const float svb = vb ? fb.x : 0.f, zvb = vb ? fb.y : 0.f;
+  st.l = fmaf(st.l, alpha, pa + pb);
+  st.zs = fmaf(st.zs, alpha, fmaf(pa, zva, pb * zvb));
+  const float wa = pa * sva, wb = pb * svb;
+  // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
+  const __half2 hab = __floats2half2_rn(wa, wb);
+  const float2 fab = __half22float2(hab);
+  const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
+  const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
+  const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
+  // B of P.V for tile slot pv_slot, column g = (slot, head, part): K slots
+  // 2tig, 2tig+1, 2tig+8, 2tig+9 hold tokens tig, tig+4, tig+8, tig+12; token u's
+  // weight lives in lane 4*(u%8) + (g>>1) (first token if u < 8, else second)
+  const uint32_t a1 = __shfl_sync(0xffffffffu, q1, li.src_a);
+  const uint32_t b1 = __shfl_sync(0xffffffffu, q1, li.src_b);
+  const uint32_t a2 = __shfl_sync(0xffffffffu, q2, li.src_a);
+  const uint32_t b2 = __shfl_sync(0xffffffffu, q2, li.src_b);
+  bw0 = prmt(a1, b1, li.pv_sel);
+  bw1 = prmt(a2, b2, li.pv_sel);
+}
+
+// P.V side of one step: rescale the accumulators, then add the T tiles.
+//   vword(i, k)   word g of the value row of token tig + 4k of tile slot i.
+template <int R, class VW>
+__device__ __forceinline__ void pv_step(float acc[8][4], const LaneInfo &li, int n_valid, uint32_t bw0, uint32_t bw1,
+                                        float alpha, VW &&vword) {
+  constexpr int T = 4 / R;
+  if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[j][k] *= alpha;
+  }
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    if (16 * i < n_valid) {
+      uint32_t v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
+      const bool mine = li.pv_slot == i;
+      pv_tile(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
+    }
   }
 }
 
 template <int R, int G>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  using S = Stage<G>;
+  using L = Layout<R, G>;
+  constexpr int T = 4 / R;           // tile slots per softmax step
+  constexpr int TPG = G / 16;        // tiles per key group
+  constexpr int NGU = L::kGroups;    // key groups per unit
+  // the combine grid may launch now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
-  const int split = blockIdx.x;
-  const int64_t bh = blockIdx.y;
-  const int b = (int)(bh / a.Hkv), kvh = (int)(bh % a.Hkv);
-  const int64_t n_groups = a.n / G;
-  const int64_t nq = n_groups * G;
-  const int r = (int)(a.n - nq);
-  const int64_t gb = (int64_t)split * a.groups_per_split;
-  const int64_t ge = min(n_groups, gb + a.groups_per_split);
-  const bool last = split == a.splits - 1;
+  const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t NW = a.n_warps, W = a.total_units;
+  const int U = (int)a.units_per_head;
+  if (gw >= NW) return;
+  const int64_t u0 = gw * W / NW, u1 = (gw + 1) * W / NW;
+  if (u0 >= u1) return;
+  const int n_my = (int)(u1 - u0);
+  const int NG = (int)(a.n / G);
+  const int r = (int)(a.n - (int64_t)NG * G);
+  const int n_code_units = (NG + NGU - 1) / NGU;  // units holding quantized keys
+  const int64_t nq = (int64_t)NG * G;
 
-  unsigned char *wbase = smem + warp * S::kWarpBytes;
-  unsigned char *frag = wbase + kStages * S::kBytes;
-  uint16_t *frag16 = reinterpret_cast<uint16_t *>(frag);
+  unsigned char *wbase = smem + warp * L::kWarpBytes;
+  unsigned char *frag = wbase + kStages * L::kStageBytes;
+  const float c0 = a.softmax_scale * kLog2e;
 
-  // this lane's query values for channels lane + 32k, heads r < R (fp32, exact)
-  float qv[R][4];
+  LaneInfo li;
+  li.g = lane >> 2;
+  li.tig = lane & 3;
+  li.slot_mine = li.tig / R;
+  li.pv_slot = (li.g >> 1) / R;
+  li.src_a = 4 * li.tig + (li.g >> 1);
+  li.src_b = li.src_a + 16;
+  li.pv_sel = (li.g & 1) ? 0x7632u : 0x5410u;
+  const int g = li.g, tig = li.tig;
+  const int head_mine = tig % R;
+  const int frag_row = 4 * (2 * ((g >> 1) % R) + (g & 1)) + tig;
+  // prep: channel c = lane + 32k lands in row 4*(2h+p) + k, half-word wh of the row
+  int wh;
+  {
+    const int i = lane & 15, i8 = i & 7;
+    const int j = 4 * (lane >> 4) + (i8 >> 1);
+    wh = (2 * j + (i8 & 1)) * 2 + (i >= 8 ? 1 : 0);
+  }
+  // codes of channel index i (mod 16) are unpacked with factor 4^(i mod 4);
+  // 4^(3 - i mod 4) brings every q.K product to code * qs * 64
+  const float mult = (float)(64 >> (2 * (lane & 3)));
+
+  // ---- staging cursor (unit u0 + kk -> head h_is, unit uu_is within the head)
+  int64_t h_is = u0 / U;
+  int uu_is = (int)(u0 - h_is * U);
+  auto issue = [&](int kk) {
+    if (kk < n_my && uu_is < n_code_units) {
+      const int g0 = uu_is * NGU;
+      const int ngr = min(NGU, NG - g0);  // 1 or 2 groups (G = 32)
+      const int rows = ngr * G;
+      unsigned char *stg = wbase + (kk % kStages) * L::kStageBytes;
+      const int64_t t0 = h_is * a.max_tokens + (int64_t)g0 * G;
+      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + t0 * kWordsPerRow);
+      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + t0 * kWordsPerRow);
+      const unsigned char *vm = reinterpret_cast<const unsigned char *>(a.v_meta + t0);
+      const unsigned char *km =
+          reinterpret_cast<const unsigned char *>(a.k_meta + (h_is * (a.max_tokens / G) + g0) * kD);
+      if (rows == kUnit) {
 #pragma unroll
-  for (int h = 0; h < R; ++h)
+        for (int c = lane; c < kUnit * 2; c += 32) {
+          cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
+          cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
+        }
+        if (lane < kUnit / 4) cp_async16(stg + L::kVMeta + lane * 16, vm + lane * 16);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) qv[h][k] = h2f(a.q[((int64_t)b * a.Hq + kvh * R + h) * kD + lane + 32 * k]);
-  // even channels meet codes unpacked with factor 1, odd channels with factor 4;
-  // both carry 2^-24.  B = qs * (4 | 1) makes every product code * qs * 2^-22.
-  const float fac = (lane & 1) ? 1.f : 4.f;
-  const float c_q = a.softmax_scale * kLog2e * 4194304.f;  // 2^22
-  const float c_b = a.softmax_scale * kLog2e;
+        for (int c = lane; c < NGU * 32; c += 32) cp_async16(stg + L::kKMeta + c * 16, km + c * 16);
+      } else {
+        for (int c = lane; c < rows * 2; c += 32) {
+          cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
+          cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
+        }
+        if (lane < rows / 4) cp_async16(stg + L::kVMeta + lane * 16, vm + lane * 16);
+        for (int c = lane; c < ngr * 32; c += 32) cp_async16(stg + L::kKMeta + c * 16, km + c * 16);
+      }
+    }
+    cp_async_commit();
+    if (++uu_is == U) {
+      uu_is = 0;
+      ++h_is;
+    }
+  };
 
-  WarpState st;
+  SoftState ss = {-INFINITY, 0.f, 0.f};
+  float acc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) st.acc[j][k] = 0.f;
-  st.m = -INFINITY;
-  st.l = 0.f;
-  st.zs = 0.f;
+    for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
+  float qv[R][4];
 
-  const int64_t first = gb + warp;
-  const int n_my = (first < ge) ? (int)((ge - first + kWarps - 1) / kWarps) : 0;
-  const uint32_t *kc_head = a.k_codes + bh * a.max_tokens * kWordsPerRow;
-  const uint32_t *vc_head = a.v_codes + bh * a.max_tokens * kWordsPerRow;
-  const uint32_t *vm_head = a.v_meta + bh * a.max_tokens;
-  const uint32_t *km_head = a.k_meta + bh * (a.max_tokens / G) * kD;
-
-  auto issue = [&](int kk) {
-    if (kk < n_my) {
-      const int64_t grp = first + (int64_t)kk * kWarps;
-      unsigned char *stg = wbase + (kk % kStages) * S::kBytes;
-      const unsigned char *kc = reinterpret_cast<const unsigned char *>(kc_head + grp * G * kWordsPerRow);
-      const unsigned char *vc = reinterpret_cast<const unsigned char *>(vc_head + grp * G * kWordsPerRow);
-      const unsigned char *vm = reinterpret_cast<const unsigned char *>(vm_head + grp * G);
-      const unsigned char *km = reinterpret_cast<const unsigned char *>(km_head + grp * kD);
+  // Write head h's partial number (gw - first warp of h) from the P.V accumulators
+  // and the softmax state (m, l, zs) that belongs to them.
+  auto emit = [&](int64_t h, const SoftState &fin) {
+    float l = fin.l, zs = fin.zs;
 #pragma unroll
-      for (int c = lane; c < G * 2; c += 32) {
-        cp_async16(stg + S::kKCodes + c * 16, kc + c * 16);
-        cp_async16(stg + S::kVCodes + c * 16, vc + c * 16);
-      }
-      if (lane < G / 4) cp_async16(stg + S::kVMeta + lane * 16, vm + lane * 16);
-      cp_async16(stg + S::kKMeta + lane * 16, km + lane * 16);
+    for (int off = 4; off < 32; off <<= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+      zs += __shfl_xor_sync(0xffffffffu, zs, off);
     }
-    cp_async_commit();
+    float o[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      o[j] = acc[j][0] + acc[j][1];
+      o[8 + j] = acc[j][2] + acc[j][3];
+    }
+    // sum the tile slots of the same head (tig bits above the head bits)
+#pragma unroll
+    for (int off = R; off < 4; off <<= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+      zs += __shfl_xor_sync(0xffffffffu, zs, off);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j] += __shfl_xor_sync(0xffffffffu, o[j], off);
+    }
+    if (li.slot_mine == 0) {
+      const int64_t b = h / a.Hkv, kvh = h - b * a.Hkv;
+      const int64_t slot = gw - owner_warp(h * U, W, NW);
+      float *dst = a.ws + ((b * a.Hq + kvh * R + head_mine) * a.pmax + slot) * (kD + 2);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        // undo the code factor 4^(j mod 4) and the 2^-24 of the subnormal codes
+        const float un = pow2i(24 - 2 * (j & 3));
+        dst[16 * g + j] = fmaf(o[j], un, zs);
+        dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs);
+      }
+      if (g == 0) {
+        dst[kD] = fin.m;
+        dst[kD + 1] = l;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
+  };
+  auto load_q = [&](int64_t h) {
+    const int64_t b = h / a.Hkv, kvh = h - b * a.Hkv;
+    const uint16_t *qh = a.q + (b * a.Hq + kvh * R) * kD + lane;
+#pragma unroll
+    for (int hh = 0; hh < R; ++hh)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qv[hh][k] = h2f(qh[hh * kD + 32 * k]);
   };
 
+  // The P.V of unit k runs in iteration k+1, after the q.K side of unit k+1, so
+  // the two independent chains interleave.  Carried between iterations:
+  uint32_t pw0[R], pw1[R];   // P.V B operands per step of the pending unit
+  float palpha[R];           // their rescale factors
+  int p_kind = 0;            // 0 none, 1 codes (stage p_stage), 2 residual
+  int p_ntok = 0, p_stage = 0;
+  int64_t p_h = -1;
+  SoftState p_fin;           // softmax state to emit with once the pending unit is added
+  bool p_emit = false;
 #pragma unroll
-  for (int kk = 0; kk < kStages - 1; ++kk) issue(kk);
+  for (int j = 0; j < R; ++j) {
+    pw0[j] = pw1[j] = 0u;
+    palpha[j] = 1.f;
+  }
 
-  for (int kk = 0; kk < n_my; ++kk) {
-    issue(kk + kStages - 1);
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const unsigned char *stg = wbase + (kk % kStages) * S::kBytes;
-
-    // ---- per-group B fragment: qs * fac split into hi/lo, and beta = q . z
-    float beta[R];
+  auto pv_pending = [&]() {
+    if (p_kind == 1) {
+      const unsigned char *stg = wbase + p_stage * L::kStageBytes;
 #pragma unroll
-    for (int h = 0; h < R; ++h) beta[h] = 0.f;
+      for (int s = 0; s < R; ++s) {
+        const int nv = min(16 * T, p_ntok - 16 * T * s);
+        if (nv <= 0) break;
+        pv_step<R>(acc, li, nv, pw0[s], pw1[s], palpha[s], [&](int i, int k) -> uint32_t {
+          return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
+        });
+      }
+    } else if (p_kind == 2) {
+      const uint32_t *vc_head = a.v_codes + (p_h * a.max_tokens + nq) * kWordsPerRow;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int c = lane + 32 * k;
-      const uint32_t mt = lds32(stg + S::kKMeta + c * 4);
-      const float s = h2f((uint16_t)(mt & 0xffffu)), z = h2f((uint16_t)(mt >> 16));
-#pragma unroll
-      for (int h = 0; h < R; ++h) {
-        const float x = qv[h][k] * s * fac;
-        const uint16_t hi = f2h(x);
-        const uint16_t lo = f2h(x - h2f(hi));
-        frag16[frag_half_index(c, 2 * h)] = hi;
-        frag16[frag_half_index(c, 2 * h + 1)] = lo;
-        beta[h] = fmaf(qv[h][k], z, beta[h]);
+      for (int s = 0; s < R; ++s) {
+        const int nv = min(16 * T, p_ntok - 16 * T * s);
+        if (nv <= 0) break;
+        pv_step<R>(acc, li, nv, pw0[s], pw1[s], palpha[s], [&](int i, int k) -> uint32_t {
+          const int slot = 16 * (s * T + i) + tig + 4 * k;
+          return vc_head[(slot < p_ntok ? slot : 0) * kWordsPerRow + g];
+        });
       }
     }
-    float beta_mine = 0.f;
-#pragma unroll
-    for (int h = 0; h < R; ++h) {
-      float v = beta[h];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (tig == h) beta_mine = v;
+    if (p_emit) {
+      emit(p_h, p_fin);
+      p_emit = false;
     }
-    const float beta2 = c_b * beta_mine;
-    __syncwarp();
-    uint32_t bf[16];
-    load_frag<R>(frag, lane, bf);
+  };
 
+  int64_t cur_h = u0 / U;
+  int uu = (int)(u0 - cur_h * U);
+  load_q(cur_h);
+  issue(0);
+
+  for (int kk = 0; kk < n_my; ++kk) {
+    issue(kk + 1);
+    cp_async_wait<1>();
+    __syncwarp();
+    const int stage = kk % kStages;
+    uint32_t nw0[R], nw1[R];
+    float nalpha[R];
 #pragma unroll
-    for (int i = 0; i < G / 16; ++i) {
-      const uint2 ka = lds64(stg + S::kKCodes + (16 * i + g) * 32 + tig * 8);
-      const uint2 kb = lds64(stg + S::kKCodes + (16 * i + g + 8) * 32 + tig * 8);
-      uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-      unpack16(ka.x, ra0);
-      unpack16(ka.y, ra1);
-      unpack16(kb.x, rb0);
-      unpack16(kb.y, rb1);
-      float sc[4];
-      qk_tile(ra0, ra1, rb0, rb1, bf, sc);
-      const float sa = fmaf(c_q, sc[0] + sc[1], beta2);
-      const float sb = fmaf(c_q, sc[2] + sc[3], beta2);
-      const uint32_t vma = lds32(stg + S::kVMeta + (16 * i + g) * 4);
-      const uint32_t vmb = lds32(stg + S::kVMeta + (16 * i + g + 8) * 4);
-      uint32_t v[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = lds32(stg + S::kVCodes + (16 * i + tig + 4 * k) * 32 + g * 4);
-      softmax_pv(st, sa, sb, true, true, vma, vmb, v, lane);
+    for (int j = 0; j < R; ++j) {
+      nw0[j] = nw1[j] = 0u;
+      nalpha[j] = 1.f;
     }
-    __syncwarp();
-  }
-  cp_async_wait<0>();
+    int n_kind, n_ntok;
 
-  // ---- fp16 residual keys (last split only): B = q itself (hi part, lo = 0)
-  if (last && r > 0) {
-    const int n_tiles = (r + 15) / 16;
-    if (warp < n_tiles) {
+    if (uu < n_code_units) {
+      const unsigned char *stg = wbase + stage * L::kStageBytes;
+      const int ngr = min(NGU, NG - uu * NGU);
+      // ---- per group: qs = q * s scaled by 2^E * mult, split hi/lo into the
+      //      group's B fragment; this lane's score scale and beta = q . z
+      float cq_g[NGU], beta_g[NGU];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = lane + 32 * k;
+      for (int gi = 0; gi < NGU; ++gi) {
+        cq_g[gi] = 0.f;
+        beta_g[gi] = 0.f;
+        if (gi < ngr) {
+          uint16_t *fb = reinterpret_cast<uint16_t *>(frag + gi * L::kFragGroupBytes);
+          float x[R][4], beta[R];
 #pragma unroll
-        for (int h = 0; h < R; ++h) {
-          frag16[frag_half_index(c, 2 * h)] = f2h(qv[h][k]);
-          frag16[frag_half_index(c, 2 * h + 1)] = 0;
+          for (int hh = 0; hh < R; ++hh) beta[hh] = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t mt = lds32(stg + L::kKMeta + (gi * kD + lane + 32 * k) * 4);
+            const float2 sz = __half22float2(u2h2(mt));
+#pragma unroll
+            for (int hh = 0; hh < R; ++hh) {
+              x[hh][k] = qv[hh][k] * sz.x;
+              beta[hh] = fmaf(qv[hh][k], sz.y, beta[hh]);
+            }
+          }
+#pragma unroll
+          for (int hh = 0; hh < R; ++hh) {
+            const float mabs =
+                fmaxf(fmaxf(fabsf(x[hh][0]), fabsf(x[hh][1])), fmaxf(fabsf(x[hh][2]), fabsf(x[hh][3])));
+            const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mabs));
+            // largest |qs| in [2^e, 2^(e+1)): scale by 2^E, E = 7 - e, so |B| < 2^14
+            const int E = min(100, max(-100, 134 - (int)(mbits >> 23)));
+            const float sc = pow2i(E) * mult;
+#pragma unroll
+            for (int k = 0; k < 4; k += 2) {
+              const float y0 = x[hh][k] * sc, y1 = x[hh][k + 1] * sc;
+              const __half2 hi = __floats2half2_rn(y0, y1);
+              const float2 fh = __half22float2(hi);
+              const __half2 lo = __floats2half2_rn(y0 - fh.x, y1 - fh.y);
+              fb[(k + 8 * hh) * (kFragRowWords * 2) + wh] = __half_as_ushort(__low2half(hi));
+              fb[(k + 1 + 8 * hh) * (kFragRowWords * 2) + wh] = __half_as_ushort(__high2half(hi));
+              fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh] = __half_as_ushort(__low2half(lo));
+              fb[(k + 1 + 8 * hh + 4) * (kFragRowWords * 2) + wh] = __half_as_ushort(__high2half(lo));
+            }
+            float bsum = beta[hh];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, off);
+            if (head_mine == hh) {
+              cq_g[gi] = c0 * pow2i(18 - E);  // products are code * qs * 2^(E - 18)
+              beta_g[gi] = c0 * bsum;
+            }
+          }
         }
       }
       __syncwarp();
-      uint32_t bf[16];
-      load_frag<R>(frag, lane, bf);
-      const float c_r = a.softmax_scale * kLog2e;
-      const uint16_t *res_head = a.k_res + bh * G * kD;
-      for (int i = warp; i < n_tiles; i += kWarps) {
-        const int sa_slot = 16 * i + g, sb_slot = 16 * i + g + 8;
-        const bool va = sa_slot < r, vb = sb_slot < r;
-        uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-        // 32 fp16 keys (channels 32tig .. 32tig+31) of each token, paired (m, m+8)
-        auto load_pairs = [&](int slot, bool valid, uint32_t r0[8], uint32_t r1[8]) {
-          uint32_t p[16];
-          if (valid) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(res_head + (int64_t)slot * kD + 32 * tig);
+      // ---- R steps of T tiles cover the unit (a trailing single group: 32 tokens)
+      auto run = [&](auto full_tag, int n_tok) {
+        constexpr bool FULL = decltype(full_tag)::value;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint4 u = __ldg(src + k);
-              p[4 * k] = u.x;
-              p[4 * k + 1] = u.y;
-              p[4 * k + 2] = u.z;
-              p[4 * k + 3] = u.w;
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) p[k] = 0u;
+        for (int s = 0; s < R; ++s) {
+          if (!FULL && 16 * T * s >= n_tok) break;
+          const int my_grp = (s * T + li.slot_mine) / TPG;
+          float cq = cq_g[0], beta = beta_g[0];
+          if (NGU > 1 && my_grp == 1) {
+            cq = cq_g[NGU - 1];
+            beta = beta_g[NGU - 1];
           }
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const uint32_t sel = (m & 1) ? 0x7632u : 0x5410u;
-            r0[m] = prmt(p[m >> 1], p[(m >> 1) + 4], sel);
-            r1[m] = prmt(p[8 + (m >> 1)], p[8 + (m >> 1) + 4], sel);
-          }
-        };
-        load_pairs(sa_slot, va, ra0, ra1);
-        load_pairs(sb_slot, vb, rb0, rb1);
-        float sc[4];
-        qk_tile(ra0, ra1, rb0, rb1, bf, sc);
-        const float sa = va ? c_r * (sc[0] + sc[1]) : -INFINITY;
-        const float sb = vb ? c_r * (sc[2] + sc[3]) : -INFINITY;
-        const int64_t t_a = nq + (va ? sa_slot : 0), t_b = nq + (vb ? sb_slot : 0);
-        const uint32_t vma = vm_head[t_a], vmb = vm_head[t_b];
-        uint32_t v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int slot = 16 * i + tig + 4 * k;
-          const int64_t t = nq + (slot < r ? slot : 0);
-          v[k] = vc_head[t * kWordsPerRow + g];
+          uint32_t bf[16];
+          auto kfill = [&](int i, float sc[4]) {
+            const int t = s * T + i;
+            // (re)load the B fragment at the first tile of each group in the step
+            if (i == 0 || t % TPG == 0)
+              load_frag(frag + (t / TPG) * L::kFragGroupBytes + frag_row * kFragRowWords * 4, bf);
+            const uint2 ka = lds64(stg + L::kKCodes + (16 * t + g) * 32 + tig * 8);
+            const uint2 kb = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
+            uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
+            unpack16(ka.x, ra0);
+            unpack16(ka.y, ra1);
+            unpack16(kb.x, rb0);
+            unpack16(kb.y, rb1);
+            qk_tile(ra0, ra1, rb0, rb1, bf, sc);
+          };
+          auto vmeta = [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + (16 * T * s + tok) * 4); };
+          qk_step<R, FULL>(ss, li, kfill, cq, beta, FULL ? 16 * T : n_tok - 16 * T * s, vmeta, nw0[s], nw1[s],
+                           nalpha[s]);
         }
-        softmax_pv(st, sa, sb, va, vb, vma, vmb, v, lane);
+      };
+      if (ngr == NGU)
+        run(std::true_type{}, kUnit);
+      else
+        run(std::false_type{}, ngr * G);
+      n_kind = 1;
+      n_ntok = ngr * G;
+    } else {
+      // ---- fp16 residual keys of head cur_h: B = q itself (hi part, lo = 0), A = keys
+      uint16_t *fb = reinterpret_cast<uint16_t *>(frag);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int hh = 0; hh < R; ++hh) {
+          fb[(k + 8 * hh) * (kFragRowWords * 2) + wh] = f2h(qv[hh][k]);
+          fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh] = 0;
+        }
+      __syncwarp();
+      uint32_t bf[16];
+      load_frag(frag + frag_row * kFragRowWords * 4, bf);
+      const uint16_t *res_head = a.k_res + cur_h * G * kD;
+      const uint32_t *vm_head = a.v_meta + cur_h * a.max_tokens + nq;
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const int base = 16 * T * s;
+        if (base >= r) break;
+        auto kfill = [&](int i, float sc[4]) {
+          const int sa_slot = base + 16 * i + g, sb_slot = sa_slot + 8;
+          uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
+          residual_pairs(res_head + sa_slot * kD, sa_slot < r, tig, ra0, ra1);
+          residual_pairs(res_head + sb_slot * kD, sb_slot < r, tig, rb0, rb1);
+          qk_tile(ra0, ra1, rb0, rb1, bf, sc);
+        };
+        auto vmeta = [&](int tok) -> uint32_t { return vm_head[base + tok]; };
+        qk_step<R, false>(ss, li, kfill, c0, 0.f, min(16 * T, r - base), vmeta, nw0[s], nw1[s], nalpha[s]);
       }
+      n_kind = 2;
+      n_ntok = r;
     }
-  }
 
-  // ---- per-warp totals, then merge the 4 warps in shared memory
+    // ---- P.V of the previous unit (independent of the q.K work above)
+    pv_pending();
+
+    // this unit becomes the pending one
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    st.l += __shfl_xor_sync(0xffffffffu, st.l, off);
-    st.zs += __shfl_xor_sync(0xffffffffu, st.zs, off);
-  }
-  __syncthreads();  // every warp is done with its stages: reuse them for the merge
-  float *mrg = reinterpret_cast<float *>(smem);  // [warp][R][kD + 2]
-  if (tig < R) {
-    float *row = mrg + (warp * R + tig) * (kD + 2);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      // undo the code factor (4 for odd j) and the 2^-24 of the subnormal codes
-      const float un = (j & 1) ? 4194304.f : 16777216.f;
-      row[16 * g + j] = fmaf(st.acc[j][0] + st.acc[j][1], un, st.zs);
-      row[16 * g + 8 + j] = fmaf(st.acc[j][2] + st.acc[j][3], un, st.zs);
+    for (int j = 0; j < R; ++j) {
+      pw0[j] = nw0[j];
+      pw1[j] = nw1[j];
+      palpha[j] = nalpha[j];
     }
-    if (g == 0) {
-      row[kD] = st.m;
-      row[kD + 1] = st.l;
-    }
-  }
-  __syncthreads();
-  const int c = threadIdx.x;  // one output channel per thread
-#pragma unroll
-  for (int h = 0; h < R; ++h) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg[(w * R + h) * (kD + 2) + kD]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float *row = mrg + (w * R + h) * (kD + 2);
-      const float sc = (row[kD] == -INFINITY) ? 0.f : ex2(row[kD] - M);
-      L = fmaf(sc, row[kD + 1], L);
-      O = fmaf(sc, row[c], O);
-    }
-    float *dst = a.ws + (((int64_t)b * a.Hq + kvh * R + h) * a.splits + split) * (kD + 2);
-    dst[c] = O;
-    if (c == 0) {
-      dst[kD] = M;
-      dst[kD + 1] = L;
+    p_kind = n_kind;
+    p_ntok = n_ntok;
+    p_stage = stage;
+    p_h = cur_h;
+    __syncwarp();
+    if (++uu == U && kk + 1 < n_my) {  // the next unit starts a new head
+      p_fin = ss;
+      p_emit = true;
+      ss.m = -INFINITY;
+      ss.l = 0.f;
+      ss.zs = 0.f;
+      uu = 0;
+      ++cur_h;
+      load_q(cur_h);
     }
   }
+  p_fin = ss;
+  p_emit = true;
+  pv_pending();
+  cp_async_wait<0>();
 }
 
-// Merge the per-split partials of one (batch, query head): one thread per channel.
-__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws, int splits,
+// Merge the partials of one (batch, query head): one thread per channel.  The
+// partials' maxima and weights go through shared memory so every load is issued
+// independently (the partials sit in L2).
+__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws, int64_t pmax, int64_t W,
+                                                      int64_t NW, int64_t U, int Hkv, int Hq,
                                                       uint16_t *__restrict__ out) {
+  __shared__ float s_w[128];
+  __shared__ float s_red[4];
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
   const int64_t row = blockIdx.x;  // b * Hq + h
-  const int c = threadIdx.x;
-  const float *p = ws + row * splits * (kD + 2);
+  const int64_t b = row / Hq, hq = row - b * Hq;
+  const int64_t head = b * Hkv + hq / (Hq / Hkv);
+  const int64_t first = owner_warp(head * U, W, NW), last = owner_warp(head * U + U - 1, W, NW);
+  const int np = (int)(last - first + 1);
+  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  const float *p = ws + row * pmax * (kD + 2);
+  // global max of the partial maxima
   float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, p[s * (kD + 2) + kD]);
-  float L = 0.f, O = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float m = p[s * (kD + 2) + kD];
-    const float sc = (m == -INFINITY) ? 0.f : ex2(m - M);
-    L = fmaf(sc, p[s * (kD + 2) + kD + 1], L);
-    O = fmaf(sc, p[s * (kD + 2) + c], O);
+  for (int s = c; s < np; s += 128) M = fmaxf(M, __ldcg(p + (int64_t)s * (kD + 2) + kD));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) s_red[warp] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+  float O = 0.f, L = 0.f;
+  for (int s0 = 0; s0 < np; s0 += 128) {
+    const int s = s0 + c;
+    float w = 0.f, lw = 0.f;
+    if (s < np) {
+      const float m = __ldcg(p + (int64_t)s * (kD + 2) + kD);
+      w = (m == -INFINITY) ? 0.f : ex2(m - M);
+      lw = w * __ldcg(p + (int64_t)s * (kD + 2) + kD + 1);
+    }
+    __syncthreads();  // previous chunk's weights are consumed
+    s_w[c] = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+    if (lane == 0) s_red[warp] = lw;
+    __syncthreads();
+    L += (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+    const int n = min(128, np - s0);
+    const float *ps = p + (int64_t)s0 * (kD + 2) + c;
+    int j = 0;
+    for (; j + 4 <= n; j += 4) {
+      const float v0 = __ldcg(ps + (int64_t)j * (kD + 2)), v1 = __ldcg(ps + (int64_t)(j + 1) * (kD + 2));
+      const float v2 = __ldcg(ps + (int64_t)(j + 2) * (kD + 2)), v3 = __ldcg(ps + (int64_t)(j + 3) * (kD + 2));
+      O = fmaf(s_w[j], v0, O);
+      O = fmaf(s_w[j + 1], v1, O);
+      O = fmaf(s_w[j + 2], v2, O);
+      O = fmaf(s_w[j + 3], v3, O);
+    }
+    for (; j < n; ++j) O = fmaf(s_w[j], __ldcg(ps + (int64_t)j * (kD + 2)), O);
   }
   out[row * kD + c] = f2h(O / L);
 }
 
 template <int R, int G>
-cudaError_t launch_rg(const DecodeArgs &a, cudaStream_t st) {
-  const int smem = Stage<G>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<R, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)a.splits, (unsigned)(a.B * a.Hkv));
-  decode_kernel<R, G><<<grid, kThreads, smem, st>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  combine_kernel<<<(unsigned)(a.B * a.Hq), 128, 0, st>>>(a.ws, a.splits, a.out);
-  return cudaGetLastError();
+const void *kernel_ptr() {
+  return reinterpret_cast<const void *>(&decode_kernel<R, G>);
+}
+
+const void *select_kernel(int R, int G) {
+  if (G == 32) return R == 1 ? kernel_ptr<1, 32>() : R == 2 ? kernel_ptr<2, 32>() : kernel_ptr<4, 32>();
+  return R == 1 ? kernel_ptr<1, 64>() : R == 2 ? kernel_ptr<2, 64>() : kernel_ptr<4, 64>();
+}
+
+int smem_bytes(int R, int G) {
+  if (G == 32) return R == 1 ? Layout<1, 32>::kSmem : R == 2 ? Layout<2, 32>::kSmem : Layout<4, 32>::kSmem;
+  return R == 1 ? Layout<1, 64>::kSmem : R == 2 ? Layout<2, 64>::kSmem : Layout<4, 64>::kSmem;
 }
 
 }  // namespace
 
-void decode_plan(int B, int Hkv, int G, int64_t n, int num_sms, int *splits, int *groups_per_split) {
-  const int64_t n_groups = n / G;
-  if (n_groups == 0) {
-    *splits = 1;
-    *groups_per_split = 1;
-    return;
-  }
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
+  const int R = Hq / Hkv;
+  const void *fn = select_kernel(R, G);
+  const int smem = smem_bytes(R, G);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem)) != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
   const int64_t heads = (int64_t)B * Hkv;
-  const int64_t target_ctas = (int64_t)num_sms * 8;
-  int64_t s = (target_ctas + heads - 1) / heads;
-  const int64_t s_max = (n_groups + kWarps - 1) / kWarps;  // at least ~one group per warp
-  if (s > s_max) s = s_max;
-  if (s < 1) s = 1;
-  int64_t gps = (n_groups + s - 1) / s;
-  gps = (gps + kWarps - 1) / kWarps * kWarps;
-  s = (n_groups + gps - 1) / gps;
-  *splits = (int)s;
-  *groups_per_split = (int)gps;
+  const int64_t ng = n / G;
+  const int64_t U = (ng * G + kUnit - 1) / kUnit + ((n % G) ? 1 : 0);
+  const int64_t W = heads * U;
+  int64_t NW = (int64_t)sms * per_sm * kWarps;
+  if (NW > W) NW = W;
+  const int64_t q = W / NW;  // every warp holds at least q units
+  out->units_per_head = U;
+  out->total_units = W;
+  out->n_warps = (int)NW;
+  out->grid = (int)((NW + kWarps - 1) / kWarps);
+  out->pmax = (int)((U + q - 1) / q + 1);
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   const int R = a.Hq / a.Hkv;
-  if (a.G == 32) {
-    if (R == 1) return launch_rg<1, 32>(a, st);
-    if (R == 2) return launch_rg<2, 32>(a, st);
-    return launch_rg<4, 32>(a, st);
-  }
-  if (R == 1) return launch_rg<1, 64>(a, st);
-  if (R == 2) return launch_rg<2, 64>(a, st);
-  return launch_rg<4, 64>(a, st);
+  const void *fn = select_kernel(R, a.G);
+  void *args[] = {const_cast<DecodeArgs *>(&a)};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)a.grid), dim3(kThreads), args, (size_t)smem_bytes(R, a.G), st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.ws, (int64_t)a.pmax, a.total_units,
+                            (int64_t)a.n_warps, a.units_per_head, a.Hkv, a.Hq, a.out);
 }
 
 }  // namespace kivi

@@ -98,25 +98,20 @@ __device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, u
 }
 
 // ---- 2-bit code unpack into fp16 MMA operands ------------------------------------------
-// A 32-bit word w holds 16 codes, code i at bits [2i, 2i+1].  Masking with
-// 0x00030003 << 2m leaves codes i and i+8 in the two 16-bit halves at bit 2m; as
-// fp16 bit patterns these are the subnormals code * 4^m * 2^-24, exact.  Shifting w
-// by 0, 4, 8, 12 and using m in {0, 1} gives:
-//   r[k] = {code_k, code_{k+8}} * f_k * 2^-24,   f_k = 1 for even k, 4 for odd k.
-// The 2^-24 and f_k are undone on the other MMA operand or after accumulation.
+// A 32-bit word w holds 16 codes, code i at bits [2i, 2i+1].  Masking w with
+// 0x00030003 << 2m (m = 0..3) leaves codes m and m+8 in the two 16-bit halves at
+// bits [2m, 2m+1]; as fp16 bit patterns these are the subnormals
+// code * 4^m * 2^-24, exact.  The same masks on w >> 8 give codes m+4 and m+12.
+// Nine integer operations therefore give
+//   r[k] = {code_k, code_{k+8}} * f_k * 2^-24,   f_k = 4^(k mod 4),   k = 0..7.
+// f_k and 2^-24 are undone on the other MMA operand or after accumulation.
 __device__ __forceinline__ void unpack16(uint32_t w, uint32_t r[8]) {
-  const uint32_t m0 = 0x00030003u, m1 = 0x000C000Cu;
-  r[0] = w & m0;
-  r[1] = w & m1;
-  uint32_t x1 = w >> 4;
-  r[2] = x1 & m0;
-  r[3] = x1 & m1;
-  uint32_t x2 = w >> 8;
-  r[4] = x2 & m0;
-  r[5] = x2 & m1;
-  uint32_t x3 = w >> 12;
-  r[6] = x3 & m0;
-  r[7] = x3 & m1;
+  const uint32_t x = w >> 8;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    r[m] = w & (0x00030003u << (2 * m));
+    r[m + 4] = x & (0x00030003u << (2 * m));
+  }
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }

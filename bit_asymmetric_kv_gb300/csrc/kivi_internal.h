@@ -31,13 +31,23 @@ struct DecodeArgs {
   int64_t max_tokens;
   int64_t n;
   int B, Hkv, Hq, G;
-  int splits;
-  int groups_per_split;
+  int64_t units_per_head;  // full key groups + 1 if there are residual keys
+  int64_t total_units;     // B * Hkv * units_per_head
+  int n_warps;             // warps of the persistent grid (each takes a contiguous unit range)
+  int grid;                // CTAs (4 warps each)
+  int pmax;                // partial slots per query head in the workspace
   float softmax_scale;
 };
 
-// Split of the context for one decode call (host heuristic, deterministic).
-void decode_plan(int B, int Hkv, int G, int64_t n, int num_sms, int *splits, int *groups_per_split);
+// Geometry of one decode call on the current device (deterministic for given sizes).
+struct DecodeGeom {
+  int64_t units_per_head;
+  int64_t total_units;
+  int n_warps;
+  int grid;
+  int pmax;
+};
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
 }  // namespace kivi

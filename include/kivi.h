@@ -118,12 +118,14 @@ KIVI_API int kivi_quantize_prefill(const kivi_dims *dims, kivi_cache *cache, con
 KIVI_API int kivi_append_token(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k_new,
                       const uint16_t *v_new, cudaStream_t stream);
 
-/* Number of context splits kivi_decode_attention uses for these sizes on the
- * current device (>= 1; 0 on bad arguments). */
+/* kivi_decode_attention splits the context of every (batch, KV head) between the
+ * GPU's warps and merges the pieces (flash-decoding).  This is the largest number
+ * of pieces one query head can have for these sizes on the current device (>= 1;
+ * 0 on bad arguments or without a device). */
 KIVI_API int kivi_decode_splits(const kivi_dims *dims, int32_t Hq, int64_t n_tokens);
 
 /* Workspace bytes kivi_decode_attention needs for these sizes on the current
- * device: B * Hq * splits * (D + 2) floats.  0 on bad arguments. */
+ * device: B * Hq * kivi_decode_splits() * (D + 2) floats.  0 on bad arguments. */
 KIVI_API size_t kivi_decode_workspace_bytes(const kivi_dims *dims, int32_t Hq, int64_t n_tokens);
 
 /*
