@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
         L.kivi_decode_workspace_bytes.restype = sz
         L.kivi_decode_attention.argtypes = [D, C, P, i32, ctypes.c_float, P, P, sz, P]
         L.kivi_dequantize_debug.argtypes = [D, C, P, P, P]
+        L.kivi_decode_attention_noalloc.argtypes = [D, C, P, i32, ctypes.c_float, P, P]
+        L.kivi_decode_attention_noalloc.restype = ctypes.c_int
+        L.kivi_decode_attention_noalloc_max_workspace.argtypes = []
+        L.kivi_decode_attention_noalloc_max_workspace.restype = sz
         L.kivi_status_string.argtypes = [ctypes.c_int]
         L.kivi_status_string.restype = ctypes.c_char_p
         for name in ("kivi_buffer_bytes", "kivi_quantize_prefill", "kivi_append_token", "kivi_decode_splits",
@@ -173,6 +177,23 @@ def kivi_decode_attention(cache: Cache, q: torch.Tensor, softmax_scale: float, o
                                        float(softmax_scale), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
                                        _stream(stream)), "kivi_decode_attention")
     return out
+
+
+def kivi_decode_attention_noalloc(cache: Cache, q: torch.Tensor, softmax_scale: float,
+                                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kivi_decode_attention with the workspace taken from the library's built-in
+    array (for callers that cannot allocate device memory); q: fp16 [B, Hq, D]."""
+    _f16(q, "q")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(lib().kivi_decode_attention_noalloc(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(q), q.shape[1],
+                                               float(softmax_scale), _ptr(out), _stream(stream)),
+           "kivi_decode_attention_noalloc")
+    return out
+
+
+def kivi_decode_attention_noalloc_max_workspace() -> int:
+    return int(lib().kivi_decode_attention_noalloc_max_workspace())
 
 
 def kivi_dequantize_debug(cache: Cache, stream=None) -> tuple[torch.Tensor, torch.Tensor]:

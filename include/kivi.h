@@ -150,6 +150,25 @@ KIVI_API int kivi_decode_attention(const kivi_dims *dims, const kivi_cache *cach
 KIVI_API int kivi_dequantize_debug(const kivi_dims *dims, const kivi_cache *cache, float *k_out,
                           float *v_out, cudaStream_t stream);
 
+/*
+ * kivi_decode_attention for callers that cannot allocate device memory (for
+ * instance a serving loop that must not call cudaMalloc between steps, or a process
+ * whose device memory is reserved up front).  The method's page has no counterpart:
+ * this is a deployment aid.  Same arguments, results and statuses as
+ * kivi_decode_attention, without the workspace: the workspace is taken from an
+ * 8 MiB array compiled into the library, which occupies device memory on every GPU
+ * that loads the library until the process exits.  Sizes whose workspace
+ * (kivi_decode_workspace_bytes) exceeds kivi_decode_attention_noalloc_max_workspace()
+ * return KIVI_ERR_WORKSPACE and launch nothing.  The first call on a device looks up
+ * the array's device address (a runtime query, done once per device), so make it
+ * before any stream capture.  Calls share the array: calls whose kernels overlap on
+ * the GPU race.  No call allocates or frees memory.
+ */
+KIVI_API size_t kivi_decode_attention_noalloc_max_workspace(void);
+KIVI_API int kivi_decode_attention_noalloc(const kivi_dims *dims, const kivi_cache *cache,
+                                           const uint16_t *q, int32_t Hq, float softmax_scale,
+                                           uint16_t *out, cudaStream_t stream);
+
 /* Human-readable name of a kivi_status. */
 KIVI_API const char *kivi_status_string(int status);
 
