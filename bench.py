@@ -382,18 +382,74 @@ def e2e_run(args, wl, pre, dev, stream, flush):
             "d2h_bytes_per_step": d2h}
 
 
+def run_compare(args):
+    """The long-context GQA decode step over the 2-bit cache next to the same step
+    over an unquantized fp16 cache (the in-build comparison kernel).  Prints one JSON
+    object with both timings; the default bench line is not printed in this mode."""
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi, synth
+
+    wl = synth.LONG_GQA
+    dev = torch.device("cuda", 0)
+    kivi.lib()
+    pre = synth.make_prefill(wl)
+    k, v, q = pre.k.to(dev), pre.v.to(dev), pre.q.to(dev)
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev)
+    kivi.kivi_quantize_prefill(cache, k, v)
+    out = torch.empty_like(q)
+    ws = kivi.workspace(cache, wl.Hq, device=dev)
+    ws16 = torch.empty(kivi.kivi_decode_fp16_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.n), dtype=torch.uint8,
+                       device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ts) / len(ts)
+
+    ms2 = timed(lambda: kivi.kivi_decode_attention(cache, q, 1.0, out=out, ws=ws, stream=stream))
+    ms16 = timed(lambda: kivi.kivi_decode_attention_fp16(k, v, q, 1.0, out=out, ws=ws16, stream=stream))
+    b2 = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, wl.n)
+    b16 = wl.B * wl.Hkv * wl.n * wl.D * 2 * 2 + 2 * wl.B * wl.Hq * wl.D * 2
+    peak, src = measured_peak()
+    print(json.dumps({
+        "mode": "comparison", "workload": wl.name, "steps": args.steps, "warmup": args.warmup,
+        "l2": "flushed by a 256 MiB write before every call",
+        "kivi_2bit": {"ms": ms2, "tokens_per_s": wl.B / (ms2 / 1e3), "bytes": b2, "GBps": b2 / ms2 / 1e6,
+                      "frac_of_peak": b2 / ms2 / 1e6 / peak},
+        "fp16_kv": {"ms": ms16, "tokens_per_s": wl.B / (ms16 / 1e3), "bytes": b16, "GBps": b16 / ms16 / 1e6,
+                    "frac_of_peak": b16 / ms16 / 1e6 / peak},
+        "speedup_2bit_over_fp16": ms16 / ms2, "bytes_ratio_fp16_over_2bit": b16 / b2,
+        "peak_GBps": peak, "peak_source": src}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["kivi", "reference"], default="kivi")
+    ap.add_argument("--compare-fp16", action="store_true",
+                    help="time the long-context GQA step over the 2-bit and an fp16 cache instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from bit_asymmetric_kv_gb300 import synth
 
     wl = synth.LLAMA2_7B_MHA
+    if args.compare_fp16:
+        return run_compare(args)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_kivi(args, wl)

@@ -174,4 +174,52 @@ int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out,
                                           st));
 }
 
+static int fp16_sizes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n, int *splits, int64_t *tps) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || n <= 0) return KIVI_ERR_ARG;
+  if (D != 128 || Hq % Hkv != 0) return KIVI_ERR_UNSUPPORTED;
+  const int R = Hq / Hkv;
+  if (R != 1 && R != 2 && R != 4) return KIVI_ERR_UNSUPPORTED;
+  if ((int64_t)B * Hkv > 65535) return KIVI_ERR_UNSUPPORTED;  // grid.y of the launch
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KIVI_ERR_CUDA;
+  kivi::fp16_plan(B, Hkv, n, sms, splits, tps);
+  return KIVI_OK;
+}
+
+size_t kivi_decode_fp16_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n) {
+  int splits = 0;
+  int64_t tps = 0;
+  if (fp16_sizes(B, Hq, Hkv, D, n, &splits, &tps) != KIVI_OK) return 0;
+  return (size_t)B * (size_t)Hq * (size_t)splits * (size_t)(D + 2) * sizeof(float);
+}
+
+int kivi_decode_attention_fp16(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n, const uint16_t *k,
+                               const uint16_t *v, const uint16_t *q, float softmax_scale, uint16_t *out, void *ws,
+                               size_t ws_bytes, cudaStream_t st) {
+  if (!k || !v || !q || !out) return KIVI_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  int splits = 0;
+  int64_t tps = 0;
+  int s = fp16_sizes(B, Hq, Hkv, D, n, &splits, &tps);
+  if (s != KIVI_OK) return s;
+  const size_t need = (size_t)B * (size_t)Hq * (size_t)splits * (size_t)(D + 2) * sizeof(float);
+  if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KIVI_ERR_ALIGN;
+  kivi::Fp16Args a;
+  a.k = k;
+  a.v = v;
+  a.q = q;
+  a.out = out;
+  a.ws = static_cast<float *>(ws);
+  a.n = n;
+  a.B = B;
+  a.Hkv = Hkv;
+  a.Hq = Hq;
+  a.splits = splits;
+  a.tiles_per_split = tps;
+  a.softmax_scale = softmax_scale;
+  return cuda_status(kivi::launch_fp16(a, st));
+}
+
 }  // extern "C"

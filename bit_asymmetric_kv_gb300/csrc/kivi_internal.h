@@ -50,4 +50,20 @@ struct DecodeGeom {
 cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
+// Decode attention over an unquantized fp16 cache (the comparison kernel).
+struct Fp16Args {
+  const uint16_t *k;  // [B][Hkv][n][128]
+  const uint16_t *v;
+  const uint16_t *q;  // [B][Hq][128]
+  uint16_t *out;
+  float *ws;
+  int64_t n;
+  int B, Hkv, Hq;
+  int splits;
+  int64_t tiles_per_split;
+  float softmax_scale;
+};
+void fp16_plan(int B, int Hkv, int64_t n, int num_sms, int *splits, int64_t *tiles_per_split);
+cudaError_t launch_fp16(const Fp16Args &a, cudaStream_t st);
+
 }  // namespace kivi

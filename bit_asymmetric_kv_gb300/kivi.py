@@ -62,6 +62,10 @@ def lib() -> ctypes.CDLL:
         L.kivi_decode_attention_noalloc.restype = ctypes.c_int
         L.kivi_decode_attention_noalloc_max_workspace.argtypes = []
         L.kivi_decode_attention_noalloc_max_workspace.restype = sz
+        L.kivi_decode_fp16_workspace_bytes.argtypes = [i32, i32, i32, i32, i64]
+        L.kivi_decode_fp16_workspace_bytes.restype = sz
+        L.kivi_decode_attention_fp16.argtypes = [i32, i32, i32, i32, i64, P, P, P, ctypes.c_float, P, P, sz, P]
+        L.kivi_decode_attention_fp16.restype = ctypes.c_int
         L.kivi_status_string.argtypes = [ctypes.c_int]
         L.kivi_status_string.restype = ctypes.c_char_p
         for name in ("kivi_buffer_bytes", "kivi_quantize_prefill", "kivi_append_token", "kivi_decode_splits",
@@ -205,6 +209,30 @@ def kivi_dequantize_debug(cache: Cache, stream=None) -> tuple[torch.Tensor, torc
     _check(lib().kivi_dequantize_debug(ctypes.byref(d), ctypes.byref(cache.c), _ptr(k), _ptr(v), _stream(stream)),
            "kivi_dequantize_debug")
     return k, v
+
+
+def kivi_decode_fp16_workspace_bytes(B: int, Hq: int, Hkv: int, n: int, D: int = 128) -> int:
+    return int(lib().kivi_decode_fp16_workspace_bytes(B, Hq, Hkv, D, n))
+
+
+def kivi_decode_attention_fp16(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, softmax_scale: float,
+                               out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                               stream=None) -> torch.Tensor:
+    """Decode attention over an unquantized fp16 cache: k, v [B, Hkv, n, D], q [B, Hq, D]."""
+    _f16(k, "k"), _f16(v, "v"), _f16(q, "q")
+    B, Hkv, n, D = k.shape
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        nbytes = kivi_decode_fp16_workspace_bytes(B, Hq, Hkv, n, D)
+        if nbytes == 0:
+            raise KiviError(KIVI_ERR_ARG, "kivi_decode_fp16_workspace_bytes")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(lib().kivi_decode_attention_fp16(B, Hq, Hkv, D, n, _ptr(k), _ptr(v), _ptr(q), float(softmax_scale),
+                                            _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "kivi_decode_attention_fp16")
+    return out
 
 
 def kivi_status_string(status: int) -> str:

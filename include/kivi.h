@@ -151,6 +151,21 @@ KIVI_API int kivi_dequantize_debug(const kivi_dims *dims, const kivi_cache *cach
                           float *v_out, cudaStream_t stream);
 
 /*
+ * Decode attention over an unquantized fp16 cache of the same shapes, the point of
+ * comparison for the 2-bit cache (the page's "Makale Bulteni" section states KIVI's
+ * savings against an FP16 KV cache).  k, v: fp16 [B][Hkv][n][D] device, read-only;
+ * q, out: fp16 [B][Hq][D]; ws: device workspace of at least
+ * kivi_decode_fp16_workspace_bytes() bytes, contents overwritten.  Same score,
+ * softmax and GQA conventions as kivi_decode_attention; D = 128, Hq/Hkv in
+ * {1, 2, 4}.  kivi_decode_fp16_workspace_bytes returns 0 on bad arguments.
+ */
+KIVI_API size_t kivi_decode_fp16_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n);
+KIVI_API int kivi_decode_attention_fp16(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n,
+                                        const uint16_t *k, const uint16_t *v, const uint16_t *q,
+                                        float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes,
+                                        cudaStream_t stream);
+
+/*
  * kivi_decode_attention for callers that cannot allocate device memory (for
  * instance a serving loop that must not call cudaMalloc between steps, or a process
  * whose device memory is reserved up front).  The method's page has no counterpart:

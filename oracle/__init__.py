@@ -71,6 +71,10 @@ def lib():
             L.oracle_append.restype = i64
             L.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, f64, P]
             L.oracle_attention.restype = i32
+            L.oracle_attention_raw_head.argtypes = [i32, i64, P, P, P, f64, P]
+            L.oracle_attention_raw_head.restype = i32
+            L.oracle_attention_raw.argtypes = [i32, i32, i32, i32, i64, P, P, P, f64, P]
+            L.oracle_attention_raw.restype = i32
             _lib = L
         return _lib
 
@@ -235,3 +239,26 @@ def prefill_head(k_head, v_head, G: int, max_tokens: int):
     kb = np.ascontiguousarray(_f16_bits(k_head))[None, None]
     vb = np.ascontiguousarray(_f16_bits(v_head))[None, None]
     return prefill(kb, vb, G, max_tokens)
+
+
+def attention_raw(k, v, q, sigma: float) -> np.ndarray:
+    """fp64 attention over an unquantized fp16 cache: k, v [B, Hkv, n, D], q [B, Hq, D]."""
+    kb, vb, qb = _f16_bits(k), _f16_bits(v), _f16_bits(q)
+    B, Hkv, n, D = kb.shape
+    Hq = qb.shape[1]
+    out = np.zeros((B, Hq, D), np.float64)
+    if lib().oracle_attention_raw(B, Hq, Hkv, D, n, _ptr(kb), _ptr(vb), _ptr(qb), float(sigma), _ptr(out)) != 0:
+        raise ValueError("oracle attention: empty cache or Hq % Hkv != 0")
+    return out
+
+
+def attention_raw_head(k_head, v_head, q_row, sigma: float) -> np.ndarray:
+    """fp64 attention of one query row over one head's fp16 [n, D] keys and values."""
+    kb = np.ascontiguousarray(_f16_bits(k_head))
+    vb = np.ascontiguousarray(_f16_bits(v_head))
+    qb = np.ascontiguousarray(_f16_bits(q_row))
+    out = np.zeros(kb.shape[1], np.float64)
+    if lib().oracle_attention_raw_head(kb.shape[1], kb.shape[0], _ptr(kb), _ptr(vb), _ptr(qb), float(sigma),
+                                       _ptr(out)) != 0:
+        raise ValueError("oracle attention: empty cache")
+    return out

@@ -311,6 +311,36 @@ int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, cons
   return 0;
 }
 
+/*
+ * Attention of one query vector over an unquantized fp16 cache (k, v: [n][D] fp16),
+ * fp64: the same definition as oracle_attention_head with K' = K and V' = V.  It is
+ * the reference for the fp16-cache decode kernel that serves as a comparison point.
+ */
+int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_t *v, const uint16_t *q,
+                              double sigma, double *out) {
+  if (n <= 0) return -1;
+  double *score = (double *)malloc((size_t)n * sizeof(double));
+  double m = -INFINITY;
+  for (int64_t t = 0; t < n; ++t) {
+    double acc = 0.0;
+    for (int c = 0; c < D; ++c) acc += (double)h2f(q[c]) * (double)h2f(k[(size_t)t * D + c]);
+    score[t] = sigma * acc;
+    if (score[t] > m) m = score[t];
+  }
+  double l = 0.0;
+  for (int64_t t = 0; t < n; ++t) {
+    score[t] = exp(score[t] - m);
+    l += score[t];
+  }
+  for (int c = 0; c < D; ++c) out[c] = 0.0;
+  for (int64_t t = 0; t < n; ++t) {
+    double p = score[t] / l;
+    for (int c = 0; c < D; ++c) out[c] += p * (double)h2f(v[(size_t)t * D + c]);
+  }
+  free(score);
+  return 0;
+}
+
 /* ---------------------------------------------------------------------------------
  * Whole-batch wrappers over the per-head functions.  Buffer shapes:
  *   k, v      [B][Hkv][n][D] fp16         k_new, v_new [B][Hkv][D] fp16
@@ -360,6 +390,22 @@ int oracle_attention(int B, int Hq, int Hkv, int D, int G, int64_t max_tokens, i
     int64_t bh = b * Hkv + h / group;
     oracle_attention_head(D, G, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), q + (size_t)bq * D, sigma,
                           out + (size_t)bq * D);
+  }
+  return 0;
+}
+
+int oracle_attention_raw(int B, int Hq, int Hkv, int D, int64_t n, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *q, double sigma, double *out) {
+  if (n <= 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
+  int group = Hq / Hkv;
+  int64_t rows = (int64_t)B * Hq;
+#pragma omp parallel for schedule(dynamic)
+  for (int64_t bq = 0; bq < rows; ++bq) {
+    int64_t b = bq / Hq;
+    int h = (int)(bq % Hq);
+    int64_t bh = b * Hkv + h / group;
+    oracle_attention_raw_head(D, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, q + (size_t)bq * D, sigma,
+                              out + (size_t)bq * D);
   }
   return 0;
 }

@@ -120,3 +120,23 @@ def test_empty_cache_is_an_error():
     c = oracle.Cache.empty(1, 1, 128, 32, 32)
     with pytest.raises(ValueError):
         oracle.attention(c, np.zeros((1, 1, 128), np.float16), 1.0)
+
+
+def test_raw_attention_matches_scipy_and_the_quantized_path_on_exact_inputs():
+    """fp64 attention over the raw fp16 cache: equal to scipy's softmax attention, and
+    equal to the quantized-cache attention when quantization is exact."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, n, G = 2, 4, 2, 70, 32
+    k, v = _exact_cache_inputs(rng, B, Hkv, n, G)
+    q = (rng.standard_normal((B, Hq, 128)) / np.sqrt(128)).astype(np.float16)
+    raw = oracle.attention_raw(k, v, q, 0.9)
+    for b in range(B):
+        for h in range(Hq):
+            K = k[b, h // 2].astype(np.float64)
+            V = v[b, h // 2].astype(np.float64)
+            p = softmax(0.9 * (K @ q[b, h].astype(np.float64)))
+            assert np.allclose(raw[b, h], p @ V, rtol=0, atol=1e-12)
+            one = oracle.attention_raw_head(k[b, h // 2], v[b, h // 2], q[b, h], 0.9)
+            assert np.array_equal(one, raw[b, h])
+    c = oracle.prefill(k, v, G, 128)
+    assert np.allclose(oracle.attention(c, q, 0.9), raw, rtol=0, atol=1e-12)
