@@ -208,6 +208,7 @@ def workload_config(wl):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
             "context_tokens": f"{wl.n}..{wl.n + CYCLE} (cache rolled back every {CYCLE} steps)", "step": "append_token + decode_attention (one new token per sequence)",
             "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
+            "api": "kivi_decode_step (append + decode attention, the attention overlapping the append)",
             "parallelism": "replicas (one independent cache per GPU)"}
 
 
@@ -244,7 +245,7 @@ def run_kivi(args, wl):
     # the inputs of one rollback cycle, resident in HBM before timing
     dev_in = [tuple(t.to(dev) for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
-    ws = kivi.workspace(cache, wl.Hq, n_tokens=n0 + CYCLE, device=dev)
+    ws = cycle_workspace(cache, wl, n0, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -257,14 +258,13 @@ def run_kivi(args, wl):
             rollback()
         k, v, q = dev_in[i % CYCLE]
         flush.fill_(i & 0xFF)
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         n_before = cache.n_tokens
         e0.record(stream)
-        kivi.kivi_append_token(cache, k, v, stream=stream)
+        kivi.kivi_decode_step(cache, k, v, q, 1.0, out=out, ws=ws, stream=stream)
         e1.record(stream)
-        kivi.kivi_decode_attention(cache, q, 1.0, out=out, ws=ws, stream=stream)
-        e2.record(stream)
-        rec.append((e0, e1, e2, cache.n_tokens, 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2))
+        # append (+ group flush every G steps), decode attention, combine
+        rec.append((e0, e1, cache.n_tokens, 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2))
 
     warm = []
     for i in range(args.warmup):
@@ -280,10 +280,8 @@ def run_kivi(args, wl):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier()
-    launches = sum(x[4] for x in rec)
-    step_ms = [e0.elapsed_time(e2) for e0, _, e2, _, _ in rec]
-    attn_ms = [e1.elapsed_time(e2) for _, e1, e2, _, _ in rec]
-    app_ms = [e0.elapsed_time(e1) for e0, e1, _, _, _ in rec]
+    launches = sum(x[3] for x in rec)
+    step_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in rec]
     ms_per_step = sum(step_ms) / len(step_ms)
     if world > 1:
         import torch.distributed as dist
@@ -292,9 +290,24 @@ def run_kivi(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_per_step = float(t.item())
     value = wl.B * world / (ms_per_step / 1e3)
-    bytes_per = [algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n) for _, _, _, n, _ in rec]
-    attn_avg_ms = sum(attn_ms) / len(attn_ms)
-    achieved = (sum(bytes_per) / len(bytes_per)) / (attn_avg_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel: kivi_decode_attention (decode + combine) alone,
+    # on the prompt's cache, timed the same way
+    rollback()
+    attn_ms = []
+    q0 = dev_in[0][2]
+    for i in range(args.warmup + max(16, args.steps // 8)):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        kivi.kivi_decode_attention(cache, q0, 1.0, out=out, ws=ws, stream=stream)
+        e1.record(stream)
+        if i >= args.warmup:
+            attn_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    attn_avg_ms = sum(a0.elapsed_time(a1) for a0, a1 in attn_ms) / len(attn_ms)
+    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0)
+    achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
     traffic = profiled_traffic(sha)
@@ -317,9 +330,8 @@ def run_kivi(args, wl):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": "kivi_decode_attention (decode_kernel + combine_kernel)",
                      "peak_source": peak_src, "attention_ms": attn_avg_ms,
-                     "algorithmic_bytes_per_launch": sum(bytes_per) / len(bytes_per),
+                     "algorithmic_bytes_per_launch": bytes_attn, "context_tokens": n0,
                      "kernel_source_sha256": sha},
-        "append_ms": sum(app_ms) / len(app_ms),
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -332,6 +344,16 @@ def run_kivi(args, wl):
 
         dist.destroy_process_group()
     return 0
+
+
+def cycle_workspace(cache, wl, n0, dev):
+    """A zero-filled decode workspace large enough for every context of a cycle."""
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi
+
+    nbytes = max(kivi.kivi_decode_workspace_bytes(cache.dims, wl.Hq, n) for n in range(n0, n0 + CYCLE + 2))
+    return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
 
 def e2e_run(args, wl, pre, dev, stream, flush):
@@ -354,7 +376,7 @@ def e2e_run(args, wl, pre, dev, stream, flush):
     dq = torch.empty_like(host[0][2], device=dev)
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     out_h = torch.empty_like(out, device="cpu").pin_memory()
-    ws = kivi.workspace(cache, wl.Hq, n_tokens=n0 + CYCLE, device=dev)
+    ws = cycle_workspace(cache, wl, n0, dev)
     times = []
     for i in range(total):
         if i % CYCLE == 0:
@@ -367,8 +389,7 @@ def e2e_run(args, wl, pre, dev, stream, flush):
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         dq.copy_(hq, non_blocking=True)
-        kivi.kivi_append_token(cache, dk, dv, stream=stream)
-        kivi.kivi_decode_attention(cache, dq, 1.0, out=out, ws=ws, stream=stream)
+        kivi.kivi_decode_step(cache, dk, dv, dq, 1.0, out=out, ws=ws, stream=stream)
         out_h.copy_(out, non_blocking=True)
         e1.record(stream)
         if i >= args.warmup:

@@ -6,5 +6,5 @@ seeded synthetic workloads.  Import is cheap: the library loads on first use.
 """
 from . import synth  # noqa: F401
 from .kivi import (Cache, KiviError, kivi_append_token, kivi_buffer_bytes, kivi_decode_attention,  # noqa: F401
-                   kivi_decode_splits, kivi_decode_workspace_bytes, kivi_dequantize_debug, kivi_quantize_prefill,
+                   kivi_decode_splits, kivi_decode_step, kivi_decode_workspace_bytes, kivi_dequantize_debug, kivi_quantize_prefill,
                    kivi_status_string, make_dims, workspace)

@@ -158,8 +158,63 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.pmax = g.pmax;
+  a.wait_tail = 0;
   a.softmax_scale = softmax_scale;
   return cuda_status(kivi::launch_decode(a, st));
+}
+
+int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, const uint16_t *v_new,
+                     const uint16_t *q, int32_t Hq, float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes,
+                     cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_heads(d, Hq)) != KIVI_OK) return s;
+  if (!k_new || !v_new || !q || !out) return KIVI_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  const int64_t n = c->n_tokens;
+  if (n < 0) return KIVI_ERR_ARG;
+  if (n >= d->max_tokens) return KIVI_ERR_CAPACITY;
+  kivi::DecodeGeom g;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, n + 1, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
+  if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KIVI_ERR_ALIGN;
+  // 1. append (and flush a full residual group)
+  const int64_t heads = (int64_t)d->B * d->Hkv;
+  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
+                                      d->max_tokens, st);
+  if (e == cudaSuccess && (n % d->G) + 1 == d->G)
+    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
+                                d->max_tokens, st);
+  if ((s = cuda_status(e)) != KIVI_OK) return s;
+  // 2. decode attention over n + 1 tokens, overlapping the append: only the last
+  //    unit of each head (the one holding the new token) waits for it
+  kivi::DecodeArgs a;
+  a.k_codes = c->k_codes;
+  a.k_meta = c->k_meta;
+  a.k_res = c->k_res;
+  a.v_codes = c->v_codes;
+  a.v_meta = c->v_meta;
+  a.q = q;
+  a.out = out;
+  a.ws = static_cast<float *>(ws);
+  a.max_tokens = d->max_tokens;
+  a.n = n + 1;
+  a.B = d->B;
+  a.Hkv = d->Hkv;
+  a.Hq = Hq;
+  a.G = d->G;
+  a.units_per_head = g.units_per_head;
+  a.total_units = g.total_units;
+  a.n_warps = g.n_warps;
+  a.grid = g.grid;
+  a.pmax = g.pmax;
+  a.wait_tail = 1;
+  a.softmax_scale = softmax_scale;
+  if ((s = cuda_status(kivi::launch_decode(a, st))) != KIVI_OK) return s;
+  c->n_tokens = n + 1;
+  return KIVI_OK;
 }
 
 int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out, float *v_out, cudaStream_t st) {

@@ -307,7 +307,14 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   // ---- staging cursor (unit u0 + kk -> head h_is, unit uu_is within the head)
   int64_t h_is = u0 / U;
   int uu_is = (int)(u0 - h_is * U);
+  bool waited = false;
   auto issue = [&](int kk) {
+    // the last unit of a head holds the token a preceding append just wrote: when
+    // this grid was launched as a programmatic dependent of that append, wait for it
+    if (a.wait_tail && !waited && kk < n_my && uu_is == U - 1) {
+      asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      waited = true;
+    }
     if (kk < n_my && uu_is < n_code_units) {
       const int g0 = uu_is * NGU;
       const int ngr = min(NGU, NG - g0);  // 1 or 2 groups (G = 32)
@@ -728,17 +735,24 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   const int R = a.Hq / a.Hkv;
   const void *fn = select_kernel(R, a.G);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3((unsigned)a.grid);
+  dcfg.blockDim = dim3(kThreads);
+  dcfg.dynamicSmemBytes = (size_t)smem_bytes(R, a.G);
+  dcfg.stream = st;
+  dcfg.attrs = attr;
+  dcfg.numAttrs = a.wait_tail ? 1 : 0;  // overlap a preceding append only when asked
   void *args[] = {const_cast<DecodeArgs *>(&a)};
-  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)a.grid), dim3(kThreads), args, (size_t)smem_bytes(R, a.G), st);
+  cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.ws, (int64_t)a.pmax, a.total_units,

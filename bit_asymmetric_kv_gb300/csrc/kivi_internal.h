@@ -36,6 +36,7 @@ struct DecodeArgs {
   int n_warps;             // warps of the persistent grid (each takes a contiguous unit range)
   int grid;                // CTAs (4 warps each)
   int pmax;                // partial slots per query head in the workspace
+  int wait_tail;           // launched as a dependent of an append: wait before each head's last unit
   float softmax_scale;
 };
 

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
                                                         int64_t groups_per_head, int64_t g0,
                                                         uint32_t *__restrict__ k_codes,
                                                         uint32_t *__restrict__ k_meta, int64_t max_tokens) {
+  // a decode launched as a programmatic dependent may start its independent work now
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   constexpr int TPL = G / 8;  // tokens per lane
   __shared__ __align__(16) uint32_t s_codes[G * kWordsPerRow];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,6 +145,8 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
                                                      int64_t n, int G, uint16_t *__restrict__ k_res,
                                                      uint32_t *__restrict__ v_codes,
                                                      uint32_t *__restrict__ v_meta, int64_t max_tokens) {
+  // a decode launched as a programmatic dependent may start its independent work now
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (bh >= heads) return;
   const int lane = threadIdx.x & 31;

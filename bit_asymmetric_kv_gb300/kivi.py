@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.kivi_decode_fp16_workspace_bytes.restype = sz
         L.kivi_decode_attention_fp16.argtypes = [i32, i32, i32, i32, i64, P, P, P, ctypes.c_float, P, P, sz, P]
         L.kivi_decode_attention_fp16.restype = ctypes.c_int
+        L.kivi_decode_step.argtypes = [D, C, P, P, P, i32, ctypes.c_float, P, P, sz, P]
+        L.kivi_decode_step.restype = ctypes.c_int
         L.kivi_status_string.argtypes = [ctypes.c_int]
         L.kivi_status_string.restype = ctypes.c_char_p
         for name in ("kivi_buffer_bytes", "kivi_quantize_prefill", "kivi_append_token", "kivi_decode_splits",
@@ -198,6 +200,21 @@ def kivi_decode_attention_noalloc(cache: Cache, q: torch.Tensor, softmax_scale: 
 
 def kivi_decode_attention_noalloc_max_workspace() -> int:
     return int(lib().kivi_decode_attention_noalloc_max_workspace())
+
+
+def kivi_decode_step(cache: Cache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor, softmax_scale: float,
+                     out: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Append (k_new, v_new fp16 [B, Hkv, D]) then attend with q fp16 [B, Hq, D]."""
+    _f16(k_new, "k_new"), _f16(v_new, "v_new"), _f16(q, "q")
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = workspace(cache, Hq, n_tokens=cache.n_tokens + 1, device=q.device)
+    _check(lib().kivi_decode_step(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                  Hq, float(softmax_scale), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "kivi_decode_step")
+    return out
 
 
 def kivi_dequantize_debug(cache: Cache, stream=None) -> tuple[torch.Tensor, torch.Tensor]:

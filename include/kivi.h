@@ -143,6 +143,20 @@ KIVI_API int kivi_decode_attention(const kivi_dims *dims, const kivi_cache *cach
                           size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * One whole decode step: kivi_append_token(k_new, v_new) followed by
+ * kivi_decode_attention(q) over the n_tokens + 1 tokens (section "Iddia ve
+ * Gerceklik", paragraphs 2-3).  Same arguments, layouts and statuses as those two
+ * calls; ws must hold kivi_decode_workspace_bytes(dims, Hq, n_tokens + 1) bytes.
+ * The attention kernel is launched as a programmatic dependent of the append, so it
+ * starts on the cached tokens while the append runs and waits for it only before
+ * the block of each head that holds the new token.  Increments cache->n_tokens on
+ * success; every argument is checked before anything is launched.
+ */
+KIVI_API int kivi_decode_step(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k_new,
+                              const uint16_t *v_new, const uint16_t *q, int32_t Hq, float softmax_scale,
+                              uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Test aid: write the dequantized cache as fp32 [B][Hkv][n_tokens][D] to k_out and
  * v_out (device, caller-owned).  Quantized entries are fp32(z) + code * fp32(s)
  * (exact product, one rounding); residual keys are copied exactly.

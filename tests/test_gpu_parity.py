@@ -166,3 +166,35 @@ def test_two_level_inputs_give_attention_of_the_raw_cache():
         p = np.exp(s - s.max())
         ref[0, h] = (p / p.sum()) @ V
     assert_close(out, ref)
+
+
+@pytest.mark.parametrize("Hq,Hkv,G,n0,steps", [(8, 2, 32, 45, 70), (4, 4, 64, 100, 70), (2, 1, 32, 0, 40)])
+def test_decode_step_equals_append_then_attention(Hq, Hkv, G, n0, steps):
+    """kivi_decode_step (append + attention, the attention overlapping the append)
+    against the oracle's append followed by its attention, every step, across group
+    flushes; the cache stays bit-exact."""
+    wl = synth.small("step", 2, Hq, Hkv, G, n0, seed=19, steps=steps, factor_lo=30, factor_hi=100)
+    pre = synth.make_prefill(wl)
+    T = wl.capacity(extra=G)
+    gpu = gpu_prefill(pre.k, pre.v, G, T)
+    orc = oracle.prefill(pre.k.numpy(), pre.v.numpy(), G, T)
+    ws = kivi.workspace(gpu, Hq, n_tokens=T)
+    for step in range(steps):
+        k_new, v_new, q = synth.make_step(wl, pre, step)
+        out = kivi.kivi_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, ws=ws)
+        oracle.append(orc, k_new.numpy(), v_new.numpy())
+        assert_close(out, oracle.attention(orc, q.numpy(), 1.0))
+    torch.cuda.synchronize()
+    assert_cache_equal(gpu, orc)
+
+
+def test_decode_step_on_a_full_cache_is_rejected_before_any_launch():
+    wl = synth.small("stepfull", 1, 2, 2, 32, 64, seed=20)
+    pre = synth.make_prefill(wl)
+    gpu = gpu_prefill(pre.k, pre.v, 32, 64)
+    k_new, v_new, q = synth.make_step(wl, pre, 0)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kivi.KiviError) as e:
+        kivi.kivi_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, ws=ws)
+    assert e.value.status == kivi.KIVI_ERR_CAPACITY
+    assert gpu.n_tokens == 64
