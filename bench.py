@@ -143,6 +143,21 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def job_throughput(ms_local: float, tokens_per_step: int, world: int, device=None):
+    """Whole-job figures of replicas that each decode `tokens_per_step` tokens per
+    step: the step time is the max over ranks (the slowest replica bounds the job),
+    throughput = tokens_per_step * world / that time.  Returns (ms, tokens/s)."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_step * world / (ms / 1e3)
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -282,14 +297,7 @@ def run_kivi(args, wl):
     barrier()
     launches = sum(x[3] for x in rec)
     step_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in rec]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = wl.B * world / (ms_per_step / 1e3)
+    ms_per_step, value = job_throughput(sum(step_ms) / len(step_ms), wl.B, world, dev)
 
     # roofline of the dominant kernel: kivi_decode_attention (decode + combine) alone,
     # on the prompt's cache, timed the same way
