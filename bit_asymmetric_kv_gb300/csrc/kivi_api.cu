@@ -36,6 +36,100 @@ int check_heads(const kivi_dims *d, int32_t Hq) {
   return KIVI_OK;
 }
 
+// ---- paged layout
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+int page_shift_of(int32_t P) {
+  int s = 0;
+  while ((1 << s) < P && s < 30) ++s;
+  return (1 << s) == P ? s : -1;
+}
+
+int check_paged_dims(const kivi_paged_dims *d) {
+  if (!d) return KIVI_ERR_ARG;
+  if (d->B <= 0 || d->Hkv <= 0 || d->page_tokens <= 0 || d->max_pages_per_seq <= 0 || d->num_pages <= 0)
+    return KIVI_ERR_ARG;
+  if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
+  if (d->B > kivi::kPagedMaxBatch) return KIVI_ERR_UNSUPPORTED;
+  const int sh = page_shift_of(d->page_tokens);
+  if (sh < 6 || sh > 24) return KIVI_ERR_UNSUPPORTED;  // a power of two, 64 .. 2^24 tokens
+  // positions and the device-side unit counts are int32
+  const int64_t cap = (int64_t)d->max_pages_per_seq << sh;
+  if (cap > INT32_MAX) return KIVI_ERR_UNSUPPORTED;
+  if ((int64_t)d->B * (cap / 64 + 1) > INT32_MAX) return KIVI_ERR_UNSUPPORTED;
+  if ((int64_t)d->B * d->Hkv > INT32_MAX / 2) return KIVI_ERR_UNSUPPORTED;
+  return KIVI_OK;
+}
+
+int check_paged_cache(const kivi_paged_cache *c) {
+  if (!c || !c->k_codes || !c->k_meta || !c->v_codes || !c->v_meta || !c->k_res || !c->block_table ||
+      !c->seq_lens)
+    return KIVI_ERR_ARG;
+  if (!aligned16(c->k_codes) || !aligned16(c->k_meta) || !aligned16(c->v_codes) || !aligned16(c->v_meta) ||
+      !aligned16(c->k_res) || !aligned4(c->block_table) || !aligned4(c->seq_lens))
+    return KIVI_ERR_ALIGN;
+  return KIVI_OK;
+}
+
+int check_paged_heads(const kivi_paged_dims *d, int32_t Hq) {
+  if (Hq <= 0) return KIVI_ERR_ARG;
+  if (Hq % d->Hkv != 0) return KIVI_ERR_UNSUPPORTED;
+  const int R = Hq / d->Hkv;
+  if (R != 1 && R != 2 && R != 4) return KIVI_ERR_UNSUPPORTED;
+  return KIVI_OK;
+}
+
+int32_t paged_cap(const kivi_paged_dims *d) { return d->max_pages_per_seq << page_shift_of(d->page_tokens); }
+
+kivi::PagedAppendArgs paged_append_args(const kivi_paged_dims *d, const kivi_paged_cache *c, const uint16_t *k_new,
+                                        const uint16_t *v_new) {
+  kivi::PagedAppendArgs a = {};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.bt = c->block_table;
+  a.seq_lens = c->seq_lens;
+  a.k_res = c->k_res;
+  a.k_codes = c->k_codes;
+  a.k_meta = c->k_meta;
+  a.v_codes = c->v_codes;
+  a.v_meta = c->v_meta;
+  a.num_pages = d->num_pages;
+  a.B = d->B;
+  a.Hkv = d->Hkv;
+  a.G = d->G;
+  a.shift = page_shift_of(d->page_tokens);
+  a.max_pages = d->max_pages_per_seq;
+  return a;
+}
+
+kivi::DecodeArgs paged_decode_args(const kivi_paged_dims *d, const kivi_paged_cache *c, const uint16_t *q,
+                                   int32_t Hq, float softmax_scale, uint16_t *out, void *ws,
+                                   const kivi::PagedGeom &g) {
+  kivi::DecodeArgs a = {};
+  a.k_codes = c->k_codes;
+  a.k_meta = c->k_meta;
+  a.k_res = c->k_res;
+  a.v_codes = c->v_codes;
+  a.v_meta = c->v_meta;
+  a.q = q;
+  a.out = out;
+  a.ws = static_cast<float *>(ws);
+  a.B = d->B;
+  a.Hkv = d->Hkv;
+  a.Hq = Hq;
+  a.G = d->G;
+  a.n_warps = g.n_warps;
+  a.grid = g.grid;
+  a.softmax_scale = softmax_scale;
+  a.block_table = c->block_table;
+  a.seq_lens = c->seq_lens;
+  a.num_pages = d->num_pages;
+  a.page_shift = page_shift_of(d->page_tokens);
+  a.max_pages = d->max_pages_per_seq;
+  a.cap_tokens = paged_cap(d);
+  return a;
+}
+
 }  // namespace
 
 extern "C" {
@@ -138,7 +232,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
-  kivi::DecodeArgs a;
+  kivi::DecodeArgs a = {};
   a.k_codes = c->k_codes;
   a.k_meta = c->k_meta;
   a.k_res = c->k_res;
@@ -190,7 +284,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   if ((s = cuda_status(e)) != KIVI_OK) return s;
   // 2. decode attention over n + 1 tokens, overlapping the append: only the last
   //    unit of each head (the one holding the new token) waits for it
-  kivi::DecodeArgs a;
+  kivi::DecodeArgs a = {};
   a.k_codes = c->k_codes;
   a.k_meta = c->k_meta;
   a.k_res = c->k_res;
@@ -275,6 +369,108 @@ int kivi_decode_attention_fp16(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, in
   a.tiles_per_split = tps;
   a.softmax_scale = softmax_scale;
   return cuda_status(kivi::launch_fp16(a, st));
+}
+
+// ---------------------------------------------------------------------- paged cache
+int kivi_paged_buffer_bytes(const kivi_paged_dims *d, size_t out[7]) {
+  int s = check_paged_dims(d);
+  if (s != KIVI_OK) return s;
+  if (!out) return KIVI_ERR_ARG;
+  const size_t rows = (size_t)d->num_pages * (size_t)d->Hkv * (size_t)d->page_tokens;
+  out[0] = rows * (d->D / 16) * sizeof(uint32_t);
+  out[1] = rows / d->G * d->D * sizeof(uint32_t);
+  out[2] = rows * (d->D / 16) * sizeof(uint32_t);
+  out[3] = rows * sizeof(uint32_t);
+  out[4] = (size_t)d->B * d->Hkv * d->G * d->D * sizeof(uint16_t);
+  out[5] = (size_t)d->B * d->max_pages_per_seq * sizeof(int32_t);
+  out[6] = (size_t)d->B * sizeof(int32_t);
+  return KIVI_OK;
+}
+
+int kivi_paged_prefill(const kivi_paged_dims *d, const kivi_paged_cache *c, int32_t seq, const uint16_t *k,
+                       const uint16_t *v, int64_t n, cudaStream_t st) {
+  int s = check_paged_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if (seq < 0 || seq >= d->B || n < 0) return KIVI_ERR_ARG;
+  if (n > paged_cap(d)) return KIVI_ERR_CAPACITY;
+  cudaError_t e = cudaSuccess;
+  if (n > 0) {
+    if (!k || !v) return KIVI_ERR_ARG;
+    if (!aligned16(k) || !aligned16(v)) return KIVI_ERR_ALIGN;
+    kivi::PageMap pm;
+    pm.bt = c->block_table + (int64_t)seq * d->max_pages_per_seq;
+    pm.num_pages = d->num_pages;
+    pm.shift = page_shift_of(d->page_tokens);
+    pm.Hkv = d->Hkv;
+    const int64_t groups = n / d->G, nq = groups * d->G;
+    e = kivi::launch_key_groups_paged(k, n * 128, d->Hkv, groups, d->G, pm, c->k_codes, c->k_meta, st);
+    if (e == cudaSuccess)
+      e = kivi::launch_residual_copy(k, d->Hkv, n, nq, d->G, c->k_res + (int64_t)seq * d->Hkv * d->G * 128, st);
+    if (e == cudaSuccess) e = kivi::launch_value_rows_paged(v, d->Hkv, n, pm, c->v_codes, c->v_meta, st);
+  }
+  if (e == cudaSuccess) e = kivi::launch_set_len(c->seq_lens, seq, (int32_t)n, st);
+  return cuda_status(e);
+}
+
+int kivi_paged_append_token(const kivi_paged_dims *d, const kivi_paged_cache *c, const uint16_t *k_new,
+                            const uint16_t *v_new, cudaStream_t st) {
+  int s = check_paged_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if (!k_new || !v_new) return KIVI_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_ERR_ALIGN;
+  cudaError_t e = kivi::launch_paged_append(paged_append_args(d, c, k_new, v_new), st);
+  if (e == cudaSuccess) e = kivi::launch_advance_lens(c->seq_lens, d->B, paged_cap(d), st);
+  return cuda_status(e);
+}
+
+size_t kivi_paged_decode_workspace_bytes(const kivi_paged_dims *d, int32_t Hq) {
+  if (check_paged_dims(d) != KIVI_OK || check_paged_heads(d, Hq) != KIVI_OK) return 0;
+  kivi::PagedGeom g;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return 0;
+  return g.ws_bytes;
+}
+
+int kivi_paged_decode_attention(const kivi_paged_dims *d, const kivi_paged_cache *c, const uint16_t *q, int32_t Hq,
+                                float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t st) {
+  int s = check_paged_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_heads(d, Hq)) != KIVI_OK) return s;
+  if (!q || !out) return KIVI_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  kivi::PagedGeom g;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (!ws || ws_bytes < g.ws_bytes) return KIVI_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KIVI_ERR_ALIGN;
+  const kivi::DecodeArgs a = paged_decode_args(d, c, q, Hq, softmax_scale, out, ws, g);
+  return cuda_status(kivi::launch_paged_decode(a, st));
+}
+
+int kivi_paged_decode_step(const kivi_paged_dims *d, const kivi_paged_cache *c, const uint16_t *k_new,
+                           const uint16_t *v_new, const uint16_t *q, int32_t Hq, float softmax_scale, uint16_t *out,
+                           void *ws, size_t ws_bytes, cudaStream_t st) {
+  int s = check_paged_dims(d);
+  if (s != KIVI_OK) return s;
+  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_heads(d, Hq)) != KIVI_OK) return s;
+  if (!k_new || !v_new || !q || !out) return KIVI_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  kivi::PagedGeom g;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (!ws || ws_bytes < g.ws_bytes) return KIVI_ERR_WORKSPACE;
+  if (!aligned16(ws)) return KIVI_ERR_ALIGN;
+  // 1. append (flushing the groups that fill), lengths unchanged
+  cudaError_t e = kivi::launch_paged_append(paged_append_args(d, c, k_new, v_new), st);
+  if ((s = cuda_status(e)) != KIVI_OK) return s;
+  // 2. attention over seq_lens + 1 tokens, overlapping the append; its combine
+  //    advances the lengths once everything before it has completed
+  kivi::DecodeArgs a = paged_decode_args(d, c, q, Hq, softmax_scale, out, ws, g);
+  a.wait_tail = 1;
+  a.len_offset = 1;
+  a.advance_lens = c->seq_lens;
+  return cuda_status(kivi::launch_paged_decode(a, st));
 }
 
 }  // extern "C"

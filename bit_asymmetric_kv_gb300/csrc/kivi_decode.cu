@@ -256,7 +256,67 @@ __device__ __forceinline__ void pv_step(float acc[8][4], const LaneInfo &li, int
   }
 }
 
-template <int R, int G>
+// Position of a warp's cursor: head h = b * Hkv + kvh, unit uu of the head, and the
+// head's geometry (units U, full key groups NG, residual keys r, code units ncu).
+// Dense caches share one geometry; paged ones take it from the sequence's length.
+struct Cursor {
+  int64_t h;
+  int b, kvh, uu;
+  int U, NG, r, ncu;
+};
+
+template <int G>
+__device__ __forceinline__ void set_geometry(Cursor &c, int64_t len) {
+  constexpr int NGU = kUnit / G;
+  c.NG = (int)(len / G);
+  c.r = (int)(len - (int64_t)c.NG * G);
+  c.ncu = (c.NG + NGU - 1) / NGU;
+  c.U = c.ncu + (c.r > 0 ? 1 : 0);
+}
+
+// Paged layout: per-sequence lengths (clamped to the block table's capacity) and the
+// exclusive prefix sum of the sequences' unit counts, in shared memory.  All threads
+// of the CTA take part; B <= 4 * kThreads.
+template <int G>
+__device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
+  constexpr int NGU = kUnit / G;
+  int *s_tot = s_cum + a.B + 1;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int u[4], loc = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int b = 4 * t + j;
+    u[j] = 0;
+    if (b < a.B) {
+      int len = a.seq_lens[b] + a.len_offset;
+      len = len < 0 ? 0 : (len > a.cap_tokens ? a.cap_tokens : len);
+      s_len[b] = len;
+      const int ng = len / G;
+      u[j] = (ng + NGU - 1) / NGU + (len - ng * G > 0 ? 1 : 0);
+    }
+    loc += u[j];
+  }
+  int inc = loc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
+  }
+  if (lane == 31) s_tot[warp] = inc;
+  __syncthreads();
+  int ex = inc - loc;
+  for (int w = 0; w < warp; ++w) ex += s_tot[w];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int b = 4 * t + j;
+    if (b < a.B) s_cum[b] = ex;
+    ex += u[j];
+  }
+  if (t == kThreads - 1) s_cum[a.B] = ex;  // the total
+  __syncthreads();
+}
+
+template <int R, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   using L = Layout<R, G>;
@@ -267,16 +327,34 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
-  const int64_t NW = a.n_warps, W = a.total_units;
-  const int U = (int)a.units_per_head;
+  int64_t NW = a.n_warps;
+  int64_t W;
+  int *s_len = nullptr, *s_cum = nullptr;
+  int2 *hdr = nullptr;
+  float *part = a.ws;
+  const int P = 1 << a.page_shift;
+  if constexpr (PAGED) {
+    s_len = reinterpret_cast<int *>(smem + L::kSmem);
+    s_cum = s_len + a.B;
+    paged_prefix<G>(a, s_len, s_cum);
+    W = (int64_t)a.Hkv * s_cum[a.B];
+    hdr = reinterpret_cast<int2 *>(a.ws);
+    part = a.ws + 2 * (int64_t)a.B * a.Hkv;
+    // sequences without tokens get an empty header (their output is zero)
+    if (blockIdx.x == 0)
+      for (int b = threadIdx.x; b < a.B; b += kThreads)
+        if (s_cum[b + 1] == s_cum[b])
+          for (int kvh = 0; kvh < a.Hkv; ++kvh) hdr[(int64_t)b * a.Hkv + kvh] = make_int2(0, 0);
+    // fewer units than warps: use one warp per unit, so that no warp between a
+    // head's first and last owner is left without units (every partial is written)
+    if (W < NW) NW = W;
+  } else {
+    W = a.total_units;
+  }
   if (gw >= NW) return;
   const int64_t u0 = gw * W / NW, u1 = (gw + 1) * W / NW;
   if (u0 >= u1) return;
   const int n_my = (int)(u1 - u0);
-  const int NG = (int)(a.n / G);
-  const int r = (int)(a.n - (int64_t)NG * G);
-  const int n_code_units = (NG + NGU - 1) / NGU;  // units holding quantized keys
-  const int64_t nq = (int64_t)NG * G;
 
   unsigned char *wbase = smem + warp * L::kWarpBytes;
   unsigned char *frag = wbase + kStages * L::kStageBytes;
@@ -304,28 +382,83 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   // 4^(3 - i mod 4) brings every q.K product to code * qs * 64
   const float mult = (float)(64 >> (2 * (lane & 3)));
 
-  // ---- staging cursor (unit u0 + kk -> head h_is, unit uu_is within the head)
-  int64_t h_is = u0 / U;
-  int uu_is = (int)(u0 - h_is * U);
+  // ---- cursors: ic stages unit u0 + kk (one ahead), cc computes it
+  Cursor ic;
+  if constexpr (PAGED) {
+    // the sequence holding unit u0: the last b with Hkv * cum[b] <= u0 (it has units)
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)a.Hkv * s_cum[mid] <= u0) lo = mid; else hi = mid - 1;
+    }
+    ic.b = lo;
+    set_geometry<G>(ic, s_len[lo]);
+    const int64_t rel = u0 - (int64_t)a.Hkv * s_cum[lo];
+    ic.kvh = (int)(rel / ic.U);
+    ic.uu = (int)(rel - (int64_t)ic.kvh * ic.U);
+    ic.h = (int64_t)ic.b * a.Hkv + ic.kvh;
+  } else {
+    set_geometry<G>(ic, a.n);
+    ic.h = u0 / ic.U;
+    ic.uu = (int)(u0 - ic.h * ic.U);
+    ic.b = ic.kvh = 0;
+  }
+  Cursor cc = ic;
+  auto advance = [&](Cursor &c) {
+    if (++c.uu == c.U) {
+      c.uu = 0;
+      if constexpr (PAGED) {
+        if (++c.kvh == a.Hkv) {
+          c.kvh = 0;
+          do {
+            ++c.b;
+          } while (c.b < a.B && s_cum[c.b + 1] == s_cum[c.b]);
+          if (c.b < a.B) set_geometry<G>(c, s_len[c.b]);
+        }
+        c.h = (int64_t)c.b * a.Hkv + c.kvh;
+      } else {
+        ++c.h;
+      }
+    }
+  };
+  // page of token tok of sequence b (ids outside the pool are clamped into it: the
+  // caller's block table is trusted for values, never for addresses)
+  auto page_of = [&](int b, int tok) -> int64_t {
+    int64_t pg = __ldg(a.block_table + (int64_t)b * a.max_pages + (tok >> a.page_shift));
+    return pg < 0 ? 0 : (pg >= a.num_pages ? a.num_pages - 1 : pg);
+  };
+  int64_t pg_next = 0;  // page of ic's unit, loaded one unit ahead of its use
+  if constexpr (PAGED) {
+    if (ic.uu < ic.ncu) pg_next = page_of(ic.b, ic.uu * kUnit);
+  }
+
   bool waited = false;
   auto issue = [&](int kk) {
     // the last unit of a head holds the token a preceding append just wrote: when
     // this grid was launched as a programmatic dependent of that append, wait for it
-    if (a.wait_tail && !waited && kk < n_my && uu_is == U - 1) {
+    if (a.wait_tail && !waited && kk < n_my && ic.uu == ic.U - 1) {
       asm volatile("griddepcontrol.wait;\n" ::: "memory");
       waited = true;
     }
-    if (kk < n_my && uu_is < n_code_units) {
-      const int g0 = uu_is * NGU;
-      const int ngr = min(NGU, NG - g0);  // 1 or 2 groups (G = 32)
+    if (kk < n_my && ic.uu < ic.ncu) {
+      const int g0 = ic.uu * NGU;
+      const int ngr = min(NGU, ic.NG - g0);  // 1 or 2 groups (G = 32)
       const int rows = ngr * G;
       unsigned char *stg = wbase + (kk % kStages) * L::kStageBytes;
-      const int64_t t0 = h_is * a.max_tokens + (int64_t)g0 * G;
-      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + t0 * kWordsPerRow);
-      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + t0 * kWordsPerRow);
-      const unsigned char *vm = reinterpret_cast<const unsigned char *>(a.v_meta + t0);
-      const unsigned char *km =
-          reinterpret_cast<const unsigned char *>(a.k_meta + (h_is * (a.max_tokens / G) + g0) * kD);
+      int64_t row0, grp0;
+      if constexpr (PAGED) {
+        const int64_t ph = pg_next * a.Hkv + ic.kvh;
+        const int off = (g0 * G) & (P - 1);
+        row0 = ph * P + off;
+        grp0 = ph * (P / G) + off / G;
+      } else {
+        row0 = ic.h * a.max_tokens + (int64_t)g0 * G;
+        grp0 = ic.h * (a.max_tokens / G) + g0;
+      }
+      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + row0 * kWordsPerRow);
+      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + row0 * kWordsPerRow);
+      const unsigned char *vm = reinterpret_cast<const unsigned char *>(a.v_meta + row0);
+      const unsigned char *km = reinterpret_cast<const unsigned char *>(a.k_meta + grp0 * kD);
       if (rows == kUnit) {
 #pragma unroll
         for (int c = lane; c < kUnit * 2; c += 32) {
@@ -345,9 +478,9 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       }
     }
     cp_async_commit();
-    if (++uu_is == U) {
-      uu_is = 0;
-      ++h_is;
+    advance(ic);
+    if constexpr (PAGED) {
+      if (kk + 1 < n_my && ic.uu < ic.ncu) pg_next = page_of(ic.b, ic.uu * kUnit);
     }
   };
 
@@ -359,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
   float qv[R][4];
 
-  // Write head h's partial number (gw - first warp of h) from the P.V accumulators
+  // Write the partial of head h (this warp's share of it) from the P.V accumulators
   // and the softmax state (m, l, zs) that belongs to them.
   auto emit = [&](int64_t h, const SoftState &fin) {
     float l = fin.l, zs = fin.zs;
@@ -383,9 +516,15 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       for (int j = 0; j < 16; ++j) o[j] += __shfl_xor_sync(0xffffffffu, o[j], off);
     }
     if (li.slot_mine == 0) {
-      const int64_t b = h / a.Hkv, kvh = h - b * a.Hkv;
-      const int64_t slot = gw - owner_warp(h * U, W, NW);
-      float *dst = a.ws + ((b * a.Hq + kvh * R + head_mine) * a.pmax + slot) * (kD + 2);
+      float *dst;
+      if constexpr (PAGED) {
+        // pair index gw + h grows strictly along the unit order: unique per (warp, head)
+        dst = part + ((gw + h) * R + head_mine) * (kD + 2);
+      } else {
+        const int64_t b = h / a.Hkv, kvh = h - b * a.Hkv;
+        const int64_t slot = gw - owner_warp(h * a.units_per_head, W, NW);
+        dst = a.ws + ((b * a.Hq + kvh * R + head_mine) * a.pmax + slot) * (kD + 2);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         // undo the code factor 4^(j mod 4) and the 2^-24 of the subnormal codes
@@ -403,8 +542,15 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
   };
-  auto load_q = [&](int64_t h) {
-    const int64_t b = h / a.Hkv, kvh = h - b * a.Hkv;
+  auto load_q = [&](const Cursor &c) {
+    int64_t b, kvh;
+    if constexpr (PAGED) {
+      b = c.b;
+      kvh = c.kvh;
+    } else {
+      b = c.h / a.Hkv;
+      kvh = c.h - b * a.Hkv;
+    }
     const uint16_t *qh = a.q + (b * a.Hq + kvh * R) * kD + lane;
 #pragma unroll
     for (int hh = 0; hh < R; ++hh)
@@ -419,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   int p_kind = 0;            // 0 none, 1 codes (stage p_stage), 2 residual
   int p_ntok = 0, p_stage = 0;
   int64_t p_h = -1;
+  int64_t p_res_row = 0;     // value row of the pending residual unit's first token
   SoftState p_fin;           // softmax state to emit with once the pending unit is added
   bool p_emit = false;
 #pragma unroll
@@ -439,7 +586,12 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         });
       }
     } else if (p_kind == 2) {
-      const uint32_t *vc_head = a.v_codes + (p_h * a.max_tokens + nq) * kWordsPerRow;
+      int64_t res_row;
+      if constexpr (PAGED)
+        res_row = p_res_row;
+      else
+        res_row = p_h * a.max_tokens + (int64_t)cc.NG * G;  // one geometry for all heads
+      const uint32_t *vc_head = a.v_codes + res_row * kWordsPerRow;
 #pragma unroll
       for (int s = 0; s < R; ++s) {
         const int nv = min(16 * T, p_ntok - 16 * T * s);
@@ -456,13 +608,19 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     }
   };
 
-  int64_t cur_h = u0 / U;
-  int uu = (int)(u0 - cur_h * U);
-  load_q(cur_h);
+  load_q(cc);
   issue(0);
 
   for (int kk = 0; kk < n_my; ++kk) {
     issue(kk + 1);
+    if constexpr (PAGED) {
+      // the warp that takes a head's first unit publishes where its partials go
+      if (cc.uu == 0 && lane == 0) {
+        const int64_t start = (int64_t)a.Hkv * s_cum[cc.b] + (int64_t)cc.kvh * cc.U;
+        const int64_t last = owner_warp(start + cc.U - 1, W, NW);
+        hdr[cc.h] = make_int2((int)(gw + cc.h), (int)(last - gw + 1));
+      }
+    }
     cp_async_wait<1>();
     __syncwarp();
     const int stage = kk % kStages;
@@ -474,10 +632,11 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       nalpha[j] = 1.f;
     }
     int n_kind, n_ntok;
+    int64_t n_res_row = 0;
 
-    if (uu < n_code_units) {
+    if (cc.uu < cc.ncu) {
       const unsigned char *stg = wbase + stage * L::kStageBytes;
-      const int ngr = min(NGU, NG - uu * NGU);
+      const int ngr = min(NGU, cc.NG - cc.uu * NGU);
       // ---- per group: qs = q * s scaled by 2^E * mult, split hi/lo into the
       //      group's B fragment; this lane's score scale and beta = q . z
       float cq_g[NGU], beta_g[NGU];
@@ -569,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       n_kind = 1;
       n_ntok = ngr * G;
     } else {
-      // ---- fp16 residual keys of head cur_h: B = q itself (hi part, lo = 0), A = keys
+      // ---- fp16 residual keys of the head: B = q itself (hi part, lo = 0), A = keys
       uint16_t *fb = reinterpret_cast<uint16_t *>(frag);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -581,8 +740,17 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       __syncwarp();
       uint32_t bf[16];
       load_frag(frag + frag_row * kFragRowWords * 4, bf);
-      const uint16_t *res_head = a.k_res + cur_h * G * kD;
-      const uint32_t *vm_head = a.v_meta + cur_h * a.max_tokens + nq;
+      const int r = cc.r;
+      const int64_t nq = (int64_t)cc.NG * G;
+      const uint16_t *res_head = a.k_res + cc.h * G * kD;
+      // value rows of the residual tokens nq .. nq + r - 1 (one page: pages hold whole groups)
+      if constexpr (PAGED) {
+        const int64_t ph = page_of(cc.b, (int)nq) * a.Hkv + cc.kvh;
+        n_res_row = ph * P + (nq & (P - 1));
+      } else {
+        n_res_row = cc.h * a.max_tokens + nq;
+      }
+      const uint32_t *vm_head = a.v_meta + n_res_row;
 #pragma unroll
       for (int s = 0; s < R; ++s) {
         const int base = 16 * T * s;
@@ -613,18 +781,21 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     }
     p_kind = n_kind;
     p_ntok = n_ntok;
+    if constexpr (PAGED) p_res_row = n_res_row;
     p_stage = stage;
-    p_h = cur_h;
+    p_h = cc.h;
     __syncwarp();
-    if (++uu == U && kk + 1 < n_my) {  // the next unit starts a new head
-      p_fin = ss;
-      p_emit = true;
-      ss.m = -INFINITY;
-      ss.l = 0.f;
-      ss.zs = 0.f;
-      uu = 0;
-      ++cur_h;
-      load_q(cur_h);
+    if (kk + 1 < n_my) {
+      const bool head_end = cc.uu + 1 == cc.U;
+      if (head_end) {  // the next unit starts a new head
+        p_fin = ss;
+        p_emit = true;
+        ss.m = -INFINITY;
+        ss.l = 0.f;
+        ss.zs = 0.f;
+      }
+      advance(cc);
+      if (head_end) load_q(cc);
     }
   }
   p_fin = ss;
@@ -633,25 +804,22 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   cp_async_wait<0>();
 }
 
-// Merge the partials of one (batch, query head): one thread per channel.  The
-// partials' maxima and weights go through shared memory so every load is issued
-// independently (the partials sit in L2).
-__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws, int64_t pmax, int64_t W,
-                                                      int64_t NW, int64_t U, int Hkv, int Hq,
-                                                      uint16_t *__restrict__ out) {
+// Merge np partials (max, sum, unnormalised output; `stride` floats apart) of one
+// (batch, query head) into out_row: one thread per channel.  The partials' maxima
+// and weights go through shared memory so every load is issued independently (the
+// partials sit in L2).  np == 0 (no tokens) writes zeros.
+__device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
+                                            uint16_t *__restrict__ out_row) {
   __shared__ float s_w[128];
   __shared__ float s_red[4];
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
-  const int64_t row = blockIdx.x;  // b * Hq + h
-  const int64_t b = row / Hq, hq = row - b * Hq;
-  const int64_t head = b * Hkv + hq / (Hq / Hkv);
-  const int64_t first = owner_warp(head * U, W, NW), last = owner_warp(head * U + U - 1, W, NW);
-  const int np = (int)(last - first + 1);
   const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
-  const float *p = ws + row * pmax * (kD + 2);
+  if (np <= 0) {
+    out_row[c] = 0;
+    return;
+  }
   // global max of the partial maxima
   float M = -INFINITY;
-  for (int s = c; s < np; s += 128) M = fmaxf(M, __ldcg(p + (int64_t)s * (kD + 2) + kD));
+  for (int s = c; s < np; s += 128) M = fmaxf(M, __ldcg(p + (int64_t)s * stride + kD));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   if (lane == 0) s_red[warp] = M;
@@ -662,9 +830,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     const int s = s0 + c;
     float w = 0.f, lw = 0.f;
     if (s < np) {
-      const float m = __ldcg(p + (int64_t)s * (kD + 2) + kD);
+      const float m = __ldcg(p + (int64_t)s * stride + kD);
       w = (m == -INFINITY) ? 0.f : ex2(m - M);
-      lw = w * __ldcg(p + (int64_t)s * (kD + 2) + kD + 1);
+      lw = w * __ldcg(p + (int64_t)s * stride + kD + 1);
     }
     __syncthreads();  // previous chunk's weights are consumed
     s_w[c] = w;
@@ -674,29 +842,65 @@ __global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ 
     __syncthreads();
     L += (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
     const int n = min(128, np - s0);
-    const float *ps = p + (int64_t)s0 * (kD + 2) + c;
+    const float *ps = p + (int64_t)s0 * stride + c;
     int j = 0;
     for (; j + 4 <= n; j += 4) {
-      const float v0 = __ldcg(ps + (int64_t)j * (kD + 2)), v1 = __ldcg(ps + (int64_t)(j + 1) * (kD + 2));
-      const float v2 = __ldcg(ps + (int64_t)(j + 2) * (kD + 2)), v3 = __ldcg(ps + (int64_t)(j + 3) * (kD + 2));
+      const float v0 = __ldcg(ps + (int64_t)j * stride), v1 = __ldcg(ps + (int64_t)(j + 1) * stride);
+      const float v2 = __ldcg(ps + (int64_t)(j + 2) * stride), v3 = __ldcg(ps + (int64_t)(j + 3) * stride);
       O = fmaf(s_w[j], v0, O);
       O = fmaf(s_w[j + 1], v1, O);
       O = fmaf(s_w[j + 2], v2, O);
       O = fmaf(s_w[j + 3], v3, O);
     }
-    for (; j < n; ++j) O = fmaf(s_w[j], __ldcg(ps + (int64_t)j * (kD + 2)), O);
+    for (; j < n; ++j) O = fmaf(s_w[j], __ldcg(ps + (int64_t)j * stride), O);
   }
-  out[row * kD + c] = f2h(O / L);
+  out_row[c] = f2h(O / L);
 }
 
-template <int R, int G>
+// Dense layout: the partials of (batch, query head) `row` sit at slots 0 .. np-1 of
+// the row's pmax slots; np follows from the unit split.
+__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws, int64_t pmax, int64_t W,
+                                                      int64_t NW, int64_t U, int Hkv, int Hq,
+                                                      uint16_t *__restrict__ out) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
+  const int64_t row = blockIdx.x;  // b * Hq + h
+  const int64_t b = row / Hq, hq = row - b * Hq;
+  const int64_t head = b * Hkv + hq / (Hq / Hkv);
+  const int64_t first = owner_warp(head * U, W, NW), last = owner_warp(head * U + U - 1, W, NW);
+  combine_row(ws + row * pmax * (kD + 2), (int)(last - first + 1), kD + 2, out + row * kD);
+}
+
+// Paged layout: the decode grid wrote, per (batch, KV head), the index of its first
+// partial pair and their count; pair i holds the R query heads' partials.  With
+// `advance`, the grid then moves every sequence's length past the token the step
+// appended (the decode grid, and so the append before it, has completed).
+__global__ void __launch_bounds__(128) paged_combine_kernel(const float *__restrict__ ws, int Hkv, int Hq, int B,
+                                                            int32_t *advance, int32_t cap,
+                                                            uint16_t *__restrict__ out) {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
+  const int64_t row = blockIdx.x;  // b * Hq + h
+  const int64_t b = row / Hq, hq = row - b * Hq;
+  const int R = Hq / Hkv;
+  const int64_t head = b * Hkv + hq / R;
+  const int2 hd = __ldcg(reinterpret_cast<const int2 *>(ws) + head);
+  const float *part = ws + 2 * (int64_t)B * Hkv;
+  combine_row(part + ((int64_t)hd.x * R + hq % R) * (kD + 2), hd.y, (int64_t)R * (kD + 2), out + row * kD);
+  if (advance && hq == 0 && threadIdx.x == 0) {
+    const int32_t len = advance[b];
+    advance[b] = len < cap ? len + 1 : cap;
+  }
+}
+
+template <int R, int G, bool PAGED>
 const void *kernel_ptr() {
-  return reinterpret_cast<const void *>(&decode_kernel<R, G>);
+  return reinterpret_cast<const void *>(&decode_kernel<R, G, PAGED>);
 }
 
+template <bool PAGED>
 const void *select_kernel(int R, int G) {
-  if (G == 32) return R == 1 ? kernel_ptr<1, 32>() : R == 2 ? kernel_ptr<2, 32>() : kernel_ptr<4, 32>();
-  return R == 1 ? kernel_ptr<1, 64>() : R == 2 ? kernel_ptr<2, 64>() : kernel_ptr<4, 64>();
+  if (G == 32)
+    return R == 1 ? kernel_ptr<1, 32, PAGED>() : R == 2 ? kernel_ptr<2, 32, PAGED>() : kernel_ptr<4, 32, PAGED>();
+  return R == 1 ? kernel_ptr<1, 64, PAGED>() : R == 2 ? kernel_ptr<2, 64, PAGED>() : kernel_ptr<4, 64, PAGED>();
 }
 
 int smem_bytes(int R, int G) {
@@ -704,12 +908,10 @@ int smem_bytes(int R, int G) {
   return R == 1 ? Layout<1, 64>::kSmem : R == 2 ? Layout<2, 64>::kSmem : Layout<4, 64>::kSmem;
 }
 
-}  // namespace
+// Paged kernels append the lengths, the unit prefix and 4 warp totals: 2B + 5 ints.
+int paged_smem_bytes(int R, int G, int B) { return smem_bytes(R, G) + ((4 * (2 * B + 5) + 15) & ~15); }
 
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
-  const int R = Hq / Hkv;
-  const void *fn = select_kernel(R, G);
-  const int smem = smem_bytes(R, G);
+cudaError_t warps_on_device(const void *fn, int smem, int *n_warps) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, per_sm = 0;
@@ -717,11 +919,22 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem)) != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
+  *n_warps = sms * per_sm * kWarps;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
+  const int R = Hq / Hkv;
+  int nw = 0;
+  cudaError_t e = warps_on_device(select_kernel<false>(R, G), smem_bytes(R, G), &nw);
+  if (e != cudaSuccess) return e;
   const int64_t heads = (int64_t)B * Hkv;
   const int64_t ng = n / G;
   const int64_t U = (ng * G + kUnit - 1) / kUnit + ((n % G) ? 1 : 0);
   const int64_t W = heads * U;
-  int64_t NW = (int64_t)sms * per_sm * kWarps;
+  int64_t NW = nw;
   if (NW > W) NW = W;
   const int64_t q = W / NW;  // every warp holds at least q units
   out->units_per_head = U;
@@ -732,9 +945,22 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom
   return cudaSuccess;
 }
 
+cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out) {
+  const int R = Hq / Hkv;
+  int nw = 0;
+  cudaError_t e = warps_on_device(select_kernel<true>(R, G), paged_smem_bytes(R, G, B), &nw);
+  if (e != cudaSuccess) return e;
+  const size_t heads = (size_t)B * Hkv;
+  out->n_warps = nw;
+  out->grid = nw / kWarps;
+  // header int2 per head; pair indices warp + head < n_warps + heads
+  out->ws_bytes = heads * 8 + ((size_t)nw + heads) * R * (kD + 2) * sizeof(float);
+  return cudaSuccess;
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   const int R = a.Hq / a.Hkv;
-  const void *fn = select_kernel(R, a.G);
+  const void *fn = select_kernel<false>(R, a.G);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -757,6 +983,33 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.ws, (int64_t)a.pmax, a.total_units,
                             (int64_t)a.n_warps, a.units_per_head, a.Hkv, a.Hq, a.out);
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
+  const int R = a.Hq / a.Hkv;
+  const void *fn = select_kernel<true>(R, a.G);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3((unsigned)a.grid);
+  dcfg.blockDim = dim3(kThreads);
+  dcfg.dynamicSmemBytes = (size_t)paged_smem_bytes(R, a.G, a.B);
+  dcfg.stream = st;
+  dcfg.attrs = attr;
+  dcfg.numAttrs = a.wait_tail ? 1 : 0;
+  void *args[] = {const_cast<DecodeArgs *>(&a)};
+  cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_combine_kernel, (const float *)a.ws, a.Hkv, a.Hq, a.B, a.advance_lens,
+                            a.cap_tokens, a.out);
 }
 
 }  // namespace kivi

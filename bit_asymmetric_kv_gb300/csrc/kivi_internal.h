@@ -15,6 +15,35 @@ cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t 
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st);
 cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, int64_t nq, int G, uint16_t *k_res,
                                  cudaStream_t st);
+// Paged destinations of a prefill: the block-table row of one sequence.
+struct PageMap {
+  const int32_t *bt;   // [max_pages] page ids of the sequence
+  int64_t num_pages;   // pages in the pool (ids outside [0, num_pages) are skipped)
+  int shift;           // log2(tokens per page)
+  int Hkv;
+};
+cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, int64_t heads,
+                                    int64_t groups_per_head, int G, const PageMap &pm, uint32_t *k_codes,
+                                    uint32_t *k_meta, cudaStream_t st);
+cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head, const PageMap &pm,
+                                    uint32_t *v_codes, uint32_t *v_meta, cudaStream_t st);
+cudaError_t launch_set_len(int32_t *seq_lens, int32_t seq, int32_t n, cudaStream_t st);
+
+// Paged append of one token per (sequence, KV head) at position seq_lens[b], with the
+// residual flush done in the same kernel.  seq_lens is read, never written: the
+// lengths are advanced afterwards (launch_advance_lens, or the paged combine).
+struct PagedAppendArgs {
+  const uint16_t *k_new, *v_new;  // [B][Hkv][128]
+  const int32_t *bt;              // [B][max_pages]
+  int32_t *seq_lens;              // [B]
+  uint16_t *k_res;                // [B][Hkv][G][128]
+  uint32_t *k_codes, *k_meta, *v_codes, *v_meta;
+  int64_t num_pages;
+  int B, Hkv, G, shift, max_pages;
+};
+cudaError_t launch_paged_append(const PagedAppendArgs &a, cudaStream_t st);
+cudaError_t launch_advance_lens(int32_t *seq_lens, int B, int32_t cap, cudaStream_t st);
+
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                            const uint32_t *v_codes, const uint32_t *v_meta, int64_t heads, int64_t n, int G,
                            int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st);
@@ -38,6 +67,16 @@ struct DecodeArgs {
   int pmax;                // partial slots per query head in the workspace
   int wait_tail;           // launched as a dependent of an append: wait before each head's last unit
   float softmax_scale;
+  // paged layout only: per-sequence lengths on the device, rows found through the
+  // block table; the partials are addressed by (warp + head) and a per-head header
+  const int32_t *block_table;  // [B][max_pages]
+  const int32_t *seq_lens;     // [B]
+  int32_t *advance_lens;       // non-null: the combine sets seq_lens[b] = min(len + 1, cap) afterwards
+  int64_t num_pages;
+  int page_shift;              // log2(tokens per page)
+  int max_pages;
+  int len_offset;              // tokens appended just before (0 or 1): the context is seq_lens[b] + len_offset
+  int32_t cap_tokens;          // max_pages << page_shift
 };
 
 // Geometry of one decode call on the current device (deterministic for given sizes).
@@ -50,6 +89,18 @@ struct DecodeGeom {
 };
 cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+
+// Paged decode: the grid fills the GPU whatever the lengths; n_warps and grid come
+// from here, the rest is found on the device.  Workspace: a header of B*Hkv int2
+// {first partial, count}, then (n_warps + B*Hkv) * R partials of 130 floats.
+struct PagedGeom {
+  int n_warps;
+  int grid;
+  size_t ws_bytes;
+};
+constexpr int kPagedMaxBatch = 512;
+cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out);
+cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st);
 
 // Decode attention over an unquantized fp16 cache (the comparison kernel).
 struct Fp16Args {

@@ -16,11 +16,21 @@ namespace kivi {
 // 16-byte chunk c4 (8 channels) of tokens t8, t8 + 8, ... so one warp instruction
 // reads 8 token rows x 64 contiguous bytes.
 // -------------------------------------------------------------------------------------
-template <int G>
+// Row of token t of head bh in a paged pool (false: the block table gives no page
+// of the pool for it, and the row is skipped).
+__device__ __forceinline__ bool paged_row(const PageMap &pm, int64_t bh, int64_t t, int64_t *row) {
+  const int64_t page = pm.bt[t >> pm.shift];
+  if (page < 0 || page >= pm.num_pages) return false;
+  *row = ((page * pm.Hkv + bh) << pm.shift) + (t & ((1 << pm.shift) - 1));
+  return true;
+}
+
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
                                                         int64_t groups_per_head, int64_t g0,
                                                         uint32_t *__restrict__ k_codes,
-                                                        uint32_t *__restrict__ k_meta, int64_t max_tokens) {
+                                                        uint32_t *__restrict__ k_meta, int64_t max_tokens,
+                                                        const PageMap pm) {
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   constexpr int TPL = G / 8;  // tokens per lane
@@ -30,6 +40,15 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   const int64_t bh = blockIdx.x / groups_per_head;
   const int64_t gi = blockIdx.x % groups_per_head;
   const int64_t g = g0 + gi;
+  // destination: first token row of the group and its (group, channel) meta row
+  int64_t row0, grp;
+  if constexpr (PAGED) {
+    if (!paged_row(pm, bh, g * G, &row0)) return;  // the whole CTA: one group, one page
+    grp = row0 / G;  // pages hold whole groups, so row0 is a multiple of G
+  } else {
+    row0 = bh * max_tokens + g * G;
+    grp = bh * (max_tokens / G) + g;
+  }
   const uint16_t *src = in + bh * in_head_stride + gi * (int64_t)G * kD + 32 * warp + 8 * c4;
 
   uint4 x[TPL];
@@ -66,7 +85,7 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   const float my_mn = h2f((uint16_t)((t8 & 1) ? (mn_bits >> 16) : (mn_bits & 0xffffu)));
   const float my_mx = h2f((uint16_t)((t8 & 1) ? (mx_bits >> 16) : (mx_bits & 0xffffu)));
   const QParams mine = make_qparams(my_mn, my_mx);
-  k_meta[(bh * (max_tokens / G) + g) * kD + 32 * warp + 8 * c4 + t8] = mine.meta;
+  k_meta[grp * kD + 32 * warp + 8 * c4 + t8] = mine.meta;
 
   QParams p[8];
 #pragma unroll
@@ -92,7 +111,7 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   }
   __syncthreads();
   // coalesced write of the G packed token rows
-  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + (bh * max_tokens + g * G) * kWordsPerRow);
+  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + row0 * kWordsPerRow);
   const uint4 *s4 = reinterpret_cast<const uint4 *>(s_codes);
   for (int i = threadIdx.x; i < G * kWordsPerRow / 4; i += blockDim.x) dst[i] = s4[i];
 }
@@ -121,10 +140,12 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
 }
 
 // rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head
+template <bool PAGED>
 __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restrict__ v, int64_t rows,
                                                          int64_t tokens_per_head, int64_t t0,
                                                          uint32_t *__restrict__ v_codes,
-                                                         uint32_t *__restrict__ v_meta, int64_t max_tokens) {
+                                                         uint32_t *__restrict__ v_meta, int64_t max_tokens,
+                                                         const PageMap pm) {
   const int lane = threadIdx.x & 31;
   const int lane16 = lane & 15;
   const uint32_t half_mask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;
@@ -132,9 +153,12 @@ __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restr
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4); row < rows; row += half_warps) {
     const int64_t bh = row / tokens_per_head;
     const int64_t t = t0 + row % tokens_per_head;
+    int64_t dst = bh * max_tokens + t;
+    if constexpr (PAGED) {
+      if (!paged_row(pm, bh, t, &dst)) continue;  // the half-warp skips the row together
+    }
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + row * kD) + lane16);
-    quantize_value_row(x, lane16, half_mask, v_codes + (bh * max_tokens + t) * kWordsPerRow,
-                       v_meta + bh * max_tokens + t);
+    quantize_value_row(x, lane16, half_mask, v_codes + dst * kWordsPerRow, v_meta + dst);
   }
 }
 
@@ -159,6 +183,83 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
     const int64_t r = n % G;
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(k_new + bh * kD) + lane16);
     reinterpret_cast<uint4 *>(k_res + (bh * G + r) * kD)[lane16] = x;
+  }
+}
+
+// Paged append: one warp per (sequence b, KV head), the token at position
+// len = seq_lens[b] of sequence b.  Lanes 0-15 quantize the value row into the page
+// that holds position len; lanes 16-31 copy the key into residual slot len mod G.
+// When that slot is the group's last one, the warp quantizes the group at once
+// (sequences of a batch fill their groups on different steps): lane l takes channels
+// 4l .. 4l+3 of the G keys (slots 0 .. G-2 from the residual, the new key from the
+// input), finds their min and max, then packs each token row.  A full sequence
+// (len at the block table's capacity) or a page id outside the pool drops the token.
+template <int G>
+__global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs a) {
+  // a decode launched as a programmatic dependent may start its independent work now
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (bh >= (int64_t)a.B * a.Hkv) return;
+  const int lane = threadIdx.x & 31, lane16 = lane & 15;
+  const int b = (int)(bh / a.Hkv), kvh = (int)(bh - (int64_t)b * a.Hkv);
+  const int32_t len = a.seq_lens[b];
+  if (len < 0 || len >= (a.max_pages << a.shift)) return;
+  const int64_t page = a.bt[(int64_t)b * a.max_pages + (len >> a.shift)];
+  if (page < 0 || page >= a.num_pages) return;
+  const int64_t P = 1 << a.shift;
+  const int64_t ph = page * a.Hkv + kvh;
+  const int64_t off = len & (P - 1);
+  const int r = len % G;
+  if (lane < 16) {
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.v_new + bh * kD) + lane16);
+    quantize_value_row(x, lane16, 0x0000ffffu, a.v_codes + (ph * P + off) * kWordsPerRow, a.v_meta + ph * P + off);
+  } else {
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.k_new + bh * kD) + lane16);
+    reinterpret_cast<uint4 *>(a.k_res + (bh * G + r) * kD)[lane16] = x;
+  }
+  if (r != G - 1) return;
+  // ---- flush: the group's G tokens are positions len-G+1 .. len, rows of one page
+  const uint16_t *res = a.k_res + bh * G * kD + 4 * lane;  // slots 0 .. G-2 (earlier launches)
+  const uint2 last = *reinterpret_cast<const uint2 *>(a.k_new + bh * kD + 4 * lane);
+  auto key = [&](int t) -> uint2 { return t == G - 1 ? last : *reinterpret_cast<const uint2 *>(res + t * kD); };
+  __half2 mn0 = u2h2(last.x), mx0 = mn0, mn1 = u2h2(last.y), mx1 = mn1;
+#pragma unroll 8
+  for (int t = 0; t < G - 1; ++t) {
+    const uint2 x = key(t);
+    mn0 = __hmin2(mn0, u2h2(x.x));
+    mx0 = __hmax2(mx0, u2h2(x.x));
+    mn1 = __hmin2(mn1, u2h2(x.y));
+    mx1 = __hmax2(mx1, u2h2(x.y));
+  }
+  const QParams p0 = make_qparams(__low2float(mn0), __low2float(mx0));
+  const QParams p1 = make_qparams(__high2float(mn0), __high2float(mx0));
+  const QParams p2 = make_qparams(__low2float(mn1), __low2float(mx1));
+  const QParams p3 = make_qparams(__high2float(mn1), __high2float(mx1));
+  const int64_t row0 = ph * P + off - (G - 1);
+  reinterpret_cast<uint4 *>(a.k_meta + (row0 / G) * kD)[lane] = make_uint4(p0.meta, p1.meta, p2.meta, p3.meta);
+  // channel 4l + j sits in word l / 4 at bits 8 (l mod 4) + 2j
+  const int shift = 8 * (lane & 3);
+  uint32_t *dst = a.k_codes + row0 * kWordsPerRow + (lane >> 2);
+#pragma unroll 8
+  for (int t = 0; t < G; ++t) {
+    const uint2 x = key(t);
+    uint32_t bits = quant_code(h2f((uint16_t)(x.x & 0xffffu)), p0) | (quant_code(h2f((uint16_t)(x.x >> 16)), p1) << 2) |
+                    (quant_code(h2f((uint16_t)(x.y & 0xffffu)), p2) << 4) |
+                    (quant_code(h2f((uint16_t)(x.y >> 16)), p3) << 6);
+    bits <<= shift;
+    bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
+    bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+    if ((lane & 3) == 0) dst[t * kWordsPerRow] = bits;
+  }
+}
+
+__global__ void set_len_kernel(int32_t *seq_lens, int32_t seq, int32_t n) { seq_lens[seq] = n; }
+
+__global__ void __launch_bounds__(128) advance_lens_kernel(int32_t *seq_lens, int B, int32_t cap) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) {
+    const int32_t len = seq_lens[b];
+    if (len >= 0) seq_lens[b] = len < cap ? len + 1 : cap;
   }
 }
 
@@ -221,12 +322,27 @@ cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_
                               cudaStream_t st) {
   const int64_t blocks = heads * groups_per_head;
   if (blocks == 0) return cudaSuccess;
+  const PageMap none = {};
   if (G == 32)
-    key_group_kernel<32><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes, k_meta,
-                                                           max_tokens);
+    key_group_kernel<32, false><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes,
+                                                                  k_meta, max_tokens, none);
   else
-    key_group_kernel<64><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes, k_meta,
-                                                           max_tokens);
+    key_group_kernel<64, false><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes,
+                                                                  k_meta, max_tokens, none);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, int64_t heads,
+                                    int64_t groups_per_head, int G, const PageMap &pm, uint32_t *k_codes,
+                                    uint32_t *k_meta, cudaStream_t st) {
+  const int64_t blocks = heads * groups_per_head;
+  if (blocks == 0) return cudaSuccess;
+  if (G == 32)
+    key_group_kernel<32, true><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, 0, k_codes,
+                                                                 k_meta, 0, pm);
+  else
+    key_group_kernel<64, true><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, 0, k_codes,
+                                                                 k_meta, 0, pm);
   return cudaGetLastError();
 }
 
@@ -234,8 +350,17 @@ cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_p
                               uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  value_rows_kernel<<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, t0, v_codes, v_meta,
-                                                                max_tokens);
+  value_rows_kernel<false><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, t0, v_codes,
+                                                                       v_meta, max_tokens, PageMap{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head, const PageMap &pm,
+                                    uint32_t *v_codes, uint32_t *v_meta, cudaStream_t st) {
+  const int64_t rows = heads * tokens_per_head;
+  if (rows == 0) return cudaSuccess;
+  value_rows_kernel<true><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, 0, v_codes, v_meta,
+                                                                      0, pm);
   return cudaGetLastError();
 }
 
@@ -243,6 +368,26 @@ cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t 
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
   append_kernel<<<(unsigned)((heads + 3) / 4), 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta,
                                                              max_tokens);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_append(const PagedAppendArgs &a, cudaStream_t st) {
+  const int64_t heads = (int64_t)a.B * a.Hkv;
+  const unsigned blocks = (unsigned)((heads + 3) / 4);
+  if (a.G == 32)
+    paged_append_kernel<32><<<blocks, 128, 0, st>>>(a);
+  else
+    paged_append_kernel<64><<<blocks, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_set_len(int32_t *seq_lens, int32_t seq, int32_t n, cudaStream_t st) {
+  set_len_kernel<<<1, 1, 0, st>>>(seq_lens, seq, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_advance_lens(int32_t *seq_lens, int B, int32_t cap, cudaStream_t st) {
+  advance_lens_kernel<<<(unsigned)((B + 127) / 128), 128, 0, st>>>(seq_lens, B, cap);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,18 @@ class kivi_cache(ctypes.Structure):
                 ("v_codes", ctypes.c_void_p), ("v_meta", ctypes.c_void_p), ("n_tokens", ctypes.c_int64)]
 
 
+class kivi_paged_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("G", ctypes.c_int32),
+                ("bits", ctypes.c_int32), ("page_tokens", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64)]
+
+
+class kivi_paged_cache(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("k_meta", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
+                ("v_meta", ctypes.c_void_p), ("k_res", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -68,6 +80,17 @@ def lib() -> ctypes.CDLL:
         L.kivi_decode_attention_fp16.restype = ctypes.c_int
         L.kivi_decode_step.argtypes = [D, C, P, P, P, i32, ctypes.c_float, P, P, sz, P]
         L.kivi_decode_step.restype = ctypes.c_int
+        PD, PC = ctypes.POINTER(kivi_paged_dims), ctypes.POINTER(kivi_paged_cache)
+        L.kivi_paged_buffer_bytes.argtypes = [PD, ctypes.POINTER(sz)]
+        L.kivi_paged_prefill.argtypes = [PD, PC, i32, P, P, i64, P]
+        L.kivi_paged_append_token.argtypes = [PD, PC, P, P, P]
+        L.kivi_paged_decode_workspace_bytes.argtypes = [PD, i32]
+        L.kivi_paged_decode_workspace_bytes.restype = sz
+        L.kivi_paged_decode_attention.argtypes = [PD, PC, P, i32, ctypes.c_float, P, P, sz, P]
+        L.kivi_paged_decode_step.argtypes = [PD, PC, P, P, P, i32, ctypes.c_float, P, P, sz, P]
+        for name in ("kivi_paged_buffer_bytes", "kivi_paged_prefill", "kivi_paged_append_token",
+                     "kivi_paged_decode_attention", "kivi_paged_decode_step"):
+            getattr(L, name).restype = ctypes.c_int
         L.kivi_status_string.argtypes = [ctypes.c_int]
         L.kivi_status_string.restype = ctypes.c_char_p
         for name in ("kivi_buffer_bytes", "kivi_quantize_prefill", "kivi_append_token", "kivi_decode_splits",
@@ -254,3 +277,109 @@ def kivi_decode_attention_fp16(k: torch.Tensor, v: torch.Tensor, q: torch.Tensor
 
 def kivi_status_string(status: int) -> str:
     return lib().kivi_status_string(status).decode()
+
+
+# ---------------------------------------------------------------------------------------
+# paged cache
+# ---------------------------------------------------------------------------------------
+def make_paged_dims(B: int, Hkv: int, G: int, page_tokens: int, max_pages_per_seq: int, num_pages: int,
+                    D: int = 128, bits: int = 2) -> kivi_paged_dims:
+    return kivi_paged_dims(B, Hkv, D, G, bits, page_tokens, max_pages_per_seq, num_pages)
+
+
+def kivi_paged_buffer_bytes(dims: kivi_paged_dims) -> list[int]:
+    out = (ctypes.c_size_t * 7)()
+    _check(lib().kivi_paged_buffer_bytes(ctypes.byref(dims), out), "kivi_paged_buffer_bytes")
+    return list(out)
+
+
+@dataclass
+class PagedCache:
+    """Caller-owned device buffers of a paged cache (layouts in include/kivi.h): a
+    page pool, per-sequence residual keys, the block table and the lengths."""
+
+    dims: kivi_paged_dims
+    k_codes: torch.Tensor      # int32 [num_pages, Hkv, P, D/16]
+    k_meta: torch.Tensor       # int32 [num_pages, Hkv, P/G, D]
+    v_codes: torch.Tensor      # int32 [num_pages, Hkv, P, D/16]
+    v_meta: torch.Tensor       # int32 [num_pages, Hkv, P]
+    k_res: torch.Tensor        # fp16  [B, Hkv, G, D]
+    block_table: torch.Tensor  # int32 [B, max_pages_per_seq]
+    seq_lens: torch.Tensor     # int32 [B]
+    c: kivi_paged_cache
+
+    @classmethod
+    def allocate(cls, B: int, Hkv: int, G: int, page_tokens: int, max_pages_per_seq: int, num_pages: int,
+                 device="cuda", D: int = 128) -> "PagedCache":
+        dims = make_paged_dims(B, Hkv, G, page_tokens, max_pages_per_seq, num_pages, D)
+        kivi_paged_buffer_bytes(dims)  # validates the geometry
+        P = page_tokens
+        kc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
+        km = torch.empty((num_pages, Hkv, P // G, D), dtype=torch.int32, device=device)
+        vc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
+        vm = torch.empty((num_pages, Hkv, P), dtype=torch.int32, device=device)
+        kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
+        bt = torch.zeros((B, max_pages_per_seq), dtype=torch.int32, device=device)
+        sl = torch.zeros((B,), dtype=torch.int32, device=device)
+        c = kivi_paged_cache(kc.data_ptr(), km.data_ptr(), vc.data_ptr(), vm.data_ptr(), kr.data_ptr(),
+                             bt.data_ptr(), sl.data_ptr())
+        return cls(dims, kc, km, vc, vm, kr, bt, sl, c)
+
+
+def kivi_paged_prefill(cache: PagedCache, seq: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    """Prompt of sequence `seq`: k, v fp16 [Hkv, n, D] on the device."""
+    _f16(k, "k"), _f16(v, "v")
+    _check(lib().kivi_paged_prefill(ctypes.byref(cache.dims), ctypes.byref(cache.c), seq, _ptr(k), _ptr(v),
+                                    k.shape[1], _stream(stream)), "kivi_paged_prefill")
+
+
+def kivi_paged_append_token(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+    """k_new, v_new: fp16 [B, Hkv, D] on the device."""
+    _f16(k_new, "k_new"), _f16(v_new, "v_new")
+    _check(lib().kivi_paged_append_token(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new),
+                                         _stream(stream)), "kivi_paged_append_token")
+
+
+def kivi_paged_decode_workspace_bytes(dims: kivi_paged_dims, Hq: int) -> int:
+    return int(lib().kivi_paged_decode_workspace_bytes(ctypes.byref(dims), Hq))
+
+
+def paged_workspace(cache: PagedCache, Hq: int, device="cuda") -> torch.Tensor:
+    nbytes = kivi_paged_decode_workspace_bytes(cache.dims, Hq)
+    if nbytes == 0:
+        raise KiviError(KIVI_ERR_ARG, "kivi_paged_decode_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def kivi_paged_decode_attention(cache: PagedCache, q: torch.Tensor, softmax_scale: float,
+                                out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                                stream=None) -> torch.Tensor:
+    """q: fp16 [B, Hq, D] -> out fp16 [B, Hq, D], each sequence over its own length."""
+    _f16(q, "q")
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = paged_workspace(cache, Hq, device=q.device)
+    _check(lib().kivi_paged_decode_attention(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(q), Hq,
+                                             float(softmax_scale), _ptr(out), _ptr(ws),
+                                             ws.numel() * ws.element_size(), _stream(stream)),
+           "kivi_paged_decode_attention")
+    return out
+
+
+def kivi_paged_decode_step(cache: PagedCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                           softmax_scale: float, out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Append (k_new, v_new fp16 [B, Hkv, D]) at every sequence's length, attend with
+    q fp16 [B, Hq, D], advance the lengths."""
+    _f16(k_new, "k_new"), _f16(v_new, "v_new"), _f16(q, "q")
+    Hq = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        ws = paged_workspace(cache, Hq, device=q.device)
+    _check(lib().kivi_paged_decode_step(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(k_new), _ptr(v_new),
+                                        _ptr(q), Hq, float(softmax_scale), _ptr(out), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)), "kivi_paged_decode_step")
+    return out

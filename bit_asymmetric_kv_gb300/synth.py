@@ -121,3 +121,13 @@ def small(name: str, B: int, Hq: int, Hkv: int, G: int, n: int, seed: int, steps
     """A reduced workload with the same distributions, for oracle-sized parity cases."""
     return Workload(name, B=B, Hq=Hq, Hkv=Hkv, D=128, G=G, n=n, steps=steps, outliers=outliers,
                     factor_lo=factor_lo, factor_hi=factor_hi, seed=seed)
+
+
+def block_table(B: int, max_pages_per_seq: int, num_pages: int, seed: int) -> torch.Tensor:
+    """int32 [B, max_pages_per_seq]: distinct pages of a pool of num_pages, drawn in a
+    seeded random order, so that consecutive positions of a sequence sit in scattered
+    pages as in a serving engine's pool after many allocations and frees."""
+    if B * max_pages_per_seq > num_pages:
+        raise ValueError("the pool holds fewer pages than the block table needs")
+    perm = torch.randperm(num_pages, generator=_gen(seed * 7_919 + 3))
+    return perm[: B * max_pages_per_seq].reshape(B, max_pages_per_seq).to(torch.int32)

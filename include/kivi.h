@@ -198,6 +198,111 @@ KIVI_API int kivi_decode_attention_noalloc(const kivi_dims *dims, const kivi_cac
                                            const uint16_t *q, int32_t Hq, float softmax_scale,
                                            uint16_t *out, cudaStream_t stream);
 
+/*
+ * ---- Paged cache -------------------------------------------------------------------
+ * The same 2-bit cache, with token storage split into fixed-size pages drawn from one
+ * pool and found through a per-sequence block table, as serving engines keep KV
+ * caches; sequences of a batch may have different lengths.  The page notes that
+ * KIVI's grouped residual and layout do not fit a paged block manager as they are,
+ * and that serving engines need paged 2-bit kernels for it (section "Kod ve
+ * Entegrasyon Haritasi", paragraph 3).  The method itself is unchanged: per-channel
+ * key groups of G tokens with an fp16 residual, per-token values, the same codes,
+ * scales and packing as above.
+ *
+ * A page holds P consecutive token positions of one sequence for all Hkv KV heads.
+ * P (page_tokens) is a power of two and a multiple of 64, so a page holds whole key
+ * groups.  Device buffers (caller-owned, 16-byte aligned):
+ *   k_codes      uint32 [num_pages][Hkv][P][D/16]   token rows of packed key codes
+ *   k_meta       uint32 [num_pages][Hkv][P/G][D]    per (group, channel) {s, z}
+ *   v_codes      uint32 [num_pages][Hkv][P][D/16]   token rows of packed value codes
+ *   v_meta       uint32 [num_pages][Hkv][P]         per token {s, z}
+ *   k_res        fp16   [B][Hkv][G][D]              residual keys of sequence b
+ *   block_table  int32  [B][max_pages_per_seq]      page of positions j*P .. j*P+P-1
+ *   seq_lens     int32  [B]                         tokens held by sequence b
+ * Position t of sequence b is row t mod P of page block_table[b][t / P].  The block
+ * table and the lengths live on the device and are the caller's: the caller assigns
+ * pages before a call needs them (a sequence at length n needs pages for positions
+ * 0 .. n, the next token included) and reads seq_lens back only when it needs them.
+ * The host sees neither, so the kernels guard them instead of the host: a length is
+ * clamped to [0, max_pages_per_seq * P]; a token appended to a full sequence, or to
+ * a position whose page id lies outside [0, num_pages), is dropped; a page id outside
+ * the pool that attention reads is clamped into it (results undefined, no access
+ * outside the buffers).  A sequence of length 0 attends to nothing: its output rows
+ * are zero.  B <= 512.
+ */
+typedef struct {
+  int32_t B;                  /* sequences (rows of the block table) */
+  int32_t Hkv;                /* KV heads */
+  int32_t D;                  /* head dim, 128 */
+  int32_t G;                  /* key group size, 32 or 64 */
+  int32_t bits;               /* code width, 2 */
+  int32_t page_tokens;        /* P: a power of two, >= 64 */
+  int32_t max_pages_per_seq;  /* columns of the block table */
+  int64_t num_pages;          /* pages in the pool */
+} kivi_paged_dims;
+
+typedef struct {
+  uint32_t *k_codes;
+  uint32_t *k_meta;
+  uint32_t *v_codes;
+  uint32_t *v_meta;
+  uint16_t *k_res;
+  const int32_t *block_table;
+  int32_t *seq_lens;
+} kivi_paged_cache;
+
+/* Bytes of the pool and per-sequence buffers, in the order k_codes, k_meta, v_codes,
+ * v_meta, k_res, block_table, seq_lens.  Pure host arithmetic. */
+KIVI_API int kivi_paged_buffer_bytes(const kivi_paged_dims *dims, size_t out_bytes[7]);
+
+/*
+ * Quantize the prompt of sequence `seq` (0 <= seq < B) into its pages, as
+ * kivi_quantize_prefill does for one batch row: k, v fp16 [Hkv][n][D] device; the
+ * keys of floor(n/G) groups are quantized per channel, the last n mod G keys go to
+ * the sequence's residual, all n values are quantized per token.  Then sets
+ * seq_lens[seq] = n on the device (stream-ordered).  n > max_pages_per_seq * P:
+ * KIVI_ERR_CAPACITY.  Other sequences are not touched.
+ */
+KIVI_API int kivi_paged_prefill(const kivi_paged_dims *dims, const kivi_paged_cache *cache, int32_t seq,
+                                const uint16_t *k, const uint16_t *v, int64_t n, cudaStream_t stream);
+
+/*
+ * Append one token to every sequence, at position seq_lens[b] (section "Iddia ve
+ * Gerceklik", paragraph 3): k_new, v_new fp16 [B][Hkv][D] device.  The value is
+ * quantized at once; the key goes to residual slot seq_lens[b] mod G, and a
+ * sequence whose residual fills has its group quantized in the same kernel.  Then
+ * seq_lens[b] += 1 on the device (capped at the capacity).
+ */
+KIVI_API int kivi_paged_append_token(const kivi_paged_dims *dims, const kivi_paged_cache *cache,
+                                     const uint16_t *k_new, const uint16_t *v_new, cudaStream_t stream);
+
+/* Workspace bytes of the paged decode calls for these sizes on the current device
+ * (independent of the lengths).  0 on bad arguments. */
+KIVI_API size_t kivi_paged_decode_workspace_bytes(const kivi_paged_dims *dims, int32_t Hq);
+
+/*
+ * kivi_decode_attention over the paged cache, each sequence over its own
+ * seq_lens[b] tokens: q, out fp16 [B][Hq][D] device; ws of at least
+ * kivi_paged_decode_workspace_bytes() bytes, contents overwritten.  The context of
+ * all sequences is split evenly between the GPU's warps on the device (the host
+ * does not know the lengths).
+ */
+KIVI_API int kivi_paged_decode_attention(const kivi_paged_dims *dims, const kivi_paged_cache *cache,
+                                         const uint16_t *q, int32_t Hq, float softmax_scale, uint16_t *out,
+                                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * One whole paged decode step: append k_new, v_new at position seq_lens[b] of every
+ * sequence, attend with q over the seq_lens[b] + 1 tokens, then seq_lens[b] += 1
+ * (capped at the capacity).  The attention overlaps the append as in
+ * kivi_decode_step.  Arguments as kivi_paged_append_token and
+ * kivi_paged_decode_attention.
+ */
+KIVI_API int kivi_paged_decode_step(const kivi_paged_dims *dims, const kivi_paged_cache *cache,
+                                    const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q, int32_t Hq,
+                                    float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes,
+                                    cudaStream_t stream);
+
 /* Human-readable name of a kivi_status. */
 KIVI_API const char *kivi_status_string(int status);
 

@@ -119,3 +119,75 @@ def test_decode_argument_checks(L):
     assert call(c) == kivi.KIVI_ERR_ARG
     assert L.kivi_decode_splits(ctypes.byref(d), 6, 10) == 0
     assert L.kivi_decode_workspace_bytes(ctypes.byref(d), 8, 0) == 0
+
+
+# ---- paged cache: geometry and argument checks on the host --------------------------
+def _pdims(**kw):
+    d = dict(B=3, Hkv=4, D=128, G=32, bits=2, page_tokens=64, max_pages_per_seq=5, num_pages=20)
+    d.update(kw)
+    return kivi.kivi_paged_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["page_tokens"],
+                                d["max_pages_per_seq"], d["num_pages"])
+
+
+def _pcache(align=0, bt_align=0):
+    return kivi.kivi_paged_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, FAKE + bt_align, FAKE)
+
+
+def test_paged_buffer_bytes(L):
+    out = kivi.kivi_paged_buffer_bytes(_pdims(B=3, Hkv=5, G=64, page_tokens=128, max_pages_per_seq=7, num_pages=11))
+    rows = 11 * 5 * 128
+    assert out == [rows * 32, rows // 64 * 128 * 4, rows * 32, rows * 4, 3 * 5 * 64 * 128 * 2, 3 * 7 * 4, 3 * 4]
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(G=16), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(page_tokens=96), kivi.KIVI_ERR_UNSUPPORTED),       # not a power of two
+    (dict(page_tokens=32), kivi.KIVI_ERR_UNSUPPORTED),       # below one 64-token unit
+    (dict(B=513), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(max_pages_per_seq=1 << 25), kivi.KIVI_ERR_UNSUPPORTED),  # capacity beyond int32 positions
+    (dict(B=0), kivi.KIVI_ERR_ARG),
+    (dict(num_pages=0), kivi.KIVI_ERR_ARG),
+    (dict(max_pages_per_seq=0), kivi.KIVI_ERR_ARG),
+])
+def test_bad_paged_dims(L, kw, status):
+    d = _pdims(**kw)
+    out = (ctypes.c_size_t * 7)()
+    assert L.kivi_paged_buffer_bytes(ctypes.byref(d), out) == status
+    c = _pcache()
+    assert L.kivi_paged_prefill(ctypes.byref(d), ctypes.byref(c), 0, FAKE, FAKE, 10, None) == status
+    assert L.kivi_paged_append_token(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, None) == status
+    assert L.kivi_paged_decode_workspace_bytes(ctypes.byref(d), 8) == 0
+
+
+def test_paged_prefill_checks(L):
+    d = _pdims()
+    c = _pcache()
+    pre = lambda seq=0, k=FAKE, n=10, c=c: L.kivi_paged_prefill(  # noqa: E731
+        ctypes.byref(d), ctypes.byref(c), seq, k, FAKE, n, None)
+    assert pre(seq=3) == kivi.KIVI_ERR_ARG            # sequence out of range
+    assert pre(seq=-1) == kivi.KIVI_ERR_ARG
+    assert pre(n=-1) == kivi.KIVI_ERR_ARG
+    assert pre(n=5 * 64 + 1) == kivi.KIVI_ERR_CAPACITY
+    assert pre(k=None) == kivi.KIVI_ERR_ARG
+    assert pre(k=FAKE + 2) == kivi.KIVI_ERR_ALIGN
+    assert pre(c=_pcache(align=4)) == kivi.KIVI_ERR_ALIGN
+    assert pre(c=_pcache(bt_align=2)) == kivi.KIVI_ERR_ALIGN
+    null = kivi.kivi_paged_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE)
+    assert pre(c=null) == kivi.KIVI_ERR_ARG
+
+
+def test_paged_decode_argument_checks(L):
+    d = _pdims()
+    c = _pcache()
+    att = lambda Hq=8, q=FAKE, out=FAKE: L.kivi_paged_decode_attention(  # noqa: E731
+        ctypes.byref(d), ctypes.byref(c), q, Hq, 1.0, out, FAKE, 1 << 30, None)
+    assert att(Hq=6) == kivi.KIVI_ERR_UNSUPPORTED
+    assert att(Hq=32) == kivi.KIVI_ERR_UNSUPPORTED
+    assert att(q=None) == kivi.KIVI_ERR_ARG
+    assert att(out=FAKE + 6) == kivi.KIVI_ERR_ALIGN
+    step = lambda k=FAKE, Hq=8: L.kivi_paged_decode_step(  # noqa: E731
+        ctypes.byref(d), ctypes.byref(c), k, FAKE, FAKE, Hq, 1.0, FAKE, FAKE, 1 << 30, None)
+    assert step(k=None) == kivi.KIVI_ERR_ARG
+    assert step(k=FAKE + 4) == kivi.KIVI_ERR_ALIGN
+    assert step(Hq=12) == kivi.KIVI_ERR_UNSUPPORTED
