@@ -14,6 +14,10 @@ count reset, residual keys restored; outside the timed events), so the context
 stays within 4113 .. 4176 tokens however many steps run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
+                  [--layout dense|paged [--page-tokens P]] [--compare-fp16]
+
+--layout paged runs the same workload through the paged cache (pages of P tokens
+from one pool, scattered by a seeded permutation; lengths on the device).
 
 --impl reference times the CPU oracle (plain C, the host's cores) on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -60,10 +64,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
 
 
-def profiled_traffic(kernel_sha: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "decode_attention_llama2-7b-mha.md")
+def profiled_traffic(kernel_sha: str, profile: str):
+    """DRAM bytes per decode launch from the committed ncu summary `profile`, if it
+    was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", profile)
     try:
         lines = open(path).read().splitlines()
     except OSError:
@@ -220,11 +224,88 @@ def run_reference(args, wl):
 
 
 def workload_config(wl):
-    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
-            "context_tokens": f"{wl.n}..{wl.n + CYCLE} (cache rolled back every {CYCLE} steps)", "step": "append_token + decode_attention (one new token per sequence)",
-            "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
-            "api": "kivi_decode_step (append + decode attention, the attention overlapping the append)",
-            "parallelism": "replicas (one independent cache per GPU)"}
+    cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
+           "context_tokens": f"{wl.n}..{wl.n + CYCLE} (cache rolled back every {CYCLE} steps)",
+           "step": "append_token + decode_attention (one new token per sequence)",
+           "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
+           "api": "kivi_decode_step (append + decode attention, the attention overlapping the append)",
+           "parallelism": "replicas (one independent cache per GPU)", "layout": "dense"}
+    return cfg
+
+
+# ----------------------------------------------------------------------------------------
+# cache layouts: the same workload in the dense cache or in a paged pool
+# ----------------------------------------------------------------------------------------
+class DenseLayout:
+    """The dense cache [B][Hkv][max_tokens]: kivi_decode_step / kivi_decode_attention."""
+
+    profile = "decode_attention_llama2-7b-mha.md"
+    kernel = "kivi_decode_attention (decode_kernel + combine_kernel)"
+
+    def __init__(self, wl, pre, dev):
+        from bit_asymmetric_kv_gb300 import kivi
+
+        self.wl, self.kivi = wl, kivi
+        self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=CYCLE + 64), device=dev)
+        kivi.kivi_quantize_prefill(self.cache, pre.k.to(dev), pre.v.to(dev))
+        self.n0 = self.cache.n_tokens
+        self.res0 = self.cache.k_res.clone()
+        self.ws = cycle_workspace(self.cache, wl, self.n0, dev)
+
+    def rollback(self):
+        self.cache.k_res.copy_(self.res0)
+        self.cache.c.n_tokens = self.n0
+
+    def step(self, k, v, q, out, stream):
+        """Returns the number of kernels the step launched."""
+        n = self.cache.n_tokens
+        self.kivi.kivi_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws, stream=stream)
+        # append (+ group flush every G steps), decode attention, combine
+        return 1 + (1 if (n % self.wl.G) + 1 == self.wl.G else 0) + 2
+
+    def attention(self, q, out, stream):
+        self.kivi.kivi_decode_attention(self.cache, q, 1.0, out=out, ws=self.ws, stream=stream)
+
+
+class PagedLayout:
+    """The paged pool: pages of P tokens scattered by a seeded permutation, lengths on
+    the device: kivi_paged_decode_step / kivi_paged_decode_attention."""
+
+    profile = "decode_attention_paged_llama2-7b-mha.md"
+    kernel = "kivi_paged_decode_attention (paged decode_kernel + paged_combine_kernel)"
+
+    def __init__(self, wl, pre, dev, page_tokens):
+        from bit_asymmetric_kv_gb300 import kivi, synth
+
+        self.wl, self.kivi, self.P = wl, kivi, page_tokens
+        maxp = math.ceil((wl.n + CYCLE + 64) / page_tokens)
+        num_pages = wl.B * maxp
+        self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev)
+        self.cache.block_table.copy_(synth.block_table(wl.B, maxp, num_pages, wl.seed))
+        for b in range(wl.B):
+            kivi.kivi_paged_prefill(self.cache, b, pre.k[b].to(dev), pre.v[b].to(dev))
+        self.n0 = wl.n
+        self.lens0 = self.cache.seq_lens.clone()
+        self.res0 = self.cache.k_res.clone()
+        self.ws = kivi.paged_workspace(self.cache, wl.Hq, device=dev)
+        self.ws.zero_()
+
+    def rollback(self):
+        self.cache.k_res.copy_(self.res0)
+        self.cache.seq_lens.copy_(self.lens0)
+
+    def step(self, k, v, q, out, stream):
+        self.kivi.kivi_paged_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws, stream=stream)
+        return 3  # append (group flush fused), decode attention, combine (advances the lengths)
+
+    def attention(self, q, out, stream):
+        self.kivi.kivi_paged_decode_attention(self.cache, q, 1.0, out=out, ws=self.ws, stream=stream)
+
+
+def make_layout(args, wl, pre, dev):
+    if args.layout == "paged":
+        return PagedLayout(wl, pre, dev, args.page_tokens)
+    return DenseLayout(wl, pre, dev)
 
 
 # ----------------------------------------------------------------------------------------
@@ -252,34 +333,24 @@ def run_kivi(args, wl):
     kivi.lib()
     pre = synth.make_prefill(wl)
     total = args.warmup + args.steps
-    T = wl.capacity(extra=CYCLE + 64)
-    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
-    kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
-    n0 = cache.n_tokens
-    res0 = cache.k_res.clone()
+    lay = make_layout(args, wl, pre, dev)
+    n0 = lay.n0
     # the inputs of one rollback cycle, resident in HBM before timing
     dev_in = [tuple(t.to(dev) for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
-    ws = cycle_workspace(cache, wl, n0, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def rollback():
-        cache.k_res.copy_(res0)
-        cache.c.n_tokens = n0
-
     def step_events(i, rec):
         if i % CYCLE == 0:
-            rollback()
+            lay.rollback()
         k, v, q = dev_in[i % CYCLE]
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_before = cache.n_tokens
         e0.record(stream)
-        kivi.kivi_decode_step(cache, k, v, q, 1.0, out=out, ws=ws, stream=stream)
+        launches = lay.step(k, v, q, out, stream)
         e1.record(stream)
-        # append (+ group flush every G steps), decode attention, combine
-        rec.append((e0, e1, cache.n_tokens, 1 + (1 if (n_before % wl.G) + 1 == wl.G else 0) + 2))
+        rec.append((e0, e1, launches))
 
     warm = []
     for i in range(args.warmup):
@@ -295,20 +366,20 @@ def run_kivi(args, wl):
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier()
-    launches = sum(x[3] for x in rec)
-    step_ms = [e0.elapsed_time(e1) for e0, e1, _, _ in rec]
+    launches = sum(x[2] for x in rec)
+    step_ms = [e0.elapsed_time(e1) for e0, e1, _ in rec]
     ms_per_step, value = job_throughput(sum(step_ms) / len(step_ms), wl.B, world, dev)
 
-    # roofline of the dominant kernel: kivi_decode_attention (decode + combine) alone,
-    # on the prompt's cache, timed the same way
-    rollback()
+    # roofline of the dominant kernel: the decode attention call (decode + combine)
+    # alone, on the prompt's cache, timed the same way
+    lay.rollback()
     attn_ms = []
     q0 = dev_in[0][2]
     for i in range(args.warmup + max(16, args.steps // 8)):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        kivi.kivi_decode_attention(cache, q0, 1.0, out=out, ws=ws, stream=stream)
+        lay.attention(q0, out, stream)
         e1.record(stream)
         if i >= args.warmup:
             attn_ms.append((e0, e1))
@@ -318,7 +389,8 @@ def run_kivi(args, wl):
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
-    traffic = profiled_traffic(sha)
+    traffic = profiled_traffic(sha, lay.profile)
+    del lay
 
     # ---- end to end through the public API: host buffers, copies inside the timing
     e2e = e2e_run(args, wl, pre, dev, stream, flush)
@@ -330,13 +402,14 @@ def run_kivi(args, wl):
             dist.destroy_process_group()
         return 0
     cb = oracle_timing(wl, pre, 64, 32, 2.0) if world == 1 else None
+    lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u2 codes, f16 q/out, f32 accumulate", "data": "synthetic (seeded, fixed outlier key channels)",
-        "config": workload_config(wl),
+        "config": {**workload_config(wl), **lay_cfg},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "kivi_decode_attention (decode_kernel + combine_kernel)",
+                     "traffic": traffic, "kernel": (PagedLayout if args.layout == "paged" else DenseLayout).kernel,
                      "peak_source": peak_src, "attention_ms": attn_avg_ms,
                      "algorithmic_bytes_per_launch": bytes_attn, "context_tokens": n0,
                      "kernel_source_sha256": sha},
@@ -352,6 +425,13 @@ def run_kivi(args, wl):
 
         dist.destroy_process_group()
     return 0
+
+
+def make_layout_config(args):
+    if args.layout == "paged":
+        return {"layout": f"paged: {args.page_tokens} tokens per page, pages scattered by a seeded permutation",
+                "api": "kivi_paged_decode_step (append + decode attention + length advance)"}
+    return {"layout": "dense"}
 
 
 def cycle_workspace(cache, wl, n0, dev):
@@ -370,26 +450,20 @@ def e2e_run(args, wl, pre, dev, stream, flush):
     the output back; the copies are inside the timed events."""
     import torch
 
-    from bit_asymmetric_kv_gb300 import kivi, synth
+    from bit_asymmetric_kv_gb300 import synth
 
     total = args.warmup + args.steps
-    T = wl.capacity(extra=CYCLE + 64)
-    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, device=dev)
-    kivi.kivi_quantize_prefill(cache, pre.k.to(dev), pre.v.to(dev))
-    n0 = cache.n_tokens
-    res0 = cache.k_res.clone()
+    lay = make_layout(args, wl, pre, dev)
     host = [tuple(t.pin_memory() for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
     dk = torch.empty_like(host[0][0], device=dev)
     dv = torch.empty_like(host[0][1], device=dev)
     dq = torch.empty_like(host[0][2], device=dev)
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     out_h = torch.empty_like(out, device="cpu").pin_memory()
-    ws = cycle_workspace(cache, wl, n0, dev)
     times = []
     for i in range(total):
         if i % CYCLE == 0:
-            cache.k_res.copy_(res0)
-            cache.c.n_tokens = n0
+            lay.rollback()
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         hk, hv, hq = host[i % CYCLE]
@@ -397,7 +471,7 @@ def e2e_run(args, wl, pre, dev, stream, flush):
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
         dq.copy_(hq, non_blocking=True)
-        kivi.kivi_decode_step(cache, dk, dv, dq, 1.0, out=out, ws=ws, stream=stream)
+        lay.step(dk, dv, dq, out, stream)
         out_h.copy_(out, non_blocking=True)
         e1.record(stream)
         if i >= args.warmup:
@@ -471,6 +545,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kivi", "reference"], default="kivi")
     ap.add_argument("--compare-fp16", action="store_true",
                     help="time the long-context GQA step over the 2-bit and an fp16 cache instead")
+    ap.add_argument("--layout", choices=["dense", "paged"], default="dense",
+                    help="cache layout of the timed path (default: the dense cache)")
+    ap.add_argument("--page-tokens", type=int, default=64, help="tokens per page of --layout paged")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -86,3 +86,65 @@ def test_full_size_streaming():
     torch.cuda.synchronize()
     for (b, kvh), orc in orcs.items():
         check_head(gpu, orc, b, kvh)
+
+
+def check_paged_head(gpu: kivi.PagedCache, bt: np.ndarray, orc: oracle.Cache, b: int, kvh: int) -> None:
+    """Sequence b, KV head kvh of the paged pool, gathered row by row through the
+    block table, against the oracle's dense cache of that head."""
+    n, G, P = orc.n, orc.G, gpu.dims.page_tokens
+    ng, nq = n // G, (n // G) * G
+    t = np.arange(n)
+    pages, rows = bt[b, t // P], t % P
+    tg = np.arange(ng) * G
+    kc = u32(gpu.k_codes[:, kvh])
+    km = u32(gpu.k_meta[:, kvh])
+    vc = u32(gpu.v_codes[:, kvh])
+    vm = u32(gpu.v_meta[:, kvh])
+    assert np.array_equal(kc[pages[:nq], rows[:nq]], orc.k_codes[0, 0, :nq])
+    assert np.array_equal(km[bt[b, tg // P], (tg % P) // G], orc.k_meta[0, 0, :ng])
+    assert np.array_equal(u16(gpu.k_res[b, kvh, :n - nq]), orc.k_res[0, 0, :n - nq])
+    assert np.array_equal(vc[pages, rows], orc.v_codes[0, 0, :n])
+    assert np.array_equal(vm[pages, rows], orc.v_meta[0, 0, :n])
+
+
+@pytest.mark.parametrize("idx,P", [(1, 64), (2, 256)], ids=["llama2-p64", "mistral-gqa-p256"])
+def test_full_size_paged_decode_steps(idx, P):
+    """The full-size workload in the paged pool (scattered pages), in the benchmark's
+    launch configuration: paged prefill of every sequence, attention over the prompt,
+    then decode steps across a key-group flush; sampled heads against the oracle."""
+    wl = synth.CONFIGS[idx]
+    pre = synth.make_prefill(wl)
+    steps = wl.G + 3
+    maxp = -(-(wl.n + steps + 1) // P)
+    num_pages = wl.B * maxp
+    gpu = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, P, maxp, num_pages)
+    bt = synth.block_table(wl.B, maxp, num_pages, wl.seed)
+    gpu.block_table.copy_(bt)
+    bt = bt.numpy()
+    for b in range(wl.B):
+        kivi.kivi_paged_prefill(gpu, b, pre.k[b].cuda(), pre.v[b].cuda())
+    T = maxp * P
+    R = wl.Hq // wl.Hkv
+    heads = sample_heads(wl, k=3, seed=5)
+    orcs = {h: oracle.prefill_head(pre.k[h[0], h[1]].numpy(), pre.v[h[0], h[1]].numpy(), wl.G, T) for h in heads}
+    out = kivi.kivi_paged_decode_attention(gpu, pre.q.cuda(), 1.0)
+    torch.cuda.synchronize()
+    for (b, kvh), orc in orcs.items():
+        check_paged_head(gpu, bt, orc, b, kvh)
+        ref = np.stack([oracle.attention_head(orc, 0, 0, pre.q[b, kvh * R + j].numpy(), 1.0) for j in range(R)])
+        assert_close(out[b, kvh * R:(kvh + 1) * R], ref)
+    ws = kivi.paged_workspace(gpu, wl.Hq)
+    for step in range(steps):
+        k_new, v_new, q = synth.make_step(wl, pre, step)
+        out = kivi.kivi_paged_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, ws=ws)
+        for (b, kvh), orc in orcs.items():
+            oracle.append(orc, k_new[b, kvh][None, None].numpy().copy(), v_new[b, kvh][None, None].numpy().copy())
+        if step in (0, steps - 4, steps - 3, steps - 1):
+            torch.cuda.synchronize()
+            for (b, kvh), orc in orcs.items():
+                ref = np.stack([oracle.attention_head(orc, 0, 0, q[b, kvh * R + j].numpy(), 1.0) for j in range(R)])
+                assert_close(out[b, kvh * R:(kvh + 1) * R], ref)
+    torch.cuda.synchronize()
+    assert gpu.seq_lens.cpu().tolist() == [wl.n + steps] * wl.B
+    for (b, kvh), orc in orcs.items():
+        check_paged_head(gpu, bt, orc, b, kvh)
