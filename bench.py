@@ -1,20 +1,21 @@
 #!/usr/bin/env python3
 """Decode-step benchmark of the KIVI 2-bit KV cache on GB300.
 
-Workload: Llama-2-7B-shaped MHA decode (batch 8, 32 heads, head dim 128, context
-4096 + 17 tokens, key groups of G = 32, 2-bit codes), seeded synthetic fp16 K/V
-with fixed outlier key channels.  The cache is quantized once (untimed); one step
-is the whole hot path for one new token per sequence: kivi_append_token (value
-quantization, residual write, group flush every 32 steps) + kivi_decode_attention
-(fused 2-bit decode attention + split combine).  The metric is decode tokens/s
-(batch / step time) with the attention kernel's achieved HBM GB/s against the
-measured copy bandwidth.  L2 is flushed (256 MiB write) before every step, outside
-the timed events.  Every 64 steps the cache is rolled back to the prompt (token
-count reset, residual keys restored; outside the timed events), so the context
-stays within 4113 .. 4176 tokens however many steps run.
+Workload (default; --workload picks another of the five): Llama-2-7B-shaped MHA
+decode (batch 8, 32 heads, head dim 128, context 4096 + 17 tokens, key groups of
+G = 32, 2-bit codes), seeded synthetic fp16 K/V with fixed outlier key channels.
+The cache is quantized once (untimed); one step is the whole hot path for one new
+token per sequence: append (value quantization, residual write, group flush every
+G steps) + fused 2-bit decode attention + split combine, through kivi_decode_step.
+The metric is decode tokens/s (batch / step time) with the attention call's
+achieved HBM GB/s against the measured copy bandwidth.  L2 is flushed (256 MiB
+write) before every step, outside the timed events.  Every 64 steps the cache is
+rolled back to the prompt (token count reset, residual keys restored; outside the
+timed events), so the context stays within n .. n + 64 tokens however many steps
+run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
-                  [--layout dense|paged [--page-tokens P]] [--compare-fp16]
+                  [--workload NAME] [--layout dense|paged [--page-tokens P]] [--compare-fp16]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
 from one pool, scattered by a seeded permutation; lengths on the device).
@@ -369,6 +370,7 @@ def run_kivi(args, wl):
     launches = sum(x[2] for x in rec)
     step_ms = [e0.elapsed_time(e1) for e0, e1, _ in rec]
     ms_per_step, value = job_throughput(sum(step_ms) / len(step_ms), wl.B, world, dev)
+    q50, q99 = np.percentile(step_ms, [50, 99])
 
     # roofline of the dominant kernel: the decode attention call (decode + combine)
     # alone, on the prompt's cache, timed the same way
@@ -405,7 +407,7 @@ def run_kivi(args, wl):
     lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_per_step, "step_ms_p50": float(q50), "step_ms_p99": float(q99), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u2 codes, f16 q/out, f32 accumulate", "data": "synthetic (seeded, fixed outlier key channels)",
         "config": {**workload_config(wl), **lay_cfg},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -548,12 +550,18 @@ def main(argv=None):
     ap.add_argument("--layout", choices=["dense", "paged"], default="dense",
                     help="cache layout of the timed path (default: the dense cache)")
     ap.add_argument("--page-tokens", type=int, default=64, help="tokens per page of --layout paged")
+    ap.add_argument("--workload", default="llama2",
+                    help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
+                         "default: the Llama-2-7B MHA decode")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from bit_asymmetric_kv_gb300 import synth
 
-    wl = synth.LLAMA2_7B_MHA
+    hits = [w for w in synth.CONFIGS if w.name.startswith(args.workload)]
+    if len(hits) != 1:
+        ap.error(f"--workload {args.workload!r}: choose one of {[w.name for w in synth.CONFIGS]}")
+    wl = hits[0]
     if args.compare_fp16:
         return run_compare(args)
     if args.impl == "reference":
