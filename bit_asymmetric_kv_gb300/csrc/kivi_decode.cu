@@ -28,7 +28,7 @@
 // head) -- one or two key groups -- plus one unit for the fp16 residual keys when
 // n mod G > 0.  The grid holds exactly as many warps as fit on the GPU at once; warp
 // w takes the contiguous unit range [w*W/NW, (w+1)*W/NW), staging each unit (codes,
-// scales, zeros) in its shared memory with cp.async one unit ahead, and runs an
+// scales, zeros) in its shared memory with cp.async two units ahead, and runs an
 // online softmax over it.  At every head boundary the warp writes a partial (max,
 // sum, unnormalised output) to the workspace; the combine kernel merges a head's
 // partials (flash-decoding) and is launched as a programmatic dependent.
@@ -51,6 +51,12 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
+// Units staged ahead of the one being computed (at most kStages - 1).
+#ifndef KIVI_DECODE_AHEAD
+#define KIVI_DECODE_AHEAD 2
+#endif
+constexpr int kAhead = KIVI_DECODE_AHEAD;
+static_assert(kAhead >= 1 && kAhead < kStages, "the ring must hold the computed unit and the staged ones");
 constexpr int kUnit = 64;                            // tokens per unit
 constexpr int kFragRowWords = 20;                    // 16 B-fragment words + 4 pad (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -162,16 +168,17 @@ struct SoftState {
 // Max over the lanes that share this lane's query head.
 template <int R>
 __device__ __forceinline__ float head_max(float x) {
-  if (R == 1) {
+  if constexpr (R == 1) {
     // one head per warp: an order-preserving integer key and one warp reduction
     const int k = __float_as_int(x);
     const int key = k ^ ((k >> 31) & 0x7fffffff);
     const int mk = __reduce_max_sync(0xffffffffu, key);
     return __int_as_float(mk ^ ((mk >> 31) & 0x7fffffff));
-  }
+  } else {
 #pragma unroll
-  for (int off = R; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
-  return x;
+    for (int off = R; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    return x;
+  }
 }
 
 // q.K side of one softmax step over T = 4/R tiles of 16 tokens.
@@ -558,61 +565,12 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       for (int k = 0; k < 4; ++k) qv[hh][k] = h2f(qh[hh * kD + 32 * k]);
   };
 
-  // The P.V of unit k runs in iteration k+1, after the q.K side of unit k+1, so
-  // the two independent chains interleave.  Carried between iterations:
-  uint32_t pw0[R], pw1[R];   // P.V B operands per step of the pending unit
-  float palpha[R];           // their rescale factors
-  int p_kind = 0;            // 0 none, 1 codes (stage p_stage), 2 residual
-  int p_ntok = 0, p_stage = 0;
-  int64_t p_h = -1;
-  int64_t p_res_row = 0;     // value row of the pending residual unit's first token
-  SoftState p_fin;           // softmax state to emit with once the pending unit is added
-  bool p_emit = false;
-#pragma unroll
-  for (int j = 0; j < R; ++j) {
-    pw0[j] = pw1[j] = 0u;
-    palpha[j] = 1.f;
-  }
-
-  auto pv_pending = [&]() {
-    if (p_kind == 1) {
-      const unsigned char *stg = wbase + p_stage * L::kStageBytes;
-#pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int nv = min(16 * T, p_ntok - 16 * T * s);
-        if (nv <= 0) break;
-        pv_step<R>(acc, li, nv, pw0[s], pw1[s], palpha[s], [&](int i, int k) -> uint32_t {
-          return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
-        });
-      }
-    } else if (p_kind == 2) {
-      int64_t res_row;
-      if constexpr (PAGED)
-        res_row = p_res_row;
-      else
-        res_row = p_h * a.max_tokens + (int64_t)cc.NG * G;  // one geometry for all heads
-      const uint32_t *vc_head = a.v_codes + res_row * kWordsPerRow;
-#pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int nv = min(16 * T, p_ntok - 16 * T * s);
-        if (nv <= 0) break;
-        pv_step<R>(acc, li, nv, pw0[s], pw1[s], palpha[s], [&](int i, int k) -> uint32_t {
-          const int slot = 16 * (s * T + i) + tig + 4 * k;
-          return vc_head[(slot < p_ntok ? slot : 0) * kWordsPerRow + g];
-        });
-      }
-    }
-    if (p_emit) {
-      emit(p_h, p_fin);
-      p_emit = false;
-    }
-  };
-
   load_q(cc);
-  issue(0);
+#pragma unroll
+  for (int kk = 0; kk < kAhead; ++kk) issue(kk);
 
   for (int kk = 0; kk < n_my; ++kk) {
-    issue(kk + 1);
+    issue(kk + kAhead);
     if constexpr (PAGED) {
       // the warp that takes a head's first unit publishes where its partials go
       if (cc.uu == 0 && lane == 0) {
@@ -621,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         hdr[cc.h] = make_int2((int)(gw + cc.h), (int)(last - gw + 1));
       }
     }
-    cp_async_wait<1>();
+    cp_async_wait<kAhead>();
     __syncwarp();
     const int stage = kk % kStages;
     uint32_t nw0[R], nw1[R];
@@ -769,123 +727,123 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       n_ntok = r;
     }
 
-    // ---- P.V of the previous unit (independent of the q.K work above)
-    pv_pending();
-
-    // this unit becomes the pending one
+    // ---- P.V of this unit: value codes from the stage, or (residual unit) from HBM
+    if (n_kind == 1) {
+      const unsigned char *stg = wbase + stage * L::kStageBytes;
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      pw0[j] = nw0[j];
-      pw1[j] = nw1[j];
-      palpha[j] = nalpha[j];
+      for (int s = 0; s < R; ++s) {
+        const int nv = min(16 * T, n_ntok - 16 * T * s);
+        if (nv <= 0) break;
+        pv_step<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
+          return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
+        });
+      }
+    } else {
+      const uint32_t *vc_head = a.v_codes + n_res_row * kWordsPerRow;
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const int nv = min(16 * T, n_ntok - 16 * T * s);
+        if (nv <= 0) break;
+        pv_step<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
+          const int slot = 16 * (s * T + i) + tig + 4 * k;
+          return vc_head[(slot < n_ntok ? slot : 0) * kWordsPerRow + g];
+        });
+      }
     }
-    p_kind = n_kind;
-    p_ntok = n_ntok;
-    if constexpr (PAGED) p_res_row = n_res_row;
-    p_stage = stage;
-    p_h = cc.h;
-    __syncwarp();
+    __syncwarp();  // this unit's stage may be refilled from now on
     if (kk + 1 < n_my) {
-      const bool head_end = cc.uu + 1 == cc.U;
-      if (head_end) {  // the next unit starts a new head
-        p_fin = ss;
-        p_emit = true;
+      if (cc.uu + 1 == cc.U) {  // the next unit starts a new head
+        emit(cc.h, ss);
         ss.m = -INFINITY;
         ss.l = 0.f;
         ss.zs = 0.f;
+        advance(cc);
+        load_q(cc);
+      } else {
+        advance(cc);
       }
-      advance(cc);
-      if (head_end) load_q(cc);
     }
   }
-  p_fin = ss;
-  p_emit = true;
-  pv_pending();
+  emit(cc.h, ss);
   cp_async_wait<0>();
 }
 
 // Merge np partials (max, sum, unnormalised output; `stride` floats apart) of one
-// (batch, query head) into out_row: one thread per channel.  The partials' maxima
-// and weights go through shared memory so every load is issued independently (the
-// partials sit in L2).  np == 0 (no tokens) writes zeros.
+// (batch, query head) into out_row with one warp: lane l owns channels 2l, 2l+1,
+// 64+2l, 64+2l+1.  Every partial's loads are issued before any is used (the
+// partials sit in L2), then an online max-rescaled sum merges them.  np == 0 (no
+// tokens) writes zeros.  Partial rows are 8-byte aligned (stride 130 floats).
 __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
-                                            uint16_t *__restrict__ out_row) {
-  __shared__ float s_w[128];
-  __shared__ float s_red[4];
-  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
-  if (np <= 0) {
-    out_row[c] = 0;
-    return;
-  }
-  // global max of the partial maxima
-  float M = -INFINITY;
-  for (int s = c; s < np; s += 128) M = fmaxf(M, __ldcg(p + (int64_t)s * stride + kD));
+                                            uint16_t *__restrict__ out_row, int lane) {
+  constexpr int kBatch = 8;
+  float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float2 ml[kBatch], lo[kBatch], hi[kBatch];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) s_red[warp] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-  float O = 0.f, L = 0.f;
-  for (int s0 = 0; s0 < np; s0 += 128) {
-    const int s = s0 + c;
-    float w = 0.f, lw = 0.f;
-    if (s < np) {
-      const float m = __ldcg(p + (int64_t)s * stride + kD);
-      w = (m == -INFINITY) ? 0.f : ex2(m - M);
-      lw = w * __ldcg(p + (int64_t)s * stride + kD + 1);
+    for (int k = 0; k < kBatch; ++k) {
+      if (j0 + k < np) {
+        const float *r = p + (int64_t)(j0 + k) * stride;
+        ml[k] = __ldcg(reinterpret_cast<const float2 *>(r + kD));
+        lo[k] = __ldcg(reinterpret_cast<const float2 *>(r + 2 * lane));
+        hi[k] = __ldcg(reinterpret_cast<const float2 *>(r + 64 + 2 * lane));
+      }
     }
-    __syncthreads();  // previous chunk's weights are consumed
-    s_w[c] = w;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
-    if (lane == 0) s_red[warp] = lw;
-    __syncthreads();
-    L += (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-    const int n = min(128, np - s0);
-    const float *ps = p + (int64_t)s0 * stride + c;
-    int j = 0;
-    for (; j + 4 <= n; j += 4) {
-      const float v0 = __ldcg(ps + (int64_t)j * stride), v1 = __ldcg(ps + (int64_t)(j + 1) * stride);
-      const float v2 = __ldcg(ps + (int64_t)(j + 2) * stride), v3 = __ldcg(ps + (int64_t)(j + 3) * stride);
-      O = fmaf(s_w[j], v0, O);
-      O = fmaf(s_w[j + 1], v1, O);
-      O = fmaf(s_w[j + 2], v2, O);
-      O = fmaf(s_w[j + 3], v3, O);
+    for (int k = 0; k < kBatch; ++k) {
+      if (j0 + k < np && ml[k].x != -INFINITY) {
+        const float m = fmaxf(M, ml[k].x);
+        const float a = ex2(M - m);  // M = -inf on the first partial: a = 0
+        const float w = ex2(ml[k].x - m);
+        L = fmaf(L, a, w * ml[k].y);
+        o0 = fmaf(o0, a, w * lo[k].x);
+        o1 = fmaf(o1, a, w * lo[k].y);
+        o2 = fmaf(o2, a, w * hi[k].x);
+        o3 = fmaf(o3, a, w * hi[k].y);
+        M = m;
+      }
     }
-    for (; j < n; ++j) O = fmaf(s_w[j], __ldcg(ps + (int64_t)j * stride), O);
   }
-  out_row[c] = f2h(O / L);
+  const float inv = np > 0 ? 1.f / L : 0.f;
+  uint32_t *dst = reinterpret_cast<uint32_t *>(out_row);
+  dst[lane] = h22u(__floats2half2_rn(o0 * inv, o1 * inv));
+  dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
 }
+
+constexpr int kCombineRows = 4;  // (batch, query head) rows per combine CTA, one warp each
 
 // Dense layout: the partials of (batch, query head) `row` sit at slots 0 .. np-1 of
 // the row's pmax slots; np follows from the unit split.
-__global__ void __launch_bounds__(128) combine_kernel(const float *__restrict__ ws, int64_t pmax, int64_t W,
-                                                      int64_t NW, int64_t U, int Hkv, int Hq,
-                                                      uint16_t *__restrict__ out) {
+__global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(const float *__restrict__ ws, int64_t pmax,
+                                                                    int64_t W, int64_t NW, int64_t U, int Hkv,
+                                                                    int Hq, int64_t rows,
+                                                                    uint16_t *__restrict__ out) {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
-  const int64_t row = blockIdx.x;  // b * Hq + h
+  const int64_t row = (int64_t)blockIdx.x * kCombineRows + (threadIdx.x >> 5);  // b * Hq + h
+  if (row >= rows) return;
   const int64_t b = row / Hq, hq = row - b * Hq;
   const int64_t head = b * Hkv + hq / (Hq / Hkv);
   const int64_t first = owner_warp(head * U, W, NW), last = owner_warp(head * U + U - 1, W, NW);
-  combine_row(ws + row * pmax * (kD + 2), (int)(last - first + 1), kD + 2, out + row * kD);
+  combine_row(ws + row * pmax * (kD + 2), (int)(last - first + 1), kD + 2, out + row * kD, threadIdx.x & 31);
 }
 
 // Paged layout: the decode grid wrote, per (batch, KV head), the index of its first
 // partial pair and their count; pair i holds the R query heads' partials.  With
 // `advance`, the grid then moves every sequence's length past the token the step
 // appended (the decode grid, and so the append before it, has completed).
-__global__ void __launch_bounds__(128) paged_combine_kernel(const float *__restrict__ ws, int Hkv, int Hq, int B,
-                                                            int32_t *advance, int32_t cap,
-                                                            uint16_t *__restrict__ out) {
+__global__ void __launch_bounds__(32 * kCombineRows) paged_combine_kernel(const float *__restrict__ ws, int Hkv,
+                                                                          int Hq, int B, int32_t *advance,
+                                                                          int32_t cap, uint16_t *__restrict__ out) {
   asm volatile("griddepcontrol.wait;\n" ::: "memory");  // the decode grid has completed
-  const int64_t row = blockIdx.x;  // b * Hq + h
+  const int64_t row = (int64_t)blockIdx.x * kCombineRows + (threadIdx.x >> 5);  // b * Hq + h
+  if (row >= (int64_t)B * Hq) return;
+  const int lane = threadIdx.x & 31;
   const int64_t b = row / Hq, hq = row - b * Hq;
   const int R = Hq / Hkv;
   const int64_t head = b * Hkv + hq / R;
   const int2 hd = __ldcg(reinterpret_cast<const int2 *>(ws) + head);
   const float *part = ws + 2 * (int64_t)B * Hkv;
-  combine_row(part + ((int64_t)hd.x * R + hq % R) * (kD + 2), hd.y, (int64_t)R * (kD + 2), out + row * kD);
-  if (advance && hq == 0 && threadIdx.x == 0) {
+  combine_row(part + ((int64_t)hd.x * R + hq % R) * (kD + 2), hd.y, (int64_t)R * (kD + 2), out + row * kD, lane);
+  if (advance && hq == 0 && lane == 0) {
     const int32_t len = advance[b];
     advance[b] = len < cap ? len + 1 : cap;
   }
@@ -975,14 +933,15 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
-  cfg.blockDim = dim3(128);
+  const int64_t rows = (int64_t)a.B * a.Hq;
+  cfg.gridDim = dim3((unsigned)((rows + kCombineRows - 1) / kCombineRows));
+  cfg.blockDim = dim3(32 * kCombineRows);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.ws, (int64_t)a.pmax, a.total_units,
-                            (int64_t)a.n_warps, a.units_per_head, a.Hkv, a.Hq, a.out);
+                            (int64_t)a.n_warps, a.units_per_head, a.Hkv, a.Hq, rows, a.out);
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
@@ -1002,8 +961,9 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
   cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.B * a.Hq));
-  cfg.blockDim = dim3(128);
+  const int64_t rows = (int64_t)a.B * a.Hq;
+  cfg.gridDim = dim3((unsigned)((rows + kCombineRows - 1) / kCombineRows));
+  cfg.blockDim = dim3(32 * kCombineRows);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cfg.attrs = attr;
