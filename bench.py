@@ -15,10 +15,12 @@ timed events), so the context stays within n .. n + 64 tokens however many steps
 run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
-                  [--workload NAME] [--layout dense|paged [--page-tokens P]] [--compare-fp16]
+                  [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
+                  [--compare-fp16]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
-from one pool, scattered by a seeded permutation; lengths on the device).
+from one pool, scattered by a seeded permutation; lengths on the device); with
+--graph each step is replayed from a CUDA graph captured once per input set.
 
 --impl reference times the CPU oracle (plain C, the host's cores) on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -267,6 +269,9 @@ class DenseLayout:
     def attention(self, q, out, stream):
         self.kivi.kivi_decode_attention(self.cache, q, 1.0, out=out, ws=self.ws, stream=stream)
 
+    def prepare(self, inputs, out):
+        pass
+
 
 class PagedLayout:
     """The paged pool: pages of P tokens scattered by a seeded permutation, lengths on
@@ -275,10 +280,11 @@ class PagedLayout:
     profile = "decode_attention_paged_llama2-7b-mha.md"
     kernel = "kivi_paged_decode_attention (paged decode_kernel + paged_combine_kernel)"
 
-    def __init__(self, wl, pre, dev, page_tokens):
+    def __init__(self, wl, pre, dev, page_tokens, graph=False):
         from bit_asymmetric_kv_gb300 import kivi, synth
 
         self.wl, self.kivi, self.P = wl, kivi, page_tokens
+        self.graph, self.graphs = graph, {}
         maxp = math.ceil((wl.n + CYCLE + 64) / page_tokens)
         num_pages = wl.B * maxp
         self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev)
@@ -295,8 +301,29 @@ class PagedLayout:
         self.cache.k_res.copy_(self.res0)
         self.cache.seq_lens.copy_(self.lens0)
 
+    def prepare(self, inputs, out):
+        """With graph replay: capture one step per input set (k, v, q), after one
+        eager step (the library's first call on a device queries it)."""
+        if not self.graph:
+            return
+        import torch
+
+        k, v, q = inputs[0]
+        self.kivi.kivi_paged_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws)
+        torch.cuda.synchronize()
+        self.rollback()
+        for k, v, q in inputs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.kivi.kivi_paged_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws)
+            self.graphs[k.data_ptr()] = g
+        torch.cuda.synchronize()
+
     def step(self, k, v, q, out, stream):
-        self.kivi.kivi_paged_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws, stream=stream)
+        if self.graph:
+            self.graphs[k.data_ptr()].replay()  # on the current stream
+        else:
+            self.kivi.kivi_paged_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws, stream=stream)
         return 3  # append (group flush fused), decode attention, combine (advances the lengths)
 
     def attention(self, q, out, stream):
@@ -305,7 +332,7 @@ class PagedLayout:
 
 def make_layout(args, wl, pre, dev):
     if args.layout == "paged":
-        return PagedLayout(wl, pre, dev, args.page_tokens)
+        return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph)
     return DenseLayout(wl, pre, dev)
 
 
@@ -341,6 +368,7 @@ def run_kivi(args, wl):
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    lay.prepare(dev_in, out)
 
     def step_events(i, rec):
         if i % CYCLE == 0:
@@ -431,8 +459,11 @@ def run_kivi(args, wl):
 
 def make_layout_config(args):
     if args.layout == "paged":
+        api = "kivi_paged_decode_step (append + decode attention + length advance)"
+        if args.graph:
+            api += ", replayed from a CUDA graph captured once per input set"
         return {"layout": f"paged: {args.page_tokens} tokens per page, pages scattered by a seeded permutation",
-                "api": "kivi_paged_decode_step (append + decode attention + length advance)"}
+                "api": api}
     return {"layout": "dense"}
 
 
@@ -448,31 +479,32 @@ def cycle_workspace(cache, wl, n0, dev):
 
 def e2e_run(args, wl, pre, dev, stream, flush):
     """Same metric through the public API with host inputs: every step copies its
-    new k, v, q from pinned host memory, runs append + decode attention and copies
-    the output back; the copies are inside the timed events."""
+    new k, v, q from pinned host memory (one buffer, one copy), runs append + decode
+    attention and copies the output back; the copies are inside the timed events."""
     import torch
 
     from bit_asymmetric_kv_gb300 import synth
 
     total = args.warmup + args.steps
     lay = make_layout(args, wl, pre, dev)
-    host = [tuple(t.pin_memory() for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
-    dk = torch.empty_like(host[0][0], device=dev)
-    dv = torch.empty_like(host[0][1], device=dev)
-    dq = torch.empty_like(host[0][2], device=dev)
+    # each step's k, v and q side by side in one pinned buffer: one copy per step
+    steps_in = [synth.make_step(wl, pre, s) for s in range(CYCLE)]
+    shapes = [t.shape for t in steps_in[0]]
+    sizes = [t.numel() for t in steps_in[0]]
+    host = [torch.cat([t.reshape(-1) for t in kvq]).pin_memory() for kvq in steps_in]
+    dbuf = host[0].to(dev)
+    dk, dv, dq = (p.view(sh) for p, sh in zip(torch.split(dbuf, sizes), shapes))
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     out_h = torch.empty_like(out, device="cpu").pin_memory()
+    lay.prepare([(dk, dv, dq)], out)
     times = []
     for i in range(total):
         if i % CYCLE == 0:
             lay.rollback()
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        hk, hv, hq = host[i % CYCLE]
         e0.record(stream)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
+        dbuf.copy_(host[i % CYCLE], non_blocking=True)
         lay.step(dk, dv, dq, out, stream)
         out_h.copy_(out, non_blocking=True)
         e1.record(stream)
@@ -481,7 +513,7 @@ def e2e_run(args, wl, pre, dev, stream, flush):
     torch.cuda.synchronize()
     ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    h2d = sum(t.numel() * t.element_size() for t in host[0])
+    h2d = host[0].numel() * host[0].element_size()
     d2h = out.numel() * out.element_size()
     return {"value": wl.B * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
@@ -550,12 +582,16 @@ def main(argv=None):
     ap.add_argument("--layout", choices=["dense", "paged"], default="dense",
                     help="cache layout of the timed path (default: the dense cache)")
     ap.add_argument("--page-tokens", type=int, default=64, help="tokens per page of --layout paged")
+    ap.add_argument("--graph", action="store_true",
+                    help="--layout paged: replay each step from a captured CUDA graph")
     ap.add_argument("--workload", default="llama2",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
                          "default: the Llama-2-7B MHA decode")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.graph and args.layout != "paged":
+        ap.error("--graph needs --layout paged (the dense step takes its token count from the host)")
     from bit_asymmetric_kv_gb300 import synth
 
     hits = [w for w in synth.CONFIGS if w.name.startswith(args.workload)]

@@ -48,7 +48,7 @@ namespace kivi {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = kDecodeWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
 // Units staged ahead of the one being computed (at most kStages - 1).
@@ -57,7 +57,7 @@ constexpr int kStages = 3;
 #endif
 constexpr int kAhead = KIVI_DECODE_AHEAD;
 static_assert(kAhead >= 1 && kAhead < kStages, "the ring must hold the computed unit and the staged ones");
-constexpr int kUnit = 64;                            // tokens per unit
+constexpr int kUnit = kDecodeUnit;                   // tokens per unit
 constexpr int kFragRowWords = 20;                    // 16 B-fragment words + 4 pad (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -809,8 +809,6 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np,
   dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
 }
 
-constexpr int kCombineRows = 4;  // (batch, query head) rows per combine CTA, one warp each
-
 // Dense layout: the partials of (batch, query head) `row` sit at slots 0 .. np-1 of
 // the row's pmax slots; np follows from the unit split.
 __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(const float *__restrict__ ws, int64_t pmax,
@@ -869,107 +867,21 @@ int smem_bytes(int R, int G) {
 // Paged kernels append the lengths, the unit prefix and 4 warp totals: 2B + 5 ints.
 int paged_smem_bytes(int R, int G, int B) { return smem_bytes(R, G) + ((4 * (2 * B + 5) + 15) & ~15); }
 
-cudaError_t warps_on_device(const void *fn, int smem, int *n_warps) {
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem)) != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  *n_warps = sms * per_sm * kWarps;
-  return cudaSuccess;
-}
-
 }  // namespace
 
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
-  const int R = Hq / Hkv;
-  int nw = 0;
-  cudaError_t e = warps_on_device(select_kernel<false>(R, G), smem_bytes(R, G), &nw);
-  if (e != cudaSuccess) return e;
-  const int64_t heads = (int64_t)B * Hkv;
-  const int64_t ng = n / G;
-  const int64_t U = (ng * G + kUnit - 1) / kUnit + ((n % G) ? 1 : 0);
-  const int64_t W = heads * U;
-  int64_t NW = nw;
-  if (NW > W) NW = W;
-  const int64_t q = W / NW;  // every warp holds at least q units
-  out->units_per_head = U;
-  out->total_units = W;
-  out->n_warps = (int)NW;
-  out->grid = (int)((NW + kWarps - 1) / kWarps);
-  out->pmax = (int)((U + q - 1) / q + 1);
-  return cudaSuccess;
-}
-
-cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out) {
-  const int R = Hq / Hkv;
-  int nw = 0;
-  cudaError_t e = warps_on_device(select_kernel<true>(R, G), paged_smem_bytes(R, G, B), &nw);
-  if (e != cudaSuccess) return e;
-  const size_t heads = (size_t)B * Hkv;
-  out->n_warps = nw;
-  out->grid = nw / kWarps;
-  // header int2 per head; pair indices warp + head < n_warps + heads
-  out->ws_bytes = heads * 8 + ((size_t)nw + heads) * R * (kD + 2) * sizeof(float);
-  return cudaSuccess;
-}
-
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
-  const int R = a.Hq / a.Hkv;
-  const void *fn = select_kernel<false>(R, a.G);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t dcfg = {};
-  dcfg.gridDim = dim3((unsigned)a.grid);
-  dcfg.blockDim = dim3(kThreads);
-  dcfg.dynamicSmemBytes = (size_t)smem_bytes(R, a.G);
-  dcfg.stream = st;
-  dcfg.attrs = attr;
-  dcfg.numAttrs = a.wait_tail ? 1 : 0;  // overlap a preceding append only when asked
-  void *args[] = {const_cast<DecodeArgs *>(&a)};
-  cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  const int64_t rows = (int64_t)a.B * a.Hq;
-  cfg.gridDim = dim3((unsigned)((rows + kCombineRows - 1) / kCombineRows));
-  cfg.blockDim = dim3(32 * kCombineRows);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)a.ws, (int64_t)a.pmax, a.total_units,
-                            (int64_t)a.n_warps, a.units_per_head, a.Hkv, a.Hq, rows, a.out);
-}
-
-cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
-  const int R = a.Hq / a.Hkv;
-  const void *fn = select_kernel<true>(R, a.G);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t dcfg = {};
-  dcfg.gridDim = dim3((unsigned)a.grid);
-  dcfg.blockDim = dim3(kThreads);
-  dcfg.dynamicSmemBytes = (size_t)paged_smem_bytes(R, a.G, a.B);
-  dcfg.stream = st;
-  dcfg.attrs = attr;
-  dcfg.numAttrs = a.wait_tail ? 1 : 0;
-  void *args[] = {const_cast<DecodeArgs *>(&a)};
-  cudaError_t e = cudaLaunchKernelExC(&dcfg, fn, args);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  const int64_t rows = (int64_t)a.B * a.Hq;
-  cfg.gridDim = dim3((unsigned)((rows + kCombineRows - 1) / kCombineRows));
-  cfg.blockDim = dim3(32 * kCombineRows);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, paged_combine_kernel, (const float *)a.ws, a.Hkv, a.Hq, a.B, a.advance_lens,
-                            a.cap_tokens, a.out);
+DecodeKernels decode_kernels(int R, int G, bool paged, int B) {
+  DecodeKernels k;
+  if (paged) {
+    k.decode = select_kernel<true>(R, G);
+    k.smem = paged_smem_bytes(R, G, B);
+    k.smem_limit = paged_smem_bytes(R, G, kPagedMaxBatch);
+    k.combine = reinterpret_cast<const void *>(&paged_combine_kernel);
+  } else {
+    k.decode = select_kernel<false>(R, G);
+    k.smem = k.smem_limit = smem_bytes(R, G);
+    k.combine = reinterpret_cast<const void *>(&combine_kernel);
+  }
+  return k;
 }
 
 }  // namespace kivi

@@ -1,0 +1,143 @@
+// kivi_decode_host.cu -- grid sizing and launches of the decode kernels in
+// kivi_decode.cu (host code only, so that the kernels' source is one file).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "kivi_internal.h"
+
+namespace kivi {
+
+namespace {
+
+constexpr int kD = 128;
+
+// Warps of `fn` resident at once on the current device with `smem` bytes of dynamic
+// shared memory.  The first query per (device, kernel, size) raises the kernel's
+// dynamic shared-memory limit to `smem_limit` (the most any launch of it uses, so
+// that an entry for one size never lowers the limit another size needs) and asks
+// the occupancy calculator; later calls read a table, so that decode calls make no
+// CUDA runtime query but cudaGetDevice (and can be captured in a CUDA graph once a
+// first call has run).
+struct WarpsEntry {
+  int dev;
+  const void *fn;
+  int smem;
+  int n_warps;
+};
+constexpr int kWarpsCache = 256;
+WarpsEntry g_warps[kWarpsCache];
+int g_warps_used = 0;
+std::mutex g_warps_lock;
+
+cudaError_t warps_on_device(const DecodeKernels &k, int *n_warps) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> guard(g_warps_lock);
+    for (int i = 0; i < g_warps_used; ++i)
+      if (g_warps[i].dev == dev && g_warps[i].fn == k.decode && g_warps[i].smem == k.smem) {
+        *n_warps = g_warps[i].n_warps;
+        return cudaSuccess;
+      }
+  }
+  e = cudaFuncSetAttribute(k.decode, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_limit);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.decode, 32 * kDecodeWarps, k.smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  *n_warps = sms * per_sm * kDecodeWarps;
+  std::lock_guard<std::mutex> guard(g_warps_lock);
+  if (g_warps_used < kWarpsCache) g_warps[g_warps_used++] = WarpsEntry{dev, k.decode, k.smem, *n_warps};
+  return cudaSuccess;
+}
+
+// Launch the decode grid (a programmatic dependent of the preceding kernel when
+// `dependent`), then the combine as a programmatic dependent of the decode grid.
+cudaError_t launch_pair(const DecodeKernels &k, const DecodeArgs &a, void **combine_args, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t dcfg = {};
+  dcfg.gridDim = dim3((unsigned)a.grid);
+  dcfg.blockDim = dim3(32 * kDecodeWarps);
+  dcfg.dynamicSmemBytes = (size_t)k.smem;
+  dcfg.stream = st;
+  dcfg.attrs = attr;
+  dcfg.numAttrs = a.wait_tail ? 1 : 0;  // overlap a preceding append only when asked
+  void *args[] = {const_cast<DecodeArgs *>(&a)};
+  cudaError_t e = cudaLaunchKernelExC(&dcfg, k.decode, args);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = (int64_t)a.B * a.Hq;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kCombineRows - 1) / kCombineRows));
+  cfg.blockDim = dim3(32 * kCombineRows);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, k.combine, combine_args);
+}
+
+}  // namespace
+
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
+  const int R = Hq / Hkv;
+  int nw = 0;
+  cudaError_t e = warps_on_device(decode_kernels(R, G, false, B), &nw);
+  if (e != cudaSuccess) return e;
+  const int64_t heads = (int64_t)B * Hkv;
+  const int64_t ng = n / G;
+  const int64_t U = (ng * G + kDecodeUnit - 1) / kDecodeUnit + ((n % G) ? 1 : 0);
+  const int64_t W = heads * U;
+  int64_t NW = nw;
+  if (NW > W) NW = W;
+  const int64_t q = W / NW;  // every warp holds at least q units
+  out->units_per_head = U;
+  out->total_units = W;
+  out->n_warps = (int)NW;
+  out->grid = (int)((NW + kDecodeWarps - 1) / kDecodeWarps);
+  out->pmax = (int)((U + q - 1) / q + 1);
+  return cudaSuccess;
+}
+
+cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out) {
+  const int R = Hq / Hkv;
+  int nw = 0;
+  cudaError_t e = warps_on_device(decode_kernels(R, G, true, B), &nw);
+  if (e != cudaSuccess) return e;
+  const size_t heads = (size_t)B * Hkv;
+  out->n_warps = nw;
+  out->grid = nw / kDecodeWarps;
+  // header int2 per head; pair indices warp + head < n_warps + heads
+  out->ws_bytes = heads * 8 + ((size_t)nw + heads) * R * (kD + 2) * sizeof(float);
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
+  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, false, a.B);
+  const float *ws = a.ws;
+  int64_t pmax = a.pmax, W = a.total_units, NW = a.n_warps, U = a.units_per_head;
+  int Hkv = a.Hkv, Hq = a.Hq;
+  int64_t rows = (int64_t)a.B * a.Hq;
+  uint16_t *out = a.out;
+  void *cargs[] = {&ws, &pmax, &W, &NW, &U, &Hkv, &Hq, &rows, &out};
+  return launch_pair(k, a, cargs, st);
+}
+
+cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
+  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, true, a.B);
+  const float *ws = a.ws;
+  int Hkv = a.Hkv, Hq = a.Hq, B = a.B;
+  int32_t *advance = a.advance_lens;
+  int32_t cap = a.cap_tokens;
+  uint16_t *out = a.out;
+  void *cargs[] = {&ws, &Hkv, &Hq, &B, &advance, &cap, &out};
+  return launch_pair(k, a, cargs, st);
+}
+
+}  // namespace kivi

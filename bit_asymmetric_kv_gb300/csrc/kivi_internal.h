@@ -79,6 +79,21 @@ struct DecodeArgs {
   int32_t cap_tokens;          // max_pages << page_shift
 };
 
+// Decode kernels (kivi_decode.cu) and their launch shape.  The host side
+// (kivi_decode_host.cu) sizes the grid from the occupancy of `decode` with `smem`
+// bytes of dynamic shared memory; `smem_limit` is the most any launch of it uses.
+constexpr int kDecodeWarps = 4;   // warps per decode CTA
+constexpr int kDecodeUnit = 64;   // tokens per unit of work
+constexpr int kCombineRows = 4;   // (batch, query head) rows per combine CTA, one warp each
+struct DecodeKernels {
+  const void *decode;
+  int smem;
+  int smem_limit;
+  const void *combine;  // dense: (ws, pmax, W, NW, U, Hkv, Hq, rows, out);
+                        // paged: (ws, Hkv, Hq, B, advance, cap, out)
+};
+DecodeKernels decode_kernels(int R, int G, bool paged, int B);
+
 // Geometry of one decode call on the current device (deterministic for given sizes).
 struct DecodeGeom {
   int64_t units_per_head;

@@ -229,3 +229,33 @@ def test_paged_workspace_too_small_is_rejected():
         kivi.kivi_paged_decode_attention(pg.cache, pg.pre.q.cuda(), 1.0, out=out, ws=ws)
     assert e.value.status == kivi.KIVI_ERR_WORKSPACE
     assert torch.all(out == 7.0)
+
+
+def test_paged_decode_step_replays_as_a_cuda_graph():
+    """The paged step keeps its lengths on the device, so one captured step replays
+    for every following token: parity with the oracle at each replay."""
+    Hq = 8
+    pg = Paged(Hq, 2, 32, 64, [30, 61, 100, 0], seed=43, steps=40, unassigned=True)
+    ws = kivi.paged_workspace(pg.cache, Hq)
+    k0, v0, q0 = pg.step_inputs(0)
+    k_buf, v_buf, q_buf = k0.cuda(), v0.cuda(), q0.cuda()
+    out = torch.empty_like(q_buf)
+    # one call outside the capture: the library's first call on a device queries it
+    kivi.kivi_paged_decode_step(pg.cache, k_buf, v_buf, q_buf, 1.0, out=out, ws=ws)
+    pg.oracle_append(k0, v0)
+    assert_close(out, pg.reference(q0, 1.0))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        kivi.kivi_paged_decode_step(pg.cache, k_buf, v_buf, q_buf, 1.0, out=out, ws=ws)
+    # capturing records the step without running it: the lengths did not move
+    assert pg.cache.seq_lens.cpu().tolist() == pg.lens
+    for step in range(1, 40):
+        k_new, v_new, q = pg.step_inputs(step)
+        k_buf.copy_(k_new)
+        v_buf.copy_(v_new)
+        q_buf.copy_(q)
+        graph.replay()
+        pg.oracle_append(k_new, v_new)
+        assert_close(out, pg.reference(q, 1.0))
+    pg.assert_cache_equal()
