@@ -11,8 +11,9 @@ it with gcc on first use and exposes numpy-level wrappers.  Every function follo
 the page "Makale Bulteni -- KIVI" (cmlonder.com radar / paper-to-prod, 2026-11-01):
 headline paragraph (keys per channel, values per token, asymmetric 2-bit) and
 section "Iddia ve Gerceklik", paragraphs 2-3 (fixed outlier key channels; G-token
-key groups with a full-precision residual buffer).  The readings R1-R8 are listed
-at the top of ``kivi_oracle.c``.
+key groups with a full-precision residual buffer).  The readings R1-R9 are listed
+at the top of ``kivi_oracle.c``; R9 is the variant with a value residual kept in
+lock-step with the key residual (``value_residual=True``).
 
 Parity pins (tests/test_oracle_*.py) check this oracle against closed forms,
 brute force and library routines, not against itself.
@@ -59,17 +60,17 @@ def lib():
             L.oracle_max_threads.restype = i32
             L.oracle_quantize_group.argtypes = [P, i64, i64, P, P, P]
             L.oracle_pack_row.argtypes = [P, i32, P]
-            L.oracle_prefill_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, P]
-            L.oracle_append_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, P]
+            L.oracle_prefill_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_append_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, P, P]
             L.oracle_append_head.restype = i64
-            L.oracle_dequantize_head_f64.argtypes = [i32, i32, i64, P, P, P, P, P, P, P]
-            L.oracle_dequantize_head_f32.argtypes = [i32, i32, i64, P, P, P, P, P, P, P]
-            L.oracle_attention_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, f64, P]
+            L.oracle_dequantize_head_f64.argtypes = [i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_dequantize_head_f32.argtypes = [i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_attention_head.argtypes = [i32, i32, i64, P, P, P, P, P, P, P, f64, P]
             L.oracle_attention_head.restype = i32
-            L.oracle_prefill.argtypes = [i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P]
-            L.oracle_append.argtypes = [i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P]
+            L.oracle_prefill.argtypes = [i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
+            L.oracle_append.argtypes = [i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
             L.oracle_append.restype = i64
-            L.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, f64, P]
+            L.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, f64, P]
             L.oracle_attention.restype = i32
             L.oracle_attention_raw_head.argtypes = [i32, i64, P, P, P, f64, P]
             L.oracle_attention_raw_head.restype = i32
@@ -136,6 +137,7 @@ class Cache:
     k_codes [B,Hkv,T,D/16] u32 | k_meta [B,Hkv,T//G,D] u32 {s | z<<16}
     k_res   [B,Hkv,G,D]   u16 (fp16 bits)
     v_codes [B,Hkv,T,D/16] u32 | v_meta [B,Hkv,T] u32 {s | z<<16}
+    v_res   [B,Hkv,G,D]   u16, or None: the value residual of reading R9
     n       tokens held;  T = max_tokens.
     """
 
@@ -150,9 +152,10 @@ class Cache:
     v_codes: np.ndarray
     v_meta: np.ndarray
     n: int = 0
+    v_res: np.ndarray | None = None
 
     @classmethod
-    def empty(cls, B, Hkv, D, G, max_tokens):
+    def empty(cls, B, Hkv, D, G, max_tokens, value_residual: bool = False):
         T = int(max_tokens)
         return cls(
             B, Hkv, D, G, T,
@@ -161,23 +164,31 @@ class Cache:
             np.zeros((B, Hkv, G, D), np.uint16),
             np.zeros((B, Hkv, T, D // 16), np.uint32),
             np.zeros((B, Hkv, T), np.uint32),
+            0,
+            np.zeros((B, Hkv, G, D), np.uint16) if value_residual else None,
         )
 
+    def _vres_ptr(self, b=None, h=None):
+        if self.v_res is None:
+            return ctypes.c_void_p(0)
+        return _ptr(self.v_res if b is None else self.v_res[b, h])
+
     def bufs(self):
-        return [_ptr(self.k_codes), _ptr(self.k_meta), _ptr(self.k_res), _ptr(self.v_codes), _ptr(self.v_meta)]
+        return [_ptr(self.k_codes), _ptr(self.k_meta), _ptr(self.k_res), _ptr(self.v_codes), _ptr(self.v_meta),
+                self._vres_ptr()]
 
     def head(self, b: int, h: int):
         """Views of one (batch, KV head) slice."""
         return (self.k_codes[b, h], self.k_meta[b, h], self.k_res[b, h], self.v_codes[b, h], self.v_meta[b, h])
 
 
-def prefill(k, v, G: int, max_tokens: int) -> Cache:
+def prefill(k, v, G: int, max_tokens: int, value_residual: bool = False) -> Cache:
     """Quantize a prompt: k, v fp16 [B, Hkv, n, D] -> Cache holding n tokens."""
     kb, vb = _f16_bits(k), _f16_bits(v)
     B, Hkv, n, D = kb.shape
     if max_tokens < n:
         raise ValueError("max_tokens < n")
-    c = Cache.empty(B, Hkv, D, G, max_tokens)
+    c = Cache.empty(B, Hkv, D, G, max_tokens, value_residual)
     lib().oracle_prefill(B, Hkv, D, G, c.max_tokens, n, _ptr(kb), _ptr(vb), *c.bufs())
     c.n = n
     return c
@@ -208,7 +219,7 @@ def dequantize(c: Cache, dtype=np.float64, heads=None):
     for b, h in todo:
         kc, km, kr, vc, vm = c.head(b, h)
         ko, vo = kd[b, h], vd[b, h]
-        fn(c.D, c.G, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm), _ptr(ko), _ptr(vo))
+        fn(c.D, c.G, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm), c._vres_ptr(b, h), _ptr(ko), _ptr(vo))
     return kd, vd
 
 
@@ -228,17 +239,18 @@ def attention_head(c: Cache, b: int, kvh: int, q_row, sigma: float) -> np.ndarra
     qb = np.ascontiguousarray(_f16_bits(q_row))
     out = np.zeros(c.D, np.float64)
     kc, km, kr, vc, vm = c.head(b, kvh)
-    rc = lib().oracle_attention_head(c.D, c.G, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm), _ptr(qb), float(sigma), _ptr(out))
+    rc = lib().oracle_attention_head(c.D, c.G, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm),
+                                     c._vres_ptr(b, kvh), _ptr(qb), float(sigma), _ptr(out))
     if rc != 0:
         raise ValueError("oracle attention: empty cache")
     return out
 
 
-def prefill_head(k_head, v_head, G: int, max_tokens: int):
+def prefill_head(k_head, v_head, G: int, max_tokens: int, value_residual: bool = False):
     """Quantize one (batch, KV head) prompt k_head, v_head fp16 [n, D] -> 1x1 Cache."""
     kb = np.ascontiguousarray(_f16_bits(k_head))[None, None]
     vb = np.ascontiguousarray(_f16_bits(v_head))[None, None]
-    return prefill(kb, vb, G, max_tokens)
+    return prefill(kb, vb, G, max_tokens, value_residual)
 
 
 def attention_raw(k, v, q, sigma: float) -> np.ndarray:

@@ -36,6 +36,10 @@
  *   R8  attention over the dequantized cache in fp64:
  *       score_t = sigma * q . K'_t,  p = softmax(score),  out = sum_t p_t V'_t,
  *       with query head h reading KV head h / (Hq / Hkv).
+ *   R9  (variant, when a value residual buffer is given) values keep the same
+ *       residual as keys: the last n mod G values stay fp16, and when the key group
+ *       flushes its G values are quantized per token (R5) at once.  Without the
+ *       buffer, R6 holds: every value is quantized when it arrives.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.  No fast-math and
  * no FMA contraction, so every fp32 operation is a single IEEE-754 RNE operation.
@@ -165,17 +169,18 @@ static void quantize_value_token(const uint16_t *row, int D, uint32_t *codes_out
 }
 
 /*
- * One (batch, KV head): quantize a prompt of n tokens (R6).
+ * One (batch, KV head): quantize a prompt of n tokens (R6, R9).
  *   k, v     : [n][D] fp16
  *   k_codes  : [max_tokens][D/16]   rows < floor(n/G)*G written
  *   k_meta   : [max_tokens/G][D]    groups < floor(n/G) written
  *   k_res    : [G][D]               slots < n mod G written (token nq + j in slot j)
- *   v_codes  : [max_tokens][D/16]   rows < n written
- *   v_meta   : [max_tokens]         entries < n written
+ *   v_codes  : [max_tokens][D/16]   rows < n written (rows < nq with a value residual)
+ *   v_meta   : [max_tokens]         entries < n written (< nq with a value residual)
+ *   v_res    : [G][D] or NULL       with a value residual: slots < n mod G written
  */
 void oracle_prefill_head(int D, int G, int64_t n, const uint16_t *k, const uint16_t *v,
                          uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
-                         uint32_t *v_codes, uint32_t *v_meta) {
+                         uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t n_groups = n / G;
   int64_t nq = n_groups * G;
   for (int64_t g = 0; g < n_groups; ++g)
@@ -183,25 +188,37 @@ void oracle_prefill_head(int D, int G, int64_t n, const uint16_t *k, const uint1
                        k_meta + (size_t)g * D);
   for (int64_t j = 0; j < n - nq; ++j)
     memcpy(k_res + (size_t)j * D, k + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
-  for (int64_t t = 0; t < n; ++t)
+  int64_t n_quantized_values = v_res ? nq : n;
+  for (int64_t t = 0; t < n_quantized_values; ++t)
     quantize_value_token(v + (size_t)t * D, D, v_codes + (size_t)t * (D / 16), v_meta + t);
+  if (v_res)
+    for (int64_t j = 0; j < n - nq; ++j)
+      memcpy(v_res + (size_t)j * D, v + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
 }
 
 /*
  * One (batch, KV head): append token n (the cache holds n tokens before the call).
- * The key goes to residual slot n mod G; the value is quantized at once; when the
- * residual fills, its G keys are quantized as group n / G and the residual empties.
- * Returns the new length n + 1.
+ * The key goes to residual slot n mod G; the value is quantized at once (R6), or
+ * with a value residual (R9) goes to the same slot of v_res.  When the residual
+ * fills, its G keys are quantized as group n / G (and, with a value residual, its
+ * G values token by token) and the residual empties.  Returns the new length n + 1.
  */
 int64_t oracle_append_head(int D, int G, int64_t n, const uint16_t *k_new, const uint16_t *v_new,
                            uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
-                           uint32_t *v_codes, uint32_t *v_meta) {
+                           uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t r = n % G;
   memcpy(k_res + (size_t)r * D, k_new, (size_t)D * sizeof(uint16_t));
-  quantize_value_token(v_new, D, v_codes + (size_t)n * (D / 16), v_meta + n);
+  if (v_res)
+    memcpy(v_res + (size_t)r * D, v_new, (size_t)D * sizeof(uint16_t));
+  else
+    quantize_value_token(v_new, D, v_codes + (size_t)n * (D / 16), v_meta + n);
   if (r + 1 == G) {
     int64_t g = n / G;
     quantize_key_group(k_res, D, G, k_codes + (size_t)g * G * (D / 16), k_meta + (size_t)g * D);
+    if (v_res)
+      for (int64_t j = 0; j < G; ++j)
+        quantize_value_token(v_res + (size_t)j * D, D, v_codes + (size_t)(g * G + j) * (D / 16),
+                             v_meta + g * G + j);
   }
   return n + 1;
 }
@@ -222,8 +239,16 @@ static void dequant_key_f64(int D, int G, int64_t n, int64_t t, const uint32_t *
   }
 }
 
-static void dequant_value_f64(int D, int64_t t, const uint32_t *v_codes, const uint32_t *v_meta,
-                              double *out) {
+/* Dequantized value t of one head, fp64: z_t + code * s_t, or with a value residual
+ * (R9) the fp16 value itself for the last n mod G tokens. */
+static void dequant_value_f64(int D, int G, int64_t n, int64_t t, const uint32_t *v_codes,
+                              const uint32_t *v_meta, const uint16_t *v_res, double *out) {
+  int64_t nq = (n / G) * G;
+  if (v_res && t >= nq) {
+    const uint16_t *res = v_res + (size_t)(t - nq) * D;
+    for (int c = 0; c < D; ++c) out[c] = (double)h2f(res[c]);
+    return;
+  }
   const uint32_t *row = v_codes + (size_t)t * (D / 16);
   double s = (double)h2f(meta_s(v_meta[t]));
   double z = (double)h2f(meta_z(v_meta[t]));
@@ -233,11 +258,11 @@ static void dequant_value_f64(int D, int64_t t, const uint32_t *v_codes, const u
 /* Dequantize one head's n tokens to fp64 [n][D] (keys and values). */
 void oracle_dequantize_head_f64(int D, int G, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
-                                const uint32_t *v_codes, const uint32_t *v_meta,
+                                const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 double *k_out, double *v_out) {
   for (int64_t t = 0; t < n; ++t) {
     dequant_key_f64(D, G, n, t, k_codes, k_meta, k_res, k_out + (size_t)t * D);
-    dequant_value_f64(D, t, v_codes, v_meta, v_out + (size_t)t * D);
+    dequant_value_f64(D, G, n, t, v_codes, v_meta, v_res, v_out + (size_t)t * D);
   }
 }
 
@@ -245,7 +270,7 @@ void oracle_dequantize_head_f64(int D, int G, int64_t n, const uint32_t *k_codes
  * a product that is exact in fp32 followed by one RNE addition. */
 void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
-                                const uint32_t *v_codes, const uint32_t *v_meta,
+                                const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 float *k_out, float *v_out) {
   int64_t nq = (n / G) * G;
   for (int64_t t = 0; t < n; ++t) {
@@ -261,10 +286,15 @@ void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes
       const uint16_t *res = k_res + (size_t)(t - nq) * D;
       for (int c = 0; c < D; ++c) ko[c] = h2f(res[c]);
     }
+    float *vo = v_out + (size_t)t * D;
+    if (v_res && t >= nq) {
+      const uint16_t *res = v_res + (size_t)(t - nq) * D;
+      for (int c = 0; c < D; ++c) vo[c] = h2f(res[c]);
+      continue;
+    }
     const uint32_t *vrow = v_codes + (size_t)t * (D / 16);
     float s = h2f(meta_s(v_meta[t]));
     float z = h2f(meta_z(v_meta[t]));
-    float *vo = v_out + (size_t)t * D;
     for (int c = 0; c < D; ++c) {
       float prod = (float)unpack_code(vrow, c) * s;
       vo[c] = z + prod;
@@ -280,7 +310,7 @@ void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes
  */
 int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, const uint32_t *k_meta,
                           const uint16_t *k_res, const uint32_t *v_codes, const uint32_t *v_meta,
-                          const uint16_t *q, double sigma, double *out) {
+                          const uint16_t *v_res, const uint16_t *q, double sigma, double *out) {
   if (n <= 0) return -1;
   double *score = (double *)malloc((size_t)n * sizeof(double));
   double *row = (double *)malloc((size_t)D * sizeof(double));
@@ -301,7 +331,7 @@ int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, cons
   }
   for (int c = 0; c < D; ++c) out[c] = 0.0;
   for (int64_t t = 0; t < n; ++t) {
-    dequant_value_f64(D, t, v_codes, v_meta, row);
+    dequant_value_f64(D, G, n, t, v_codes, v_meta, v_res, row);
     double p = score[t] / l;
     for (int c = 0; c < D; ++c) out[c] += p * row[c];
   }
@@ -354,32 +384,34 @@ int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_
 #define KR(bh) (k_res + (size_t)(bh) * G * D)
 #define VC(bh) (v_codes + (size_t)(bh) * max_tokens * (D / 16))
 #define VM(bh) (v_meta + (size_t)(bh) * max_tokens)
+#define VR(bh) (v_res ? v_res + (size_t)(bh) * G * D : NULL)
 
 void oracle_prefill(int B, int Hkv, int D, int G, int64_t max_tokens, int64_t n, const uint16_t *k,
                     const uint16_t *v, uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
-                    uint32_t *v_codes, uint32_t *v_meta) {
+                    uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(dynamic)
   for (int64_t bh = 0; bh < heads; ++bh)
     oracle_prefill_head(D, G, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, KC(bh), KM(bh),
-                        KR(bh), VC(bh), VM(bh));
+                        KR(bh), VC(bh), VM(bh), VR(bh));
 }
 
 int64_t oracle_append(int B, int Hkv, int D, int G, int64_t max_tokens, int64_t n,
                       const uint16_t *k_new, const uint16_t *v_new, uint32_t *k_codes,
-                      uint32_t *k_meta, uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta) {
+                      uint32_t *k_meta, uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta,
+                      uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(static)
   for (int64_t bh = 0; bh < heads; ++bh)
     oracle_append_head(D, G, n, k_new + (size_t)bh * D, v_new + (size_t)bh * D, KC(bh), KM(bh),
-                       KR(bh), VC(bh), VM(bh));
+                       KR(bh), VC(bh), VM(bh), VR(bh));
   return n + 1;
 }
 
 int oracle_attention(int B, int Hq, int Hkv, int D, int G, int64_t max_tokens, int64_t n,
                      const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
-                     const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *q, double sigma,
-                     double *out) {
+                     const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
+                     const uint16_t *q, double sigma, double *out) {
   if (n <= 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
   int group = Hq / Hkv;
   int64_t rows = (int64_t)B * Hq;
@@ -388,8 +420,8 @@ int oracle_attention(int B, int Hq, int Hkv, int D, int G, int64_t max_tokens, i
     int64_t b = bq / Hq;
     int h = (int)(bq % Hq);
     int64_t bh = b * Hkv + h / group;
-    oracle_attention_head(D, G, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), q + (size_t)bq * D, sigma,
-                          out + (size_t)bq * D);
+    oracle_attention_head(D, G, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
+                          sigma, out + (size_t)bq * D);
   }
   return 0;
 }
