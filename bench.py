@@ -16,7 +16,7 @@ run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
                   [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
-                  [--compare-fp16]
+                  [--value-residual] [--compare-fp16]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
 from one pool, scattered by a seeded permutation; lengths on the device); with
@@ -49,12 +49,14 @@ L2_FLUSH_BYTES = 256 << 20
 CYCLE = 64  # steps between cache rollbacks
 
 
-def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int) -> int:
+def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False) -> int:
     """Bytes one decode-attention launch must move at context n (D = 128):
-    per (batch, KV head) nq*(32 + 512/G) + r*256 + n*36, plus q and out."""
+    per (batch, KV head) nq*(32 + 512/G) + r*256 + n*36, plus q and out; with a
+    value residual the last r values are fp16: nq*36 + r*256 instead of n*36."""
     nq = (n // G) * G
     r = n - nq
-    per_head = nq * 32 + (nq // G) * 512 + r * 256 + n * 36
+    values = nq * 36 + r * 256 if value_residual else n * 36
+    per_head = nq * 32 + (nq // G) * 512 + r * 256 + values
     return B * Hkv * per_head + 2 * B * Hq * 128 * 2
 
 
@@ -175,7 +177,7 @@ def dist_env():
 # ----------------------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
-def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float):
+def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
     cache) on `sample_heads` of the workload's KV heads; scale to the whole batch."""
     import oracle
@@ -185,7 +187,7 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float):
     T = wl.capacity(extra=steps + 64)
     k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
     v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
-    c = oracle.prefill(k, v, wl.G, T)  # untimed, like the GPU's prefill
+    c = oracle.prefill(k, v, wl.G, T, value_residual=value_residual)  # untimed, like the GPU's prefill
     R = wl.Hq // wl.Hkv
     t_total, done = 0.0, 0
     for step in range(steps):
@@ -215,12 +217,12 @@ def run_reference(args, wl):
     pre = synth.make_prefill(wl)
     for w in range(args.warmup):  # untimed warm-up: the first call builds the oracle
         oracle_timing(wl, pre, 1, 4, 0.0)
-    cb = oracle_timing(wl, pre, args.steps, 32, 60.0)
+    cb = oracle_timing(wl, pre, args.steps, 32, 60.0, args.value_residual)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B / cb["value"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u2 codes, f16 inputs, f64 attention (CPU oracle)", "data": "synthetic",
-            "config": workload_config(wl), "cpu_baseline": cb,
+            "config": {**workload_config(wl), **make_layout_config(args)}, "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -245,26 +247,32 @@ class DenseLayout:
     profile = "decode_attention_llama2-7b-mha.md"
     kernel = "kivi_decode_attention (decode_kernel + combine_kernel)"
 
-    def __init__(self, wl, pre, dev):
+    def __init__(self, wl, pre, dev, value_residual=False):
         from bit_asymmetric_kv_gb300 import kivi
 
         self.wl, self.kivi = wl, kivi
-        self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=CYCLE + 64), device=dev)
+        self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=CYCLE + 64), device=dev,
+                                         value_residual=value_residual)
         kivi.kivi_quantize_prefill(self.cache, pre.k.to(dev), pre.v.to(dev))
         self.n0 = self.cache.n_tokens
         self.res0 = self.cache.k_res.clone()
+        self.vres0 = None if self.cache.v_res is None else self.cache.v_res.clone()
         self.ws = cycle_workspace(self.cache, wl, self.n0, dev)
 
     def rollback(self):
         self.cache.k_res.copy_(self.res0)
+        if self.vres0 is not None:
+            self.cache.v_res.copy_(self.vres0)
         self.cache.c.n_tokens = self.n0
 
     def step(self, k, v, q, out, stream):
         """Returns the number of kernels the step launched."""
         n = self.cache.n_tokens
         self.kivi.kivi_decode_step(self.cache, k, v, q, 1.0, out=out, ws=self.ws, stream=stream)
-        # append (+ group flush every G steps), decode attention, combine
-        return 1 + (1 if (n % self.wl.G) + 1 == self.wl.G else 0) + 2
+        # append (+ key group flush, and value rows with a value residual, every G
+        # steps), decode attention, combine
+        flush = (n % self.wl.G) + 1 == self.wl.G
+        return 1 + (0 if not flush else (2 if self.vres0 is not None else 1)) + 2
 
     def attention(self, q, out, stream):
         self.kivi.kivi_decode_attention(self.cache, q, 1.0, out=out, ws=self.ws, stream=stream)
@@ -280,25 +288,29 @@ class PagedLayout:
     profile = "decode_attention_paged_llama2-7b-mha.md"
     kernel = "kivi_paged_decode_attention (paged decode_kernel + paged_combine_kernel)"
 
-    def __init__(self, wl, pre, dev, page_tokens, graph=False):
+    def __init__(self, wl, pre, dev, page_tokens, graph=False, value_residual=False):
         from bit_asymmetric_kv_gb300 import kivi, synth
 
         self.wl, self.kivi, self.P = wl, kivi, page_tokens
         self.graph, self.graphs = graph, {}
         maxp = math.ceil((wl.n + CYCLE + 64) / page_tokens)
         num_pages = wl.B * maxp
-        self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev)
+        self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev,
+                                              value_residual=value_residual)
         self.cache.block_table.copy_(synth.block_table(wl.B, maxp, num_pages, wl.seed))
         for b in range(wl.B):
             kivi.kivi_paged_prefill(self.cache, b, pre.k[b].to(dev), pre.v[b].to(dev))
         self.n0 = wl.n
         self.lens0 = self.cache.seq_lens.clone()
         self.res0 = self.cache.k_res.clone()
+        self.vres0 = None if self.cache.v_res is None else self.cache.v_res.clone()
         self.ws = kivi.paged_workspace(self.cache, wl.Hq, device=dev)
         self.ws.zero_()
 
     def rollback(self):
         self.cache.k_res.copy_(self.res0)
+        if self.vres0 is not None:
+            self.cache.v_res.copy_(self.vres0)
         self.cache.seq_lens.copy_(self.lens0)
 
     def prepare(self, inputs, out):
@@ -332,8 +344,8 @@ class PagedLayout:
 
 def make_layout(args, wl, pre, dev):
     if args.layout == "paged":
-        return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph)
-    return DenseLayout(wl, pre, dev)
+        return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph, value_residual=args.value_residual)
+    return DenseLayout(wl, pre, dev, value_residual=args.value_residual)
 
 
 # ----------------------------------------------------------------------------------------
@@ -415,7 +427,7 @@ def run_kivi(args, wl):
             attn_ms.append((e0, e1))
     torch.cuda.synchronize()
     attn_avg_ms = sum(a0.elapsed_time(a1) for a0, a1 in attn_ms) / len(attn_ms)
-    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0)
+    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0, args.value_residual)
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
@@ -431,7 +443,7 @@ def run_kivi(args, wl):
 
             dist.destroy_process_group()
         return 0
-    cb = oracle_timing(wl, pre, 64, 32, 2.0) if world == 1 else None
+    cb = oracle_timing(wl, pre, 64, 32, 2.0, args.value_residual) if world == 1 else None
     lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -458,13 +470,15 @@ def run_kivi(args, wl):
 
 
 def make_layout_config(args):
+    cfg = {"layout": "dense"}
     if args.layout == "paged":
         api = "kivi_paged_decode_step (append + decode attention + length advance)"
         if args.graph:
             api += ", replayed from a CUDA graph captured once per input set"
-        return {"layout": f"paged: {args.page_tokens} tokens per page, pages scattered by a seeded permutation",
-                "api": api}
-    return {"layout": "dense"}
+        cfg = {"layout": f"paged: {args.page_tokens} tokens per page, pages scattered by a seeded permutation",
+               "api": api}
+    cfg["value_residual"] = bool(args.value_residual)
+    return cfg
 
 
 def cycle_workspace(cache, wl, n0, dev):
@@ -584,6 +598,8 @@ def main(argv=None):
     ap.add_argument("--page-tokens", type=int, default=64, help="tokens per page of --layout paged")
     ap.add_argument("--graph", action="store_true",
                     help="--layout paged: replay each step from a captured CUDA graph")
+    ap.add_argument("--value-residual", action="store_true",
+                    help="keep the last n mod G values in fp16 beside the key residual (the variant cache)")
     ap.add_argument("--workload", default="llama2",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
                          "default: the Llama-2-7B MHA decode")

@@ -15,15 +15,37 @@ int check_dims(const kivi_dims *d) {
   if (d->B <= 0 || d->Hkv <= 0 || d->max_tokens <= 0) return KIVI_ERR_ARG;
   if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->max_tokens % d->G != 0) return KIVI_ERR_ARG;
+  if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
   return KIVI_OK;
 }
 
-int check_cache(const kivi_cache *c) {
+int check_cache(const kivi_dims *d, const kivi_cache *c) {
   if (!c || !c->k_codes || !c->k_meta || !c->k_res || !c->v_codes || !c->v_meta) return KIVI_ERR_ARG;
+  if (d->value_residual && !c->v_res) return KIVI_ERR_ARG;
   if (!aligned16(c->k_codes) || !aligned16(c->k_meta) || !aligned16(c->k_res) || !aligned16(c->v_codes) ||
-      !aligned16(c->v_meta))
+      !aligned16(c->v_meta) || (d->value_residual && !aligned16(c->v_res)))
     return KIVI_ERR_ALIGN;
   return KIVI_OK;
+}
+
+// The value residual buffer the kernels use: null without the variant.
+uint16_t *vres(const kivi_dims *d, const kivi_cache *c) { return d->value_residual ? c->v_res : nullptr; }
+
+// Append token n of every (batch, KV head); when that fills the residual, quantize
+// it as group n / G (keys per channel; with a value residual, values per token).
+cudaError_t append_and_flush(const kivi_dims *d, const kivi_cache *c, const uint16_t *k_new,
+                             const uint16_t *v_new, int64_t n, cudaStream_t st) {
+  const int64_t heads = (int64_t)d->B * d->Hkv;
+  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
+                                      d->max_tokens, vres(d, c), st);
+  if (e == cudaSuccess && (n % d->G) + 1 == d->G) {
+    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
+                                d->max_tokens, st);
+    if (e == cudaSuccess && d->value_residual)
+      e = kivi::launch_value_rows(c->v_res, heads, d->G, d->G, (n / d->G) * d->G, c->v_codes, c->v_meta,
+                                  d->max_tokens, st);
+  }
+  return e;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KIVI_OK : KIVI_ERR_CUDA; }
@@ -49,6 +71,7 @@ int check_paged_dims(const kivi_paged_dims *d) {
   if (!d) return KIVI_ERR_ARG;
   if (d->B <= 0 || d->Hkv <= 0 || d->page_tokens <= 0 || d->max_pages_per_seq <= 0 || d->num_pages <= 0)
     return KIVI_ERR_ARG;
+  if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
   if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->B > kivi::kPagedMaxBatch) return KIVI_ERR_UNSUPPORTED;
   const int sh = page_shift_of(d->page_tokens);
@@ -61,14 +84,20 @@ int check_paged_dims(const kivi_paged_dims *d) {
   return KIVI_OK;
 }
 
-int check_paged_cache(const kivi_paged_cache *c) {
+int check_paged_cache(const kivi_paged_dims *d, const kivi_paged_cache *c) {
   if (!c || !c->k_codes || !c->k_meta || !c->v_codes || !c->v_meta || !c->k_res || !c->block_table ||
       !c->seq_lens)
     return KIVI_ERR_ARG;
+  if (d->value_residual && !c->v_res) return KIVI_ERR_ARG;
   if (!aligned16(c->k_codes) || !aligned16(c->k_meta) || !aligned16(c->v_codes) || !aligned16(c->v_meta) ||
-      !aligned16(c->k_res) || !aligned4(c->block_table) || !aligned4(c->seq_lens))
+      !aligned16(c->k_res) || !aligned4(c->block_table) || !aligned4(c->seq_lens) ||
+      (d->value_residual && !aligned16(c->v_res)))
     return KIVI_ERR_ALIGN;
   return KIVI_OK;
+}
+
+uint16_t *paged_vres(const kivi_paged_dims *d, const kivi_paged_cache *c) {
+  return d->value_residual ? c->v_res : nullptr;
 }
 
 int check_paged_heads(const kivi_paged_dims *d, int32_t Hq) {
@@ -89,6 +118,7 @@ kivi::PagedAppendArgs paged_append_args(const kivi_paged_dims *d, const kivi_pag
   a.bt = c->block_table;
   a.seq_lens = c->seq_lens;
   a.k_res = c->k_res;
+  a.v_res = paged_vres(d, c);
   a.k_codes = c->k_codes;
   a.k_meta = c->k_meta;
   a.v_codes = c->v_codes;
@@ -111,6 +141,7 @@ kivi::DecodeArgs paged_decode_args(const kivi_paged_dims *d, const kivi_paged_ca
   a.k_res = c->k_res;
   a.v_codes = c->v_codes;
   a.v_meta = c->v_meta;
+  a.v_res = paged_vres(d, c);
   a.q = q;
   a.out = out;
   a.ws = static_cast<float *>(ws);
@@ -147,7 +178,7 @@ const char *kivi_status_string(int s) {
   }
 }
 
-int kivi_buffer_bytes(const kivi_dims *d, size_t out[5]) {
+int kivi_buffer_bytes(const kivi_dims *d, size_t out[6]) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
   if (!out) return KIVI_ERR_ARG;
@@ -158,6 +189,7 @@ int kivi_buffer_bytes(const kivi_dims *d, size_t out[5]) {
   out[2] = heads * (size_t)d->G * d->D * sizeof(uint16_t);
   out[3] = heads * T * (d->D / 16) * sizeof(uint32_t);
   out[4] = heads * T * sizeof(uint32_t);
+  out[5] = d->value_residual ? out[2] : 0;
   return KIVI_OK;
 }
 
@@ -165,7 +197,7 @@ int kivi_quantize_prefill(const kivi_dims *d, kivi_cache *c, const uint16_t *k, 
                           cudaStream_t st) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_cache(d, c)) != KIVI_OK) return s;
   if (n < 0) return KIVI_ERR_ARG;
   if (n > d->max_tokens) return KIVI_ERR_CAPACITY;
   if (n > 0) {
@@ -176,8 +208,11 @@ int kivi_quantize_prefill(const kivi_dims *d, kivi_cache *c, const uint16_t *k, 
     cudaError_t e = kivi::launch_key_groups(k, n * 128, heads, groups, 0, d->G, c->k_codes, c->k_meta,
                                             d->max_tokens, st);
     if (e == cudaSuccess) e = kivi::launch_residual_copy(k, heads, n, nq, d->G, c->k_res, st);
+    // values: all n quantized, or with a value residual the first nq and the rest kept
+    const int64_t nv = d->value_residual ? nq : n;
     if (e == cudaSuccess)
-      e = kivi::launch_value_rows(v, heads, n, 0, c->v_codes, c->v_meta, d->max_tokens, st);
+      e = kivi::launch_value_rows(v, heads, nv, n, 0, c->v_codes, c->v_meta, d->max_tokens, st);
+    if (e == cudaSuccess && d->value_residual) e = kivi::launch_residual_copy(v, heads, n, nq, d->G, c->v_res, st);
     if ((s = cuda_status(e)) != KIVI_OK) return s;
   }
   c->n_tokens = n;
@@ -188,19 +223,13 @@ int kivi_append_token(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, 
                       cudaStream_t st) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_cache(d, c)) != KIVI_OK) return s;
   if (!k_new || !v_new) return KIVI_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_ERR_ALIGN;
   const int64_t n = c->n_tokens;
   if (n < 0) return KIVI_ERR_ARG;
   if (n >= d->max_tokens) return KIVI_ERR_CAPACITY;
-  const int64_t heads = (int64_t)d->B * d->Hkv;
-  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
-                                      d->max_tokens, st);
-  if (e == cudaSuccess && (n % d->G) + 1 == d->G)  // the residual is full: flush it as group n / G
-    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
-                                d->max_tokens, st);
-  if ((s = cuda_status(e)) != KIVI_OK) return s;
+  if ((s = cuda_status(append_and_flush(d, c, k_new, v_new, n, st))) != KIVI_OK) return s;
   c->n_tokens = n + 1;
   return KIVI_OK;
 }
@@ -222,7 +251,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
                           float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t st) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_cache(d, c)) != KIVI_OK) return s;
   if ((s = check_heads(d, Hq)) != KIVI_OK) return s;
   if (!q || !out) return KIVI_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
@@ -238,6 +267,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.k_res = c->k_res;
   a.v_codes = c->v_codes;
   a.v_meta = c->v_meta;
+  a.v_res = vres(d, c);
   a.q = q;
   a.out = out;
   a.ws = static_cast<float *>(ws);
@@ -262,7 +292,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
                      cudaStream_t st) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_cache(d, c)) != KIVI_OK) return s;
   if ((s = check_heads(d, Hq)) != KIVI_OK) return s;
   if (!k_new || !v_new || !q || !out) return KIVI_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
@@ -275,13 +305,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
   // 1. append (and flush a full residual group)
-  const int64_t heads = (int64_t)d->B * d->Hkv;
-  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
-                                      d->max_tokens, st);
-  if (e == cudaSuccess && (n % d->G) + 1 == d->G)
-    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
-                                d->max_tokens, st);
-  if ((s = cuda_status(e)) != KIVI_OK) return s;
+  if ((s = cuda_status(append_and_flush(d, c, k_new, v_new, n, st))) != KIVI_OK) return s;
   // 2. decode attention over n + 1 tokens, overlapping the append: only the last
   //    unit of each head (the one holding the new token) waits for it
   kivi::DecodeArgs a = {};
@@ -290,6 +314,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   a.k_res = c->k_res;
   a.v_codes = c->v_codes;
   a.v_meta = c->v_meta;
+  a.v_res = vres(d, c);
   a.q = q;
   a.out = out;
   a.ws = static_cast<float *>(ws);
@@ -314,11 +339,11 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
 int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out, float *v_out, cudaStream_t st) {
   int s = check_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_cache(c)) != KIVI_OK) return s;
+  if ((s = check_cache(d, c)) != KIVI_OK) return s;
   if (!k_out || !v_out) return KIVI_ERR_ARG;
   if (!aligned16(k_out) || !aligned16(v_out)) return KIVI_ERR_ALIGN;
   if (c->n_tokens < 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
-  return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta,
+  return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta, vres(d, c),
                                           (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->max_tokens, k_out, v_out,
                                           st));
 }
@@ -372,7 +397,7 @@ int kivi_decode_attention_fp16(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, in
 }
 
 // ---------------------------------------------------------------------- paged cache
-int kivi_paged_buffer_bytes(const kivi_paged_dims *d, size_t out[7]) {
+int kivi_paged_buffer_bytes(const kivi_paged_dims *d, size_t out[8]) {
   int s = check_paged_dims(d);
   if (s != KIVI_OK) return s;
   if (!out) return KIVI_ERR_ARG;
@@ -384,6 +409,7 @@ int kivi_paged_buffer_bytes(const kivi_paged_dims *d, size_t out[7]) {
   out[4] = (size_t)d->B * d->Hkv * d->G * d->D * sizeof(uint16_t);
   out[5] = (size_t)d->B * d->max_pages_per_seq * sizeof(int32_t);
   out[6] = (size_t)d->B * sizeof(int32_t);
+  out[7] = d->value_residual ? out[4] : 0;
   return KIVI_OK;
 }
 
@@ -391,7 +417,7 @@ int kivi_paged_prefill(const kivi_paged_dims *d, const kivi_paged_cache *c, int3
                        const uint16_t *v, int64_t n, cudaStream_t st) {
   int s = check_paged_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_cache(d, c)) != KIVI_OK) return s;
   if (seq < 0 || seq >= d->B || n < 0) return KIVI_ERR_ARG;
   if (n > paged_cap(d)) return KIVI_ERR_CAPACITY;
   cudaError_t e = cudaSuccess;
@@ -407,7 +433,10 @@ int kivi_paged_prefill(const kivi_paged_dims *d, const kivi_paged_cache *c, int3
     e = kivi::launch_key_groups_paged(k, n * 128, d->Hkv, groups, d->G, pm, c->k_codes, c->k_meta, st);
     if (e == cudaSuccess)
       e = kivi::launch_residual_copy(k, d->Hkv, n, nq, d->G, c->k_res + (int64_t)seq * d->Hkv * d->G * 128, st);
-    if (e == cudaSuccess) e = kivi::launch_value_rows_paged(v, d->Hkv, n, pm, c->v_codes, c->v_meta, st);
+    const int64_t nv = d->value_residual ? nq : n;
+    if (e == cudaSuccess) e = kivi::launch_value_rows_paged(v, d->Hkv, nv, n, pm, c->v_codes, c->v_meta, st);
+    if (e == cudaSuccess && d->value_residual)
+      e = kivi::launch_residual_copy(v, d->Hkv, n, nq, d->G, c->v_res + (int64_t)seq * d->Hkv * d->G * 128, st);
   }
   if (e == cudaSuccess) e = kivi::launch_set_len(c->seq_lens, seq, (int32_t)n, st);
   return cuda_status(e);
@@ -417,7 +446,7 @@ int kivi_paged_append_token(const kivi_paged_dims *d, const kivi_paged_cache *c,
                             const uint16_t *v_new, cudaStream_t st) {
   int s = check_paged_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_cache(d, c)) != KIVI_OK) return s;
   if (!k_new || !v_new) return KIVI_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_ERR_ALIGN;
   cudaError_t e = kivi::launch_paged_append(paged_append_args(d, c, k_new, v_new), st);
@@ -436,7 +465,7 @@ int kivi_paged_decode_attention(const kivi_paged_dims *d, const kivi_paged_cache
                                 float softmax_scale, uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t st) {
   int s = check_paged_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_cache(d, c)) != KIVI_OK) return s;
   if ((s = check_paged_heads(d, Hq)) != KIVI_OK) return s;
   if (!q || !out) return KIVI_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
@@ -453,7 +482,7 @@ int kivi_paged_decode_step(const kivi_paged_dims *d, const kivi_paged_cache *c, 
                            void *ws, size_t ws_bytes, cudaStream_t st) {
   int s = check_paged_dims(d);
   if (s != KIVI_OK) return s;
-  if ((s = check_paged_cache(c)) != KIVI_OK) return s;
+  if ((s = check_paged_cache(d, c)) != KIVI_OK) return s;
   if ((s = check_paged_heads(d, Hq)) != KIVI_OK) return s;
   if (!k_new || !v_new || !q || !out) return KIVI_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;

@@ -323,6 +323,50 @@ __device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
   __syncthreads();
 }
 
+// P.V of one step over fp16 values (the value residual): the same tile and column
+// layout as pv_step, with A built from the values of tokens tig, tig+4, tig+8,
+// tig+12 of each tile (channels 16g + j and 16g + 8 + j for MMA j) instead of
+// unpacked codes.  `rows` points at the step's first token row; tokens at or beyond
+// n_valid read as zero.  The accumulators must hold output units (no code factors).
+template <int R>
+__device__ __forceinline__ void pv_step_f16(float acc[8][4], const LaneInfo &li, int n_valid, uint32_t bw0,
+                                            uint32_t bw1, float alpha, const uint16_t *rows) {
+  constexpr int T = 4 / R;
+  if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[j][k] *= alpha;
+  }
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    if (16 * i < n_valid) {
+      uint32_t w[4][8];  // token tig + 4k: channels 16g .. 16g+15 as 8 half2 words
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int tok = 16 * i + li.tig + 4 * k;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if (tok < n_valid) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(rows + tok * kD + 16 * li.g);
+          lo = __ldg(src);
+          hi = __ldg(src + 1);
+        }
+        w[k][0] = lo.x; w[k][1] = lo.y; w[k][2] = lo.z; w[k][3] = lo.w;
+        w[k][4] = hi.x; w[k][5] = hi.y; w[k][6] = hi.z; w[k][7] = hi.w;
+      }
+      const bool mine = li.pv_slot == i;
+      const uint32_t b0 = mine ? bw0 : 0u, b1 = mine ? bw1 : 0u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+        const int x = j >> 1, y = 4 + (j >> 1);  // words of channels 16g + j and 16g + 8 + j
+        mma16816(acc[j], prmt(w[0][x], w[1][x], sel), prmt(w[0][y], w[1][y], sel), prmt(w[2][x], w[3][x], sel),
+                 prmt(w[2][y], w[3][y], sel), b0, b1);
+      }
+    }
+  }
+}
+
 template <int R, int G, bool PAGED>
 __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -500,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   float qv[R][4];
 
   // Write the partial of head h (this warp's share of it) from the P.V accumulators
-  // and the softmax state (m, l, zs) that belongs to them.
+  // and the softmax state (m, l, zs) that belongs to them.  acc_true: the
+  // accumulators already hold output units (a value residual was added to them).
+  bool acc_true = false;
   auto emit = [&](int64_t h, const SoftState &fin) {
     float l = fin.l, zs = fin.zs;
 #pragma unroll
@@ -535,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         // undo the code factor 4^(j mod 4) and the 2^-24 of the subnormal codes
-        const float un = pow2i(24 - 2 * (j & 3));
+        const float un = acc_true ? 1.f : pow2i(24 - 2 * (j & 3));
         dst[16 * g + j] = fmaf(o[j], un, zs);
         dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs);
       }
@@ -548,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     for (int j = 0; j < 8; ++j)
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
+    acc_true = false;
   };
   auto load_q = [&](const Cursor &c) {
     int64_t b, kvh;
@@ -720,7 +767,9 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
           residual_pairs(res_head + sb_slot * kD, sb_slot < r, tig, rb0, rb1);
           qk_tile(ra0, ra1, rb0, rb1, bf, sc);
         };
-        auto vmeta = [&](int tok) -> uint32_t { return vm_head[base + tok]; };
+        // residual values are quantized ({s, z} of their row) or, with a value
+        // residual, fp16 themselves: weight p with s = 1, z = 0
+        auto vmeta = [&](int tok) -> uint32_t { return a.v_res ? 0x00003C00u : vm_head[base + tok]; };
         qk_step<R, false>(ss, li, kfill, c0, 0.f, min(16 * T, r - base), vmeta, nw0[s], nw1[s], nalpha[s]);
       }
       n_kind = 2;
@@ -737,6 +786,23 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         pv_step<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
           return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
         });
+      }
+    } else if (a.v_res) {
+      // fp16 residual values: this is the head's last unit, so the accumulators move
+      // to output units here and the head's partial is written without code factors
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float un = pow2i(24 - 2 * (j & 3));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[j][k] *= un;
+      }
+      acc_true = true;
+      const uint16_t *vres_head = a.v_res + cc.h * G * kD;
+#pragma unroll
+      for (int s = 0; s < R; ++s) {
+        const int nv = min(16 * T, n_ntok - 16 * T * s);
+        if (nv <= 0) break;
+        pv_step_f16<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], vres_head + 16 * T * s * kD);
       }
     } else {
       const uint32_t *vc_head = a.v_codes + n_res_row * kWordsPerRow;

@@ -9,10 +9,11 @@ namespace kivi {
 cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_t heads, int64_t groups_per_head,
                               int64_t g0, int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
                               cudaStream_t st);
-cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t t0,
-                              uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st);
+cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
+                              int64_t t0, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st);
 cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G,
-                          uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st);
+                          uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
+                          cudaStream_t st);
 cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, int64_t nq, int G, uint16_t *k_res,
                                  cudaStream_t st);
 // Paged destinations of a prefill: the block-table row of one sequence.
@@ -25,8 +26,9 @@ struct PageMap {
 cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, int64_t heads,
                                     int64_t groups_per_head, int G, const PageMap &pm, uint32_t *k_codes,
                                     uint32_t *k_meta, cudaStream_t st);
-cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head, const PageMap &pm,
-                                    uint32_t *v_codes, uint32_t *v_meta, cudaStream_t st);
+cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head,
+                                    int64_t in_rows_per_head, const PageMap &pm, uint32_t *v_codes,
+                                    uint32_t *v_meta, cudaStream_t st);
 cudaError_t launch_set_len(int32_t *seq_lens, int32_t seq, int32_t n, cudaStream_t st);
 
 // Paged append of one token per (sequence, KV head) at position seq_lens[b], with the
@@ -37,6 +39,7 @@ struct PagedAppendArgs {
   const int32_t *bt;              // [B][max_pages]
   int32_t *seq_lens;              // [B]
   uint16_t *k_res;                // [B][Hkv][G][128]
+  uint16_t *v_res;                // [B][Hkv][G][128] with a value residual, else null
   uint32_t *k_codes, *k_meta, *v_codes, *v_meta;
   int64_t num_pages;
   int B, Hkv, G, shift, max_pages;
@@ -45,8 +48,8 @@ cudaError_t launch_paged_append(const PagedAppendArgs &a, cudaStream_t st);
 cudaError_t launch_advance_lens(int32_t *seq_lens, int B, int32_t cap, cudaStream_t st);
 
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
-                           const uint32_t *v_codes, const uint32_t *v_meta, int64_t heads, int64_t n, int G,
-                           int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st);
+                           const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
+                           int64_t n, int G, int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st);
 
 struct DecodeArgs {
   const uint32_t *k_codes;
@@ -54,6 +57,7 @@ struct DecodeArgs {
   const uint16_t *k_res;
   const uint32_t *v_codes;
   const uint32_t *v_meta;
+  const uint16_t *v_res;   // fp16 residual values [B][Hkv][G][128], or null (values all quantized)
   const uint16_t *q;
   uint16_t *out;
   float *ws;

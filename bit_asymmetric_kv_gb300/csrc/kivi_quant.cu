@@ -139,11 +139,12 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   if (lane16 == 0) *meta_out = p.meta;
 }
 
-// rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head
+// rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
+// read from input row (head * in_rows_per_head + r % tokens_per_head)
 template <bool PAGED>
 __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restrict__ v, int64_t rows,
-                                                         int64_t tokens_per_head, int64_t t0,
-                                                         uint32_t *__restrict__ v_codes,
+                                                         int64_t tokens_per_head, int64_t in_rows_per_head,
+                                                         int64_t t0, uint32_t *__restrict__ v_codes,
                                                          uint32_t *__restrict__ v_meta, int64_t max_tokens,
                                                          const PageMap pm) {
   const int lane = threadIdx.x & 31;
@@ -152,23 +153,26 @@ __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restr
   const int64_t half_warps = (int64_t)gridDim.x * (blockDim.x >> 4);
   for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4); row < rows; row += half_warps) {
     const int64_t bh = row / tokens_per_head;
-    const int64_t t = t0 + row % tokens_per_head;
+    const int64_t i = row - bh * tokens_per_head;
+    const int64_t t = t0 + i;
     int64_t dst = bh * max_tokens + t;
     if constexpr (PAGED) {
       if (!paged_row(pm, bh, t, &dst)) continue;  // the half-warp skips the row together
     }
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + row * kD) + lane16);
+    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + lane16);
     quantize_value_row(x, lane16, half_mask, v_codes + dst * kWordsPerRow, v_meta + dst);
   }
 }
 
-// Append: one warp per (batch, KV head).  Lanes 0-15 quantize the new value row;
-// lanes 16-31 copy the new key (256 bytes) into residual slot r.
+// Append: one warp per (batch, KV head).  Lanes 0-15 quantize the new value row (or,
+// with a value residual, copy it into residual slot r); lanes 16-31 copy the new
+// key (256 bytes) into residual slot r.
 __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict__ k_new,
                                                      const uint16_t *__restrict__ v_new, int64_t heads,
                                                      int64_t n, int G, uint16_t *__restrict__ k_res,
                                                      uint32_t *__restrict__ v_codes,
-                                                     uint32_t *__restrict__ v_meta, int64_t max_tokens) {
+                                                     uint32_t *__restrict__ v_meta, int64_t max_tokens,
+                                                     uint16_t *__restrict__ v_res) {
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -177,8 +181,11 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
   const int lane16 = lane & 15;
   if (lane < 16) {
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v_new + bh * kD) + lane16);
-    quantize_value_row(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * kWordsPerRow,
-                       v_meta + bh * max_tokens + n);
+    if (v_res)
+      reinterpret_cast<uint4 *>(v_res + (bh * G + n % G) * kD)[lane16] = x;
+    else
+      quantize_value_row(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * kWordsPerRow,
+                         v_meta + bh * max_tokens + n);
   } else {
     const int64_t r = n % G;
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(k_new + bh * kD) + lane16);
@@ -188,7 +195,9 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
 
 // Paged append: one warp per (sequence b, KV head), the token at position
 // len = seq_lens[b] of sequence b.  Lanes 0-15 quantize the value row into the page
-// that holds position len; lanes 16-31 copy the key into residual slot len mod G.
+// that holds position len (with a value residual: copy it into residual slot
+// len mod G, and the group's G values are quantized row by row at the flush);
+// lanes 16-31 copy the key into residual slot len mod G.
 // When that slot is the group's last one, the warp quantizes the group at once
 // (sequences of a batch fill their groups on different steps): lane l takes channels
 // 4l .. 4l+3 of the G keys (slots 0 .. G-2 from the residual, the new key from the
@@ -212,7 +221,11 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
   const int r = len % G;
   if (lane < 16) {
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.v_new + bh * kD) + lane16);
-    quantize_value_row(x, lane16, 0x0000ffffu, a.v_codes + (ph * P + off) * kWordsPerRow, a.v_meta + ph * P + off);
+    if (a.v_res)
+      reinterpret_cast<uint4 *>(a.v_res + (bh * G + r) * kD)[lane16] = x;
+    else
+      quantize_value_row(x, lane16, 0x0000ffffu, a.v_codes + (ph * P + off) * kWordsPerRow,
+                         a.v_meta + ph * P + off);
   } else {
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.k_new + bh * kD) + lane16);
     reinterpret_cast<uint4 *>(a.k_res + (bh * G + r) * kD)[lane16] = x;
@@ -251,6 +264,17 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
     bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
     if ((lane & 3) == 0) dst[t * kWordsPerRow] = bits;
   }
+  if (a.v_res) {
+    // the group's values, one token row per half-warp (slots 0 .. G-2 from the
+    // residual, the new value from the input)
+    const int half = lane >> 4;
+    const uint32_t half_mask = half ? 0xffff0000u : 0x0000ffffu;
+    for (int t = half; t < G; t += 2) {
+      const uint16_t *src = (t == G - 1) ? a.v_new + bh * kD : a.v_res + (bh * G + t) * kD;
+      const uint4 x = reinterpret_cast<const uint4 *>(src)[lane16];
+      quantize_value_row(x, lane16, half_mask, a.v_codes + (row0 + t) * kWordsPerRow, a.v_meta + row0 + t);
+    }
+  }
 }
 
 __global__ void set_len_kernel(int32_t *seq_lens, int32_t seq, int32_t n) { seq_lens[seq] = n; }
@@ -280,7 +304,8 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
                                                       const uint32_t *__restrict__ v_codes,
                                                       const uint32_t *__restrict__ v_meta, int64_t heads, int64_t n,
                                                       int G, int64_t max_tokens, float *__restrict__ k_out,
-                                                      float *__restrict__ v_out) {
+                                                      float *__restrict__ v_out,
+                                                      const uint16_t *__restrict__ v_res) {
   const int64_t total = heads * n * (kD / 8);
   const int64_t nq = (n / G) * G;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -302,6 +327,12 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
       const uint16_t *res = k_res + (bh * G + (t - nq)) * kD + c0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) ko[j] = h2f(res[j]);
+    }
+    if (v_res && t >= nq) {
+      const uint16_t *res = v_res + (bh * G + (t - nq)) * kD + c0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) vo[j] = h2f(res[j]);
+      continue;
     }
     const uint32_t vm = v_meta[bh * max_tokens + t];
     const float s = h2f((uint16_t)(vm & 0xffffu)), z = h2f((uint16_t)(vm >> 16));
@@ -346,28 +377,30 @@ cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t t0,
-                              uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
+cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
+                              int64_t t0, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  value_rows_kernel<false><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, t0, v_codes,
-                                                                       v_meta, max_tokens, PageMap{});
+  value_rows_kernel<false><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head,
+                                                                       t0, v_codes, v_meta, max_tokens, PageMap{});
   return cudaGetLastError();
 }
 
-cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head, const PageMap &pm,
-                                    uint32_t *v_codes, uint32_t *v_meta, cudaStream_t st) {
+cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head,
+                                    int64_t in_rows_per_head, const PageMap &pm, uint32_t *v_codes,
+                                    uint32_t *v_meta, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  value_rows_kernel<true><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, 0, v_codes, v_meta,
-                                                                      0, pm);
+  value_rows_kernel<true><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0,
+                                                                      v_codes, v_meta, 0, pm);
   return cudaGetLastError();
 }
 
 cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G,
-                          uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
+                          uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
+                          cudaStream_t st) {
   append_kernel<<<(unsigned)((heads + 3) / 4), 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta,
-                                                             max_tokens);
+                                                             max_tokens, v_res);
   return cudaGetLastError();
 }
 
@@ -399,12 +432,12 @@ cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, in
 }
 
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
-                           const uint32_t *v_codes, const uint32_t *v_meta, int64_t heads, int64_t n, int G,
-                           int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st) {
+                           const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
+                           int64_t n, int G, int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st) {
   const int64_t total = heads * n * (kD / 8);
   if (total == 0) return cudaSuccess;
   dequant_kernel<<<grid_cap((total + 255) / 256), 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G,
-                                                                max_tokens, k_out, v_out);
+                                                                max_tokens, k_out, v_out, v_res);
   return cudaGetLastError();
 }
 

@@ -30,24 +30,25 @@ class KiviError(RuntimeError):
 
 class kivi_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("G", ctypes.c_int32),
-                ("bits", ctypes.c_int32), ("max_tokens", ctypes.c_int64)]
+                ("bits", ctypes.c_int32), ("value_residual", ctypes.c_int32), ("max_tokens", ctypes.c_int64)]
 
 
 class kivi_cache(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_meta", ctypes.c_void_p), ("k_res", ctypes.c_void_p),
-                ("v_codes", ctypes.c_void_p), ("v_meta", ctypes.c_void_p), ("n_tokens", ctypes.c_int64)]
+                ("v_codes", ctypes.c_void_p), ("v_meta", ctypes.c_void_p), ("v_res", ctypes.c_void_p),
+                ("n_tokens", ctypes.c_int64)]
 
 
 class kivi_paged_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("G", ctypes.c_int32),
-                ("bits", ctypes.c_int32), ("page_tokens", ctypes.c_int32), ("max_pages_per_seq", ctypes.c_int32),
-                ("num_pages", ctypes.c_int64)]
+                ("bits", ctypes.c_int32), ("value_residual", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("num_pages", ctypes.c_int64)]
 
 
 class kivi_paged_cache(ctypes.Structure):
     _fields_ = [("k_codes", ctypes.c_void_p), ("k_meta", ctypes.c_void_p), ("v_codes", ctypes.c_void_p),
-                ("v_meta", ctypes.c_void_p), ("k_res", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
-                ("seq_lens", ctypes.c_void_p)]
+                ("v_meta", ctypes.c_void_p), ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p)]
 
 
 _lib = None
@@ -121,12 +122,13 @@ def _f16(t: torch.Tensor, name: str) -> torch.Tensor:
     return t
 
 
-def make_dims(B: int, Hkv: int, G: int, max_tokens: int, D: int = 128, bits: int = 2) -> kivi_dims:
-    return kivi_dims(B, Hkv, D, G, bits, max_tokens)
+def make_dims(B: int, Hkv: int, G: int, max_tokens: int, D: int = 128, bits: int = 2,
+              value_residual: bool = False) -> kivi_dims:
+    return kivi_dims(B, Hkv, D, G, bits, int(value_residual), max_tokens)
 
 
 def kivi_buffer_bytes(dims: kivi_dims) -> list[int]:
-    out = (ctypes.c_size_t * 5)()
+    out = (ctypes.c_size_t * 6)()
     _check(lib().kivi_buffer_bytes(ctypes.byref(dims), out), "kivi_buffer_bytes")
     return list(out)
 
@@ -142,14 +144,16 @@ class Cache:
     v_codes: torch.Tensor  # int32 [B, Hkv, T, D/16]
     v_meta: torch.Tensor   # int32 [B, Hkv, T]
     c: kivi_cache
+    v_res: torch.Tensor | None = None  # fp16 [B, Hkv, G, D] with a value residual
 
     @property
     def n_tokens(self) -> int:
         return int(self.c.n_tokens)
 
     @classmethod
-    def allocate(cls, B: int, Hkv: int, G: int, max_tokens: int, device="cuda", D: int = 128) -> "Cache":
-        dims = make_dims(B, Hkv, G, max_tokens, D)
+    def allocate(cls, B: int, Hkv: int, G: int, max_tokens: int, device="cuda", D: int = 128,
+                 value_residual: bool = False) -> "Cache":
+        dims = make_dims(B, Hkv, G, max_tokens, D, value_residual=value_residual)
         kivi_buffer_bytes(dims)  # validates the geometry
         T = max_tokens
         kc = torch.empty((B, Hkv, T, D // 16), dtype=torch.int32, device=device)
@@ -157,8 +161,10 @@ class Cache:
         kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
         vc = torch.empty((B, Hkv, T, D // 16), dtype=torch.int32, device=device)
         vm = torch.empty((B, Hkv, T), dtype=torch.int32, device=device)
-        c = kivi_cache(kc.data_ptr(), km.data_ptr(), kr.data_ptr(), vc.data_ptr(), vm.data_ptr(), 0)
-        return cls(dims, kc, km, kr, vc, vm, c)
+        vr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device) if value_residual else None
+        c = kivi_cache(kc.data_ptr(), km.data_ptr(), kr.data_ptr(), vc.data_ptr(), vm.data_ptr(),
+                       0 if vr is None else vr.data_ptr(), 0)
+        return cls(dims, kc, km, kr, vc, vm, c, vr)
 
 
 def kivi_quantize_prefill(cache: Cache, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
@@ -283,12 +289,12 @@ def kivi_status_string(status: int) -> str:
 # paged cache
 # ---------------------------------------------------------------------------------------
 def make_paged_dims(B: int, Hkv: int, G: int, page_tokens: int, max_pages_per_seq: int, num_pages: int,
-                    D: int = 128, bits: int = 2) -> kivi_paged_dims:
-    return kivi_paged_dims(B, Hkv, D, G, bits, page_tokens, max_pages_per_seq, num_pages)
+                    D: int = 128, bits: int = 2, value_residual: bool = False) -> kivi_paged_dims:
+    return kivi_paged_dims(B, Hkv, D, G, bits, int(value_residual), page_tokens, max_pages_per_seq, num_pages)
 
 
 def kivi_paged_buffer_bytes(dims: kivi_paged_dims) -> list[int]:
-    out = (ctypes.c_size_t * 7)()
+    out = (ctypes.c_size_t * 8)()
     _check(lib().kivi_paged_buffer_bytes(ctypes.byref(dims), out), "kivi_paged_buffer_bytes")
     return list(out)
 
@@ -307,11 +313,13 @@ class PagedCache:
     block_table: torch.Tensor  # int32 [B, max_pages_per_seq]
     seq_lens: torch.Tensor     # int32 [B]
     c: kivi_paged_cache
+    v_res: torch.Tensor | None = None  # fp16 [B, Hkv, G, D] with a value residual
 
     @classmethod
     def allocate(cls, B: int, Hkv: int, G: int, page_tokens: int, max_pages_per_seq: int, num_pages: int,
-                 device="cuda", D: int = 128) -> "PagedCache":
-        dims = make_paged_dims(B, Hkv, G, page_tokens, max_pages_per_seq, num_pages, D)
+                 device="cuda", D: int = 128, value_residual: bool = False) -> "PagedCache":
+        dims = make_paged_dims(B, Hkv, G, page_tokens, max_pages_per_seq, num_pages, D,
+                               value_residual=value_residual)
         kivi_paged_buffer_bytes(dims)  # validates the geometry
         P = page_tokens
         kc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
@@ -319,11 +327,12 @@ class PagedCache:
         vc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
         vm = torch.empty((num_pages, Hkv, P), dtype=torch.int32, device=device)
         kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
+        vr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device) if value_residual else None
         bt = torch.zeros((B, max_pages_per_seq), dtype=torch.int32, device=device)
         sl = torch.zeros((B,), dtype=torch.int32, device=device)
         c = kivi_paged_cache(kc.data_ptr(), km.data_ptr(), vc.data_ptr(), vm.data_ptr(), kr.data_ptr(),
-                             bt.data_ptr(), sl.data_ptr())
-        return cls(dims, kc, km, vc, vm, kr, bt, sl, c)
+                             0 if vr is None else vr.data_ptr(), bt.data_ptr(), sl.data_ptr())
+        return cls(dims, kc, km, vc, vm, kr, bt, sl, c, vr)
 
 
 def kivi_paged_prefill(cache: PagedCache, seq: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:

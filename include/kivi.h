@@ -21,6 +21,9 @@
  *   - one (scale, zero) pair per value token per KV head over all D channels;
  *   - only keys have a residual; a key group is quantized ("flushed") as soon as it
  *     holds G tokens, so the residual holds n mod G tokens;
+ *   - variant (value_residual = 1): the values keep the same residual as the keys,
+ *     in fp16, and the G values of a group are quantized token by token when the
+ *     key group flushes;
  *   - query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
  *
  * Supported shapes: D = 128, bits = 2, G in {32, 64}, Hq / Hkv in {1, 2, 4}.
@@ -33,12 +36,14 @@
  *   k_res    fp16   [B][Hkv][G][D]              residual keys, slot j = token nq + j
  *   v_codes  uint32 [B][Hkv][max_tokens][D/16]  token rows of packed value codes
  *   v_meta   uint32 [B][Hkv][max_tokens]        per token {s, z}
+ *   v_res    fp16   [B][Hkv][G][D]              residual values (value_residual = 1
+ *                                               only; NULL otherwise)
  * A {s, z} word holds the fp16 scale in bits 0-15 and the fp16 zero in bits 16-31.
  * Packing: word w of a token row holds channels 16w .. 16w+15; channel 16w+i sits
  * in bits [2i, 2i+1].  fp16 buffers are IEEE binary16 bit patterns (uint16_t).
  * nq = floor(n / G) * G tokens are quantized keys; rows at or beyond nq of k_codes,
  * groups at or beyond n / G of k_meta, residual slots at or beyond n mod G and
- * value rows at or beyond n are not read.
+ * value rows at or beyond n (at or beyond nq with a value residual) are not read.
  *
  * Streams and state: every compute call is asynchronous on the given stream and
  * never synchronises with the host.  The only state is the caller's kivi_cache;
@@ -81,6 +86,7 @@ typedef struct {
   int32_t D;         /* head dim, 128 */
   int32_t G;         /* key group size, 32 or 64 */
   int32_t bits;      /* code width, 2 */
+  int32_t value_residual; /* 1: values keep an fp16 residual beside the keys'; 0: none */
   int64_t max_tokens;
 } kivi_dims;
 
@@ -91,18 +97,20 @@ typedef struct {
   uint16_t *k_res;
   uint32_t *v_codes;
   uint32_t *v_meta;
+  uint16_t *v_res;   /* value_residual = 1 only; may be NULL otherwise */
   int64_t n_tokens;
 } kivi_cache;
 
-/* Bytes of the five cache buffers, in the order k_codes, k_meta, k_res, v_codes,
- * v_meta.  Pure host arithmetic. */
-KIVI_API int kivi_buffer_bytes(const kivi_dims *dims, size_t out_bytes[5]);
+/* Bytes of the cache buffers, in the order k_codes, k_meta, k_res, v_codes, v_meta,
+ * v_res (0 without a value residual).  Pure host arithmetic. */
+KIVI_API int kivi_buffer_bytes(const kivi_dims *dims, size_t out_bytes[6]);
 
 /*
  * Quantize a prompt of n tokens into an empty cache (headline paragraph; section
  * "Iddia ve Gerceklik", paragraphs 2-3).  k, v: fp16 [B][Hkv][n][D] device.
  * Keys of the floor(n/G) full groups are quantized per channel; the last n mod G
- * keys are copied to k_res; all n values are quantized per token.  Sets
+ * keys are copied to k_res; all n values are quantized per token (with a value
+ * residual: the first floor(n/G)*G, the last n mod G go to v_res).  Sets
  * cache->n_tokens = n.  n == 0 launches nothing.  n > max_tokens: KIVI_ERR_CAPACITY.
  */
 KIVI_API int kivi_quantize_prefill(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k,
@@ -111,9 +119,10 @@ KIVI_API int kivi_quantize_prefill(const kivi_dims *dims, kivi_cache *cache, con
 /*
  * Append one token per (batch, KV head) (section "Iddia ve Gerceklik", paragraph 3).
  * k_new, v_new: fp16 [B][Hkv][D] device.  The key goes to residual slot
- * n_tokens mod G; the value is quantized at once; when the residual fills, its G
- * keys are quantized as one group in the same call.  Increments cache->n_tokens.
- * A full cache returns KIVI_ERR_CAPACITY.
+ * n_tokens mod G; the value is quantized at once (with a value residual: it goes
+ * to the same slot of v_res); when the residual fills, its G keys are quantized as
+ * one group in the same call (with a value residual, its G values too, token by
+ * token).  Increments cache->n_tokens.  A full cache returns KIVI_ERR_CAPACITY.
  */
 KIVI_API int kivi_append_token(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k_new,
                       const uint16_t *v_new, cudaStream_t stream);
@@ -217,6 +226,7 @@ KIVI_API int kivi_decode_attention_noalloc(const kivi_dims *dims, const kivi_cac
  *   v_codes      uint32 [num_pages][Hkv][P][D/16]   token rows of packed value codes
  *   v_meta       uint32 [num_pages][Hkv][P]         per token {s, z}
  *   k_res        fp16   [B][Hkv][G][D]              residual keys of sequence b
+ *   v_res        fp16   [B][Hkv][G][D]              residual values (value_residual = 1)
  *   block_table  int32  [B][max_pages_per_seq]      page of positions j*P .. j*P+P-1
  *   seq_lens     int32  [B]                         tokens held by sequence b
  * Position t of sequence b is row t mod P of page block_table[b][t / P].  The block
@@ -236,6 +246,7 @@ typedef struct {
   int32_t D;                  /* head dim, 128 */
   int32_t G;                  /* key group size, 32 or 64 */
   int32_t bits;               /* code width, 2 */
+  int32_t value_residual;     /* as kivi_dims.value_residual */
   int32_t page_tokens;        /* P: a power of two, >= 64 */
   int32_t max_pages_per_seq;  /* columns of the block table */
   int64_t num_pages;          /* pages in the pool */
@@ -247,13 +258,15 @@ typedef struct {
   uint32_t *v_codes;
   uint32_t *v_meta;
   uint16_t *k_res;
+  uint16_t *v_res;            /* [B][Hkv][G][D] fp16, value_residual = 1 only */
   const int32_t *block_table;
   int32_t *seq_lens;
 } kivi_paged_cache;
 
 /* Bytes of the pool and per-sequence buffers, in the order k_codes, k_meta, v_codes,
- * v_meta, k_res, block_table, seq_lens.  Pure host arithmetic. */
-KIVI_API int kivi_paged_buffer_bytes(const kivi_paged_dims *dims, size_t out_bytes[7]);
+ * v_meta, k_res, block_table, seq_lens, v_res (0 without a value residual).  Pure
+ * host arithmetic. */
+KIVI_API int kivi_paged_buffer_bytes(const kivi_paged_dims *dims, size_t out_bytes[8]);
 
 /*
  * Quantize the prompt of sequence `seq` (0 <= seq < B) into its pages, as

@@ -43,22 +43,24 @@ def test_status_strings(L):
 
 
 def _dims(**kw):
-    d = dict(B=2, Hkv=4, D=128, G=32, bits=2, max_tokens=256)
+    d = dict(B=2, Hkv=4, D=128, G=32, bits=2, value_residual=0, max_tokens=256)
     d.update(kw)
-    return kivi.kivi_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["max_tokens"])
+    return kivi.kivi_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["value_residual"], d["max_tokens"])
 
 
 FAKE = 1 << 20  # an aligned, never dereferenced address
 
 
-def _cache(n=0, align=0):
-    return kivi.kivi_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, n)
+def _cache(n=0, align=0, v_res=FAKE):
+    return kivi.kivi_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, v_res, n)
 
 
 def test_buffer_bytes(L):
     out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640))
     heads = 15
-    assert out == [heads * 640 * 32, heads * 10 * 128 * 4, heads * 64 * 128 * 2, heads * 640 * 32, heads * 640 * 4]
+    assert out == [heads * 640 * 32, heads * 10 * 128 * 4, heads * 64 * 128 * 2, heads * 640 * 32, heads * 640 * 4, 0]
+    out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640, value_residual=1))
+    assert out[5] == heads * 64 * 128 * 2
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -67,10 +69,11 @@ def test_buffer_bytes(L):
     (dict(G=16), kivi.KIVI_ERR_UNSUPPORTED),
     (dict(B=0), kivi.KIVI_ERR_ARG),
     (dict(max_tokens=100), kivi.KIVI_ERR_ARG),   # not a multiple of G
+    (dict(value_residual=2), kivi.KIVI_ERR_ARG),
 ])
 def test_bad_dims(L, kw, status):
     d = _dims(**kw)
-    out = (ctypes.c_size_t * 5)()
+    out = (ctypes.c_size_t * 6)()
     assert L.kivi_buffer_bytes(ctypes.byref(d), out) == status
     c = _cache()
     assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, 10, None) == status
@@ -86,8 +89,16 @@ def test_prefill_checks(L):
     assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), FAKE, FAKE, -1, None) == kivi.KIVI_ERR_ARG
     bad = _cache(align=4)
     assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(bad), FAKE, FAKE, 10, None) == kivi.KIVI_ERR_ALIGN
-    null = kivi.kivi_cache(FAKE, 0, FAKE, FAKE, FAKE, 0)
+    null = kivi.kivi_cache(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 0)
     assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(null), FAKE, FAKE, 10, None) == kivi.KIVI_ERR_ARG
+    # a value residual needs its buffer, 16-byte aligned; without the variant it is not read
+    dv = _dims(value_residual=1)
+    assert L.kivi_quantize_prefill(ctypes.byref(dv), ctypes.byref(_cache(v_res=0)), FAKE, FAKE, 10,
+                                   None) == kivi.KIVI_ERR_ARG
+    assert L.kivi_quantize_prefill(ctypes.byref(dv), ctypes.byref(_cache(v_res=FAKE + 8)), FAKE, FAKE, 10,
+                                   None) == kivi.KIVI_ERR_ALIGN
+    c0 = _cache(v_res=0)
+    assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c0), None, None, 0, None) == kivi.KIVI_OK
     # n == 0 launches nothing and succeeds
     c.n_tokens = 7
     assert L.kivi_quantize_prefill(ctypes.byref(d), ctypes.byref(c), None, None, 0, None) == kivi.KIVI_OK
@@ -123,20 +134,23 @@ def test_decode_argument_checks(L):
 
 # ---- paged cache: geometry and argument checks on the host --------------------------
 def _pdims(**kw):
-    d = dict(B=3, Hkv=4, D=128, G=32, bits=2, page_tokens=64, max_pages_per_seq=5, num_pages=20)
+    d = dict(B=3, Hkv=4, D=128, G=32, bits=2, value_residual=0, page_tokens=64, max_pages_per_seq=5, num_pages=20)
     d.update(kw)
-    return kivi.kivi_paged_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["page_tokens"],
-                                d["max_pages_per_seq"], d["num_pages"])
+    return kivi.kivi_paged_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["value_residual"],
+                                d["page_tokens"], d["max_pages_per_seq"], d["num_pages"])
 
 
-def _pcache(align=0, bt_align=0):
-    return kivi.kivi_paged_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, FAKE + bt_align, FAKE)
+def _pcache(align=0, bt_align=0, v_res=FAKE):
+    return kivi.kivi_paged_cache(FAKE + align, FAKE, FAKE, FAKE, FAKE, v_res, FAKE + bt_align, FAKE)
 
 
 def test_paged_buffer_bytes(L):
     out = kivi.kivi_paged_buffer_bytes(_pdims(B=3, Hkv=5, G=64, page_tokens=128, max_pages_per_seq=7, num_pages=11))
     rows = 11 * 5 * 128
-    assert out == [rows * 32, rows // 64 * 128 * 4, rows * 32, rows * 4, 3 * 5 * 64 * 128 * 2, 3 * 7 * 4, 3 * 4]
+    assert out == [rows * 32, rows // 64 * 128 * 4, rows * 32, rows * 4, 3 * 5 * 64 * 128 * 2, 3 * 7 * 4, 3 * 4, 0]
+    out = kivi.kivi_paged_buffer_bytes(_pdims(B=3, Hkv=5, G=64, page_tokens=128, max_pages_per_seq=7, num_pages=11,
+                                              value_residual=1))
+    assert out[7] == 3 * 5 * 64 * 128 * 2
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -149,10 +163,11 @@ def test_paged_buffer_bytes(L):
     (dict(B=0), kivi.KIVI_ERR_ARG),
     (dict(num_pages=0), kivi.KIVI_ERR_ARG),
     (dict(max_pages_per_seq=0), kivi.KIVI_ERR_ARG),
+    (dict(value_residual=-1), kivi.KIVI_ERR_ARG),
 ])
 def test_bad_paged_dims(L, kw, status):
     d = _pdims(**kw)
-    out = (ctypes.c_size_t * 7)()
+    out = (ctypes.c_size_t * 8)()
     assert L.kivi_paged_buffer_bytes(ctypes.byref(d), out) == status
     c = _pcache()
     assert L.kivi_paged_prefill(ctypes.byref(d), ctypes.byref(c), 0, FAKE, FAKE, 10, None) == status
@@ -173,8 +188,13 @@ def test_paged_prefill_checks(L):
     assert pre(k=FAKE + 2) == kivi.KIVI_ERR_ALIGN
     assert pre(c=_pcache(align=4)) == kivi.KIVI_ERR_ALIGN
     assert pre(c=_pcache(bt_align=2)) == kivi.KIVI_ERR_ALIGN
-    null = kivi.kivi_paged_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE)
+    null = kivi.kivi_paged_cache(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE)
     assert pre(c=null) == kivi.KIVI_ERR_ARG
+    dv = _pdims(value_residual=1)
+    assert L.kivi_paged_prefill(ctypes.byref(dv), ctypes.byref(_pcache(v_res=0)), 0, FAKE, FAKE, 10,
+                                None) == kivi.KIVI_ERR_ARG
+    assert L.kivi_paged_prefill(ctypes.byref(dv), ctypes.byref(_pcache(v_res=FAKE + 2)), 0, FAKE, FAKE, 10,
+                                None) == kivi.KIVI_ERR_ALIGN
 
 
 def test_paged_decode_argument_checks(L):

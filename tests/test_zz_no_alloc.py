@@ -54,6 +54,6 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     need = kivi.kivi_decode_workspace_bytes(d, 32, 64)
     assert need > kivi.kivi_decode_attention_noalloc_max_workspace()
     fake = 1 << 20  # never dereferenced: the size check comes first
-    cache = kivi.kivi_cache(fake, fake, fake, fake, fake, 64)
+    cache = kivi.kivi_cache(fake, fake, fake, fake, fake, 0, 64)
     st = kivi.lib().kivi_decode_attention_noalloc(ctypes.byref(d), ctypes.byref(cache), fake, 32, 1.0, fake, None)
     assert st == kivi.KIVI_ERR_WORKSPACE
