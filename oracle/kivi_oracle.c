@@ -36,6 +36,10 @@
  *   R8  attention over the dequantized cache in fp64:
  *       score_t = sigma * q . K'_t,  p = softmax(score),  out = sum_t p_t V'_t,
  *       with query head h reading KV head h / (Hq / Hkv).
+ *   R10 (variant, bits = 4) the same rule with 2^4 - 1 = 15 levels:
+ *       s = (max - min) / 15, code = clamp(round_half_even((x - min) / s), 0, 15),
+ *       packed 8 per word: word w holds channels 8w..8w+7, channel 8w+i in bits
+ *       [4i, 4i+3].  bits = 2 is R1-R7 unchanged.
  *   R9  (variant, when a value residual buffer is given) values keep the same
  *       residual as keys: the last n mod G values stay fp16, and when the key group
  *       flushes its G values are quantized per token (R5) at once.  Without the
@@ -85,8 +89,9 @@ int oracle_max_threads(void) {
  * row of D channels.  Writes the fp16 scale and zero bit patterns and one code
  * (0..3) per element.
  */
-void oracle_quantize_group(const uint16_t *x, int64_t count, int64_t stride,
+void oracle_quantize_group(const uint16_t *x, int64_t count, int64_t stride, int bits,
                            uint16_t *s_out, uint16_t *z_out, uint8_t *codes) {
+  const float levels = (float)((1 << bits) - 1); /* 3 (R1) or 15 (R10) */
   /* step 1: min and max (exact: both are fp16 values) */
   float mn = h2f(x[0]);
   float mx = mn;
@@ -95,9 +100,9 @@ void oracle_quantize_group(const uint16_t *x, int64_t count, int64_t stride,
     if (v < mn) mn = v;
     if (v > mx) mx = v;
   }
-  /* step 2: scale = (max - min) / (2^2 - 1) in fp32, then stored as fp16 */
+  /* step 2: scale = (max - min) / (2^bits - 1) in fp32, then stored as fp16 */
   float range = mx - mn;
-  float s32 = range / 3.0f;
+  float s32 = range / levels;
   uint16_t s16 = f2h(s32);
   float s = h2f(s16);
   /* step 3: zero-point = min, stored as fp16 (exact); -0 is stored as +0 */
@@ -105,7 +110,7 @@ void oracle_quantize_group(const uint16_t *x, int64_t count, int64_t stride,
   if (z16 == 0x8000u) z16 = 0x0000u;
   *s_out = s16;
   *z_out = z16;
-  /* step 4: code = clamp(round_half_even((x - min) / s), 0, 3) */
+  /* step 4: code = clamp(round_half_even((x - min) / s), 0, 2^bits - 1) */
   for (int64_t i = 0; i < count; ++i) {
     if (s == 0.0f) {
       codes[i] = 0;
@@ -115,23 +120,31 @@ void oracle_quantize_group(const uint16_t *x, int64_t count, int64_t stride,
     float u = d / s;
     float r = rintf(u); /* default rounding mode: nearest, ties to even */
     if (r < 0.0f) r = 0.0f;
-    if (r > 3.0f) r = 3.0f;
+    if (r > levels) r = levels;
     codes[i] = (uint8_t)r;
   }
 }
 
-/* R7: pack the D codes of one token row into D/16 words. */
-void oracle_pack_row(const uint8_t *codes, int D, uint32_t *words) {
-  for (int w = 0; w < D / 16; ++w) {
+/* R7 / R10: pack the D codes of one token row into D * bits / 32 words: word w
+ * holds the 32 / bits channels starting at w * 32 / bits, channel i of the word in
+ * bits [bits * i, bits * i + bits - 1]. */
+void oracle_pack_row(const uint8_t *codes, int D, int bits, uint32_t *words) {
+  const int per_word = 32 / bits;
+  const uint32_t mask = (1u << bits) - 1u;
+  for (int w = 0; w < D / per_word; ++w) {
     uint32_t word = 0;
-    for (int i = 0; i < 16; ++i) word |= (uint32_t)(codes[16 * w + i] & 3u) << (2 * i);
+    for (int i = 0; i < per_word; ++i) word |= (uint32_t)(codes[per_word * w + i] & mask) << (bits * i);
     words[w] = word;
   }
 }
 
+/* words of one packed token row */
+#define WPR(D, bits) ((D) * (bits) / 32)
+
 /* inverse of oracle_pack_row */
-static uint8_t unpack_code(const uint32_t *row, int c) {
-  return (uint8_t)((row[c / 16] >> (2 * (c % 16))) & 3u);
+static uint8_t unpack_code(const uint32_t *row, int bits, int c) {
+  const int per_word = 32 / bits;
+  return (uint8_t)((row[c / per_word] >> (bits * (c % per_word))) & ((1u << bits) - 1u));
 }
 
 static uint32_t meta_word(uint16_t s, uint16_t z) { return (uint32_t)s | ((uint32_t)z << 16); }
@@ -141,29 +154,29 @@ static uint16_t meta_z(uint32_t m) { return (uint16_t)(m >> 16); }
 /*
  * Key group quantization (R1-R4, R7): `rows` holds G token rows of D fp16 channels.
  * Each channel is quantized over the G tokens; the codes are packed per token row
- * into codes_out (G rows of D/16 words) and the per-channel {s, z} go to meta_out[D].
+ * into codes_out (G rows of D*bits/32 words) and the per-channel {s, z} go to meta_out[D].
  */
-static void quantize_key_group(const uint16_t *rows, int D, int G, uint32_t *codes_out,
+static void quantize_key_group(const uint16_t *rows, int D, int G, int bits, uint32_t *codes_out,
                                uint32_t *meta_out) {
   uint8_t *col = (uint8_t *)malloc((size_t)G);
   uint8_t *mat = (uint8_t *)malloc((size_t)G * D); /* [G][D] codes */
   for (int c = 0; c < D; ++c) {
     uint16_t s, z;
-    oracle_quantize_group(rows + c, G, D, &s, &z, col);
+    oracle_quantize_group(rows + c, G, D, bits, &s, &z, col);
     meta_out[c] = meta_word(s, z);
     for (int t = 0; t < G; ++t) mat[(size_t)t * D + c] = col[t];
   }
-  for (int t = 0; t < G; ++t) oracle_pack_row(mat + (size_t)t * D, D, codes_out + (size_t)t * (D / 16));
+  for (int t = 0; t < G; ++t) oracle_pack_row(mat + (size_t)t * D, D, bits, codes_out + (size_t)t * WPR(D, bits));
   free(mat);
   free(col);
 }
 
-/* Value token quantization (R5, R7): one row of D channels -> D/16 words + {s, z}. */
-static void quantize_value_token(const uint16_t *row, int D, uint32_t *codes_out, uint32_t *meta_out) {
+/* Value token quantization (R5, R7, R10): one row of D channels -> D*bits/32 words + {s, z}. */
+static void quantize_value_token(const uint16_t *row, int D, int bits, uint32_t *codes_out, uint32_t *meta_out) {
   uint8_t *codes = (uint8_t *)malloc((size_t)D);
   uint16_t s, z;
-  oracle_quantize_group(row, D, 1, &s, &z, codes);
-  oracle_pack_row(codes, D, codes_out);
+  oracle_quantize_group(row, D, 1, bits, &s, &z, codes);
+  oracle_pack_row(codes, D, bits, codes_out);
   *meta_out = meta_word(s, z);
   free(codes);
 }
@@ -171,26 +184,26 @@ static void quantize_value_token(const uint16_t *row, int D, uint32_t *codes_out
 /*
  * One (batch, KV head): quantize a prompt of n tokens (R6, R9).
  *   k, v     : [n][D] fp16
- *   k_codes  : [max_tokens][D/16]   rows < floor(n/G)*G written
+ *   k_codes  : [max_tokens][D*bits/32]   rows < floor(n/G)*G written
  *   k_meta   : [max_tokens/G][D]    groups < floor(n/G) written
  *   k_res    : [G][D]               slots < n mod G written (token nq + j in slot j)
- *   v_codes  : [max_tokens][D/16]   rows < n written (rows < nq with a value residual)
+ *   v_codes  : [max_tokens][D*bits/32]   rows < n written (rows < nq with a value residual)
  *   v_meta   : [max_tokens]         entries < n written (< nq with a value residual)
  *   v_res    : [G][D] or NULL       with a value residual: slots < n mod G written
  */
-void oracle_prefill_head(int D, int G, int64_t n, const uint16_t *k, const uint16_t *v,
+void oracle_prefill_head(int D, int G, int bits, int64_t n, const uint16_t *k, const uint16_t *v,
                          uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                          uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t n_groups = n / G;
   int64_t nq = n_groups * G;
   for (int64_t g = 0; g < n_groups; ++g)
-    quantize_key_group(k + (size_t)g * G * D, D, G, k_codes + (size_t)g * G * (D / 16),
+    quantize_key_group(k + (size_t)g * G * D, D, G, bits, k_codes + (size_t)g * G * WPR(D, bits),
                        k_meta + (size_t)g * D);
   for (int64_t j = 0; j < n - nq; ++j)
     memcpy(k_res + (size_t)j * D, k + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
   int64_t n_quantized_values = v_res ? nq : n;
   for (int64_t t = 0; t < n_quantized_values; ++t)
-    quantize_value_token(v + (size_t)t * D, D, v_codes + (size_t)t * (D / 16), v_meta + t);
+    quantize_value_token(v + (size_t)t * D, D, bits, v_codes + (size_t)t * WPR(D, bits), v_meta + t);
   if (v_res)
     for (int64_t j = 0; j < n - nq; ++j)
       memcpy(v_res + (size_t)j * D, v + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
@@ -203,7 +216,7 @@ void oracle_prefill_head(int D, int G, int64_t n, const uint16_t *k, const uint1
  * fills, its G keys are quantized as group n / G (and, with a value residual, its
  * G values token by token) and the residual empties.  Returns the new length n + 1.
  */
-int64_t oracle_append_head(int D, int G, int64_t n, const uint16_t *k_new, const uint16_t *v_new,
+int64_t oracle_append_head(int D, int G, int bits, int64_t n, const uint16_t *k_new, const uint16_t *v_new,
                            uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                            uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t r = n % G;
@@ -211,13 +224,13 @@ int64_t oracle_append_head(int D, int G, int64_t n, const uint16_t *k_new, const
   if (v_res)
     memcpy(v_res + (size_t)r * D, v_new, (size_t)D * sizeof(uint16_t));
   else
-    quantize_value_token(v_new, D, v_codes + (size_t)n * (D / 16), v_meta + n);
+    quantize_value_token(v_new, D, bits, v_codes + (size_t)n * WPR(D, bits), v_meta + n);
   if (r + 1 == G) {
     int64_t g = n / G;
-    quantize_key_group(k_res, D, G, k_codes + (size_t)g * G * (D / 16), k_meta + (size_t)g * D);
+    quantize_key_group(k_res, D, G, bits, k_codes + (size_t)g * G * WPR(D, bits), k_meta + (size_t)g * D);
     if (v_res)
       for (int64_t j = 0; j < G; ++j)
-        quantize_value_token(v_res + (size_t)j * D, D, v_codes + (size_t)(g * G + j) * (D / 16),
+        quantize_value_token(v_res + (size_t)j * D, D, bits, v_codes + (size_t)(g * G + j) * WPR(D, bits),
                              v_meta + g * G + j);
   }
   return n + 1;
@@ -225,14 +238,14 @@ int64_t oracle_append_head(int D, int G, int64_t n, const uint16_t *k_new, const
 
 /* Dequantized key t of one head, fp64: z + code * s for quantized tokens, the fp16
  * residual value itself for the last n mod G tokens. */
-static void dequant_key_f64(int D, int G, int64_t n, int64_t t, const uint32_t *k_codes,
+static void dequant_key_f64(int D, int G, int bits, int64_t n, int64_t t, const uint32_t *k_codes,
                             const uint32_t *k_meta, const uint16_t *k_res, double *out) {
   int64_t nq = (n / G) * G;
   if (t < nq) {
-    const uint32_t *row = k_codes + (size_t)t * (D / 16);
+    const uint32_t *row = k_codes + (size_t)t * WPR(D, bits);
     const uint32_t *meta = k_meta + (size_t)(t / G) * D;
     for (int c = 0; c < D; ++c)
-      out[c] = (double)h2f(meta_z(meta[c])) + (double)unpack_code(row, c) * (double)h2f(meta_s(meta[c]));
+      out[c] = (double)h2f(meta_z(meta[c])) + (double)unpack_code(row, bits, c) * (double)h2f(meta_s(meta[c]));
   } else {
     const uint16_t *res = k_res + (size_t)(t - nq) * D;
     for (int c = 0; c < D; ++c) out[c] = (double)h2f(res[c]);
@@ -241,7 +254,7 @@ static void dequant_key_f64(int D, int G, int64_t n, int64_t t, const uint32_t *
 
 /* Dequantized value t of one head, fp64: z_t + code * s_t, or with a value residual
  * (R9) the fp16 value itself for the last n mod G tokens. */
-static void dequant_value_f64(int D, int G, int64_t n, int64_t t, const uint32_t *v_codes,
+static void dequant_value_f64(int D, int G, int bits, int64_t n, int64_t t, const uint32_t *v_codes,
                               const uint32_t *v_meta, const uint16_t *v_res, double *out) {
   int64_t nq = (n / G) * G;
   if (v_res && t >= nq) {
@@ -249,26 +262,26 @@ static void dequant_value_f64(int D, int G, int64_t n, int64_t t, const uint32_t
     for (int c = 0; c < D; ++c) out[c] = (double)h2f(res[c]);
     return;
   }
-  const uint32_t *row = v_codes + (size_t)t * (D / 16);
+  const uint32_t *row = v_codes + (size_t)t * WPR(D, bits);
   double s = (double)h2f(meta_s(v_meta[t]));
   double z = (double)h2f(meta_z(v_meta[t]));
-  for (int c = 0; c < D; ++c) out[c] = z + (double)unpack_code(row, c) * s;
+  for (int c = 0; c < D; ++c) out[c] = z + (double)unpack_code(row, bits, c) * s;
 }
 
 /* Dequantize one head's n tokens to fp64 [n][D] (keys and values). */
-void oracle_dequantize_head_f64(int D, int G, int64_t n, const uint32_t *k_codes,
+void oracle_dequantize_head_f64(int D, int G, int bits, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
                                 const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 double *k_out, double *v_out) {
   for (int64_t t = 0; t < n; ++t) {
-    dequant_key_f64(D, G, n, t, k_codes, k_meta, k_res, k_out + (size_t)t * D);
-    dequant_value_f64(D, G, n, t, v_codes, v_meta, v_res, v_out + (size_t)t * D);
+    dequant_key_f64(D, G, bits, n, t, k_codes, k_meta, k_res, k_out + (size_t)t * D);
+    dequant_value_f64(D, G, bits, n, t, v_codes, v_meta, v_res, v_out + (size_t)t * D);
   }
 }
 
 /* Dequantize one head's n tokens to fp32 [n][D]: fp32(z) + fp32(code) * fp32(s),
  * a product that is exact in fp32 followed by one RNE addition. */
-void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes,
+void oracle_dequantize_head_f32(int D, int G, int bits, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
                                 const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 float *k_out, float *v_out) {
@@ -276,10 +289,10 @@ void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes
   for (int64_t t = 0; t < n; ++t) {
     float *ko = k_out + (size_t)t * D;
     if (t < nq) {
-      const uint32_t *row = k_codes + (size_t)t * (D / 16);
+      const uint32_t *row = k_codes + (size_t)t * WPR(D, bits);
       const uint32_t *meta = k_meta + (size_t)(t / G) * D;
       for (int c = 0; c < D; ++c) {
-        float prod = (float)unpack_code(row, c) * h2f(meta_s(meta[c]));
+        float prod = (float)unpack_code(row, bits, c) * h2f(meta_s(meta[c]));
         ko[c] = h2f(meta_z(meta[c])) + prod;
       }
     } else {
@@ -292,11 +305,11 @@ void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes
       for (int c = 0; c < D; ++c) vo[c] = h2f(res[c]);
       continue;
     }
-    const uint32_t *vrow = v_codes + (size_t)t * (D / 16);
+    const uint32_t *vrow = v_codes + (size_t)t * WPR(D, bits);
     float s = h2f(meta_s(v_meta[t]));
     float z = h2f(meta_z(v_meta[t]));
     for (int c = 0; c < D; ++c) {
-      float prod = (float)unpack_code(vrow, c) * s;
+      float prod = (float)unpack_code(vrow, bits, c) * s;
       vo[c] = z + prod;
     }
   }
@@ -308,7 +321,7 @@ void oracle_dequantize_head_f32(int D, int G, int64_t n, const uint32_t *k_codes
  *   out_c = sum_t p_t V'_{t,c}.
  * Returns 0, or -1 when n <= 0 (softmax over an empty set is undefined).
  */
-int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, const uint32_t *k_meta,
+int oracle_attention_head(int D, int G, int bits, int64_t n, const uint32_t *k_codes, const uint32_t *k_meta,
                           const uint16_t *k_res, const uint32_t *v_codes, const uint32_t *v_meta,
                           const uint16_t *v_res, const uint16_t *q, double sigma, double *out) {
   if (n <= 0) return -1;
@@ -318,7 +331,7 @@ int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, cons
   for (int c = 0; c < D; ++c) qd[c] = (double)h2f(q[c]);
   double m = -INFINITY;
   for (int64_t t = 0; t < n; ++t) {
-    dequant_key_f64(D, G, n, t, k_codes, k_meta, k_res, row);
+    dequant_key_f64(D, G, bits, n, t, k_codes, k_meta, k_res, row);
     double acc = 0.0;
     for (int c = 0; c < D; ++c) acc += qd[c] * row[c];
     score[t] = sigma * acc;
@@ -331,7 +344,7 @@ int oracle_attention_head(int D, int G, int64_t n, const uint32_t *k_codes, cons
   }
   for (int c = 0; c < D; ++c) out[c] = 0.0;
   for (int64_t t = 0; t < n; ++t) {
-    dequant_value_f64(D, G, n, t, v_codes, v_meta, v_res, row);
+    dequant_value_f64(D, G, bits, n, t, v_codes, v_meta, v_res, row);
     double p = score[t] / l;
     for (int c = 0; c < D; ++c) out[c] += p * row[c];
   }
@@ -374,41 +387,41 @@ int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_
 /* ---------------------------------------------------------------------------------
  * Whole-batch wrappers over the per-head functions.  Buffer shapes:
  *   k, v      [B][Hkv][n][D] fp16         k_new, v_new [B][Hkv][D] fp16
- *   k_codes   [B][Hkv][max_tokens][D/16]  k_meta [B][Hkv][max_tokens/G][D]
- *   k_res     [B][Hkv][G][D] fp16         v_codes [B][Hkv][max_tokens][D/16]
+ *   k_codes   [B][Hkv][max_tokens][D*bits/32]  k_meta [B][Hkv][max_tokens/G][D]
+ *   k_res     [B][Hkv][G][D] fp16         v_codes [B][Hkv][max_tokens][D*bits/32]
  *   v_meta    [B][Hkv][max_tokens]        q [B][Hq][D] fp16, out [B][Hq][D] fp64
  * Heads are independent, so the loops run in parallel over (b, head).
  * ------------------------------------------------------------------------------- */
-#define KC(bh) (k_codes + (size_t)(bh) * max_tokens * (D / 16))
+#define KC(bh) (k_codes + (size_t)(bh) * max_tokens * WPR(D, bits))
 #define KM(bh) (k_meta + (size_t)(bh) * (max_tokens / G) * D)
 #define KR(bh) (k_res + (size_t)(bh) * G * D)
-#define VC(bh) (v_codes + (size_t)(bh) * max_tokens * (D / 16))
+#define VC(bh) (v_codes + (size_t)(bh) * max_tokens * WPR(D, bits))
 #define VM(bh) (v_meta + (size_t)(bh) * max_tokens)
 #define VR(bh) (v_res ? v_res + (size_t)(bh) * G * D : NULL)
 
-void oracle_prefill(int B, int Hkv, int D, int G, int64_t max_tokens, int64_t n, const uint16_t *k,
+void oracle_prefill(int B, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n, const uint16_t *k,
                     const uint16_t *v, uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                     uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(dynamic)
   for (int64_t bh = 0; bh < heads; ++bh)
-    oracle_prefill_head(D, G, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, KC(bh), KM(bh),
+    oracle_prefill_head(D, G, bits, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, KC(bh), KM(bh),
                         KR(bh), VC(bh), VM(bh), VR(bh));
 }
 
-int64_t oracle_append(int B, int Hkv, int D, int G, int64_t max_tokens, int64_t n,
+int64_t oracle_append(int B, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n,
                       const uint16_t *k_new, const uint16_t *v_new, uint32_t *k_codes,
                       uint32_t *k_meta, uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta,
                       uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(static)
   for (int64_t bh = 0; bh < heads; ++bh)
-    oracle_append_head(D, G, n, k_new + (size_t)bh * D, v_new + (size_t)bh * D, KC(bh), KM(bh),
+    oracle_append_head(D, G, bits, n, k_new + (size_t)bh * D, v_new + (size_t)bh * D, KC(bh), KM(bh),
                        KR(bh), VC(bh), VM(bh), VR(bh));
   return n + 1;
 }
 
-int oracle_attention(int B, int Hq, int Hkv, int D, int G, int64_t max_tokens, int64_t n,
+int oracle_attention(int B, int Hq, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n,
                      const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                      const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                      const uint16_t *q, double sigma, double *out) {
@@ -420,7 +433,7 @@ int oracle_attention(int B, int Hq, int Hkv, int D, int G, int64_t max_tokens, i
     int64_t b = bq / Hq;
     int h = (int)(bq % Hq);
     int64_t bh = b * Hkv + h / group;
-    oracle_attention_head(D, G, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
+    oracle_attention_head(D, G, bits, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
                           sigma, out + (size_t)bq * D);
   }
   return 0;
