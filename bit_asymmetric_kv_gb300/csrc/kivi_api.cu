@@ -13,7 +13,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 int check_dims(const kivi_dims *d) {
   if (!d) return KIVI_ERR_ARG;
   if (d->B <= 0 || d->Hkv <= 0 || d->max_tokens <= 0) return KIVI_ERR_ARG;
-  if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
+  if (d->D != 128 || (d->bits != 2 && d->bits != 4) || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->max_tokens % d->G != 0) return KIVI_ERR_ARG;
   if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
   return KIVI_OK;
@@ -36,13 +36,13 @@ uint16_t *vres(const kivi_dims *d, const kivi_cache *c) { return d->value_residu
 cudaError_t append_and_flush(const kivi_dims *d, const kivi_cache *c, const uint16_t *k_new,
                              const uint16_t *v_new, int64_t n, cudaStream_t st) {
   const int64_t heads = (int64_t)d->B * d->Hkv;
-  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, c->k_res, c->v_codes, c->v_meta,
+  cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, d->bits, c->k_res, c->v_codes, c->v_meta,
                                       d->max_tokens, vres(d, c), st);
   if (e == cudaSuccess && (n % d->G) + 1 == d->G) {
-    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, c->k_codes, c->k_meta,
-                                d->max_tokens, st);
+    e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, d->bits, c->k_codes,
+                                c->k_meta, d->max_tokens, st);
     if (e == cudaSuccess && d->value_residual)
-      e = kivi::launch_value_rows(c->v_res, heads, d->G, d->G, (n / d->G) * d->G, c->v_codes, c->v_meta,
+      e = kivi::launch_value_rows(c->v_res, heads, d->G, d->G, (n / d->G) * d->G, d->bits, c->v_codes, c->v_meta,
                                   d->max_tokens, st);
   }
   return e;
@@ -72,7 +72,7 @@ int check_paged_dims(const kivi_paged_dims *d) {
   if (d->B <= 0 || d->Hkv <= 0 || d->page_tokens <= 0 || d->max_pages_per_seq <= 0 || d->num_pages <= 0)
     return KIVI_ERR_ARG;
   if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
-  if (d->D != 128 || d->bits != 2 || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
+  if (d->D != 128 || (d->bits != 2 && d->bits != 4) || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->B > kivi::kPagedMaxBatch) return KIVI_ERR_UNSUPPORTED;
   const int sh = page_shift_of(d->page_tokens);
   if (sh < 6 || sh > 24) return KIVI_ERR_UNSUPPORTED;  // a power of two, 64 .. 2^24 tokens
@@ -127,6 +127,7 @@ kivi::PagedAppendArgs paged_append_args(const kivi_paged_dims *d, const kivi_pag
   a.B = d->B;
   a.Hkv = d->Hkv;
   a.G = d->G;
+  a.bits = d->bits;
   a.shift = page_shift_of(d->page_tokens);
   a.max_pages = d->max_pages_per_seq;
   return a;
@@ -149,6 +150,7 @@ kivi::DecodeArgs paged_decode_args(const kivi_paged_dims *d, const kivi_paged_ca
   a.Hkv = d->Hkv;
   a.Hq = Hq;
   a.G = d->G;
+  a.bits = d->bits;
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.softmax_scale = softmax_scale;
@@ -184,10 +186,11 @@ int kivi_buffer_bytes(const kivi_dims *d, size_t out[6]) {
   if (!out) return KIVI_ERR_ARG;
   const size_t heads = (size_t)d->B * (size_t)d->Hkv;
   const size_t T = (size_t)d->max_tokens;
-  out[0] = heads * T * (d->D / 16) * sizeof(uint32_t);
+  const size_t wpr = (size_t)d->D * d->bits / 32;  // words of a packed token row
+  out[0] = heads * T * wpr * sizeof(uint32_t);
   out[1] = heads * (T / d->G) * d->D * sizeof(uint32_t);
   out[2] = heads * (size_t)d->G * d->D * sizeof(uint16_t);
-  out[3] = heads * T * (d->D / 16) * sizeof(uint32_t);
+  out[3] = heads * T * wpr * sizeof(uint32_t);
   out[4] = heads * T * sizeof(uint32_t);
   out[5] = d->value_residual ? out[2] : 0;
   return KIVI_OK;
@@ -205,13 +208,13 @@ int kivi_quantize_prefill(const kivi_dims *d, kivi_cache *c, const uint16_t *k, 
     if (!aligned16(k) || !aligned16(v)) return KIVI_ERR_ALIGN;
     const int64_t heads = (int64_t)d->B * d->Hkv;
     const int64_t groups = n / d->G, nq = groups * d->G;
-    cudaError_t e = kivi::launch_key_groups(k, n * 128, heads, groups, 0, d->G, c->k_codes, c->k_meta,
+    cudaError_t e = kivi::launch_key_groups(k, n * 128, heads, groups, 0, d->G, d->bits, c->k_codes, c->k_meta,
                                             d->max_tokens, st);
     if (e == cudaSuccess) e = kivi::launch_residual_copy(k, heads, n, nq, d->G, c->k_res, st);
     // values: all n quantized, or with a value residual the first nq and the rest kept
     const int64_t nv = d->value_residual ? nq : n;
     if (e == cudaSuccess)
-      e = kivi::launch_value_rows(v, heads, nv, n, 0, c->v_codes, c->v_meta, d->max_tokens, st);
+      e = kivi::launch_value_rows(v, heads, nv, n, 0, d->bits, c->v_codes, c->v_meta, d->max_tokens, st);
     if (e == cudaSuccess && d->value_residual) e = kivi::launch_residual_copy(v, heads, n, nq, d->G, c->v_res, st);
     if ((s = cuda_status(e)) != KIVI_OK) return s;
   }
@@ -237,7 +240,7 @@ int kivi_append_token(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, 
 int kivi_decode_splits(const kivi_dims *d, int32_t Hq, int64_t n) {
   if (check_dims(d) != KIVI_OK || check_heads(d, Hq) != KIVI_OK || n <= 0) return 0;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, n, &g) != cudaSuccess) return 0;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n, &g) != cudaSuccess) return 0;
   return g.pmax;
 }
 
@@ -257,7 +260,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
   if (c->n_tokens <= 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, c->n_tokens, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, c->n_tokens, &g) != cudaSuccess) return KIVI_ERR_CUDA;
   const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
@@ -277,6 +280,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.Hkv = d->Hkv;
   a.Hq = Hq;
   a.G = d->G;
+  a.bits = d->bits;
   a.units_per_head = g.units_per_head;
   a.total_units = g.total_units;
   a.n_warps = g.n_warps;
@@ -300,7 +304,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   if (n < 0) return KIVI_ERR_ARG;
   if (n >= d->max_tokens) return KIVI_ERR_CAPACITY;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, n + 1, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n + 1, &g) != cudaSuccess) return KIVI_ERR_CUDA;
   const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
@@ -324,6 +328,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   a.Hkv = d->Hkv;
   a.Hq = Hq;
   a.G = d->G;
+  a.bits = d->bits;
   a.units_per_head = g.units_per_head;
   a.total_units = g.total_units;
   a.n_warps = g.n_warps;
@@ -344,7 +349,7 @@ int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out,
   if (!aligned16(k_out) || !aligned16(v_out)) return KIVI_ERR_ALIGN;
   if (c->n_tokens < 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
   return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta, vres(d, c),
-                                          (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->max_tokens, k_out, v_out,
+                                          (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->bits, d->max_tokens, k_out, v_out,
                                           st));
 }
 
@@ -402,9 +407,10 @@ int kivi_paged_buffer_bytes(const kivi_paged_dims *d, size_t out[8]) {
   if (s != KIVI_OK) return s;
   if (!out) return KIVI_ERR_ARG;
   const size_t rows = (size_t)d->num_pages * (size_t)d->Hkv * (size_t)d->page_tokens;
-  out[0] = rows * (d->D / 16) * sizeof(uint32_t);
+  const size_t wpr = (size_t)d->D * d->bits / 32;  // words of a packed token row
+  out[0] = rows * wpr * sizeof(uint32_t);
   out[1] = rows / d->G * d->D * sizeof(uint32_t);
-  out[2] = rows * (d->D / 16) * sizeof(uint32_t);
+  out[2] = rows * wpr * sizeof(uint32_t);
   out[3] = rows * sizeof(uint32_t);
   out[4] = (size_t)d->B * d->Hkv * d->G * d->D * sizeof(uint16_t);
   out[5] = (size_t)d->B * d->max_pages_per_seq * sizeof(int32_t);
@@ -430,11 +436,12 @@ int kivi_paged_prefill(const kivi_paged_dims *d, const kivi_paged_cache *c, int3
     pm.shift = page_shift_of(d->page_tokens);
     pm.Hkv = d->Hkv;
     const int64_t groups = n / d->G, nq = groups * d->G;
-    e = kivi::launch_key_groups_paged(k, n * 128, d->Hkv, groups, d->G, pm, c->k_codes, c->k_meta, st);
+    e = kivi::launch_key_groups_paged(k, n * 128, d->Hkv, groups, d->G, d->bits, pm, c->k_codes, c->k_meta, st);
     if (e == cudaSuccess)
       e = kivi::launch_residual_copy(k, d->Hkv, n, nq, d->G, c->k_res + (int64_t)seq * d->Hkv * d->G * 128, st);
     const int64_t nv = d->value_residual ? nq : n;
-    if (e == cudaSuccess) e = kivi::launch_value_rows_paged(v, d->Hkv, nv, n, pm, c->v_codes, c->v_meta, st);
+    if (e == cudaSuccess)
+      e = kivi::launch_value_rows_paged(v, d->Hkv, nv, n, d->bits, pm, c->v_codes, c->v_meta, st);
     if (e == cudaSuccess && d->value_residual)
       e = kivi::launch_residual_copy(v, d->Hkv, n, nq, d->G, c->v_res + (int64_t)seq * d->Hkv * d->G * 128, st);
   }
@@ -457,7 +464,7 @@ int kivi_paged_append_token(const kivi_paged_dims *d, const kivi_paged_cache *c,
 size_t kivi_paged_decode_workspace_bytes(const kivi_paged_dims *d, int32_t Hq) {
   if (check_paged_dims(d) != KIVI_OK || check_paged_heads(d, Hq) != KIVI_OK) return 0;
   kivi::PagedGeom g;
-  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return 0;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, &g) != cudaSuccess) return 0;
   return g.ws_bytes;
 }
 
@@ -470,7 +477,7 @@ int kivi_paged_decode_attention(const kivi_paged_dims *d, const kivi_paged_cache
   if (!q || !out) return KIVI_ERR_ARG;
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
   kivi::PagedGeom g;
-  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, &g) != cudaSuccess) return KIVI_ERR_CUDA;
   if (!ws || ws_bytes < g.ws_bytes) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
   const kivi::DecodeArgs a = paged_decode_args(d, c, q, Hq, softmax_scale, out, ws, g);
@@ -487,7 +494,7 @@ int kivi_paged_decode_step(const kivi_paged_dims *d, const kivi_paged_cache *c, 
   if (!k_new || !v_new || !q || !out) return KIVI_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
   kivi::PagedGeom g;
-  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::paged_decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, &g) != cudaSuccess) return KIVI_ERR_CUDA;
   if (!ws || ws_bytes < g.ws_bytes) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
   // 1. append (flushing the groups that fill), lengths unchanged

@@ -61,17 +61,25 @@ constexpr int kUnit = kDecodeUnit;                   // tokens per unit
 constexpr int kFragRowWords = 20;                    // 16 B-fragment words + 4 pad (bank spread)
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int R, int G>
+// Shared-memory layout of one warp's ring for BITS-bit codes.  4-bit rows are twice
+// as long, so their ring has two stages (one unit staged ahead) to keep two CTAs
+// per SM; 2-bit rows keep three.
+template <int R, int G, int BITS = 2>
 struct Layout {
-  static constexpr int kGroups = kUnit / G;          // key groups per unit
-  static constexpr int kKCodes = 0;                  // 64 rows x 32 B
-  static constexpr int kVCodes = kUnit * 32;         // 64 rows x 32 B
-  static constexpr int kVMeta = 2 * kUnit * 32;      // 64 x 4 B
-  static constexpr int kKMeta = kVMeta + kUnit * 4;  // kGroups x 128 x 4 B
+  static constexpr int kRowBytes = 16 * BITS;                 // packed codes of one token row
+  static constexpr int kRowChunks = kRowBytes / 16;           // 16-byte copies per row
+  static constexpr int kStages = BITS == 2 ? 3 : 2;
+  static constexpr int kAheadUnits = BITS == 2 ? kAhead : 1;  // units staged ahead of the computed one
+  static constexpr int kGroups = kUnit / G;                   // key groups per unit
+  static constexpr int kKCodes = 0;                           // 64 rows
+  static constexpr int kVCodes = kUnit * kRowBytes;           // 64 rows
+  static constexpr int kVMeta = 2 * kUnit * kRowBytes;        // 64 x 4 B
+  static constexpr int kKMeta = kVMeta + kUnit * 4;           // kGroups x 128 x 4 B
   static constexpr int kStageBytes = kKMeta + kGroups * kD * 4;
   static constexpr int kFragGroupBytes = 8 * R * kFragRowWords * 4;  // rows 4*(2h+p)+tig
   static constexpr int kWarpBytes = kStages * kStageBytes + kGroups * kFragGroupBytes;
   static constexpr int kSmem = kWarps * kWarpBytes;
+  static_assert(kAheadUnits >= 1 && kAheadUnits < kStages, "the ring holds the computed unit and the staged ones");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -121,6 +129,25 @@ __device__ __forceinline__ void pv_tile(float acc[8][4], const uint32_t v[4], ui
   unpack16(prmt(v[2], v[3], 0x7632u), y23);
 #pragma unroll
   for (int j = 0; j < 8; ++j) mma16816(acc[j], x01[j], y01[j], x23[j], y23[j], bw0, bw1);
+}
+
+// P.V of one 16-token tile from 4-bit value codes: v[k] = words 2g and 2g+1 of
+// token tig + 4k (channels 16g .. 16g+15).  One prmt pairs two tokens' halves of a
+// word, unpack8 splits them into channel registers; MMA j takes channel 16g + j
+// (row g) and 16g + 8 + j (row g+8), with code factor 16^(j mod 2).
+__device__ __forceinline__ void pv_tile4(float acc[8][4], const uint2 v[4], uint32_t bw0, uint32_t bw1) {
+  uint32_t a01[2][8], a23[2][8];  // [word 2g + p][channel within the word], tokens (tig, tig+4) / (tig+8, tig+12)
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const uint32_t w0 = p ? v[0].y : v[0].x, w1 = p ? v[1].y : v[1].x;
+    const uint32_t w2 = p ? v[2].y : v[2].x, w3 = p ? v[3].y : v[3].x;
+    unpack8(prmt(w0, w1, 0x5410u), a01[p]);
+    unpack8(prmt(w0, w1, 0x7632u), a01[p] + 4);
+    unpack8(prmt(w2, w3, 0x5410u), a23[p]);
+    unpack8(prmt(w2, w3, 0x7632u), a23[p] + 4);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mma16816(acc[j], a01[0][j], a01[1][j], a23[0][j], a23[1][j], bw0, bw1);
 }
 
 // 32 fp16 keys (channels 32tig .. 32tig+31) of one residual token, paired (m, m+8)
@@ -241,7 +268,7 @@ __device__ __forceinline__ void qk_step(SoftState &st, const LaneInfo &li, KF &&
 
 // P.V side of one step: rescale the accumulators, then add the T tiles.
 //   vword(i, k)   word g of the value row of token tig + 4k of tile slot i.
-template <int R, class VW>
+template <int R, int BITS, class VW>
 __device__ __forceinline__ void pv_step(float acc[8][4], const LaneInfo &li, int n_valid, uint32_t bw0, uint32_t bw1,
                                         float alpha, VW &&vword) {
   constexpr int T = 4 / R;
@@ -254,11 +281,18 @@ __device__ __forceinline__ void pv_step(float acc[8][4], const LaneInfo &li, int
 #pragma unroll
   for (int i = 0; i < T; ++i) {
     if (16 * i < n_valid) {
-      uint32_t v[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
       const bool mine = li.pv_slot == i;
-      pv_tile(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
+      if constexpr (BITS == 2) {
+        uint32_t v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
+        pv_tile(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
+      } else {
+        uint2 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
+        pv_tile4(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
+      }
     }
   }
 }
@@ -367,10 +401,13 @@ __device__ __forceinline__ void pv_step_f16(float acc[8][4], const LaneInfo &li,
   }
 }
 
-template <int R, int G, bool PAGED>
+template <int R, int G, bool PAGED, int BITS>
 __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  using L = Layout<R, G>;
+  using L = Layout<R, G, BITS>;
+  constexpr int WPR = words_per_row<BITS>();
+  constexpr int kStages = L::kStages;
+  constexpr int kAhead = L::kAheadUnits;
   constexpr int T = 4 / R;           // tile slots per softmax step
   constexpr int TPG = G / 16;        // tiles per key group
   constexpr int NGU = L::kGroups;    // key groups per unit
@@ -423,15 +460,31 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   const int head_mine = tig % R;
   const int frag_row = 4 * (2 * ((g >> 1) % R) + (g & 1)) + tig;
   // prep: channel c = lane + 32k lands in row 4*(2h+p) + k, half-word wh of the row
-  int wh;
+  // (the same position for the channels lane + 32k of every k: the row differs).
+  // wh_pairs is the order of the fp16 residual keys (residual_pairs), which is also
+  // the order of the unpacked 2-bit codes: B half-word 2i + d of lane tig holds
+  // channel 32tig + 16(i >= 8) + (i mod 8) + 8d.
+  int wh_pairs;
   {
     const int i = lane & 15, i8 = i & 7;
     const int j = 4 * (lane >> 4) + (i8 >> 1);
-    wh = (2 * j + (i8 & 1)) * 2 + (i >= 8 ? 1 : 0);
+    wh_pairs = (2 * j + (i8 & 1)) * 2 + (i >= 8 ? 1 : 0);
   }
-  // codes of channel index i (mod 16) are unpacked with factor 4^(i mod 4);
-  // 4^(3 - i mod 4) brings every q.K product to code * qs * 64
-  const float mult = (float)(64 >> (2 * (lane & 3)));
+  int wh;
+  float mult;
+  if constexpr (BITS == 2) {
+    wh = wh_pairs;
+    // codes of channel index i (mod 16) are unpacked with factor 4^(i mod 4);
+    // 4^(3 - i mod 4) brings every q.K product to code * qs * 64
+    mult = (float)(64 >> (2 * (lane & 3)));
+  } else {
+    // B half-word 2i + d holds channel 32tig + 16(i >= 8) + 8q + t + 4d, i = 8(i >= 8) + 4q + t
+    const int t = lane & 3, d = (lane >> 2) & 1, q = (lane >> 3) & 1, s16 = lane >> 4;
+    wh = 2 * (8 * s16 + 4 * q + t) + d;
+    // channel position t is unpacked with factor 16^(t mod 2); 16^(1 - t mod 2) brings
+    // every q.K product to code * qs * 16
+    mult = (t & 1) ? 1.f : 16.f;
+  }
 
   // ---- cursors: ic stages unit u0 + kk (one ahead), cc computes it
   Cursor ic;
@@ -506,13 +559,13 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         row0 = ic.h * a.max_tokens + (int64_t)g0 * G;
         grp0 = ic.h * (a.max_tokens / G) + g0;
       }
-      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + row0 * kWordsPerRow);
-      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + row0 * kWordsPerRow);
+      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + row0 * WPR);
+      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + row0 * WPR);
       const unsigned char *vm = reinterpret_cast<const unsigned char *>(a.v_meta + row0);
       const unsigned char *km = reinterpret_cast<const unsigned char *>(a.k_meta + grp0 * kD);
       if (rows == kUnit) {
 #pragma unroll
-        for (int c = lane; c < kUnit * 2; c += 32) {
+        for (int c = lane; c < kUnit * L::kRowChunks; c += 32) {
           cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
           cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
         }
@@ -520,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
         for (int c = lane; c < NGU * 32; c += 32) cp_async16(stg + L::kKMeta + c * 16, km + c * 16);
       } else {
-        for (int c = lane; c < rows * 2; c += 32) {
+        for (int c = lane; c < rows * L::kRowChunks; c += 32) {
           cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
           cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
         }
@@ -581,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         // undo the code factor 4^(j mod 4) and the 2^-24 of the subnormal codes
-        const float un = acc_true ? 1.f : pow2i(24 - 2 * (j & 3));
+        const float un = acc_true ? 1.f : pow2i(BITS == 2 ? 24 - 2 * (j & 3) : 24 - 4 * (j & 1));
         dst[16 * g + j] = fmaf(o[j], un, zs);
         dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs);
       }
@@ -687,7 +740,8 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, off);
             if (head_mine == hh) {
-              cq_g[gi] = c0 * pow2i(18 - E);  // products are code * qs * 2^(E - 18)
+              // products are code * qs * 2^(E - 18) (2-bit) or 2^(E - 20) (4-bit)
+              cq_g[gi] = c0 * pow2i((BITS == 2 ? 18 : 20) - E);
               beta_g[gi] = c0 * bsum;
             }
           }
@@ -712,13 +766,28 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
             // (re)load the B fragment at the first tile of each group in the step
             if (i == 0 || t % TPG == 0)
               load_frag(frag + (t / TPG) * L::kFragGroupBytes + frag_row * kFragRowWords * 4, bf);
-            const uint2 ka = lds64(stg + L::kKCodes + (16 * t + g) * 32 + tig * 8);
-            const uint2 kb = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
             uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-            unpack16(ka.x, ra0);
-            unpack16(ka.y, ra1);
-            unpack16(kb.x, rb0);
-            unpack16(kb.y, rb1);
+            if constexpr (BITS == 2) {
+              // words 2tig, 2tig+1 of tokens g and g+8: channels 32tig .. 32tig+31
+              const uint2 ka = lds64(stg + L::kKCodes + (16 * t + g) * 32 + tig * 8);
+              const uint2 kb = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
+              unpack16(ka.x, ra0);
+              unpack16(ka.y, ra1);
+              unpack16(kb.x, rb0);
+              unpack16(kb.y, rb1);
+            } else {
+              // words 4tig .. 4tig+3 of tokens g and g+8: channels 32tig .. 32tig+31
+              const uint4 ka = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g) * 64 + tig * 16);
+              const uint4 kb = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g + 8) * 64 + tig * 16);
+              unpack8(ka.x, ra0);
+              unpack8(ka.y, ra0 + 4);
+              unpack8(ka.z, ra1);
+              unpack8(ka.w, ra1 + 4);
+              unpack8(kb.x, rb0);
+              unpack8(kb.y, rb0 + 4);
+              unpack8(kb.z, rb1);
+              unpack8(kb.w, rb1 + 4);
+            }
             qk_tile(ra0, ra1, rb0, rb1, bf, sc);
           };
           auto vmeta = [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + (16 * T * s + tok) * 4); };
@@ -739,8 +808,8 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       for (int k = 0; k < 4; ++k)
 #pragma unroll
         for (int hh = 0; hh < R; ++hh) {
-          fb[(k + 8 * hh) * (kFragRowWords * 2) + wh] = f2h(qv[hh][k]);
-          fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh] = 0;
+          fb[(k + 8 * hh) * (kFragRowWords * 2) + wh_pairs] = f2h(qv[hh][k]);
+          fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh_pairs] = 0;
         }
       __syncwarp();
       uint32_t bf[16];
@@ -783,16 +852,22 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       for (int s = 0; s < R; ++s) {
         const int nv = min(16 * T, n_ntok - 16 * T * s);
         if (nv <= 0) break;
-        pv_step<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
-          return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
-        });
+        if constexpr (BITS == 2) {
+          pv_step<R, 2>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
+            return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
+          });
+        } else {
+          pv_step<R, 4>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint2 {
+            return lds64(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 64 + g * 8);
+          });
+        }
       }
     } else if (a.v_res) {
       // fp16 residual values: this is the head's last unit, so the accumulators move
       // to output units here and the head's partial is written without code factors
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float un = pow2i(24 - 2 * (j & 3));
+        const float un = pow2i(BITS == 2 ? 24 - 2 * (j & 3) : 24 - 4 * (j & 1));
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[j][k] *= un;
       }
@@ -805,15 +880,22 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         pv_step_f16<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], vres_head + 16 * T * s * kD);
       }
     } else {
-      const uint32_t *vc_head = a.v_codes + n_res_row * kWordsPerRow;
+      const uint32_t *vc_head = a.v_codes + n_res_row * WPR;
 #pragma unroll
       for (int s = 0; s < R; ++s) {
         const int nv = min(16 * T, n_ntok - 16 * T * s);
         if (nv <= 0) break;
-        pv_step<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
-          const int slot = 16 * (s * T + i) + tig + 4 * k;
-          return vc_head[(slot < n_ntok ? slot : 0) * kWordsPerRow + g];
-        });
+        if constexpr (BITS == 2) {
+          pv_step<R, 2>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
+            const int slot = 16 * (s * T + i) + tig + 4 * k;
+            return vc_head[(slot < n_ntok ? slot : 0) * WPR + g];
+          });
+        } else {
+          pv_step<R, 4>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint2 {
+            const int slot = 16 * (s * T + i) + tig + 4 * k;
+            return *reinterpret_cast<const uint2 *>(vc_head + (slot < n_ntok ? slot : 0) * WPR + 2 * g);
+          });
+        }
       }
     }
     __syncwarp();  // this unit's stage may be refilled from now on
@@ -913,38 +995,43 @@ __global__ void __launch_bounds__(32 * kCombineRows) paged_combine_kernel(const 
   }
 }
 
-template <int R, int G, bool PAGED>
+template <int R, int G, bool PAGED, int BITS>
 const void *kernel_ptr() {
-  return reinterpret_cast<const void *>(&decode_kernel<R, G, PAGED>);
+  return reinterpret_cast<const void *>(&decode_kernel<R, G, PAGED, BITS>);
 }
 
-template <bool PAGED>
+template <bool PAGED, int BITS>
 const void *select_kernel(int R, int G) {
   if (G == 32)
-    return R == 1 ? kernel_ptr<1, 32, PAGED>() : R == 2 ? kernel_ptr<2, 32, PAGED>() : kernel_ptr<4, 32, PAGED>();
-  return R == 1 ? kernel_ptr<1, 64, PAGED>() : R == 2 ? kernel_ptr<2, 64, PAGED>() : kernel_ptr<4, 64, PAGED>();
+    return R == 1   ? kernel_ptr<1, 32, PAGED, BITS>()
+           : R == 2 ? kernel_ptr<2, 32, PAGED, BITS>()
+                    : kernel_ptr<4, 32, PAGED, BITS>();
+  return R == 1 ? kernel_ptr<1, 64, PAGED, BITS>() : R == 2 ? kernel_ptr<2, 64, PAGED, BITS>() : kernel_ptr<4, 64, PAGED, BITS>();
 }
 
+template <int BITS>
 int smem_bytes(int R, int G) {
-  if (G == 32) return R == 1 ? Layout<1, 32>::kSmem : R == 2 ? Layout<2, 32>::kSmem : Layout<4, 32>::kSmem;
-  return R == 1 ? Layout<1, 64>::kSmem : R == 2 ? Layout<2, 64>::kSmem : Layout<4, 64>::kSmem;
+  if (G == 32)
+    return R == 1 ? Layout<1, 32, BITS>::kSmem : R == 2 ? Layout<2, 32, BITS>::kSmem : Layout<4, 32, BITS>::kSmem;
+  return R == 1 ? Layout<1, 64, BITS>::kSmem : R == 2 ? Layout<2, 64, BITS>::kSmem : Layout<4, 64, BITS>::kSmem;
 }
 
 // Paged kernels append the lengths, the unit prefix and 4 warp totals: 2B + 5 ints.
-int paged_smem_bytes(int R, int G, int B) { return smem_bytes(R, G) + ((4 * (2 * B + 5) + 15) & ~15); }
+constexpr int paged_extra(int B) { return (4 * (2 * B + 5) + 15) & ~15; }
 
 }  // namespace
 
-DecodeKernels decode_kernels(int R, int G, bool paged, int B) {
+DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B) {
   DecodeKernels k;
+  const int base = bits == 2 ? smem_bytes<2>(R, G) : smem_bytes<4>(R, G);
   if (paged) {
-    k.decode = select_kernel<true>(R, G);
-    k.smem = paged_smem_bytes(R, G, B);
-    k.smem_limit = paged_smem_bytes(R, G, kPagedMaxBatch);
+    k.decode = bits == 2 ? select_kernel<true, 2>(R, G) : select_kernel<true, 4>(R, G);
+    k.smem = base + paged_extra(B);
+    k.smem_limit = base + paged_extra(kPagedMaxBatch);
     k.combine = reinterpret_cast<const void *>(&paged_combine_kernel);
   } else {
-    k.decode = select_kernel<false>(R, G);
-    k.smem = k.smem_limit = smem_bytes(R, G);
+    k.decode = bits == 2 ? select_kernel<false, 2>(R, G) : select_kernel<false, 4>(R, G);
+    k.smem = k.smem_limit = base;
     k.combine = reinterpret_cast<const void *>(&combine_kernel);
   }
   return k;

@@ -85,10 +85,10 @@ cudaError_t launch_pair(const DecodeKernels &k, const DecodeArgs &a, void **comb
 
 }  // namespace
 
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out) {
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out) {
   const int R = Hq / Hkv;
   int nw = 0;
-  cudaError_t e = warps_on_device(decode_kernels(R, G, false, B), &nw);
+  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, false, B), &nw);
   if (e != cudaSuccess) return e;
   const int64_t heads = (int64_t)B * Hkv;
   const int64_t ng = n / G;
@@ -105,10 +105,10 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom
   return cudaSuccess;
 }
 
-cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out) {
+cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, int bits, PagedGeom *out) {
   const int R = Hq / Hkv;
   int nw = 0;
-  cudaError_t e = warps_on_device(decode_kernels(R, G, true, B), &nw);
+  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, true, B), &nw);
   if (e != cudaSuccess) return e;
   const size_t heads = (size_t)B * Hkv;
   out->n_warps = nw;
@@ -119,7 +119,7 @@ cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out)
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
-  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, false, a.B);
+  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, a.bits, false, a.B);
   const float *ws = a.ws;
   int64_t pmax = a.pmax, W = a.total_units, NW = a.n_warps, U = a.units_per_head;
   int Hkv = a.Hkv, Hq = a.Hq;
@@ -130,7 +130,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st) {
-  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, true, a.B);
+  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, a.bits, true, a.B);
   const float *ws = a.ws;
   int Hkv = a.Hkv, Hq = a.Hq, B = a.B;
   int32_t *advance = a.advance_lens;

@@ -9,6 +9,8 @@ namespace kivi {
 
 constexpr int kD = 128;          // head dim
 constexpr int kWordsPerRow = 8;  // 128 channels x 2 bits / 32
+template <int BITS>
+__host__ __device__ constexpr int words_per_row() { return kD * BITS / 32; }  // 8 (2-bit) or 16 (4-bit)
 
 // ---- fp16 bit-pattern helpers ----------------------------------------------------
 __device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
@@ -27,20 +29,28 @@ __device__ __forceinline__ uint16_t f2h(float x) { return __half_as_ushort(__flo
 // one ulp of 3s/2), and fl32(d/s) > 5/2 iff d > 5s/2.  round_half_even then gives
 // code >= 1, >= 2, >= 3 exactly at these three events, and d <= max - min keeps the
 // code at most 3.  When the fp16 scale is 0 all codes are 0 (thresholds = +inf).
+//
+// The 4-bit width (15 levels) evaluates the rule as written: u = fl32(fl32(x - mn) / s)
+// with an IEEE division, then round-half-even and a clamp to 15; fp32 operations of
+// the same order as the definition, so the codes are the definition's.
 struct QParams {
-  float mn, t1, t2, t3;
-  uint32_t meta;  // fp16 s | fp16 z << 16
+  float mn, t1, t2, t3;  // 2-bit thresholds
+  float s;               // the fp16 scale in fp32 (0: every code is 0)
+  uint32_t meta;         // fp16 s | fp16 z << 16
 };
 
+template <int BITS = 2>
 __device__ __forceinline__ QParams make_qparams(float mn, float mx) {
+  static_assert(BITS == 2 || BITS == 4, "2- or 4-bit codes");
   QParams p;
   float range = __fsub_rn(mx, mn);
-  float s32 = __fdiv_rn(range, 3.0f);
+  float s32 = __fdiv_rn(range, BITS == 2 ? 3.0f : 15.0f);
   uint16_t s16 = f2h(s32);
   float s = h2f(s16);
   uint16_t z16 = f2h(mn);  // exact: mn is an fp16 value
   if (z16 == 0x8000u) z16 = 0;  // -0 is stored as +0
   p.mn = mn;
+  p.s = (s16 == 0) ? 0.f : s;
   if (s16 == 0) {
     p.t1 = p.t2 = p.t3 = __int_as_float(0x7f800000);  // +inf: every code is 0
   } else {
@@ -52,13 +62,22 @@ __device__ __forceinline__ QParams make_qparams(float mn, float mx) {
   return p;
 }
 
+template <int BITS = 2>
 __device__ __forceinline__ uint32_t quant_code(float x, const QParams &p) {
   float d = __fsub_rn(x, p.mn);
-  return (uint32_t)(d > p.t1) + (uint32_t)(d >= p.t2) + (uint32_t)(d > p.t3);
+  if constexpr (BITS == 2) {
+    return (uint32_t)(d > p.t1) + (uint32_t)(d >= p.t2) + (uint32_t)(d > p.t3);
+  } else {
+    if (p.s == 0.f) return 0u;
+    const int c = __float2int_rn(__fdiv_rn(d, p.s));  // round half to even
+    return (uint32_t)(c < 0 ? 0 : (c > 15 ? 15 : c));
+  }
 }
 
-// Codes of the 8 channels held in one 16-byte chunk (4 half2), packed 2 bits each
-// into the low 16 bits: channel j of the chunk at bits [2j, 2j+1].
+// Codes of the 8 channels held in one 16-byte chunk (4 half2), channel j of the
+// chunk at bits [BITS*j, BITS*j + BITS - 1]: 16 bits for 2-bit codes, a whole
+// word for 4-bit codes.
+template <int BITS = 2>
 __device__ __forceinline__ uint32_t quant_chunk8(const uint4 &c, const QParams &p) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   uint32_t bits = 0;
@@ -66,8 +85,8 @@ __device__ __forceinline__ uint32_t quant_chunk8(const uint4 &c, const QParams &
   for (int k = 0; k < 4; ++k) {
     float lo = h2f((uint16_t)(w[k] & 0xffffu));
     float hi = h2f((uint16_t)(w[k] >> 16));
-    bits |= quant_code(lo, p) << (4 * k);
-    bits |= quant_code(hi, p) << (4 * k + 2);
+    bits |= quant_code<BITS>(lo, p) << (2 * BITS * k);
+    bits |= quant_code<BITS>(hi, p) << (2 * BITS * k + BITS);
   }
   return bits;
 }
@@ -112,6 +131,19 @@ __device__ __forceinline__ void unpack16(uint32_t w, uint32_t r[8]) {
     r[m] = w & (0x00030003u << (2 * m));
     r[m + 4] = x & (0x00030003u << (2 * m));
   }
+}
+
+// ---- 4-bit code unpack -------------------------------------------------------------------
+// A word holds 8 codes, code i at bits [4i, 4i+3].  Masks 0x000F000F and 0x00F000F0 on
+// w and on w >> 8 leave, in the two 16-bit halves, the fp16 subnormals
+//   r[0] = {c0, c4} * 2^-24,  r[1] = {c1, c5} * 16 * 2^-24,
+//   r[2] = {c2, c6} * 2^-24,  r[3] = {c3, c7} * 16 * 2^-24   (bits 0..7 are mantissa).
+__device__ __forceinline__ void unpack8(uint32_t w, uint32_t r[4]) {
+  const uint32_t x = w >> 8;
+  r[0] = w & 0x000F000Fu;
+  r[1] = w & 0x00F000F0u;
+  r[2] = x & 0x000F000Fu;
+  r[3] = x & 0x00F000F0u;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }

@@ -6,12 +6,14 @@
 
 namespace kivi {
 
+// `bits` is the code width, 2 or 4.
 cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_t heads, int64_t groups_per_head,
-                              int64_t g0, int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
+                              int64_t g0, int G, int bits, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
                               cudaStream_t st);
 cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
-                              int64_t t0, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st);
-cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G,
+                              int64_t t0, int bits, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens,
+                              cudaStream_t st);
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G, int bits,
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
                           cudaStream_t st);
 cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, int64_t nq, int G, uint16_t *k_res,
@@ -24,10 +26,10 @@ struct PageMap {
   int Hkv;
 };
 cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, int64_t heads,
-                                    int64_t groups_per_head, int G, const PageMap &pm, uint32_t *k_codes,
+                                    int64_t groups_per_head, int G, int bits, const PageMap &pm, uint32_t *k_codes,
                                     uint32_t *k_meta, cudaStream_t st);
 cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head,
-                                    int64_t in_rows_per_head, const PageMap &pm, uint32_t *v_codes,
+                                    int64_t in_rows_per_head, int bits, const PageMap &pm, uint32_t *v_codes,
                                     uint32_t *v_meta, cudaStream_t st);
 cudaError_t launch_set_len(int32_t *seq_lens, int32_t seq, int32_t n, cudaStream_t st);
 
@@ -42,14 +44,15 @@ struct PagedAppendArgs {
   uint16_t *v_res;                // [B][Hkv][G][128] with a value residual, else null
   uint32_t *k_codes, *k_meta, *v_codes, *v_meta;
   int64_t num_pages;
-  int B, Hkv, G, shift, max_pages;
+  int B, Hkv, G, bits, shift, max_pages;
 };
 cudaError_t launch_paged_append(const PagedAppendArgs &a, cudaStream_t st);
 cudaError_t launch_advance_lens(int32_t *seq_lens, int B, int32_t cap, cudaStream_t st);
 
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                            const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
-                           int64_t n, int G, int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st);
+                           int64_t n, int G, int bits, int64_t max_tokens, float *k_out, float *v_out,
+                           cudaStream_t st);
 
 struct DecodeArgs {
   const uint32_t *k_codes;
@@ -64,6 +67,7 @@ struct DecodeArgs {
   int64_t max_tokens;
   int64_t n;
   int B, Hkv, Hq, G;
+  int bits;                // code width: 2 or 4
   int64_t units_per_head;  // full key groups + 1 if there are residual keys
   int64_t total_units;     // B * Hkv * units_per_head
   int n_warps;             // warps of the persistent grid (each takes a contiguous unit range)
@@ -96,7 +100,7 @@ struct DecodeKernels {
   const void *combine;  // dense: (ws, pmax, W, NW, U, Hkv, Hq, rows, out);
                         // paged: (ws, Hkv, Hq, B, advance, cap, out)
 };
-DecodeKernels decode_kernels(int R, int G, bool paged, int B);
+DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B);
 
 // Geometry of one decode call on the current device (deterministic for given sizes).
 struct DecodeGeom {
@@ -106,7 +110,7 @@ struct DecodeGeom {
   int grid;
   int pmax;
 };
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int64_t n, DecodeGeom *out);
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
 // Paged decode: the grid fills the GPU whatever the lengths; n_warps and grid come
@@ -118,7 +122,7 @@ struct PagedGeom {
   size_t ws_bytes;
 };
 constexpr int kPagedMaxBatch = 512;
-cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, PagedGeom *out);
+cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, int bits, PagedGeom *out);
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st);
 
 // Decode attention over an unquantized fp16 cache (the comparison kernel).

@@ -25,7 +25,7 @@ __device__ __forceinline__ bool paged_row(const PageMap &pm, int64_t bh, int64_t
   return true;
 }
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, int BITS>
 __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
                                                         int64_t groups_per_head, int64_t g0,
                                                         uint32_t *__restrict__ k_codes,
@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   constexpr int TPL = G / 8;  // tokens per lane
-  __shared__ __align__(16) uint32_t s_codes[G * kWordsPerRow];
+  constexpr int WPR = words_per_row<BITS>();
+  __shared__ __align__(16) uint32_t s_codes[G * WPR];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t8 = lane >> 2, c4 = lane & 3;
   const int64_t bh = blockIdx.x / groups_per_head;
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   const uint32_t mn_bits = h22u(mn[t8 >> 1]), mx_bits = h22u(mx[t8 >> 1]);
   const float my_mn = h2f((uint16_t)((t8 & 1) ? (mn_bits >> 16) : (mn_bits & 0xffffu)));
   const float my_mx = h2f((uint16_t)((t8 & 1) ? (mx_bits >> 16) : (mx_bits & 0xffffu)));
-  const QParams mine = make_qparams(my_mn, my_mx);
+  const QParams mine = make_qparams<BITS>(my_mn, my_mx);
   k_meta[grp * kD + 32 * warp + 8 * c4 + t8] = mine.meta;
 
   QParams p[8];
@@ -92,9 +93,13 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   for (int j = 0; j < 8; ++j) {
     const int src_lane = 4 * j + c4;
     p[j].mn = __shfl_sync(0xffffffffu, mine.mn, src_lane);
-    p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
-    p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
-    p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
+    if constexpr (BITS == 2) {
+      p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
+      p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
+      p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
+    } else {
+      p[j].s = __shfl_sync(0xffffffffu, mine.s, src_lane);
+    }
   }
 #pragma unroll
   for (int k = 0; k < TPL; ++k) {
@@ -102,24 +107,30 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
     uint32_t bits = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      bits |= quant_code(h2f((uint16_t)(wk[j] & 0xffffu)), p[2 * j]) << (4 * j);
-      bits |= quant_code(h2f((uint16_t)(wk[j] >> 16)), p[2 * j + 1]) << (4 * j + 2);
+      bits |= quant_code<BITS>(h2f((uint16_t)(wk[j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
+      bits |= quant_code<BITS>(h2f((uint16_t)(wk[j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
     }
-    // chunks 2m and 2m+1 form word 2*warp + m of the token row
-    const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
-    if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * kWordsPerRow + 2 * warp + (c4 >> 1)] = bits | (other << 16);
+    if constexpr (BITS == 2) {
+      // chunks 2m and 2m+1 form word 2*warp + m of the token row
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+      if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * WPR + 2 * warp + (c4 >> 1)] = bits | (other << 16);
+    } else {
+      // chunk c4 of warp w is word 4w + c4 of the token row
+      s_codes[(t8 + 8 * k) * WPR + 4 * warp + c4] = bits;
+    }
   }
   __syncthreads();
   // coalesced write of the G packed token rows
-  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + row0 * kWordsPerRow);
+  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + row0 * WPR);
   const uint4 *s4 = reinterpret_cast<const uint4 *>(s_codes);
-  for (int i = threadIdx.x; i < G * kWordsPerRow / 4; i += blockDim.x) dst[i] = s4[i];
+  for (int i = threadIdx.x; i < G * WPR / 4; i += blockDim.x) dst[i] = s4[i];
 }
 
 // -------------------------------------------------------------------------------------
 // Value tokens: 16 lanes per token row (one 16-byte chunk of 8 channels each).
 // quantize_value_row works on one half-warp; `lane16` is the lane within it.
 // -------------------------------------------------------------------------------------
+template <int BITS>
 __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, uint32_t half_mask,
                                                    uint32_t *codes_row, uint32_t *meta_out) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -132,16 +143,20 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   for (int off = 1; off < 16; off <<= 1) red = __hmin2(red, u2h2(__shfl_xor_sync(half_mask, h22u(red), off)));
   const float fmn = __low2float(red);
   const float fmx = -__high2float(red);
-  const QParams p = make_qparams(fmn, fmx);
-  const uint32_t bits = quant_chunk8(x, p);
-  const uint32_t other = __shfl_xor_sync(half_mask, bits, 1);
-  if ((lane16 & 1) == 0) codes_row[lane16 >> 1] = bits | (other << 16);
+  const QParams p = make_qparams<BITS>(fmn, fmx);
+  const uint32_t bits = quant_chunk8<BITS>(x, p);
+  if constexpr (BITS == 2) {
+    const uint32_t other = __shfl_xor_sync(half_mask, bits, 1);
+    if ((lane16 & 1) == 0) codes_row[lane16 >> 1] = bits | (other << 16);
+  } else {
+    codes_row[lane16] = bits;  // chunk lane16 = channels 8*lane16 .. +7 = word lane16
+  }
   if (lane16 == 0) *meta_out = p.meta;
 }
 
 // rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
 // read from input row (head * in_rows_per_head + r % tokens_per_head)
-template <bool PAGED>
+template <bool PAGED, int BITS>
 __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restrict__ v, int64_t rows,
                                                          int64_t tokens_per_head, int64_t in_rows_per_head,
                                                          int64_t t0, uint32_t *__restrict__ v_codes,
@@ -160,13 +175,14 @@ __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restr
       if (!paged_row(pm, bh, t, &dst)) continue;  // the half-warp skips the row together
     }
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + lane16);
-    quantize_value_row(x, lane16, half_mask, v_codes + dst * kWordsPerRow, v_meta + dst);
+    quantize_value_row<BITS>(x, lane16, half_mask, v_codes + dst * words_per_row<BITS>(), v_meta + dst);
   }
 }
 
 // Append: one warp per (batch, KV head).  Lanes 0-15 quantize the new value row (or,
 // with a value residual, copy it into residual slot r); lanes 16-31 copy the new
 // key (256 bytes) into residual slot r.
+template <int BITS>
 __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict__ k_new,
                                                      const uint16_t *__restrict__ v_new, int64_t heads,
                                                      int64_t n, int G, uint16_t *__restrict__ k_res,
@@ -184,8 +200,8 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
     if (v_res)
       reinterpret_cast<uint4 *>(v_res + (bh * G + n % G) * kD)[lane16] = x;
     else
-      quantize_value_row(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * kWordsPerRow,
-                         v_meta + bh * max_tokens + n);
+      quantize_value_row<BITS>(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * words_per_row<BITS>(),
+                               v_meta + bh * max_tokens + n);
   } else {
     const int64_t r = n % G;
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(k_new + bh * kD) + lane16);
@@ -203,8 +219,9 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
 // 4l .. 4l+3 of the G keys (slots 0 .. G-2 from the residual, the new key from the
 // input), finds their min and max, then packs each token row.  A full sequence
 // (len at the block table's capacity) or a page id outside the pool drops the token.
-template <int G>
+template <int G, int BITS>
 __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs a) {
+  constexpr int WPR = words_per_row<BITS>();
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -224,8 +241,7 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
     if (a.v_res)
       reinterpret_cast<uint4 *>(a.v_res + (bh * G + r) * kD)[lane16] = x;
     else
-      quantize_value_row(x, lane16, 0x0000ffffu, a.v_codes + (ph * P + off) * kWordsPerRow,
-                         a.v_meta + ph * P + off);
+      quantize_value_row<BITS>(x, lane16, 0x0000ffffu, a.v_codes + (ph * P + off) * WPR, a.v_meta + ph * P + off);
   } else {
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(a.k_new + bh * kD) + lane16);
     reinterpret_cast<uint4 *>(a.k_res + (bh * G + r) * kD)[lane16] = x;
@@ -244,25 +260,28 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
     mn1 = __hmin2(mn1, u2h2(x.y));
     mx1 = __hmax2(mx1, u2h2(x.y));
   }
-  const QParams p0 = make_qparams(__low2float(mn0), __low2float(mx0));
-  const QParams p1 = make_qparams(__high2float(mn0), __high2float(mx0));
-  const QParams p2 = make_qparams(__low2float(mn1), __low2float(mx1));
-  const QParams p3 = make_qparams(__high2float(mn1), __high2float(mx1));
+  const QParams p0 = make_qparams<BITS>(__low2float(mn0), __low2float(mx0));
+  const QParams p1 = make_qparams<BITS>(__high2float(mn0), __high2float(mx0));
+  const QParams p2 = make_qparams<BITS>(__low2float(mn1), __low2float(mx1));
+  const QParams p3 = make_qparams<BITS>(__high2float(mn1), __high2float(mx1));
   const int64_t row0 = ph * P + off - (G - 1);
   reinterpret_cast<uint4 *>(a.k_meta + (row0 / G) * kD)[lane] = make_uint4(p0.meta, p1.meta, p2.meta, p3.meta);
-  // channel 4l + j sits in word l / 4 at bits 8 (l mod 4) + 2j
-  const int shift = 8 * (lane & 3);
-  uint32_t *dst = a.k_codes + row0 * kWordsPerRow + (lane >> 2);
+  // 2-bit: channel 4l + j sits in word l / 4 at bits 8 (l mod 4) + 2j;
+  // 4-bit: in word l / 2 at bits 16 (l mod 2) + 4j
+  constexpr int LPW = 32 / (4 * BITS);  // lanes per word: 4 or 2
+  const int shift = 4 * BITS * (lane & (LPW - 1));
+  uint32_t *dst = a.k_codes + row0 * WPR + lane / LPW;
 #pragma unroll 8
   for (int t = 0; t < G; ++t) {
     const uint2 x = key(t);
-    uint32_t bits = quant_code(h2f((uint16_t)(x.x & 0xffffu)), p0) | (quant_code(h2f((uint16_t)(x.x >> 16)), p1) << 2) |
-                    (quant_code(h2f((uint16_t)(x.y & 0xffffu)), p2) << 4) |
-                    (quant_code(h2f((uint16_t)(x.y >> 16)), p3) << 6);
+    uint32_t bits = quant_code<BITS>(h2f((uint16_t)(x.x & 0xffffu)), p0) |
+                    (quant_code<BITS>(h2f((uint16_t)(x.x >> 16)), p1) << BITS) |
+                    (quant_code<BITS>(h2f((uint16_t)(x.y & 0xffffu)), p2) << (2 * BITS)) |
+                    (quant_code<BITS>(h2f((uint16_t)(x.y >> 16)), p3) << (3 * BITS));
     bits <<= shift;
     bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
-    bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
-    if ((lane & 3) == 0) dst[t * kWordsPerRow] = bits;
+    if constexpr (LPW == 4) bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
+    if ((lane & (LPW - 1)) == 0) dst[t * WPR] = bits;
   }
   if (a.v_res) {
     // the group's values, one token row per half-warp (slots 0 .. G-2 from the
@@ -272,7 +291,7 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
     for (int t = half; t < G; t += 2) {
       const uint16_t *src = (t == G - 1) ? a.v_new + bh * kD : a.v_res + (bh * G + t) * kD;
       const uint4 x = reinterpret_cast<const uint4 *>(src)[lane16];
-      quantize_value_row(x, lane16, half_mask, a.v_codes + (row0 + t) * kWordsPerRow, a.v_meta + row0 + t);
+      quantize_value_row<BITS>(x, lane16, half_mask, a.v_codes + (row0 + t) * WPR, a.v_meta + row0 + t);
     }
   }
 }
@@ -298,6 +317,7 @@ __global__ void __launch_bounds__(128) residual_copy_kernel(const uint16_t *__re
 }
 
 // Dequantize (test aid): thread per (head, token, 8-channel chunk).
+template <int BITS>
 __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict__ k_codes,
                                                       const uint32_t *__restrict__ k_meta,
                                                       const uint16_t *__restrict__ k_res,
@@ -316,12 +336,14 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
     float *ko = k_out + (bh * n + t) * kD + c0;
     float *vo = v_out + (bh * n + t) * kD + c0;
     if (t < nq) {
-      const uint32_t word = k_codes[(bh * max_tokens + t) * kWordsPerRow + (c0 >> 4)] >> (2 * (c0 & 15));
+      // the chunk's 8 codes: BITS * 8 bits starting at bit BITS * c0 of the row
+      const uint32_t word = k_codes[(bh * max_tokens + t) * words_per_row<BITS>() + (c0 * BITS) / 32] >>
+                            ((c0 * BITS) % 32);
       const uint32_t *meta = k_meta + (bh * (max_tokens / G) + t / G) * kD + c0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float s = h2f((uint16_t)(meta[j] & 0xffffu)), z = h2f((uint16_t)(meta[j] >> 16));
-        ko[j] = __fadd_rn(z, __fmul_rn((float)((word >> (2 * j)) & 3u), s));
+        ko[j] = __fadd_rn(z, __fmul_rn((float)((word >> (BITS * j)) & ((1u << BITS) - 1u)), s));
       }
     } else {
       const uint16_t *res = k_res + (bh * G + (t - nq)) * kD + c0;
@@ -336,9 +358,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
     }
     const uint32_t vm = v_meta[bh * max_tokens + t];
     const float s = h2f((uint16_t)(vm & 0xffffu)), z = h2f((uint16_t)(vm >> 16));
-    const uint32_t word = v_codes[(bh * max_tokens + t) * kWordsPerRow + (c0 >> 4)] >> (2 * (c0 & 15));
+    const uint32_t word = v_codes[(bh * max_tokens + t) * words_per_row<BITS>() + (c0 * BITS) / 32] >>
+                          ((c0 * BITS) % 32);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) vo[j] = __fadd_rn(z, __fmul_rn((float)((word >> (2 * j)) & 3u), s));
+    for (int j = 0; j < 8; ++j) vo[j] = __fadd_rn(z, __fmul_rn((float)((word >> (BITS * j)) & ((1u << BITS) - 1u)), s));
   }
 }
 
@@ -348,59 +371,80 @@ static int grid_cap(int64_t want) {
   return (int)(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
+template <bool PAGED, int BITS>
+void key_groups(const uint16_t *in, int64_t in_head_stride, int64_t blocks, int64_t groups_per_head, int64_t g0,
+                int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens, const PageMap &pm, cudaStream_t st) {
+  if (G == 32)
+    key_group_kernel<32, PAGED, BITS><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0,
+                                                                        k_codes, k_meta, max_tokens, pm);
+  else
+    key_group_kernel<64, PAGED, BITS><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0,
+                                                                        k_codes, k_meta, max_tokens, pm);
+}
+
 cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_t heads, int64_t groups_per_head,
-                              int64_t g0, int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
+                              int64_t g0, int G, int bits, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
                               cudaStream_t st) {
   const int64_t blocks = heads * groups_per_head;
   if (blocks == 0) return cudaSuccess;
   const PageMap none = {};
-  if (G == 32)
-    key_group_kernel<32, false><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes,
-                                                                  k_meta, max_tokens, none);
+  if (bits == 2)
+    key_groups<false, 2>(in, in_head_stride, blocks, groups_per_head, g0, G, k_codes, k_meta, max_tokens, none, st);
   else
-    key_group_kernel<64, false><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0, k_codes,
-                                                                  k_meta, max_tokens, none);
+    key_groups<false, 4>(in, in_head_stride, blocks, groups_per_head, g0, G, k_codes, k_meta, max_tokens, none, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, int64_t heads,
-                                    int64_t groups_per_head, int G, const PageMap &pm, uint32_t *k_codes,
+                                    int64_t groups_per_head, int G, int bits, const PageMap &pm, uint32_t *k_codes,
                                     uint32_t *k_meta, cudaStream_t st) {
   const int64_t blocks = heads * groups_per_head;
   if (blocks == 0) return cudaSuccess;
-  if (G == 32)
-    key_group_kernel<32, true><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, 0, k_codes,
-                                                                 k_meta, 0, pm);
+  if (bits == 2)
+    key_groups<true, 2>(in, in_head_stride, blocks, groups_per_head, 0, G, k_codes, k_meta, 0, pm, st);
   else
-    key_group_kernel<64, true><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, 0, k_codes,
-                                                                 k_meta, 0, pm);
+    key_groups<true, 4>(in, in_head_stride, blocks, groups_per_head, 0, G, k_codes, k_meta, 0, pm, st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
-                              int64_t t0, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, cudaStream_t st) {
+                              int64_t t0, int bits, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens,
+                              cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  value_rows_kernel<false><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head,
-                                                                       t0, v_codes, v_meta, max_tokens, PageMap{});
+  const int grid = grid_cap((rows + 15) / 16);
+  if (bits == 2)
+    value_rows_kernel<false, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
+                                                       max_tokens, PageMap{});
+  else
+    value_rows_kernel<false, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
+                                                       max_tokens, PageMap{});
   return cudaGetLastError();
 }
 
 cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t tokens_per_head,
-                                    int64_t in_rows_per_head, const PageMap &pm, uint32_t *v_codes,
+                                    int64_t in_rows_per_head, int bits, const PageMap &pm, uint32_t *v_codes,
                                     uint32_t *v_meta, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  value_rows_kernel<true><<<grid_cap((rows + 15) / 16), 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0,
-                                                                      v_codes, v_meta, 0, pm);
+  const int grid = grid_cap((rows + 15) / 16);
+  if (bits == 2)
+    value_rows_kernel<true, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
+                                                      0, pm);
+  else
+    value_rows_kernel<true, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
+                                                      0, pm);
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G,
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G, int bits,
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
                           cudaStream_t st) {
-  append_kernel<<<(unsigned)((heads + 3) / 4), 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta,
-                                                             max_tokens, v_res);
+  const unsigned grid = (unsigned)((heads + 3) / 4);
+  if (bits == 2)
+    append_kernel<2><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res);
+  else
+    append_kernel<4><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res);
   return cudaGetLastError();
 }
 
@@ -408,9 +452,9 @@ cudaError_t launch_paged_append(const PagedAppendArgs &a, cudaStream_t st) {
   const int64_t heads = (int64_t)a.B * a.Hkv;
   const unsigned blocks = (unsigned)((heads + 3) / 4);
   if (a.G == 32)
-    paged_append_kernel<32><<<blocks, 128, 0, st>>>(a);
+    (a.bits == 2 ? paged_append_kernel<32, 2> : paged_append_kernel<32, 4>)<<<blocks, 128, 0, st>>>(a);
   else
-    paged_append_kernel<64><<<blocks, 128, 0, st>>>(a);
+    (a.bits == 2 ? paged_append_kernel<64, 2> : paged_append_kernel<64, 4>)<<<blocks, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -433,11 +477,17 @@ cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, in
 
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                            const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
-                           int64_t n, int G, int64_t max_tokens, float *k_out, float *v_out, cudaStream_t st) {
+                           int64_t n, int G, int bits, int64_t max_tokens, float *k_out, float *v_out,
+                           cudaStream_t st) {
   const int64_t total = heads * n * (kD / 8);
   if (total == 0) return cudaSuccess;
-  dequant_kernel<<<grid_cap((total + 255) / 256), 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G,
-                                                                max_tokens, k_out, v_out, v_res);
+  const int grid = grid_cap((total + 255) / 256);
+  if (bits == 2)
+    dequant_kernel<2><<<grid, 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G, max_tokens, k_out,
+                                            v_out, v_res);
+  else
+    dequant_kernel<4><<<grid, 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G, max_tokens, k_out,
+                                            v_out, v_res);
   return cudaGetLastError();
 }
 

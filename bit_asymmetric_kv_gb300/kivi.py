@@ -138,10 +138,10 @@ class Cache:
     """Caller-owned device buffers of one quantized KV cache (layouts in include/kivi.h)."""
 
     dims: kivi_dims
-    k_codes: torch.Tensor  # int32 [B, Hkv, T, D/16]   (uint32 bit patterns)
+    k_codes: torch.Tensor  # int32 [B, Hkv, T, D*bits/32]   (uint32 bit patterns)
     k_meta: torch.Tensor   # int32 [B, Hkv, T/G, D]    ({s, z} fp16 pairs)
     k_res: torch.Tensor    # fp16  [B, Hkv, G, D]
-    v_codes: torch.Tensor  # int32 [B, Hkv, T, D/16]
+    v_codes: torch.Tensor  # int32 [B, Hkv, T, D*bits/32]
     v_meta: torch.Tensor   # int32 [B, Hkv, T]
     c: kivi_cache
     v_res: torch.Tensor | None = None  # fp16 [B, Hkv, G, D] with a value residual
@@ -152,14 +152,15 @@ class Cache:
 
     @classmethod
     def allocate(cls, B: int, Hkv: int, G: int, max_tokens: int, device="cuda", D: int = 128,
-                 value_residual: bool = False) -> "Cache":
-        dims = make_dims(B, Hkv, G, max_tokens, D, value_residual=value_residual)
+                 value_residual: bool = False, bits: int = 2) -> "Cache":
+        dims = make_dims(B, Hkv, G, max_tokens, D, bits=bits, value_residual=value_residual)
         kivi_buffer_bytes(dims)  # validates the geometry
         T = max_tokens
-        kc = torch.empty((B, Hkv, T, D // 16), dtype=torch.int32, device=device)
+        W = D * bits // 32  # words of a packed token row
+        kc = torch.empty((B, Hkv, T, W), dtype=torch.int32, device=device)
         km = torch.empty((B, Hkv, T // G, D), dtype=torch.int32, device=device)
         kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
-        vc = torch.empty((B, Hkv, T, D // 16), dtype=torch.int32, device=device)
+        vc = torch.empty((B, Hkv, T, W), dtype=torch.int32, device=device)
         vm = torch.empty((B, Hkv, T), dtype=torch.int32, device=device)
         vr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device) if value_residual else None
         c = kivi_cache(kc.data_ptr(), km.data_ptr(), kr.data_ptr(), vc.data_ptr(), vm.data_ptr(),
@@ -317,14 +318,15 @@ class PagedCache:
 
     @classmethod
     def allocate(cls, B: int, Hkv: int, G: int, page_tokens: int, max_pages_per_seq: int, num_pages: int,
-                 device="cuda", D: int = 128, value_residual: bool = False) -> "PagedCache":
-        dims = make_paged_dims(B, Hkv, G, page_tokens, max_pages_per_seq, num_pages, D,
+                 device="cuda", D: int = 128, value_residual: bool = False, bits: int = 2) -> "PagedCache":
+        dims = make_paged_dims(B, Hkv, G, page_tokens, max_pages_per_seq, num_pages, D, bits=bits,
                                value_residual=value_residual)
         kivi_paged_buffer_bytes(dims)  # validates the geometry
         P = page_tokens
-        kc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
+        W = D * bits // 32  # words of a packed token row
+        kc = torch.empty((num_pages, Hkv, P, W), dtype=torch.int32, device=device)
         km = torch.empty((num_pages, Hkv, P // G, D), dtype=torch.int32, device=device)
-        vc = torch.empty((num_pages, Hkv, P, D // 16), dtype=torch.int32, device=device)
+        vc = torch.empty((num_pages, Hkv, P, W), dtype=torch.int32, device=device)
         vm = torch.empty((num_pages, Hkv, P), dtype=torch.int32, device=device)
         kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
         vr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device) if value_residual else None

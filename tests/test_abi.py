@@ -61,11 +61,14 @@ def test_buffer_bytes(L):
     assert out == [heads * 640 * 32, heads * 10 * 128 * 4, heads * 64 * 128 * 2, heads * 640 * 32, heads * 640 * 4, 0]
     out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640, value_residual=1))
     assert out[5] == heads * 64 * 128 * 2
+    out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640, bits=4))
+    assert out[0] == out[3] == heads * 640 * 64 and out[1] == heads * 10 * 128 * 4
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(D=64), kivi.KIVI_ERR_UNSUPPORTED),
-    (dict(bits=4), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(bits=3), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(bits=8), kivi.KIVI_ERR_UNSUPPORTED),
     (dict(G=16), kivi.KIVI_ERR_UNSUPPORTED),
     (dict(B=0), kivi.KIVI_ERR_ARG),
     (dict(max_tokens=100), kivi.KIVI_ERR_ARG),   # not a multiple of G
@@ -156,6 +159,7 @@ def test_paged_buffer_bytes(L):
 @pytest.mark.parametrize("kw,status", [
     (dict(D=64), kivi.KIVI_ERR_UNSUPPORTED),
     (dict(G=16), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(bits=3), kivi.KIVI_ERR_UNSUPPORTED),
     (dict(page_tokens=96), kivi.KIVI_ERR_UNSUPPORTED),       # not a power of two
     (dict(page_tokens=32), kivi.KIVI_ERR_UNSUPPORTED),       # below one 64-token unit
     (dict(B=513), kivi.KIVI_ERR_UNSUPPORTED),
