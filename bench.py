@@ -16,7 +16,7 @@ run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
                   [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
-                  [--value-residual] [--compare-fp16]
+                  [--value-residual] [--bits 2|4] [--compare-fp16]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
 from one pool, scattered by a seeded permutation; lengths on the device); with
@@ -49,14 +49,16 @@ L2_FLUSH_BYTES = 256 << 20
 CYCLE = 64  # steps between cache rollbacks
 
 
-def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False) -> int:
-    """Bytes one decode-attention launch must move at context n (D = 128):
-    per (batch, KV head) nq*(32 + 512/G) + r*256 + n*36, plus q and out; with a
-    value residual the last r values are fp16: nq*36 + r*256 instead of n*36."""
+def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2) -> int:
+    """Bytes one decode-attention launch must move at context n (D = 128, c = 16*bits
+    bytes of codes per token row): per (batch, KV head) nq*(c + 512/G) + r*256 +
+    n*(c + 4), plus q and out; with a value residual the last r values are fp16:
+    nq*(c + 4) + r*256 instead of n*(c + 4)."""
+    c = 16 * bits
     nq = (n // G) * G
     r = n - nq
-    values = nq * 36 + r * 256 if value_residual else n * 36
-    per_head = nq * 32 + (nq // G) * 512 + r * 256 + values
+    values = nq * (c + 4) + r * 256 if value_residual else n * (c + 4)
+    per_head = nq * c + (nq // G) * 512 + r * 256 + values
     return B * Hkv * per_head + 2 * B * Hq * 128 * 2
 
 
@@ -177,7 +179,8 @@ def dist_env():
 # ----------------------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
-def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False):
+def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False,
+                  bits: int = 2):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
     cache) on `sample_heads` of the workload's KV heads; scale to the whole batch."""
     import oracle
@@ -187,7 +190,7 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
     T = wl.capacity(extra=steps + 64)
     k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
     v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
-    c = oracle.prefill(k, v, wl.G, T, value_residual=value_residual)  # untimed, like the GPU's prefill
+    c = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits)  # untimed, like the GPU's prefill
     R = wl.Hq // wl.Hkv
     t_total, done = 0.0, 0
     for step in range(steps):
@@ -217,11 +220,11 @@ def run_reference(args, wl):
     pre = synth.make_prefill(wl)
     for w in range(args.warmup):  # untimed warm-up: the first call builds the oracle
         oracle_timing(wl, pre, 1, 4, 0.0)
-    cb = oracle_timing(wl, pre, args.steps, 32, 60.0, args.value_residual)
+    cb = oracle_timing(wl, pre, args.steps, 32, 60.0, args.value_residual, args.bits)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B / cb["value"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "u2 codes, f16 inputs, f64 attention (CPU oracle)", "data": "synthetic",
+            "dtype": f"u{args.bits} codes, f16 inputs, f64 attention (CPU oracle)", "data": "synthetic",
             "config": {**workload_config(wl), **make_layout_config(args)}, "cpu_baseline": cb,
             "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -247,12 +250,12 @@ class DenseLayout:
     profile = "decode_attention_llama2-7b-mha.md"
     kernel = "kivi_decode_attention (decode_kernel + combine_kernel)"
 
-    def __init__(self, wl, pre, dev, value_residual=False):
+    def __init__(self, wl, pre, dev, value_residual=False, bits=2):
         from bit_asymmetric_kv_gb300 import kivi
 
         self.wl, self.kivi = wl, kivi
         self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=CYCLE + 64), device=dev,
-                                         value_residual=value_residual)
+                                         value_residual=value_residual, bits=bits)
         kivi.kivi_quantize_prefill(self.cache, pre.k.to(dev), pre.v.to(dev))
         self.n0 = self.cache.n_tokens
         self.res0 = self.cache.k_res.clone()
@@ -288,7 +291,7 @@ class PagedLayout:
     profile = "decode_attention_paged_llama2-7b-mha.md"
     kernel = "kivi_paged_decode_attention (paged decode_kernel + paged_combine_kernel)"
 
-    def __init__(self, wl, pre, dev, page_tokens, graph=False, value_residual=False):
+    def __init__(self, wl, pre, dev, page_tokens, graph=False, value_residual=False, bits=2):
         from bit_asymmetric_kv_gb300 import kivi, synth
 
         self.wl, self.kivi, self.P = wl, kivi, page_tokens
@@ -296,7 +299,7 @@ class PagedLayout:
         maxp = math.ceil((wl.n + CYCLE + 64) / page_tokens)
         num_pages = wl.B * maxp
         self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev,
-                                              value_residual=value_residual)
+                                              value_residual=value_residual, bits=bits)
         self.cache.block_table.copy_(synth.block_table(wl.B, maxp, num_pages, wl.seed))
         for b in range(wl.B):
             kivi.kivi_paged_prefill(self.cache, b, pre.k[b].to(dev), pre.v[b].to(dev))
@@ -344,8 +347,9 @@ class PagedLayout:
 
 def make_layout(args, wl, pre, dev):
     if args.layout == "paged":
-        return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph, value_residual=args.value_residual)
-    return DenseLayout(wl, pre, dev, value_residual=args.value_residual)
+        return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph, value_residual=args.value_residual,
+                           bits=args.bits)
+    return DenseLayout(wl, pre, dev, value_residual=args.value_residual, bits=args.bits)
 
 
 # ----------------------------------------------------------------------------------------
@@ -427,7 +431,7 @@ def run_kivi(args, wl):
             attn_ms.append((e0, e1))
     torch.cuda.synchronize()
     attn_avg_ms = sum(a0.elapsed_time(a1) for a0, a1 in attn_ms) / len(attn_ms)
-    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0, args.value_residual)
+    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0, args.value_residual, args.bits)
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
@@ -443,12 +447,12 @@ def run_kivi(args, wl):
 
             dist.destroy_process_group()
         return 0
-    cb = oracle_timing(wl, pre, 64, 32, 2.0, args.value_residual) if world == 1 else None
+    cb = oracle_timing(wl, pre, 64, 32, 2.0, args.value_residual, args.bits) if world == 1 else None
     lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "step_ms_p50": float(q50), "step_ms_p99": float(q99), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "u2 codes, f16 q/out, f32 accumulate", "data": "synthetic (seeded, fixed outlier key channels)",
+        "dtype": f"u{args.bits} codes, f16 q/out, f32 accumulate", "data": "synthetic (seeded, fixed outlier key channels)",
         "config": {**workload_config(wl), **lay_cfg},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": (PagedLayout if args.layout == "paged" else DenseLayout).kernel,
@@ -478,6 +482,7 @@ def make_layout_config(args):
         cfg = {"layout": f"paged: {args.page_tokens} tokens per page, pages scattered by a seeded permutation",
                "api": api}
     cfg["value_residual"] = bool(args.value_residual)
+    cfg["bits"] = args.bits
     return cfg
 
 
@@ -600,6 +605,7 @@ def main(argv=None):
                     help="--layout paged: replay each step from a captured CUDA graph")
     ap.add_argument("--value-residual", action="store_true",
                     help="keep the last n mod G values in fp16 beside the key residual (the variant cache)")
+    ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
     ap.add_argument("--workload", default="llama2",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
                          "default: the Llama-2-7B MHA decode")
