@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   __shared__ __align__(16) uint32_t s_codes[G * WPR];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t8 = lane >> 2, c4 = lane & 3;
-  const int64_t bh = blockIdx.x / groups_per_head;
-  const int64_t gi = blockIdx.x % groups_per_head;
+  // 32-bit division: the grid has fewer than 2^31 CTAs (a 64-bit one is a called routine)
+  const int64_t bh = (int64_t)(blockIdx.x / (uint32_t)groups_per_head);
+  const int64_t gi = (int64_t)(blockIdx.x % (uint32_t)groups_per_head);
   const int64_t g = g0 + gi;
   // destination: first token row of the group and its (group, channel) meta row
   int64_t row0, grp;
@@ -52,24 +53,27 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   }
   const uint16_t *src = in + bh * in_head_stride + gi * (int64_t)G * kD + 32 * warp + 8 * c4;
 
-  uint4 x[TPL];
+  // the lane's G/8 chunks as words (registers: every index below is a constant)
+  uint32_t x[TPL][4];
 #pragma unroll
-  for (int k = 0; k < TPL; ++k) x[k] = __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)(t8 + 8 * k) * kD));
+  for (int k = 0; k < TPL; ++k) {
+    const uint4 c = __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)(t8 + 8 * k) * kD));
+    x[k][0] = c.x;
+    x[k][1] = c.y;
+    x[k][2] = c.z;
+    x[k][3] = c.w;
+  }
 
   // per-channel min and max over the G tokens: local, then across the 8 token lanes
   __half2 mn[4], mx[4];
-  {
-    const uint32_t *w0 = reinterpret_cast<const uint32_t *>(&x[0]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mn[j] = mx[j] = u2h2(w0[j]);
-  }
+  for (int j = 0; j < 4; ++j) mn[j] = mx[j] = u2h2(x[0][j]);
 #pragma unroll
   for (int k = 1; k < TPL; ++k) {
-    const uint32_t *wk = reinterpret_cast<const uint32_t *>(&x[k]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      mn[j] = __hmin2(mn[j], u2h2(wk[j]));
-      mx[j] = __hmax2(mx[j], u2h2(wk[j]));
+      mn[j] = __hmin2(mn[j], u2h2(x[k][j]));
+      mx[j] = __hmax2(mx[j], u2h2(x[k][j]));
     }
   }
 #pragma unroll
@@ -82,7 +86,13 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   }
   // lane (t8, c4) derives the parameters of channel t8 of its chunk, then they are
   // broadcast to the 8 lanes that hold the chunk
-  const uint32_t mn_bits = h22u(mn[t8 >> 1]), mx_bits = h22u(mx[t8 >> 1]);
+  uint32_t mn_bits = h22u(mn[0]), mx_bits = h22u(mx[0]);
+#pragma unroll
+  for (int j = 1; j < 4; ++j)
+    if ((t8 >> 1) == j) {
+      mn_bits = h22u(mn[j]);
+      mx_bits = h22u(mx[j]);
+    }
   const float my_mn = h2f((uint16_t)((t8 & 1) ? (mn_bits >> 16) : (mn_bits & 0xffffu)));
   const float my_mx = h2f((uint16_t)((t8 & 1) ? (mx_bits >> 16) : (mx_bits & 0xffffu)));
   const QParams mine = make_qparams<BITS>(my_mn, my_mx);
@@ -103,12 +113,11 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   }
 #pragma unroll
   for (int k = 0; k < TPL; ++k) {
-    const uint32_t *wk = reinterpret_cast<const uint32_t *>(&x[k]);
     uint32_t bits = 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      bits |= quant_code<BITS>(h2f((uint16_t)(wk[j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
-      bits |= quant_code<BITS>(h2f((uint16_t)(wk[j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
+      bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
+      bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
     }
     if constexpr (BITS == 2) {
       // chunks 2m and 2m+1 form word 2*warp + m of the token row
@@ -166,16 +175,32 @@ __global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restr
   const int lane16 = lane & 15;
   const uint32_t half_mask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;
   const int64_t half_warps = (int64_t)gridDim.x * (blockDim.x >> 4);
-  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4); row < rows; row += half_warps) {
-    const int64_t bh = row / tokens_per_head;
-    const int64_t i = row - bh * tokens_per_head;
-    const int64_t t = t0 + i;
-    int64_t dst = bh * max_tokens + t;
-    if constexpr (PAGED) {
-      if (!paged_row(pm, bh, t, &dst)) continue;  // the half-warp skips the row together
+  // kRows rows per half-warp and iteration: their loads are all issued before the
+  // first row is reduced, so each lane keeps kRows 16-byte loads in flight
+  constexpr int kRows = 4;
+  for (int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4)) * kRows; row0 < rows;
+       row0 += half_warps * kRows) {
+    uint4 x[kRows];
+    int64_t dst[kRows];
+    bool ok[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const int64_t row = row0 + u;
+      ok[u] = row < rows;
+      const int64_t bh = ok[u] ? row / tokens_per_head : 0;
+      const int64_t i = ok[u] ? row - bh * tokens_per_head : 0;
+      const int64_t t = t0 + i;
+      dst[u] = bh * max_tokens + t;
+      if constexpr (PAGED) {
+        if (ok[u] && !paged_row(pm, bh, t, &dst[u])) ok[u] = false;  // the half-warp skips the row together
+      }
+      x[u] = ok[u] ? __ldg(reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + lane16)
+                   : make_uint4(0u, 0u, 0u, 0u);
     }
-    const uint4 x = __ldg(reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + lane16);
-    quantize_value_row<BITS>(x, lane16, half_mask, v_codes + dst * words_per_row<BITS>(), v_meta + dst);
+#pragma unroll
+    for (int u = 0; u < kRows; ++u)
+      if (ok[u])
+        quantize_value_row<BITS>(x[u], lane16, half_mask, v_codes + dst[u] * words_per_row<BITS>(), v_meta + dst[u]);
   }
 }
 
@@ -387,6 +412,7 @@ cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_
                               cudaStream_t st) {
   const int64_t blocks = heads * groups_per_head;
   if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;  // one CTA per key group
   const PageMap none = {};
   if (bits == 2)
     key_groups<false, 2>(in, in_head_stride, blocks, groups_per_head, g0, G, k_codes, k_meta, max_tokens, none, st);
@@ -400,6 +426,7 @@ cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, 
                                     uint32_t *k_meta, cudaStream_t st) {
   const int64_t blocks = heads * groups_per_head;
   if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;  // one CTA per key group
   if (bits == 2)
     key_groups<true, 2>(in, in_head_stride, blocks, groups_per_head, 0, G, k_codes, k_meta, 0, pm, st);
   else
@@ -412,7 +439,7 @@ cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_p
                               cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  const int grid = grid_cap((rows + 15) / 16);
+  const int grid = grid_cap((rows + 63) / 64);  // 16 half-warps of 4 rows per CTA
   if (bits == 2)
     value_rows_kernel<false, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
                                                        max_tokens, PageMap{});
@@ -427,7 +454,7 @@ cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t to
                                     uint32_t *v_meta, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  const int grid = grid_cap((rows + 15) / 16);
+  const int grid = grid_cap((rows + 63) / 64);  // 16 half-warps of 4 rows per CTA
   if (bits == 2)
     value_rows_kernel<true, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
                                                       0, pm);

@@ -121,6 +121,45 @@ def test_many_splits_long_context_small_batch():
     assert_close(out, oracle.attention(orc, pre.q.numpy(), 1.0))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,G,n", [
+    (2, 8, 2, 32, 32 * 40 + 9),   # every head split between warps
+    (64, 64, 64, 32, 100),        # 4096 heads of 3 units: most heads held whole by one warp
+    (1, 4, 1, 32, 32 * 300 + 7),  # one head over many warps
+], ids=["split", "whole-heads", "one-long-head"])
+def test_workspace_contents_do_not_matter_and_one_workspace_serves_many_calls(B, Hq, Hkv, G, n):
+    """The workspace holds the split partials: filled with 0xFF bytes (NaN) beforehand
+    and reused by consecutive calls, it gives the oracle's attention every time, and
+    every output row is written."""
+    wl = synth.small("wsfill", B, Hq, Hkv, G, n, seed=21)
+    pre = synth.make_prefill(wl)
+    T = wl.capacity(extra=G)
+    orc = oracle.prefill(pre.k.numpy(), pre.v.numpy(), G, T)
+    gpu = gpu_prefill(pre.k, pre.v, G, T)
+    ref = oracle.attention(orc, pre.q.numpy(), 1.0)
+    ws = torch.full((kivi.kivi_decode_workspace_bytes(gpu.dims, Hq, n),), 0xFF, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float16, device="cuda")
+        kivi.kivi_decode_attention(gpu, pre.q.cuda(), 1.0, out=out, ws=ws)
+        assert_close(out, ref)
+
+
+def test_decode_step_with_a_garbage_workspace():
+    """kivi_decode_step with a workspace of 0xFF bytes (NaN) gives the oracle's result
+    on every step."""
+    wl = synth.small("stepws", 2, 8, 2, 32, 32 * 20 + 30, seed=22, steps=4, factor_lo=30, factor_hi=100)
+    pre = synth.make_prefill(wl)
+    T = wl.capacity(extra=32)
+    gpu = gpu_prefill(pre.k, pre.v, 32, T)
+    orc = oracle.prefill(pre.k.numpy(), pre.v.numpy(), 32, T)
+    ws = torch.full((kivi.kivi_decode_workspace_bytes(gpu.dims, 8, T),), 0xFF, dtype=torch.uint8, device="cuda")
+    for step in range(4):
+        k_new, v_new, q = synth.make_step(wl, pre, step)
+        out = torch.full((2, 8, 128), float("nan"), dtype=torch.float16, device="cuda")
+        kivi.kivi_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, out=out, ws=ws)
+        oracle.append(orc, k_new.numpy(), v_new.numpy())
+        assert_close(out, oracle.attention(orc, q.numpy(), 1.0))
+
+
 def test_workspace_too_small_is_rejected_and_launches_nothing():
     wl = synth.small("ws", 1, 2, 2, 32, 100, seed=16)
     pre = synth.make_prefill(wl)
