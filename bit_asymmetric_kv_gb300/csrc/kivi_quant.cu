@@ -10,6 +10,76 @@
 
 namespace kivi {
 
+// ---- 2-bit codes by fp16 comparisons -------------------------------------------------
+// The 2-bit code [d > t1] + [d >= t2] + [d > t3] of d = fl32(x - mn) never decreases as
+// the fp16 input x grows (fp32 subtraction rounds monotonically), so each of its three
+// terms is [x > X] for one fp16 threshold X: the largest fp16 x for which the term is
+// 0.  fp16_threshold finds it from the estimate c = fp16 round-down of fl32(mn + t) and
+// proves it with two evaluations of the term itself: X = c when the term is 0 at c and
+// 1 at the next fp16 above c, X = the fp16 below c when the term is 1 at c and 0 there.
+// Anything else clears `ok` and the caller takes the per-element fp32 path: that needs
+// fp16 steps near mn + t finer than the fp32 rounding of d, i.e. mn + t close to zero
+// next to a large t (a minimum far below zero).  With s = 0 every term is 0: X = +inf.
+
+// Order-preserving key of fp16 bits (finite or infinite, not NaN): -0 and +0 share 0x8000.
+__device__ __forceinline__ uint32_t h16_key(uint32_t b) {
+  return (b & 0x8000u) ? 0x8000u - (b & 0x7fffu) : 0x8000u + b;
+}
+__device__ __forceinline__ uint32_t h16_from_key(uint32_t k) {
+  return k >= 0x8000u ? k - 0x8000u : (0x8000u | (0x8000u - k));
+}
+
+// strict: the term is [d >= t] (X = the largest x with d < t); else [d > t].
+__device__ __forceinline__ uint32_t fp16_threshold(float mn, float t, bool strict, bool &ok) {
+  const uint32_t c = __half_as_ushort(__float2half_rd(__fadd_rn(mn, t)));
+  const float dc = __fsub_rn(h2f((uint16_t)c), mn);
+  const bool below_c = strict ? (dc < t) : (dc <= t);  // the term is 0 at c
+  const uint32_t kc = h16_key(c);
+  const uint32_t nb = h16_from_key(below_c ? kc + 1u : kc - 1u);  // the neighbour to test
+  const float dn = __fsub_rn(h2f((uint16_t)nb), mn);
+  const bool below_n = strict ? (dn < t) : (dn <= t);
+  ok = below_c ? !below_n : below_n;
+  return below_c ? c : nb;
+}
+
+// Thresholds (X1, X2, X3) of one set of 2-bit parameters; ok as above.
+__device__ __forceinline__ void fp16_thresholds(const QParams &p, uint32_t &x1, uint32_t &x2, uint32_t &x3,
+                                                bool &ok) {
+  if (p.s == 0.f) {
+    x1 = x2 = x3 = 0x7c00u;  // +inf: every code is 0
+    ok = true;
+    return;
+  }
+  bool o1, o2, o3;
+  x1 = fp16_threshold(p.mn, p.t1, false, o1);
+  x2 = fp16_threshold(p.mn, p.t2, true, o2);
+  x3 = fp16_threshold(p.mn, p.t3, false, o3);
+  ok = o1 && o2 && o3;
+}
+
+// 2-bit codes of the 8 channels of a 16-byte chunk from fp16 thresholds: pair j of the
+// chunk (channels 2j, 2j+1) is compared with the half2 thresholds X1[j], X2[j], X3[j]
+// (one threshold per channel).  The three masks are nested, so the code's low bit is
+// their parity and its high bit the middle mask.  Channel i of the chunk lands at bits
+// [2i, 2i+1] of the low 16 bits of the result (the high 16 bits are left over).
+__device__ __forceinline__ uint32_t codes2_chunk8(const uint32_t x[4], const uint32_t X1[4], const uint32_t X2[4],
+                                                  const uint32_t X3[4]) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2 v = u2h2(x[j]);
+    const uint32_t m1 = __hgt2_mask(v, u2h2(X1[j]));
+    const uint32_t m2 = __hgt2_mask(v, u2h2(X2[j]));
+    const uint32_t m3 = __hgt2_mask(v, u2h2(X3[j]));
+    const uint32_t odd = m1 ^ m2 ^ m3;
+    // channel 2j at bits 4j, 4j+1 (low half); channel 2j+1 at bits 16 + 4j+2, +3
+    const uint32_t k0 = (1u << (4 * j)) | (1u << (18 + 4 * j));
+    r |= (odd & k0) | (m2 & (k0 << 1));
+  }
+  return r | (r >> 16);
+}
+
+
 // -------------------------------------------------------------------------------------
 // Key groups: one CTA (4 warps) quantizes one G-token group of one (batch, KV head).
 // Warp w owns channels 32w .. 32w+31.  Lane = 4 * t8 + c4: the lane loads the
@@ -98,34 +168,68 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   const QParams mine = make_qparams<BITS>(my_mn, my_mx);
   k_meta[grp * kD + 32 * warp + 8 * c4 + t8] = mine.meta;
 
-  QParams p[8];
+  // 2-bit codes by fp16 comparisons with the channels' thresholds (exact whenever every
+  // threshold of the warp is proven; else the per-element fp32 form below)
+  bool fast = false;
+  if constexpr (BITS == 2) {
+    uint32_t X1, X2, X3;
+    bool ok;
+    fp16_thresholds(mine, X1, X2, X3, ok);
+    fast = __all_sync(0xffffffffu, ok);
+    if (fast) {
+      // half2 thresholds of channel pair (t8 & ~1, t8 | 1): the odd channel is lane ^ 4
+      const uint32_t o1 = __shfl_xor_sync(0xffffffffu, X1, 4);
+      const uint32_t o2 = __shfl_xor_sync(0xffffffffu, X2, 4);
+      const uint32_t o3 = __shfl_xor_sync(0xffffffffu, X3, 4);
+      const uint32_t sel = (t8 & 1) ? 0x1054u : 0x5410u;  // (even channel, odd channel)
+      const uint32_t P1 = __byte_perm(X1, o1, sel), P2 = __byte_perm(X2, o2, sel), P3 = __byte_perm(X3, o3, sel);
+      uint32_t T1[4], T2[4], T3[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int src_lane = 4 * j + c4;
-    p[j].mn = __shfl_sync(0xffffffffu, mine.mn, src_lane);
-    if constexpr (BITS == 2) {
-      p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
-      p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
-      p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
-    } else {
-      p[j].s = __shfl_sync(0xffffffffu, mine.s, src_lane);
+      for (int j = 0; j < 4; ++j) {
+        const int src_lane = 8 * j + c4;  // the lane of channel 2j of this chunk
+        T1[j] = __shfl_sync(0xffffffffu, P1, src_lane);
+        T2[j] = __shfl_sync(0xffffffffu, P2, src_lane);
+        T3[j] = __shfl_sync(0xffffffffu, P3, src_lane);
+      }
+#pragma unroll
+      for (int k = 0; k < TPL; ++k) {
+        const uint32_t bits = codes2_chunk8(x[k], T1, T2, T3);
+        // chunks 2m and 2m+1 form word 2*warp + m of the token row
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+        if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * WPR + 2 * warp + (c4 >> 1)] = __byte_perm(bits, other, 0x5410);
+      }
     }
   }
+  if (!fast) {
+    QParams p[8];
 #pragma unroll
-  for (int k = 0; k < TPL; ++k) {
-    uint32_t bits = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
-      bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
+    for (int j = 0; j < 8; ++j) {
+      const int src_lane = 4 * j + c4;
+      p[j].mn = __shfl_sync(0xffffffffu, mine.mn, src_lane);
+      if constexpr (BITS == 2) {
+        p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
+        p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
+        p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
+      } else {
+        p[j].s = __shfl_sync(0xffffffffu, mine.s, src_lane);
+      }
     }
-    if constexpr (BITS == 2) {
-      // chunks 2m and 2m+1 form word 2*warp + m of the token row
-      const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
-      if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * WPR + 2 * warp + (c4 >> 1)] = bits | (other << 16);
-    } else {
-      // chunk c4 of warp w is word 4w + c4 of the token row
-      s_codes[(t8 + 8 * k) * WPR + 4 * warp + c4] = bits;
+#pragma unroll
+    for (int k = 0; k < TPL; ++k) {
+      uint32_t bits = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
+        bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
+      }
+      if constexpr (BITS == 2) {
+        // chunks 2m and 2m+1 form word 2*warp + m of the token row
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, bits, 1);
+        if ((c4 & 1) == 0) s_codes[(t8 + 8 * k) * WPR + 2 * warp + (c4 >> 1)] = bits | (other << 16);
+      } else {
+        // chunk c4 of warp w is word 4w + c4 of the token row
+        s_codes[(t8 + 8 * k) * WPR + 4 * warp + c4] = bits;
+      }
     }
   }
   __syncthreads();
@@ -161,6 +265,88 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
     codes_row[lane16] = bits;  // chunk lane16 = channels 8*lane16 .. +7 = word lane16
   }
   if (lane16 == 0) *meta_out = p.meta;
+}
+
+// 2-bit value rows, 4 lanes per row and 8 rows per warp: lane q of a row holds the
+// 16-byte chunks q, q+4, q+8, q+12 (channels 8(q+4k) .. 8(q+4k)+7), so that every load
+// instruction reads 64 contiguous bytes of each row.  The 4 lanes share the row's min
+// and max and its parameters; lanes 0-2 each prove one fp16 threshold of the row, and
+// the codes are fp16 comparisons with them (the fp32 form when a threshold of the warp
+// is not proven).  Rows map to the cache as in value_rows_kernel.
+template <bool PAGED>
+__global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__restrict__ v, int64_t rows,
+                                                          int64_t tokens_per_head, int64_t in_rows_per_head,
+                                                          int64_t t0, uint32_t *__restrict__ v_codes,
+                                                          uint32_t *__restrict__ v_meta, int64_t max_tokens,
+                                                          const PageMap pm) {
+  const int lane = threadIdx.x & 31, q = lane & 3;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8; row0 < rows;
+       row0 += warps * 8) {
+    const int64_t row = row0 + (lane >> 2);
+    bool ok_row = row < rows;
+    int64_t bh = 0, i = 0, dst = 0;
+    if (ok_row) {
+      bh = row / tokens_per_head;
+      i = row - bh * tokens_per_head;
+      const int64_t t = t0 + i;
+      dst = bh * max_tokens + t;
+      if constexpr (PAGED) ok_row = paged_row(pm, bh, t, &dst);
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + q;
+    uint32_t x[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 c = ok_row ? __ldg(src + 4 * k) : make_uint4(0u, 0u, 0u, 0u);
+      x[k][0] = c.x;
+      x[k][1] = c.y;
+      x[k][2] = c.z;
+      x[k][3] = c.w;
+    }
+    __half2 mn = u2h2(x[0][0]), mx = mn;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = (k == 0 ? 1 : 0); j < 4; ++j) {
+        mn = __hmin2(mn, u2h2(x[k][j]));
+        mx = __hmax2(mx, u2h2(x[k][j]));
+      }
+    // (min, -max) so that one __hmin2 reduces both over the row's 4 lanes
+    __half2 red = __halves2half2(__hmin(__low2half(mn), __high2half(mn)),
+                                 __hneg(__hmax(__low2half(mx), __high2half(mx))));
+    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 1)));
+    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 2)));
+    const QParams p = make_qparams<2>(__low2float(red), -__high2float(red));
+    // lane q < 3 proves threshold q + 1 (X2 is the strict one: d >= t2)
+    bool ok = true;
+    uint32_t xq = 0x7c00u;
+    if (p.s != 0.f && q < 3) xq = fp16_threshold(p.mn, q == 0 ? p.t1 : (q == 1 ? p.t2 : p.t3), q == 1, ok);
+    const int base = lane & ~3;
+    const uint32_t x1 = __shfl_sync(0xffffffffu, xq, base), x2 = __shfl_sync(0xffffffffu, xq, base + 1),
+                   x3 = __shfl_sync(0xffffffffu, xq, base + 2);
+    uint32_t r[4];
+    if (__all_sync(0xffffffffu, ok)) {
+      const uint32_t p1 = x1 | (x1 << 16), p2 = x2 | (x2 << 16), p3 = x3 | (x3 << 16);
+      const uint32_t X1[4] = {p1, p1, p1, p1}, X2[4] = {p2, p2, p2, p2}, X3[4] = {p3, p3, p3, p3};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) r[k] = codes2_chunk8(x[k], X1, X2, X3);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) r[k] = quant_chunk8<2>(make_uint4(x[k][0], x[k][1], x[k][2], x[k][3]), p);
+    }
+    // word w of the row = chunk 2w (low 16 bits) | chunk 2w+1 (high 16 bits): lanes q and
+    // q^1 hold the two halves of words q/2 + 2k; the even lane stores k = 0, 1, the odd k = 2, 3
+    const uint32_t A = __byte_perm(r[0], r[1], 0x5410), B = __byte_perm(r[2], r[3], 0x5410);
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, (q & 1) ? A : B, 1);
+    const uint32_t lo = (q & 1) ? recv : A, hi = (q & 1) ? B : recv;
+    if (ok_row) {
+      uint32_t *codes_row = v_codes + dst * 8;
+      const int w = (q >> 1) + ((q & 1) ? 4 : 0);
+      codes_row[w] = __byte_perm(lo, hi, 0x5410);
+      codes_row[w + 2] = __byte_perm(lo, hi, 0x7632);
+      if (q == 0) v_meta[dst] = p.meta;
+    }
+  }
 }
 
 // rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
@@ -439,10 +625,10 @@ cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_p
                               cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  const int grid = grid_cap((rows + 63) / 64);  // 16 half-warps of 4 rows per CTA
+  const int grid = grid_cap((rows + 63) / 64);  // 64 rows per CTA and pass
   if (bits == 2)
-    value_rows_kernel<false, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
-                                                       max_tokens, PageMap{});
+    value_rows2_kernel<false><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
+                                                     max_tokens, PageMap{});
   else
     value_rows_kernel<false, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
                                                        max_tokens, PageMap{});
@@ -454,10 +640,10 @@ cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t to
                                     uint32_t *v_meta, cudaStream_t st) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
-  const int grid = grid_cap((rows + 63) / 64);  // 16 half-warps of 4 rows per CTA
+  const int grid = grid_cap((rows + 63) / 64);  // 64 rows per CTA and pass
   if (bits == 2)
-    value_rows_kernel<true, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
-                                                      0, pm);
+    value_rows2_kernel<true><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta, 0,
+                                                    pm);
   else
     value_rows_kernel<true, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
                                                       0, pm);
