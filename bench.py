@@ -16,11 +16,13 @@ run.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
                   [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
-                  [--value-residual] [--bits 2|4] [--compare-fp16]
+                  [--value-residual] [--bits 2|4] [--compare-fp16] [--prefill-only]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
 from one pool, scattered by a seeded permutation; lengths on the device); with
 --graph each step is replayed from a CUDA graph captured once per input set.
+
+--prefill-only times the prompt quantization alone (a separate JSON line).
 
 --impl reference times the CPU oracle (plain C, the host's cores) on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -489,7 +491,7 @@ def make_layout_config(args):
     return cfg
 
 
-def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5):
+def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int = 1):
     """Quantize the whole prompt (kivi_quantize_prefill, dense cache) with L2 flushed
     before each call: the quantizers' throughput over fp16 K and V read once and the
     codes, scales and residual written (rows a1-a3)."""
@@ -501,14 +503,14 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5):
                                 bits=args.bits)
     k, v = pre.k.to(dev), pre.v.to(dev)
     ms = []
-    for i in range(reps + 1):
+    for i in range(reps + warmup):
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         kivi.kivi_quantize_prefill(cache, k, v, stream=stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        if i:
+        if i >= warmup:
             ms.append(e0.elapsed_time(e1))
     n, G = wl.n, wl.G
     nq = (n // G) * G
@@ -519,8 +521,36 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5):
     moved = 2 * k.numel() * 2 + written
     best = min(ms)
     peak, _ = measured_peak()
-    return {"ms": best, "bytes": moved, "GBps": moved / best / 1e6, "frac": moved / best / 1e6 / peak,
-            "reps": reps, "note": "best of reps; fp16 K and V read once, codes, scales and residual written"}
+    return {"ms": best, "ms_mean": sum(ms) / len(ms), "bytes": moved, "GBps": moved / best / 1e6,
+            "frac": moved / best / 1e6 / peak, "reps": reps,
+            "note": "best of reps; fp16 K and V read once, codes, scales and residual written"}
+
+
+def run_prefill(args, wl):
+    """--prefill-only: time kivi_quantize_prefill alone on the workload's prompt (W
+    untimed calls, then K timed ones, L2 flushed before each) and print one JSON line."""
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kivi.lib()
+    pre = synth.make_prefill(wl)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    p = prefill_timing(args, wl, pre, dev, torch.cuda.current_stream(dev), flush, reps=args.steps,
+                       warmup=args.warmup)
+    peak, src = measured_peak()
+    print(json.dumps({
+        "metric": "prefill quantization GB/s (kivi_quantize_prefill: fp16 K and V in, codes, scales, residual out)",
+        "value": p["GBps"], "unit": "GB/s", "higher_is_better": True, "steps": args.steps, "warmup": args.warmup,
+        "ms_best": p["ms"], "ms_mean": p["ms_mean"], "bytes_per_call": p["bytes"],
+        "roofline": {"bound": "hbm", "achieved": p["GBps"], "peak": peak, "unit": "GB/s", "frac": p["frac"],
+                     "peak_source": src},
+        "dtype": "fp16 in, 2-bit codes out" if args.bits == 2 else "fp16 in, 4-bit codes out", "data": "synthetic",
+        "config": {**workload_config(wl), **make_layout_config(args), "layout": "dense",
+                   "l2": "flushed by a 256 MiB write before every call (outside the timed events)"}}))
+    return 0
 
 
 def cycle_workspace(cache, wl, n0, dev):
@@ -643,6 +673,8 @@ def main(argv=None):
     ap.add_argument("--value-residual", action="store_true",
                     help="keep the last n mod G values in fp16 beside the key residual (the variant cache)")
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prompt quantization (kivi_quantize_prefill) of the workload")
     ap.add_argument("--workload", default="llama2",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
                          "default: the Llama-2-7B MHA decode")
@@ -661,6 +693,8 @@ def main(argv=None):
         return run_compare(args)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.prefill_only:
+        return run_prefill(args, wl)
     return run_kivi(args, wl)
 
 
