@@ -923,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 // tokens) writes zeros.  Partial rows are 8-byte aligned (stride 130 floats).
 __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
                                             uint16_t *__restrict__ out_row, int lane) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
   for (int j0 = 0; j0 < np; j0 += kBatch) {
     float2 ml[kBatch], lo[kBatch], hi[kBatch];
