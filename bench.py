@@ -64,6 +64,18 @@ def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual:
     return B * Hkv * per_head + 2 * B * Hq * 128 * 2
 
 
+def prefill_bytes(B: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2) -> int:
+    """Bytes one prompt quantization must move (D = 128, c = 16*bits bytes of codes per
+    token row): fp16 K and V read once (2 * n * 256 per (batch, KV head)), then written
+    nq*(c + 512/G) + r*256 for the keys and n*(c + 4) for the values (with a value
+    residual nq*(c + 4) + r*256)."""
+    c = 16 * bits
+    nq = (n // G) * G
+    r = n - nq
+    values = nq * (c + 4) + r * 256 if value_residual else n * (c + 4)
+    return B * Hkv * (2 * n * 256 + nq * c + (nq // G) * 512 + r * 256 + values)
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -512,13 +524,7 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int
         torch.cuda.synchronize()
         if i >= warmup:
             ms.append(e0.elapsed_time(e1))
-    n, G = wl.n, wl.G
-    nq = (n // G) * G
-    heads = wl.B * wl.Hkv
-    row = 16 * args.bits
-    values = nq * (row + 4) + (n - nq) * 256 if args.value_residual else n * (row + 4)
-    written = heads * (nq * row + (nq // G) * 512 + (n - nq) * 256 + values)
-    moved = 2 * k.numel() * 2 + written
+    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, wl.n, args.value_residual, args.bits)
     best = min(ms)
     peak, _ = measured_peak()
     return {"ms": best, "ms_mean": sum(ms) / len(ms), "bytes": moved, "GBps": moved / best / 1e6,
