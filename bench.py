@@ -514,6 +514,7 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int
     cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_residual=args.value_residual,
                                 bits=args.bits)
     k, v = pre.k.to(dev), pre.v.to(dev)
+    assert k.shape[2] == wl.n, (k.shape, wl.n)
     ms = []
     for i in range(reps + warmup):
         flush.fill_(i & 0xFF)
