@@ -196,19 +196,26 @@ def dist_env():
 def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False,
                   bits: int = 2):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
-    cache) on `sample_heads` of the workload's KV heads; scale to the whole batch."""
+    cache) on `sample_heads` of the workload's KV heads; scale to the whole batch.
+    Like the GPU loop, the cache is rolled back to the prompt every CYCLE steps
+    (untimed), so the context stays within n .. n + CYCLE."""
+    import copy
+
     import oracle
     from bit_asymmetric_kv_gb300 import synth
 
     heads = [(i % wl.B, (i * 7) % wl.Hkv) for i in range(sample_heads)]
-    T = wl.capacity(extra=steps + 64)
+    T = wl.capacity(extra=CYCLE + 64)
     k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
     v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
-    c = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits)  # untimed, like the GPU's prefill
+    c0 = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits)  # untimed, like the GPU's prefill
     R = wl.Hq // wl.Hkv
     t_total, done = 0.0, 0
+    c = c0
     for step in range(steps):
-        k_new, v_new, q = synth.make_step(wl, pre, step)
+        if step % CYCLE == 0:
+            c = copy.deepcopy(c0)
+        k_new, v_new, q = synth.make_step(wl, pre, step % CYCLE)
         kn = np.stack([k_new[b, h].numpy() for b, h in heads])[None]
         vn = np.stack([v_new[b, h].numpy() for b, h in heads])[None]
         qs = np.stack([q[b, h * R + j].numpy() for b, h in heads for j in range(R)])[None]
@@ -463,7 +470,7 @@ def run_kivi(args, wl):
 
             dist.destroy_process_group()
         return 0
-    cb = oracle_timing(wl, pre, 64, 32, 2.0, args.value_residual, args.bits) if world == 1 else None
+    cb = oracle_timing(wl, pre, 100000, 32, 10.0, args.value_residual, args.bits) if world == 1 else None
     lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
