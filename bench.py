@@ -85,9 +85,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
 
 
-def profiled_traffic(kernel_sha: str, profile: str):
+def profiled_traffic(kernel_sha: str, profile: str, workload: str, variant: str):
     """DRAM bytes per decode launch from the committed ncu summary `profile`, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source, on this workload and cache variant (else
+    None)."""
     path = os.path.join(ROOT, "profiles", profile)
     try:
         lines = open(path).read().splitlines()
@@ -98,7 +99,8 @@ def profiled_traffic(kernel_sha: str, profile: str):
         if ln.startswith("- ") and ":" in ln:
             k, v = ln[2:].split(":", 1)
             fields[k.strip()] = v.strip().strip("`")
-    if fields.get("kernel_source_sha256") != kernel_sha:
+    if (fields.get("kernel_source_sha256") != kernel_sha or fields.get("workload") != workload
+            or fields.get("variant") != variant):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])
@@ -456,7 +458,8 @@ def run_kivi(args, wl):
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
-    traffic = profiled_traffic(sha, lay.profile)
+    traffic = profiled_traffic(sha, lay.profile, wl.name,
+                               f"bits={args.bits}, value_residual={int(bool(args.value_residual))}")
     del lay
 
     prefill = prefill_timing(args, wl, pre, dev, stream, flush)
