@@ -79,6 +79,53 @@ __device__ __forceinline__ uint32_t codes2_chunk8(const uint32_t x[4], const uin
   return r | (r >> 16);
 }
 
+// ---- 4-bit codes without a division per element -------------------------------------
+// The 4-bit code is clamp(rint(fl32(d / s)), 0, 15) with d = fl32(x - mn) >= 0 and the
+// fp16 scale s > 0.  With rs = 1/s rounded to nearest, q = fl32(d * rs) lies within
+// Q * 2^-23 of the quotient Q = d / s, and the correctly rounded quotient within
+// Q * 2^-24 of Q; below 64 both are under 2^-16.  So when q is more than 2^-15 from
+// every half-integer, the division rounds to the same integer as q; only there
+// does the division itself run.  q >= 64 means Q > 63: the code is 15.
+__device__ __forceinline__ uint32_t code4(float x, float mn, float s, float rs) {
+  if (s == 0.f) return 0u;
+  const float d = __fsub_rn(x, mn);
+  const float q = __fmul_rn(d, rs);
+  if (q >= 64.f) return 15u;
+  float c = rintf(q);                                   // half to even, like the division's rounding
+  if (fabsf(q - c) > 0.5f - 0x1p-15f) c = rintf(__fdiv_rn(d, s));  // q - c is exact
+  const int ci = (int)c;
+  return (uint32_t)(ci > 15 ? 15 : ci);
+}
+
+// One code of either width; rs = 1/s (used by 4-bit codes only).
+template <int BITS>
+__device__ __forceinline__ uint32_t qcode(float x, const QParams &p, float rs) {
+  if constexpr (BITS == 2) {
+    return quant_code<2>(x, p);
+  } else {
+    return code4(x, p.mn, p.s, rs);
+  }
+}
+
+// Codes of the 8 channels of a 16-byte chunk under one set of parameters (channel j at
+// bits [BITS*j, BITS*j + BITS - 1]).
+template <int BITS>
+__device__ __forceinline__ uint32_t qchunk8(const uint4 &c, const QParams &p) {
+  if constexpr (BITS == 2) {
+    return quant_chunk8<2>(c, p);
+  } else {
+    const float rs = __frcp_rn(p.s);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t bits = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      bits |= code4(h2f((uint16_t)(w[k] & 0xffffu)), p.mn, p.s, rs) << (8 * k);
+      bits |= code4(h2f((uint16_t)(w[k] >> 16)), p.mn, p.s, rs) << (8 * k + 4);
+    }
+    return bits;
+  }
+}
+
 
 // -------------------------------------------------------------------------------------
 // Key groups: one CTA (4 warps) quantizes one G-token group of one (batch, KV head).
@@ -214,13 +261,16 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
         p[j].s = __shfl_sync(0xffffffffu, mine.s, src_lane);
       }
     }
+    float rs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) rs[j] = BITS == 4 ? __frcp_rn(p[j].s) : 0.f;
 #pragma unroll
     for (int k = 0; k < TPL; ++k) {
       uint32_t bits = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j]) << (2 * BITS * j);
-        bits |= quant_code<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1]) << (2 * BITS * j + BITS);
+        bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j], rs[2 * j]) << (2 * BITS * j);
+        bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1], rs[2 * j + 1]) << (2 * BITS * j + BITS);
       }
       if constexpr (BITS == 2) {
         // chunks 2m and 2m+1 form word 2*warp + m of the token row
@@ -257,7 +307,7 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   const float fmn = __low2float(red);
   const float fmx = -__high2float(red);
   const QParams p = make_qparams<BITS>(fmn, fmx);
-  const uint32_t bits = quant_chunk8<BITS>(x, p);
+  const uint32_t bits = qchunk8<BITS>(x, p);
   if constexpr (BITS == 2) {
     const uint32_t other = __shfl_xor_sync(half_mask, bits, 1);
     if ((lane16 & 1) == 0) codes_row[lane16 >> 1] = bits | (other << 16);
@@ -475,6 +525,8 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
   const QParams p1 = make_qparams<BITS>(__high2float(mn0), __high2float(mx0));
   const QParams p2 = make_qparams<BITS>(__low2float(mn1), __low2float(mx1));
   const QParams p3 = make_qparams<BITS>(__high2float(mn1), __high2float(mx1));
+  const float rs0 = BITS == 4 ? __frcp_rn(p0.s) : 0.f, rs1 = BITS == 4 ? __frcp_rn(p1.s) : 0.f;
+  const float rs2 = BITS == 4 ? __frcp_rn(p2.s) : 0.f, rs3 = BITS == 4 ? __frcp_rn(p3.s) : 0.f;
   const int64_t row0 = ph * P + off - (G - 1);
   reinterpret_cast<uint4 *>(a.k_meta + (row0 / G) * kD)[lane] = make_uint4(p0.meta, p1.meta, p2.meta, p3.meta);
   // 2-bit: channel 4l + j sits in word l / 4 at bits 8 (l mod 4) + 2j;
@@ -485,10 +537,10 @@ __global__ void __launch_bounds__(128) paged_append_kernel(const PagedAppendArgs
 #pragma unroll 8
   for (int t = 0; t < G; ++t) {
     const uint2 x = key(t);
-    uint32_t bits = quant_code<BITS>(h2f((uint16_t)(x.x & 0xffffu)), p0) |
-                    (quant_code<BITS>(h2f((uint16_t)(x.x >> 16)), p1) << BITS) |
-                    (quant_code<BITS>(h2f((uint16_t)(x.y & 0xffffu)), p2) << (2 * BITS)) |
-                    (quant_code<BITS>(h2f((uint16_t)(x.y >> 16)), p3) << (3 * BITS));
+    uint32_t bits = qcode<BITS>(h2f((uint16_t)(x.x & 0xffffu)), p0, rs0) |
+                    (qcode<BITS>(h2f((uint16_t)(x.x >> 16)), p1, rs1) << BITS) |
+                    (qcode<BITS>(h2f((uint16_t)(x.y & 0xffffu)), p2, rs2) << (2 * BITS)) |
+                    (qcode<BITS>(h2f((uint16_t)(x.y >> 16)), p3, rs3) << (3 * BITS));
     bits <<= shift;
     bits |= __shfl_xor_sync(0xffffffffu, bits, 1);
     if constexpr (LPW == 4) bits |= __shfl_xor_sync(0xffffffffu, bits, 2);
