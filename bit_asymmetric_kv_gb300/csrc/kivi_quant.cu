@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
 }
 
 // -------------------------------------------------------------------------------------
-// Value tokens: 16 lanes per token row (one 16-byte chunk of 8 channels each).
+// Value tokens at append: 16 lanes per token row (one 16-byte chunk of 8 channels each).
 // quantize_value_row works on one half-warp; `lane16` is the lane within it.
 // -------------------------------------------------------------------------------------
 template <int BITS>
@@ -317,13 +317,16 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   if (lane16 == 0) *meta_out = p.meta;
 }
 
-// 2-bit value rows, 4 lanes per row and 8 rows per warp: lane q of a row holds the
-// 16-byte chunks q, q+4, q+8, q+12 (channels 8(q+4k) .. 8(q+4k)+7), so that every load
+// Value rows, 4 lanes per row and 8 rows per warp: lane q of a row holds the 16-byte
+// chunks q, q+4, q+8, q+12 (channels 8(q+4k) .. 8(q+4k)+7), so that every load
 // instruction reads 64 contiguous bytes of each row.  The 4 lanes share the row's min
-// and max and its parameters; lanes 0-2 each prove one fp16 threshold of the row, and
-// the codes are fp16 comparisons with them (the fp32 form when a threshold of the warp
-// is not proven).  Rows map to the cache as in value_rows_kernel.
-template <bool PAGED>
+// and max and its parameters.  2-bit codes: lanes 0-2 each prove one fp16 threshold
+// of the row and the codes are fp16 comparisons with them (the fp32 form when a
+// threshold of the warp is not proven).  4-bit codes: the reciprocal product (code4);
+// chunk c of a row is code word c.
+// rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
+// read from input row (head * in_rows_per_head + r % tokens_per_head)
+template <bool PAGED, int BITS>
 __global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__restrict__ v, int64_t rows,
                                                           int64_t tokens_per_head, int64_t in_rows_per_head,
                                                           int64_t t0, uint32_t *__restrict__ v_codes,
@@ -366,7 +369,16 @@ __global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__rest
                                  __hneg(__hmax(__low2half(mx), __high2half(mx))));
     red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 1)));
     red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 2)));
-    const QParams p = make_qparams<2>(__low2float(red), -__high2float(red));
+    const QParams p = make_qparams<BITS>(__low2float(red), -__high2float(red));
+    if constexpr (BITS == 4) {
+      if (ok_row) {
+        uint32_t *codes_row = v_codes + dst * 16;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) codes_row[q + 4 * k] = qchunk8<4>(make_uint4(x[k][0], x[k][1], x[k][2], x[k][3]), p);
+        if (q == 0) v_meta[dst] = p.meta;
+      }
+      continue;
+    }
     // lane q < 3 proves threshold q + 1 (X2 is the strict one: d >= t2)
     bool ok = true;
     uint32_t xq = 0x7c00u;
@@ -399,46 +411,6 @@ __global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__rest
   }
 }
 
-// rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
-// read from input row (head * in_rows_per_head + r % tokens_per_head)
-template <bool PAGED, int BITS>
-__global__ void __launch_bounds__(256) value_rows_kernel(const uint16_t *__restrict__ v, int64_t rows,
-                                                         int64_t tokens_per_head, int64_t in_rows_per_head,
-                                                         int64_t t0, uint32_t *__restrict__ v_codes,
-                                                         uint32_t *__restrict__ v_meta, int64_t max_tokens,
-                                                         const PageMap pm) {
-  const int lane = threadIdx.x & 31;
-  const int lane16 = lane & 15;
-  const uint32_t half_mask = (lane < 16) ? 0x0000ffffu : 0xffff0000u;
-  const int64_t half_warps = (int64_t)gridDim.x * (blockDim.x >> 4);
-  // kRows rows per half-warp and iteration: their loads are all issued before the
-  // first row is reduced, so each lane keeps kRows 16-byte loads in flight
-  constexpr int kRows = 4;
-  for (int64_t row0 = ((int64_t)blockIdx.x * (blockDim.x >> 4) + (threadIdx.x >> 4)) * kRows; row0 < rows;
-       row0 += half_warps * kRows) {
-    uint4 x[kRows];
-    int64_t dst[kRows];
-    bool ok[kRows];
-#pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      const int64_t row = row0 + u;
-      ok[u] = row < rows;
-      const int64_t bh = ok[u] ? row / tokens_per_head : 0;
-      const int64_t i = ok[u] ? row - bh * tokens_per_head : 0;
-      const int64_t t = t0 + i;
-      dst[u] = bh * max_tokens + t;
-      if constexpr (PAGED) {
-        if (ok[u] && !paged_row(pm, bh, t, &dst[u])) ok[u] = false;  // the half-warp skips the row together
-      }
-      x[u] = ok[u] ? __ldg(reinterpret_cast<const uint4 *>(v + (bh * in_rows_per_head + i) * kD) + lane16)
-                   : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kRows; ++u)
-      if (ok[u])
-        quantize_value_row<BITS>(x[u], lane16, half_mask, v_codes + dst[u] * words_per_row<BITS>(), v_meta + dst[u]);
-  }
-}
 
 // Append: one warp per (batch, KV head).  Lanes 0-15 quantize the new value row (or,
 // with a value residual, copy it into residual slot r); lanes 16-31 copy the new
@@ -679,11 +651,11 @@ cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_p
   if (rows == 0) return cudaSuccess;
   const int grid = grid_cap((rows + 63) / 64);  // 64 rows per CTA and pass
   if (bits == 2)
-    value_rows2_kernel<false><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
-                                                     max_tokens, PageMap{});
+    value_rows2_kernel<false, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes,
+                                                        v_meta, max_tokens, PageMap{});
   else
-    value_rows_kernel<false, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes, v_meta,
-                                                       max_tokens, PageMap{});
+    value_rows2_kernel<false, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes,
+                                                        v_meta, max_tokens, PageMap{});
   return cudaGetLastError();
 }
 
@@ -694,11 +666,11 @@ cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t to
   if (rows == 0) return cudaSuccess;
   const int grid = grid_cap((rows + 63) / 64);  // 64 rows per CTA and pass
   if (bits == 2)
-    value_rows2_kernel<true><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta, 0,
-                                                    pm);
+    value_rows2_kernel<true, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
+                                                       0, pm);
   else
-    value_rows_kernel<true, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
-                                                      0, pm);
+    value_rows2_kernel<true, 4><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, 0, v_codes, v_meta,
+                                                       0, pm);
   return cudaGetLastError();
 }
 
