@@ -516,7 +516,7 @@ def make_layout_config(args):
 def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int = 1):
     """Quantize the whole prompt (kivi_quantize_prefill, dense cache) with L2 flushed
     before each call: the quantizers' throughput over fp16 K and V read once and the
-    codes, scales and residual written (rows a1-a3)."""
+    codes, scales and residual written."""
     import torch
 
     from bit_asymmetric_kv_gb300 import kivi
