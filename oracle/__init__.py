@@ -11,10 +11,10 @@ it with gcc on first use and exposes numpy-level wrappers.  Every function follo
 the page "Makale Bulteni -- KIVI" (cmlonder.com radar / paper-to-prod, 2026-11-01):
 headline paragraph (keys per channel, values per token, asymmetric 2-bit) and
 section "Iddia ve Gerceklik", paragraphs 2-3 (fixed outlier key channels; G-token
-key groups with a full-precision residual buffer).  The readings R1-R10 are listed
+key groups with a full-precision residual buffer).  The readings R1-R11 are listed
 at the top of ``kivi_oracle.c``; R9 is the variant with a value residual kept in
 lock-step with the key residual (``value_residual=True``), R10 the 4-bit code
-width (``bits=4``).
+width (``bits=4``), R11 value channel groups of ``value_group`` < D channels.
 
 Parity pins (tests/test_oracle_*.py) check this oracle against closed forms,
 brute force and library routines, not against itself.
@@ -61,17 +61,18 @@ def lib():
             L.oracle_max_threads.restype = i32
             L.oracle_quantize_group.argtypes = [P, i64, i64, i32, P, P, P]
             L.oracle_pack_row.argtypes = [P, i32, i32, P]
-            L.oracle_prefill_head.argtypes = [i32, i32, i32, i64, P, P, P, P, P, P, P, P]
-            L.oracle_append_head.argtypes = [i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_prefill_head.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_append_head.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
             L.oracle_append_head.restype = i64
-            L.oracle_dequantize_head_f64.argtypes = [i32, i32, i32, i64, P, P, P, P, P, P, P, P]
-            L.oracle_dequantize_head_f32.argtypes = [i32, i32, i32, i64, P, P, P, P, P, P, P, P]
-            L.oracle_attention_head.argtypes = [i32, i32, i32, i64, P, P, P, P, P, P, P, f64, P]
+            L.oracle_dequantize_head_f64.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_dequantize_head_f32.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
+            L.oracle_attention_head.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, f64, P]
             L.oracle_attention_head.restype = i32
-            L.oracle_prefill.argtypes = [i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
-            L.oracle_append.argtypes = [i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
+            L.oracle_prefill.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
+            L.oracle_append.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, P]
             L.oracle_append.restype = i64
-            L.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, f64, P]
+            L.oracle_attention.argtypes = [i32, i32, i32, i32, i32, i32, i32, i64, i64, P, P, P, P, P, P, P, f64,
+                                           P]
             L.oracle_attention.restype = i32
             L.oracle_attention_raw_head.argtypes = [i32, i64, P, P, P, f64, P]
             L.oracle_attention_raw_head.restype = i32
@@ -138,6 +139,7 @@ class Cache:
     k_codes [B,Hkv,T,D*bits/32] u32 | k_meta [B,Hkv,T//G,D] u32 {s | z<<16}
     k_res   [B,Hkv,G,D]   u16 (fp16 bits)
     v_codes [B,Hkv,T,D*bits/32] u32 | v_meta [B,Hkv,T] u32 {s | z<<16}
+                                       ([B,Hkv,T,D/vg] with value groups of vg < D, R11)
     v_res   [B,Hkv,G,D]   u16, or None: the value residual of reading R9
     n       tokens held;  T = max_tokens;  bits = 2 (R1-R7) or 4 (R10).
     """
@@ -155,22 +157,33 @@ class Cache:
     n: int = 0
     v_res: np.ndarray | None = None
     bits: int = 2
+    vg: int = 0  # value channel group (R11); 0 or D: one group per token (R5)
 
     @classmethod
-    def empty(cls, B, Hkv, D, G, max_tokens, value_residual: bool = False, bits: int = 2):
+    def empty(cls, B, Hkv, D, G, max_tokens, value_residual: bool = False, bits: int = 2,
+              value_group: int | None = None):
         T = int(max_tokens)
         W = D * bits // 32
+        vg = D if not value_group else int(value_group)
+        if vg <= 0 or D % vg != 0:
+            raise ValueError(f"value_group {value_group} must divide D = {D}")
+        v_meta = np.zeros((B, Hkv, T), np.uint32) if vg == D else np.zeros((B, Hkv, T, D // vg), np.uint32)
         return cls(
             B, Hkv, D, G, T,
             np.zeros((B, Hkv, T, W), np.uint32),
             np.zeros((B, Hkv, T // G, D), np.uint32),
             np.zeros((B, Hkv, G, D), np.uint16),
             np.zeros((B, Hkv, T, W), np.uint32),
-            np.zeros((B, Hkv, T), np.uint32),
+            v_meta,
             0,
             np.zeros((B, Hkv, G, D), np.uint16) if value_residual else None,
             bits,
+            vg,
         )
+
+    @property
+    def value_group(self) -> int:
+        return self.vg if self.vg else self.D
 
     def _vres_ptr(self, b=None, h=None):
         if self.v_res is None:
@@ -186,14 +199,15 @@ class Cache:
         return (self.k_codes[b, h], self.k_meta[b, h], self.k_res[b, h], self.v_codes[b, h], self.v_meta[b, h])
 
 
-def prefill(k, v, G: int, max_tokens: int, value_residual: bool = False, bits: int = 2) -> Cache:
+def prefill(k, v, G: int, max_tokens: int, value_residual: bool = False, bits: int = 2,
+            value_group: int | None = None) -> Cache:
     """Quantize a prompt: k, v fp16 [B, Hkv, n, D] -> Cache holding n tokens."""
     kb, vb = _f16_bits(k), _f16_bits(v)
     B, Hkv, n, D = kb.shape
     if max_tokens < n:
         raise ValueError("max_tokens < n")
-    c = Cache.empty(B, Hkv, D, G, max_tokens, value_residual, bits)
-    lib().oracle_prefill(B, Hkv, D, G, bits, c.max_tokens, n, _ptr(kb), _ptr(vb), *c.bufs())
+    c = Cache.empty(B, Hkv, D, G, max_tokens, value_residual, bits, value_group)
+    lib().oracle_prefill(B, Hkv, D, G, bits, c.value_group, c.max_tokens, n, _ptr(kb), _ptr(vb), *c.bufs())
     c.n = n
     return c
 
@@ -203,7 +217,8 @@ def append(c: Cache, k_new, v_new) -> Cache:
     kb, vb = _f16_bits(k_new), _f16_bits(v_new)
     if c.n >= c.max_tokens:
         raise ValueError("cache full")
-    c.n = int(lib().oracle_append(c.B, c.Hkv, c.D, c.G, c.bits, c.max_tokens, c.n, _ptr(kb), _ptr(vb), *c.bufs()))
+    c.n = int(lib().oracle_append(c.B, c.Hkv, c.D, c.G, c.bits, c.value_group, c.max_tokens, c.n, _ptr(kb),
+                                  _ptr(vb), *c.bufs()))
     return c
 
 
@@ -223,8 +238,8 @@ def dequantize(c: Cache, dtype=np.float64, heads=None):
     for b, h in todo:
         kc, km, kr, vc, vm = c.head(b, h)
         ko, vo = kd[b, h], vd[b, h]
-        fn(c.D, c.G, c.bits, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm), c._vres_ptr(b, h), _ptr(ko),
-           _ptr(vo))
+        fn(c.D, c.G, c.bits, c.value_group, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm),
+           c._vres_ptr(b, h), _ptr(ko), _ptr(vo))
     return kd, vd
 
 
@@ -233,8 +248,8 @@ def attention(c: Cache, q, sigma: float) -> np.ndarray:
     qb = _f16_bits(q)
     B, Hq, D = qb.shape
     out = np.zeros((B, Hq, D), np.float64)
-    rc = lib().oracle_attention(B, Hq, c.Hkv, D, c.G, c.bits, c.max_tokens, c.n, *c.bufs(), _ptr(qb), float(sigma),
-                                _ptr(out))
+    rc = lib().oracle_attention(B, Hq, c.Hkv, D, c.G, c.bits, c.value_group, c.max_tokens, c.n, *c.bufs(),
+                                _ptr(qb), float(sigma), _ptr(out))
     if rc != 0:
         raise ValueError("oracle attention: empty cache or Hq % Hkv != 0")
     return out
@@ -245,18 +260,19 @@ def attention_head(c: Cache, b: int, kvh: int, q_row, sigma: float) -> np.ndarra
     qb = np.ascontiguousarray(_f16_bits(q_row))
     out = np.zeros(c.D, np.float64)
     kc, km, kr, vc, vm = c.head(b, kvh)
-    rc = lib().oracle_attention_head(c.D, c.G, c.bits, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc), _ptr(vm),
-                                     c._vres_ptr(b, kvh), _ptr(qb), float(sigma), _ptr(out))
+    rc = lib().oracle_attention_head(c.D, c.G, c.bits, c.value_group, c.n, _ptr(kc), _ptr(km), _ptr(kr), _ptr(vc),
+                                     _ptr(vm), c._vres_ptr(b, kvh), _ptr(qb), float(sigma), _ptr(out))
     if rc != 0:
         raise ValueError("oracle attention: empty cache")
     return out
 
 
-def prefill_head(k_head, v_head, G: int, max_tokens: int, value_residual: bool = False, bits: int = 2):
+def prefill_head(k_head, v_head, G: int, max_tokens: int, value_residual: bool = False, bits: int = 2,
+                 value_group: int | None = None):
     """Quantize one (batch, KV head) prompt k_head, v_head fp16 [n, D] -> 1x1 Cache."""
     kb = np.ascontiguousarray(_f16_bits(k_head))[None, None]
     vb = np.ascontiguousarray(_f16_bits(v_head))[None, None]
-    return prefill(kb, vb, G, max_tokens, value_residual, bits)
+    return prefill(kb, vb, G, max_tokens, value_residual, bits, value_group)
 
 
 def attention_raw(k, v, q, sigma: float) -> np.ndarray:

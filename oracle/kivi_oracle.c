@@ -44,6 +44,10 @@
  *       residual as keys: the last n mod G values stay fp16, and when the key group
  *       flushes its G values are quantized per token (R5) at once.  Without the
  *       buffer, R6 holds: every value is quantized when it arrives.
+ *   R11 (variant, value group vg < D) a value token is quantized in D / vg groups of
+ *       vg consecutive channels, group g = channels g*vg .. g*vg + vg - 1, each with
+ *       its own {s, z} by R1-R4 (R10 for bits = 4); the token's meta entries are
+ *       its groups in order.  vg = D is R5.  The codes are packed as in R7 / R10.
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.  No fast-math and
  * no FMA contraction, so every fp32 operation is a single IEEE-754 RNE operation.
@@ -171,13 +175,20 @@ static void quantize_key_group(const uint16_t *rows, int D, int G, int bits, uin
   free(col);
 }
 
-/* Value token quantization (R5, R7, R10): one row of D channels -> D*bits/32 words + {s, z}. */
-static void quantize_value_token(const uint16_t *row, int D, int bits, uint32_t *codes_out, uint32_t *meta_out) {
+/* Meta entries per value token: one per channel group (R5, R11). */
+#define VMW(D, vg) ((D) / (vg))
+
+/* Value token quantization (R5, R7, R10, R11): one row of D channels -> D*bits/32
+ * words + D/vg {s, z}, group g over channels g*vg .. g*vg + vg - 1. */
+static void quantize_value_token(const uint16_t *row, int D, int bits, int vg, uint32_t *codes_out,
+                                 uint32_t *meta_out) {
   uint8_t *codes = (uint8_t *)malloc((size_t)D);
-  uint16_t s, z;
-  oracle_quantize_group(row, D, 1, bits, &s, &z, codes);
+  for (int g = 0; g < VMW(D, vg); ++g) {
+    uint16_t s, z;
+    oracle_quantize_group(row + (size_t)g * vg, vg, 1, bits, &s, &z, codes + (size_t)g * vg);
+    meta_out[g] = meta_word(s, z);
+  }
   oracle_pack_row(codes, D, bits, codes_out);
-  *meta_out = meta_word(s, z);
   free(codes);
 }
 
@@ -188,10 +199,10 @@ static void quantize_value_token(const uint16_t *row, int D, int bits, uint32_t 
  *   k_meta   : [max_tokens/G][D]    groups < floor(n/G) written
  *   k_res    : [G][D]               slots < n mod G written (token nq + j in slot j)
  *   v_codes  : [max_tokens][D*bits/32]   rows < n written (rows < nq with a value residual)
- *   v_meta   : [max_tokens]         entries < n written (< nq with a value residual)
+ *   v_meta   : [max_tokens][D/vg]   rows < n written (< nq with a value residual)
  *   v_res    : [G][D] or NULL       with a value residual: slots < n mod G written
  */
-void oracle_prefill_head(int D, int G, int bits, int64_t n, const uint16_t *k, const uint16_t *v,
+void oracle_prefill_head(int D, int G, int bits, int vg, int64_t n, const uint16_t *k, const uint16_t *v,
                          uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                          uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t n_groups = n / G;
@@ -203,7 +214,8 @@ void oracle_prefill_head(int D, int G, int bits, int64_t n, const uint16_t *k, c
     memcpy(k_res + (size_t)j * D, k + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
   int64_t n_quantized_values = v_res ? nq : n;
   for (int64_t t = 0; t < n_quantized_values; ++t)
-    quantize_value_token(v + (size_t)t * D, D, bits, v_codes + (size_t)t * WPR(D, bits), v_meta + t);
+    quantize_value_token(v + (size_t)t * D, D, bits, vg, v_codes + (size_t)t * WPR(D, bits),
+                         v_meta + (size_t)t * VMW(D, vg));
   if (v_res)
     for (int64_t j = 0; j < n - nq; ++j)
       memcpy(v_res + (size_t)j * D, v + (size_t)(nq + j) * D, (size_t)D * sizeof(uint16_t));
@@ -216,7 +228,7 @@ void oracle_prefill_head(int D, int G, int bits, int64_t n, const uint16_t *k, c
  * fills, its G keys are quantized as group n / G (and, with a value residual, its
  * G values token by token) and the residual empties.  Returns the new length n + 1.
  */
-int64_t oracle_append_head(int D, int G, int bits, int64_t n, const uint16_t *k_new, const uint16_t *v_new,
+int64_t oracle_append_head(int D, int G, int bits, int vg, int64_t n, const uint16_t *k_new, const uint16_t *v_new,
                            uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                            uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t r = n % G;
@@ -224,14 +236,14 @@ int64_t oracle_append_head(int D, int G, int bits, int64_t n, const uint16_t *k_
   if (v_res)
     memcpy(v_res + (size_t)r * D, v_new, (size_t)D * sizeof(uint16_t));
   else
-    quantize_value_token(v_new, D, bits, v_codes + (size_t)n * WPR(D, bits), v_meta + n);
+    quantize_value_token(v_new, D, bits, vg, v_codes + (size_t)n * WPR(D, bits), v_meta + (size_t)n * VMW(D, vg));
   if (r + 1 == G) {
     int64_t g = n / G;
     quantize_key_group(k_res, D, G, bits, k_codes + (size_t)g * G * WPR(D, bits), k_meta + (size_t)g * D);
     if (v_res)
       for (int64_t j = 0; j < G; ++j)
-        quantize_value_token(v_res + (size_t)j * D, D, bits, v_codes + (size_t)(g * G + j) * WPR(D, bits),
-                             v_meta + g * G + j);
+        quantize_value_token(v_res + (size_t)j * D, D, bits, vg, v_codes + (size_t)(g * G + j) * WPR(D, bits),
+                             v_meta + (size_t)(g * G + j) * VMW(D, vg));
   }
   return n + 1;
 }
@@ -252,9 +264,9 @@ static void dequant_key_f64(int D, int G, int bits, int64_t n, int64_t t, const 
   }
 }
 
-/* Dequantized value t of one head, fp64: z_t + code * s_t, or with a value residual
- * (R9) the fp16 value itself for the last n mod G tokens. */
-static void dequant_value_f64(int D, int G, int bits, int64_t n, int64_t t, const uint32_t *v_codes,
+/* Dequantized value t of one head, fp64: z + code * s of the channel's group (R11),
+ * or with a value residual (R9) the fp16 value itself for the last n mod G tokens. */
+static void dequant_value_f64(int D, int G, int bits, int vg, int64_t n, int64_t t, const uint32_t *v_codes,
                               const uint32_t *v_meta, const uint16_t *v_res, double *out) {
   int64_t nq = (n / G) * G;
   if (v_res && t >= nq) {
@@ -263,25 +275,28 @@ static void dequant_value_f64(int D, int G, int bits, int64_t n, int64_t t, cons
     return;
   }
   const uint32_t *row = v_codes + (size_t)t * WPR(D, bits);
-  double s = (double)h2f(meta_s(v_meta[t]));
-  double z = (double)h2f(meta_z(v_meta[t]));
-  for (int c = 0; c < D; ++c) out[c] = z + (double)unpack_code(row, bits, c) * s;
+  const uint32_t *meta = v_meta + (size_t)t * VMW(D, vg);
+  for (int c = 0; c < D; ++c) {
+    double s = (double)h2f(meta_s(meta[c / vg]));
+    double z = (double)h2f(meta_z(meta[c / vg]));
+    out[c] = z + (double)unpack_code(row, bits, c) * s;
+  }
 }
 
 /* Dequantize one head's n tokens to fp64 [n][D] (keys and values). */
-void oracle_dequantize_head_f64(int D, int G, int bits, int64_t n, const uint32_t *k_codes,
+void oracle_dequantize_head_f64(int D, int G, int bits, int vg, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
                                 const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 double *k_out, double *v_out) {
   for (int64_t t = 0; t < n; ++t) {
     dequant_key_f64(D, G, bits, n, t, k_codes, k_meta, k_res, k_out + (size_t)t * D);
-    dequant_value_f64(D, G, bits, n, t, v_codes, v_meta, v_res, v_out + (size_t)t * D);
+    dequant_value_f64(D, G, bits, vg, n, t, v_codes, v_meta, v_res, v_out + (size_t)t * D);
   }
 }
 
 /* Dequantize one head's n tokens to fp32 [n][D]: fp32(z) + fp32(code) * fp32(s),
  * a product that is exact in fp32 followed by one RNE addition. */
-void oracle_dequantize_head_f32(int D, int G, int bits, int64_t n, const uint32_t *k_codes,
+void oracle_dequantize_head_f32(int D, int G, int bits, int vg, int64_t n, const uint32_t *k_codes,
                                 const uint32_t *k_meta, const uint16_t *k_res,
                                 const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                                 float *k_out, float *v_out) {
@@ -306,11 +321,10 @@ void oracle_dequantize_head_f32(int D, int G, int bits, int64_t n, const uint32_
       continue;
     }
     const uint32_t *vrow = v_codes + (size_t)t * WPR(D, bits);
-    float s = h2f(meta_s(v_meta[t]));
-    float z = h2f(meta_z(v_meta[t]));
+    const uint32_t *vmeta = v_meta + (size_t)t * VMW(D, vg);
     for (int c = 0; c < D; ++c) {
-      float prod = (float)unpack_code(vrow, bits, c) * s;
-      vo[c] = z + prod;
+      float prod = (float)unpack_code(vrow, bits, c) * h2f(meta_s(vmeta[c / vg]));
+      vo[c] = h2f(meta_z(vmeta[c / vg])) + prod;
     }
   }
 }
@@ -321,7 +335,8 @@ void oracle_dequantize_head_f32(int D, int G, int bits, int64_t n, const uint32_
  *   out_c = sum_t p_t V'_{t,c}.
  * Returns 0, or -1 when n <= 0 (softmax over an empty set is undefined).
  */
-int oracle_attention_head(int D, int G, int bits, int64_t n, const uint32_t *k_codes, const uint32_t *k_meta,
+int oracle_attention_head(int D, int G, int bits, int vg, int64_t n, const uint32_t *k_codes,
+                          const uint32_t *k_meta,
                           const uint16_t *k_res, const uint32_t *v_codes, const uint32_t *v_meta,
                           const uint16_t *v_res, const uint16_t *q, double sigma, double *out) {
   if (n <= 0) return -1;
@@ -344,7 +359,7 @@ int oracle_attention_head(int D, int G, int bits, int64_t n, const uint32_t *k_c
   }
   for (int c = 0; c < D; ++c) out[c] = 0.0;
   for (int64_t t = 0; t < n; ++t) {
-    dequant_value_f64(D, G, bits, n, t, v_codes, v_meta, v_res, row);
+    dequant_value_f64(D, G, bits, vg, n, t, v_codes, v_meta, v_res, row);
     double p = score[t] / l;
     for (int c = 0; c < D; ++c) out[c] += p * row[c];
   }
@@ -389,39 +404,39 @@ int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_
  *   k, v      [B][Hkv][n][D] fp16         k_new, v_new [B][Hkv][D] fp16
  *   k_codes   [B][Hkv][max_tokens][D*bits/32]  k_meta [B][Hkv][max_tokens/G][D]
  *   k_res     [B][Hkv][G][D] fp16         v_codes [B][Hkv][max_tokens][D*bits/32]
- *   v_meta    [B][Hkv][max_tokens]        q [B][Hq][D] fp16, out [B][Hq][D] fp64
+ *   v_meta    [B][Hkv][max_tokens][D/vg]  q [B][Hq][D] fp16, out [B][Hq][D] fp64
  * Heads are independent, so the loops run in parallel over (b, head).
  * ------------------------------------------------------------------------------- */
 #define KC(bh) (k_codes + (size_t)(bh) * max_tokens * WPR(D, bits))
 #define KM(bh) (k_meta + (size_t)(bh) * (max_tokens / G) * D)
 #define KR(bh) (k_res + (size_t)(bh) * G * D)
 #define VC(bh) (v_codes + (size_t)(bh) * max_tokens * WPR(D, bits))
-#define VM(bh) (v_meta + (size_t)(bh) * max_tokens)
+#define VM(bh) (v_meta + (size_t)(bh) * max_tokens * VMW(D, vg))
 #define VR(bh) (v_res ? v_res + (size_t)(bh) * G * D : NULL)
 
-void oracle_prefill(int B, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n, const uint16_t *k,
+void oracle_prefill(int B, int Hkv, int D, int G, int bits, int vg, int64_t max_tokens, int64_t n, const uint16_t *k,
                     const uint16_t *v, uint32_t *k_codes, uint32_t *k_meta, uint16_t *k_res,
                     uint32_t *v_codes, uint32_t *v_meta, uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(dynamic)
   for (int64_t bh = 0; bh < heads; ++bh)
-    oracle_prefill_head(D, G, bits, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, KC(bh), KM(bh),
+    oracle_prefill_head(D, G, bits, vg, n, k + (size_t)bh * n * D, v + (size_t)bh * n * D, KC(bh), KM(bh),
                         KR(bh), VC(bh), VM(bh), VR(bh));
 }
 
-int64_t oracle_append(int B, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n,
+int64_t oracle_append(int B, int Hkv, int D, int G, int bits, int vg, int64_t max_tokens, int64_t n,
                       const uint16_t *k_new, const uint16_t *v_new, uint32_t *k_codes,
                       uint32_t *k_meta, uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta,
                       uint16_t *v_res) {
   int64_t heads = (int64_t)B * Hkv;
 #pragma omp parallel for schedule(static)
   for (int64_t bh = 0; bh < heads; ++bh)
-    oracle_append_head(D, G, bits, n, k_new + (size_t)bh * D, v_new + (size_t)bh * D, KC(bh), KM(bh),
+    oracle_append_head(D, G, bits, vg, n, k_new + (size_t)bh * D, v_new + (size_t)bh * D, KC(bh), KM(bh),
                        KR(bh), VC(bh), VM(bh), VR(bh));
   return n + 1;
 }
 
-int oracle_attention(int B, int Hq, int Hkv, int D, int G, int bits, int64_t max_tokens, int64_t n,
+int oracle_attention(int B, int Hq, int Hkv, int D, int G, int bits, int vg, int64_t max_tokens, int64_t n,
                      const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                      const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res,
                      const uint16_t *q, double sigma, double *out) {
@@ -433,7 +448,7 @@ int oracle_attention(int B, int Hq, int Hkv, int D, int G, int bits, int64_t max
     int64_t b = bq / Hq;
     int h = (int)(bq % Hq);
     int64_t bh = b * Hkv + h / group;
-    oracle_attention_head(D, G, bits, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
+    oracle_attention_head(D, G, bits, vg, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
                           sigma, out + (size_t)bq * D);
   }
   return 0;
