@@ -1,10 +1,13 @@
-// kivi_quant.cu -- quantize / pack kernels of the KIVI 2-bit KV cache (sm_103a).
+// kivi_quant.cu -- quantize / pack kernels of the KIVI 2-bit KV cache and its 4-bit
+// variant (sm_103a).
 //
 // KIVI page ("Makale Bulteni -- KIVI", cmlonder.com radar / paper-to-prod,
 // 2026-11-01): headline paragraph (keys per channel, values per token, asymmetric
 // 2-bit) and section "Iddia ve Gerceklik", paragraphs 2-3 (G-token key groups, a
-// full-precision residual for the unfilled group).  All kernels here stream fp16
-// inputs once from HBM and write 1/8 of that in codes: they are bandwidth-bound.
+// full-precision residual for the unfilled group).  The kernels here stream fp16
+// inputs once from HBM and write 1/8 (2-bit) or 1/4 (4-bit) of that in codes; the
+// per-element work is kept small (fp16 comparisons, a reciprocal product) so that
+// the memory stream, not the arithmetic, sets their speed.
 #include "kivi_device.cuh"
 #include "kivi_internal.h"
 
@@ -127,12 +130,6 @@ __device__ __forceinline__ uint32_t qchunk8(const uint4 &c, const QParams &p) {
 }
 
 
-// -------------------------------------------------------------------------------------
-// Key groups: one CTA (4 warps) quantizes one G-token group of one (batch, KV head).
-// Warp w owns channels 32w .. 32w+31.  Lane = 4 * t8 + c4: the lane loads the
-// 16-byte chunk c4 (8 channels) of tokens t8, t8 + 8, ... so one warp instruction
-// reads 8 token rows x 64 contiguous bytes.
-// -------------------------------------------------------------------------------------
 // Row of token t of head bh in a paged pool (false: the block table gives no page
 // of the pool for it, and the row is skipped).
 __device__ __forceinline__ bool paged_row(const PageMap &pm, int64_t bh, int64_t t, int64_t *row) {
@@ -142,6 +139,12 @@ __device__ __forceinline__ bool paged_row(const PageMap &pm, int64_t bh, int64_t
   return true;
 }
 
+// -------------------------------------------------------------------------------------
+// Key groups: one CTA (4 warps) quantizes one G-token group of one (batch, KV head).
+// Warp w owns channels 32w .. 32w+31.  Lane = 4 * t8 + c4: the lane loads the
+// 16-byte chunk c4 (8 channels) of tokens t8, t8 + 8, ... so one warp instruction
+// reads 8 token rows x 64 contiguous bytes.
+// -------------------------------------------------------------------------------------
 template <int G, bool PAGED, int BITS>
 __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
                                                         int64_t groups_per_head, int64_t g0,
