@@ -14,7 +14,8 @@ section "Iddia ve Gerceklik", paragraphs 2-3 (fixed outlier key channels; G-toke
 key groups with a full-precision residual buffer).  The readings R1-R11 are listed
 at the top of ``kivi_oracle.c``; R9 is the variant with a value residual kept in
 lock-step with the key residual (``value_residual=True``), R10 the 4-bit code
-width (``bits=4``), R11 value channel groups of ``value_group`` < D channels.
+width (``bits=4``), R11 value channel groups of ``value_group`` < D channels,
+R12 the causal full-precision prefill attention (``prefill_attention``).
 
 Parity pins (tests/test_oracle_*.py) check this oracle against closed forms,
 brute force and library routines, not against itself.
@@ -78,6 +79,10 @@ def lib():
             L.oracle_attention_raw_head.restype = i32
             L.oracle_attention_raw.argtypes = [i32, i32, i32, i32, i64, P, P, P, f64, P]
             L.oracle_attention_raw.restype = i32
+            L.oracle_prefill_attention_head.argtypes = [i32, i64, P, P, P, f64, P]
+            L.oracle_prefill_attention_head.restype = i32
+            L.oracle_prefill_attention.argtypes = [i32, i32, i32, i32, i64, P, P, P, f64, P]
+            L.oracle_prefill_attention.restype = i32
             _lib = L
         return _lib
 
@@ -295,4 +300,16 @@ def attention_raw_head(k_head, v_head, q_row, sigma: float) -> np.ndarray:
     if lib().oracle_attention_raw_head(kb.shape[1], kb.shape[0], _ptr(kb), _ptr(vb), _ptr(qb), float(sigma),
                                        _ptr(out)) != 0:
         raise ValueError("oracle attention: empty cache")
+    return out
+
+
+def prefill_attention(q, k, v, sigma: float) -> np.ndarray:
+    """R12: causal fp64 attention of the prompt over itself, on the raw fp16 values.
+    q [B, Hq, n, D], k, v [B, Hkv, n, D] fp16 -> out [B, Hq, n, D] fp64."""
+    qb, kb, vb = _f16_bits(q), _f16_bits(k), _f16_bits(v)
+    B, Hq, n, D = qb.shape
+    Hkv = kb.shape[1]
+    out = np.zeros((B, Hq, n, D), np.float64)
+    if lib().oracle_prefill_attention(B, Hq, Hkv, D, n, _ptr(qb), _ptr(kb), _ptr(vb), float(sigma), _ptr(out)) != 0:
+        raise ValueError("oracle prefill attention: empty prompt or Hq % Hkv != 0")
     return out

@@ -48,6 +48,11 @@
  *       vg consecutive channels, group g = channels g*vg .. g*vg + vg - 1, each with
  *       its own {s, z} by R1-R4 (R10 for bits = 4); the token's meta entries are
  *       its groups in order.  vg = D is R5.  The codes are packed as in R7 / R10.
+ *   R12 (prefill attention, "Kod ve Entegrasyon Haritasi": FlashAttention runs the
+ *       prefill) the prompt attends to itself in full precision, causally: for
+ *       position i, out_i = sum_{j <= i} softmax_j(sigma * q_i . k_j) v_j over the
+ *       raw fp16 keys and values, fp64, query head h reading KV head h / (Hq / Hkv);
+ *       the cache is then quantized from the same fp16 K and V (R1-R11).
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC.  No fast-math and
  * no FMA contraction, so every fp32 operation is a single IEEE-754 RNE operation.
@@ -399,6 +404,40 @@ int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_
   return 0;
 }
 
+/*
+ * R12: causal prefill attention of one query head over one KV head's prompt, fp64.
+ *   q [n][D], k [n][D], v [n][D] fp16;  out [n][D] fp64 with, for every position i,
+ *   out_i = sum_{j <= i} p_ij v_j,  p_i = softmax_j (sigma * q_i . k_j) over j <= i.
+ * Returns 0, or -1 when n <= 0.
+ */
+int oracle_prefill_attention_head(int D, int64_t n, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                  double sigma, double *out) {
+  if (n <= 0) return -1;
+  double *score = (double *)malloc((size_t)n * sizeof(double));
+  for (int64_t i = 0; i < n; ++i) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= i; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < D; ++c) acc += (double)h2f(q[(size_t)i * D + c]) * (double)h2f(k[(size_t)j * D + c]);
+      score[j] = sigma * acc;
+      if (score[j] > m) m = score[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+      score[j] = exp(score[j] - m);
+      l += score[j];
+    }
+    double *o = out + (size_t)i * D;
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+      double p = score[j] / l;
+      for (int c = 0; c < D; ++c) o[c] += p * (double)h2f(v[(size_t)j * D + c]);
+    }
+  }
+  free(score);
+  return 0;
+}
+
 /* ---------------------------------------------------------------------------------
  * Whole-batch wrappers over the per-head functions.  Buffer shapes:
  *   k, v      [B][Hkv][n][D] fp16         k_new, v_new [B][Hkv][D] fp16
@@ -450,6 +489,23 @@ int oracle_attention(int B, int Hq, int Hkv, int D, int G, int bits, int vg, int
     int64_t bh = b * Hkv + h / group;
     oracle_attention_head(D, G, bits, vg, n, KC(bh), KM(bh), KR(bh), VC(bh), VM(bh), VR(bh), q + (size_t)bq * D,
                           sigma, out + (size_t)bq * D);
+  }
+  return 0;
+}
+
+/* R12 for the batch: q [B][Hq][n][D], k, v [B][Hkv][n][D] fp16 -> out [B][Hq][n][D] fp64. */
+int oracle_prefill_attention(int B, int Hq, int Hkv, int D, int64_t n, const uint16_t *q, const uint16_t *k,
+                             const uint16_t *v, double sigma, double *out) {
+  if (n <= 0 || Hkv <= 0 || Hq % Hkv != 0) return -1;
+  int group = Hq / Hkv;
+  int64_t rows = (int64_t)B * Hq;
+#pragma omp parallel for schedule(dynamic)
+  for (int64_t bq = 0; bq < rows; ++bq) {
+    int64_t b = bq / Hq;
+    int h = (int)(bq % Hq);
+    int64_t bh = b * Hkv + h / group;
+    oracle_prefill_attention_head(D, n, q + (size_t)bq * n * D, k + (size_t)bh * n * D, v + (size_t)bh * n * D,
+                                  sigma, out + (size_t)bq * n * D);
   }
   return 0;
 }
