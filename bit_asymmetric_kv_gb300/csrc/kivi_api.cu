@@ -10,12 +10,19 @@ namespace {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Most token rows (B * Hkv * max_tokens, or pool pages * Hkv * page tokens) a cache may
+// have: 2^40, far beyond any device memory and far inside int64 row arithmetic.
+constexpr uint64_t kMaxRows = 1ull << 40;
+
 int check_dims(const kivi_dims *d) {
   if (!d) return KIVI_ERR_ARG;
   if (d->B <= 0 || d->Hkv <= 0 || d->max_tokens <= 0) return KIVI_ERR_ARG;
   if (d->D != 128 || (d->bits != 2 && d->bits != 4) || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->max_tokens % d->G != 0) return KIVI_ERR_ARG;
   if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
+  // token rows are indexed with int64 and buffer sizes in size_t: keep far from both
+  const uint64_t heads = (uint64_t)d->B * (uint64_t)d->Hkv;  // below 2^62
+  if (heads > kMaxRows || (uint64_t)d->max_tokens > kMaxRows / heads) return KIVI_ERR_UNSUPPORTED;
   return KIVI_OK;
 }
 
@@ -81,6 +88,8 @@ int check_paged_dims(const kivi_paged_dims *d) {
   if (cap > INT32_MAX) return KIVI_ERR_UNSUPPORTED;
   if ((int64_t)d->B * (cap / 64 + 1) > INT32_MAX) return KIVI_ERR_UNSUPPORTED;
   if ((int64_t)d->B * d->Hkv > INT32_MAX / 2) return KIVI_ERR_UNSUPPORTED;
+  const uint64_t rows_per_page = (uint64_t)d->Hkv << sh;  // below 2^55
+  if ((uint64_t)d->num_pages > kMaxRows / rows_per_page) return KIVI_ERR_UNSUPPORTED;
   return KIVI_OK;
 }
 

@@ -73,19 +73,21 @@ typedef enum {
   KIVI_OK = 0,
   KIVI_ERR_ARG = 1,          /* null pointer, non-positive size, n > max_tokens ... */
   KIVI_ERR_ALIGN = 2,        /* a buffer is not 16-byte aligned */
-  KIVI_ERR_UNSUPPORTED = 3,  /* D != 128, bits != 2, G not in {32, 64}, Hq/Hkv not in {1,2,4} */
+  KIVI_ERR_UNSUPPORTED = 3,  /* D != 128, bits not 2 or 4, G not in {32, 64}, Hq/Hkv not in {1,2,4},
+                                sizes beyond the supported range */
   KIVI_ERR_CAPACITY = 4,     /* append on a full cache, prefill longer than max_tokens */
   KIVI_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
   KIVI_ERR_CUDA = 6          /* a CUDA runtime call or launch failed */
 } kivi_status;
 
-/* Cache geometry.  max_tokens must be a positive multiple of G. */
+/* Cache geometry.  max_tokens must be a positive multiple of G, and B * Hkv *
+ * max_tokens at most 2^40 token rows (KIVI_ERR_UNSUPPORTED beyond). */
 typedef struct {
   int32_t B;         /* batch */
   int32_t Hkv;       /* KV heads */
   int32_t D;         /* head dim, 128 */
   int32_t G;         /* key group size, 32 or 64 */
-  int32_t bits;      /* code width, 2 */
+  int32_t bits;      /* code width, 2 or 4 */
   int32_t value_residual; /* 1: values keep an fp16 residual beside the keys'; 0: none */
   int64_t max_tokens;
 } kivi_dims;
@@ -245,11 +247,11 @@ typedef struct {
   int32_t Hkv;                /* KV heads */
   int32_t D;                  /* head dim, 128 */
   int32_t G;                  /* key group size, 32 or 64 */
-  int32_t bits;               /* code width, 2 */
+  int32_t bits;               /* code width, 2 or 4 */
   int32_t value_residual;     /* as kivi_dims.value_residual */
   int32_t page_tokens;        /* P: a power of two, >= 64 */
   int32_t max_pages_per_seq;  /* columns of the block table */
-  int64_t num_pages;          /* pages in the pool */
+  int64_t num_pages;          /* pages in the pool; num_pages * Hkv * P at most 2^40 */
 } kivi_paged_dims;
 
 typedef struct {

@@ -73,6 +73,9 @@ def test_buffer_bytes(L):
     (dict(B=0), kivi.KIVI_ERR_ARG),
     (dict(max_tokens=100), kivi.KIVI_ERR_ARG),   # not a multiple of G
     (dict(value_residual=2), kivi.KIVI_ERR_ARG),
+    (dict(max_tokens=1 << 62), kivi.KIVI_ERR_UNSUPPORTED),                    # beyond 2^40 token rows
+    (dict(B=1 << 20, Hkv=1 << 10, max_tokens=1 << 12), kivi.KIVI_ERR_UNSUPPORTED),  # 2^42 rows
+    (dict(B=2147483647, Hkv=2147483647, max_tokens=32), kivi.KIVI_ERR_UNSUPPORTED),  # no overflow
 ])
 def test_bad_dims(L, kw, status):
     d = _dims(**kw)
@@ -168,6 +171,8 @@ def test_paged_buffer_bytes(L):
     (dict(num_pages=0), kivi.KIVI_ERR_ARG),
     (dict(max_pages_per_seq=0), kivi.KIVI_ERR_ARG),
     (dict(value_residual=-1), kivi.KIVI_ERR_ARG),
+    (dict(num_pages=1 << 40), kivi.KIVI_ERR_UNSUPPORTED),   # pool beyond 2^40 token rows
+    (dict(num_pages=(1 << 62) + 1), kivi.KIVI_ERR_UNSUPPORTED),
 ])
 def test_bad_paged_dims(L, kw, status):
     d = _pdims(**kw)
