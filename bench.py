@@ -1,18 +1,21 @@
 #!/usr/bin/env python3
 """Decode-step benchmark of the KIVI 2-bit KV cache on GB300.
 
-Workload (default; --workload picks another of the five): Llama-2-7B-shaped MHA
-decode (batch 8, 32 heads, head dim 128, context 4096 + 17 tokens, key groups of
-G = 32, 2-bit codes), seeded synthetic fp16 K/V with fixed outlier key channels.
-The cache is quantized once (untimed); one step is the whole hot path for one new
-token per sequence: append (value quantization, residual write, group flush every
-G steps) + fused 2-bit decode attention + split combine, through kivi_decode_step.
-The metric is decode tokens/s (batch / step time) with the attention call's
-achieved HBM GB/s against the measured copy bandwidth.  L2 is flushed (256 MiB
-write) before every step, outside the timed events.  Every 64 steps the cache is
-rolled back to the prompt (token count reset, residual keys restored; outside the
-timed events), so the context stays within n .. n + 64 tokens however many steps
-run.
+Workload (default; --workload picks another of the five): streaming generation,
+batch 64, 32 heads, head dim 128, an 8192-token fp16 prompt quantized with key
+groups of G = 32 and 2-bit codes, then 512 decode steps, seeded synthetic fp16
+K/V with fixed outlier key channels.  The prompt is quantized once (untimed); one
+step is the whole hot path for one new token per sequence: append (value
+quantization, residual write, group flush every G steps) + fused 2-bit decode
+attention + split combine, through kivi_decode_step.  The context grows by one
+token per step, as in the workload's schedule; after its 512 steps the schedule
+starts again from the prompt (token count reset, residual keys restored, outside
+the timed events).  The fixed-context workloads instead roll back every 64 steps,
+so their context stays within n .. n + 64 tokens.  The metric is decode tokens/s
+(batch / step time) with the attention call's achieved HBM GB/s against the
+measured copy bandwidth.  L2 is flushed (256 MiB write) before every step,
+outside the timed events.  With no flags the timed steps cover one schedule:
+16 warm-up steps and 496 timed ones.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
                   [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
@@ -48,7 +51,15 @@ METRIC = "decode-attention tokens/s and achieved HBM GB/s (fraction of peak) on 
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
-CYCLE = 64  # steps between cache rollbacks
+SHORT_CYCLE = 64  # steps between cache rollbacks of the fixed-context workloads
+
+
+def cycle_of(wl) -> int:
+    """Steps between cache rollbacks: the streaming workload runs its whole schedule
+    (prefill, then `wl.steps` append + attend steps, the context growing by one token
+    per step) before it starts again from the prompt; the fixed-context workloads
+    stay within n .. n + 64 tokens."""
+    return wl.steps if wl.steps else SHORT_CYCLE
 
 
 def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2) -> int:
@@ -199,15 +210,16 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
                   bits: int = 2):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
     cache) on `sample_heads` of the workload's KV heads; scale to the whole batch.
-    Like the GPU loop, the cache is rolled back to the prompt every CYCLE steps
-    (untimed), so the context stays within n .. n + CYCLE."""
+    Like the GPU loop, the cache is rolled back to the prompt every cycle_of(wl)
+    steps (untimed)."""
     import copy
 
     import oracle
     from bit_asymmetric_kv_gb300 import synth
 
     heads = [(i % wl.B, (i * 7) % wl.Hkv) for i in range(sample_heads)]
-    T = wl.capacity(extra=CYCLE + 64)
+    cycle = cycle_of(wl)
+    T = wl.capacity(extra=cycle + 64)
     k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
     v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
     c0 = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits)  # untimed, like the GPU's prefill
@@ -215,9 +227,9 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
     t_total, done = 0.0, 0
     c = c0
     for step in range(steps):
-        if step % CYCLE == 0:
+        if step % cycle == 0:
             c = copy.deepcopy(c0)
-        k_new, v_new, q = synth.make_step(wl, pre, step % CYCLE)
+        k_new, v_new, q = synth.make_step(wl, pre, step % cycle)
         kn = np.stack([k_new[b, h].numpy() for b, h in heads])[None]
         vn = np.stack([v_new[b, h].numpy() for b, h in heads])[None]
         qs = np.stack([q[b, h * R + j].numpy() for b, h in heads for j in range(R)])[None]
@@ -254,9 +266,18 @@ def run_reference(args, wl):
     return 0
 
 
+def context_desc(wl, steps_run: int | None = None) -> str:
+    """The contexts the timed steps attend over."""
+    cycle = cycle_of(wl)
+    if wl.steps:
+        return (f"grows from {wl.n}: step i appends token {wl.n} + i and attends over {wl.n} + i + 1 tokens "
+                f"(the schedule restarts from the {wl.n}-token prompt every {cycle} steps)")
+    return f"{wl.n}..{wl.n + cycle} (cache rolled back every {cycle} steps)"
+
+
 def workload_config(wl):
     cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D, "G": wl.G, "bits": 2,
-           "context_tokens": f"{wl.n}..{wl.n + CYCLE} (cache rolled back every {CYCLE} steps)",
+           "context_tokens": context_desc(wl),
            "step": "append_token + decode_attention (one new token per sequence)",
            "l2": "flushed by a 256 MiB write before every step (outside the timed events)",
            "api": "kivi_decode_step (append + decode attention, the attention overlapping the append)",
@@ -277,7 +298,7 @@ class DenseLayout:
         from bit_asymmetric_kv_gb300 import kivi
 
         self.wl, self.kivi = wl, kivi
-        self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=CYCLE + 64), device=dev,
+        self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=cycle_of(wl) + 64), device=dev,
                                          value_residual=value_residual, bits=bits)
         kivi.kivi_quantize_prefill(self.cache, pre.k.to(dev), pre.v.to(dev))
         self.n0 = self.cache.n_tokens
@@ -319,7 +340,7 @@ class PagedLayout:
 
         self.wl, self.kivi, self.P = wl, kivi, page_tokens
         self.graph, self.graphs = graph, {}
-        maxp = math.ceil((wl.n + CYCLE + 64) / page_tokens)
+        maxp = math.ceil((wl.n + cycle_of(wl) + 64) / page_tokens)
         num_pages = wl.B * maxp
         self.cache = kivi.PagedCache.allocate(wl.B, wl.Hkv, wl.G, page_tokens, maxp, num_pages, device=dev,
                                               value_residual=value_residual, bits=bits)
@@ -400,19 +421,22 @@ def run_kivi(args, wl):
     kivi.lib()
     pre = synth.make_prefill(wl)
     total = args.warmup + args.steps
+    cycle = cycle_of(wl)
     lay = make_layout(args, wl, pre, dev)
     n0 = lay.n0
-    # the inputs of one rollback cycle, resident in HBM before timing
-    dev_in = [tuple(t.to(dev) for t in synth.make_step(wl, pre, s)) for s in range(CYCLE)]
+    # the inputs of the steps that run (at most one rollback cycle), drawn once on
+    # the host; resident in HBM before timing
+    steps_host = [synth.make_step(wl, pre, s) for s in range(min(cycle, total))]
+    dev_in = [tuple(t.to(dev) for t in kvq) for kvq in steps_host]
     out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     lay.prepare(dev_in, out)
 
     def step_events(i, rec):
-        if i % CYCLE == 0:
+        if i % cycle == 0:
             lay.rollback()
-        k, v, q = dev_in[i % CYCLE]
+        k, v, q = dev_in[i % cycle]
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -465,7 +489,7 @@ def run_kivi(args, wl):
     prefill = prefill_timing(args, wl, pre, dev, stream, flush)
 
     # ---- end to end through the public API: host buffers, copies inside the timing
-    e2e = e2e_run(args, wl, pre, dev, stream, flush)
+    e2e = e2e_run(args, wl, pre, steps_host, dev, stream, flush)
 
     if rank != 0:
         if world > 1:
@@ -576,22 +600,21 @@ def cycle_workspace(cache, wl, n0, dev):
 
     from bit_asymmetric_kv_gb300 import kivi
 
-    nbytes = max(kivi.kivi_decode_workspace_bytes(cache.dims, wl.Hq, n) for n in range(n0, n0 + CYCLE + 2))
+    nbytes = max(kivi.kivi_decode_workspace_bytes(cache.dims, wl.Hq, n) for n in range(n0, n0 + cycle_of(wl) + 2))
     return torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
 
-def e2e_run(args, wl, pre, dev, stream, flush):
+def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
     """Same metric through the public API with host inputs: every step copies its
     new k, v, q from pinned host memory (one buffer, one copy), runs append + decode
-    attention and copies the output back; the copies are inside the timed events."""
+    attention and copies the output back; the copies are inside the timed events.
+    steps_in: the host inputs (k, v, q) of the steps of one rollback cycle."""
     import torch
 
-    from bit_asymmetric_kv_gb300 import synth
-
     total = args.warmup + args.steps
+    cycle = cycle_of(wl)
     lay = make_layout(args, wl, pre, dev)
     # each step's k, v and q side by side in one pinned buffer: one copy per step
-    steps_in = [synth.make_step(wl, pre, s) for s in range(CYCLE)]
     shapes = [t.shape for t in steps_in[0]]
     sizes = [t.numel() for t in steps_in[0]]
     host = [torch.cat([t.reshape(-1) for t in kvq]).pin_memory() for kvq in steps_in]
@@ -602,12 +625,12 @@ def e2e_run(args, wl, pre, dev, stream, flush):
     lay.prepare([(dk, dv, dq)], out)
     times = []
     for i in range(total):
-        if i % CYCLE == 0:
+        if i % cycle == 0:
             lay.rollback()
         flush.fill_(i & 0xFF)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        dbuf.copy_(host[i % CYCLE], non_blocking=True)
+        dbuf.copy_(host[i % cycle], non_blocking=True)
         lay.step(dk, dv, dq, out, stream)
         out_h.copy_(out, non_blocking=True)
         e1.record(stream)
@@ -677,7 +700,7 @@ def run_compare(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2048)
+    ap.add_argument("--steps", type=int, default=496)
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--impl", choices=["kivi", "reference"], default="kivi")
     ap.add_argument("--compare-fp16", action="store_true",
@@ -692,9 +715,10 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt quantization (kivi_quantize_prefill) of the workload")
-    ap.add_argument("--workload", default="llama2",
+    ap.add_argument("--workload", default="streaming",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
-                         "default: the Llama-2-7B MHA decode")
+                         "default: the streaming generation (B64, H32, 8192-token prompt, 512 steps), "
+                         "the largest of the five")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -12,10 +12,12 @@
 // cudaGetSymbolAddress (the array's name in host code is only a host-side handle,
 // not a device address), once per device, the first time the entry point runs on
 // that device.  That first call therefore performs a runtime query and should be
-// made before any stream capture.  Every call shares the array: calls whose kernels
-// overlap on the GPU (different streams, or different threads on the same device)
-// race on it.  The decode kernels fully overwrite the part of the array they read,
-// so nothing needs clearing between calls.
+// made before any stream capture.  The looked-up address is kept for the life of
+// the process: after a cudaDeviceReset of a device the entry point must not be used
+// on that device again.  Every call shares the array: calls whose kernels overlap
+// on the GPU (different streams, or different threads on the same device) race on
+// it.  The decode kernels fully overwrite the part of the array they read, so
+// nothing needs clearing between calls.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,11 +61,13 @@ size_t kivi_decode_attention_noalloc_max_workspace(void) { return kNoAllocBytes;
 
 int kivi_decode_attention_noalloc(const kivi_dims *d, const kivi_cache *c, const uint16_t *q, int32_t Hq,
                                   float softmax_scale, uint16_t *out, cudaStream_t st) {
-  const size_t need = kivi_decode_workspace_bytes(d, Hq, c ? c->n_tokens : 0);
-  if (need == 0) {
-    // invalid sizes or no device: let the checked entry point report the status
-    return kivi_decode_attention(d, c, q, Hq, softmax_scale, out, nullptr, 0, st);
-  }
+  // Every argument check of the workspace entry point, in its order, without a
+  // launch: given no workspace it returns KIVI_ERR_WORKSPACE exactly when all the
+  // other arguments are valid, and the first failing check's status otherwise.
+  const int s = kivi_decode_attention(d, c, q, Hq, softmax_scale, out, nullptr, 0, st);
+  if (s != KIVI_ERR_WORKSPACE) return s;
+  const size_t need = kivi_decode_workspace_bytes(d, Hq, c->n_tokens);
+  if (need == 0) return KIVI_ERR_CUDA;  // the sizes passed the checks: only a device query can fail here
   if (need > kNoAllocBytes) return KIVI_ERR_WORKSPACE;
   void *ws = nullptr;
   if (noalloc_address(&ws) != cudaSuccess) return KIVI_ERR_CUDA;

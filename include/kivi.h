@@ -26,7 +26,8 @@
  *     key group flushes;
  *   - query head h reads KV head h / (Hq / Hkv) (grouped-query attention).
  *
- * Supported shapes: D = 128, bits = 2, G in {32, 64}, Hq / Hkv in {1, 2, 4}.
+ * Supported shapes: D = 128, bits in {2, 4} (the code width; 4 is a variant, see
+ * kivi_dims.bits), G in {32, 64}, Hq / Hkv in {1, 2, 4}.
  * Inputs must be finite; codes for non-finite inputs are unspecified.
  *
  * Memory: every buffer is device memory owned by the caller (nothing is allocated
@@ -46,10 +47,27 @@
  * value rows at or beyond n (at or beyond nq with a value residual) are not read.
  *
  * Streams and state: every compute call is asynchronous on the given stream and
- * never synchronises with the host.  The only state is the caller's kivi_cache;
+ * never synchronises with the host.  The cache state is the caller's kivi_cache;
  * its n_tokens field is host memory, updated by the library when a call succeeds
  * and left unchanged when it fails.  Concurrent calls on the same cache race.
  * No call throws across the ABI; every call returns a kivi_status.
+ *
+ * Process-wide tables: the decode calls size their grids from the occupancy of
+ * their kernels on the current device.  The first decode call for a given (device,
+ * kernel, shared-memory size) asks the CUDA runtime (it raises the kernel's
+ * dynamic shared-memory limit and queries the occupancy calculator) and records the
+ * answer in a table inside the library, guarded by a mutex; later calls only read
+ * it, so they make no runtime query but cudaGetDevice and can be captured in a CUDA
+ * graph.  Make a first decode call (or a kivi_decode_workspace_bytes /
+ * kivi_paged_decode_workspace_bytes query) on each device before capturing.  The
+ * table holds no cache data and never changes a result.  The allocation-free entry
+ * point keeps a second table (see kivi_decode_attention_noalloc).
+ *
+ * Device dependence: the split of the context between the GPU's warps, and with it
+ * kivi_decode_splits, kivi_decode_workspace_bytes and
+ * kivi_paged_decode_workspace_bytes, depend on the current device (its SM count
+ * and the kernels' occupancy on it).  Query them with the device current that the
+ * calls will run on, and re-query after switching devices.
  */
 #ifndef KIVI_H
 #define KIVI_H
@@ -161,7 +179,11 @@ KIVI_API int kivi_decode_attention(const kivi_dims *dims, const kivi_cache *cach
  * The attention kernel is launched as a programmatic dependent of the append, so it
  * starts on the cached tokens while the append runs and waits for it only before
  * the block of each head that holds the new token.  Increments cache->n_tokens on
- * success; every argument is checked before anything is launched.
+ * success; every argument is checked before anything is launched.  If a launch
+ * fails (KIVI_ERR_CUDA) after the append was queued, n_tokens is left unchanged
+ * although the append may have written token n_tokens (its residual slot, its value
+ * row and, on a flush, its key group); calling kivi_decode_step again with the same
+ * k_new and v_new rewrites that token with the same bits, so a retry is safe.
  */
 KIVI_API int kivi_decode_step(const kivi_dims *dims, kivi_cache *cache, const uint16_t *k_new,
                               const uint16_t *v_new, const uint16_t *q, int32_t Hq, float softmax_scale,
@@ -199,10 +221,13 @@ KIVI_API int kivi_decode_attention_fp16(int32_t B, int32_t Hq, int32_t Hkv, int3
  * 8 MiB array compiled into the library, which occupies device memory on every GPU
  * that loads the library until the process exits.  Sizes whose workspace
  * (kivi_decode_workspace_bytes) exceeds kivi_decode_attention_noalloc_max_workspace()
- * return KIVI_ERR_WORKSPACE and launch nothing.  The first call on a device looks up
- * the array's device address (a runtime query, done once per device), so make it
- * before any stream capture.  Calls share the array: calls whose kernels overlap on
- * the GPU race.  No call allocates or frees memory.
+ * return KIVI_ERR_WORKSPACE and launch nothing; every other argument is checked
+ * first, in the order and with the statuses of kivi_decode_attention.  The first
+ * call on a device looks up the array's device address (a runtime query, done once
+ * per device), so make it before any stream capture.  The address is kept for the
+ * life of the process: after a cudaDeviceReset of a device, do not call this entry
+ * point on that device again.  Calls share the array: calls whose kernels overlap
+ * on the GPU race.  No call allocates or frees memory.
  */
 KIVI_API size_t kivi_decode_attention_noalloc_max_workspace(void);
 KIVI_API int kivi_decode_attention_noalloc(const kivi_dims *dims, const kivi_cache *cache,

@@ -138,6 +138,26 @@ def test_decode_argument_checks(L):
     assert L.kivi_decode_workspace_bytes(ctypes.byref(d), 8, 0) == 0
 
 
+def test_noalloc_reports_the_workspace_entry_points_statuses(L):
+    """Invalid arguments get the same status from the allocation-free entry point as
+    from kivi_decode_attention (its size check comes after every argument check)."""
+    d = _dims()
+
+    def both(c, Hq=8, q=FAKE, out=FAKE):
+        ref = L.kivi_decode_attention(ctypes.byref(d), ctypes.byref(c), q, Hq, 1.0, out, FAKE, 1 << 30, None)
+        got = L.kivi_decode_attention_noalloc(ctypes.byref(d), ctypes.byref(c), q, Hq, 1.0, out, None)
+        return ref, got
+
+    cases = [(_cache(n=0), {}), (_cache(n=300), {}), (_cache(n=257), {}), (_cache(n=-1), {}),
+             (_cache(n=10), dict(Hq=6)), (_cache(n=10), dict(Hq=32)), (_cache(n=10), dict(q=None)),
+             (_cache(n=10), dict(out=FAKE + 6)), (_cache(n=10, align=4), {}),
+             (kivi.kivi_cache(FAKE, 0, FAKE, FAKE, FAKE, FAKE, 10), {})]
+    for c, kw in cases:
+        ref, got = both(c, **kw)
+        assert ref != kivi.KIVI_OK and got == ref, (c.n_tokens, kw, ref, got)
+    assert both(_cache(n=300))[1] == kivi.KIVI_ERR_ARG  # n_tokens > max_tokens
+
+
 # ---- paged cache: geometry and argument checks on the host --------------------------
 def _pdims(**kw):
     d = dict(B=3, Hkv=4, D=128, G=32, bits=2, value_residual=0, page_tokens=64, max_pages_per_seq=5, num_pages=20)

@@ -88,6 +88,54 @@ def test_full_size_streaming():
         check_head(gpu, orc, b, kvh)
 
 
+def flush_neighbourhood(n0: int, G: int, steps: int, cycles: int = 2) -> set:
+    """Steps of a stream that starts at n0 tokens: the first two, and the step
+    before, at and after each of the first `cycles` key-group flushes (step i
+    appends token n0 + i; it flushes when (n0 + i) mod G == G - 1), and the last."""
+    first = (G - 1 - n0 % G) % G
+    picked = {0, 1, steps - 1}
+    for c in range(cycles):
+        f = first + c * G
+        picked |= {f - 1, f, f + 1}
+    return {s for s in picked if 0 <= s < steps}
+
+
+@pytest.mark.parametrize("idx,steps", [(1, 2 * 32 + 20), (3, 512)], ids=["llama2-7b-mha", "streaming"])
+def test_full_size_decode_step(idx, steps):
+    """kivi_decode_step, the call the benchmark times, at full size in the benchmark's
+    launch configuration (one workspace sized for the whole run, the attention grid
+    launched as a programmatic dependent of the append): every query head of sampled
+    KV heads against the oracle's append followed by its attention, on the steps
+    around two key-group flushes, and the sampled heads' final cache bit for bit."""
+    wl = synth.CONFIGS[idx]
+    pre = synth.make_prefill(wl)
+    T = wl.capacity(extra=steps)
+    gpu = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T)
+    kivi.kivi_quantize_prefill(gpu, pre.k.cuda(), pre.v.cuda())
+    R = wl.Hq // wl.Hkv
+    heads = sample_heads(wl, k=4, seed=idx + 11)
+    orcs = {h: oracle.prefill_head(pre.k[h[0], h[1]].numpy(), pre.v[h[0], h[1]].numpy(), wl.G, T) for h in heads}
+    nbytes = max(kivi.kivi_decode_workspace_bytes(gpu.dims, wl.Hq, n) for n in range(wl.n + 1, wl.n + steps + 1))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    check = flush_neighbourhood(wl.n, wl.G, steps)
+    checked = 0
+    for step in range(steps):
+        k_new, v_new, q = synth.make_step(wl, pre, step)
+        out = kivi.kivi_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, ws=ws)
+        for (b, kvh), orc in orcs.items():
+            oracle.append(orc, k_new[b, kvh][None, None].numpy().copy(), v_new[b, kvh][None, None].numpy().copy())
+        if step in check:
+            torch.cuda.synchronize()
+            for (b, kvh), orc in orcs.items():
+                ref = np.stack([oracle.attention_head(orc, 0, 0, q[b, kvh * R + j].numpy(), 1.0) for j in range(R)])
+                assert_close(out[b, kvh * R:(kvh + 1) * R], ref)
+            checked += 1
+    torch.cuda.synchronize()
+    assert gpu.n_tokens == wl.n + steps and checked == len(check) >= 8
+    for (b, kvh), orc in orcs.items():
+        check_head(gpu, orc, b, kvh)
+
+
 def check_paged_head(gpu: kivi.PagedCache, bt: np.ndarray, orc: oracle.Cache, b: int, kvh: int) -> None:
     """Sequence b, KV head kvh of the paged pool, gathered row by row through the
     block table, against the oracle's dense cache of that head."""
