@@ -291,7 +291,7 @@ def workload_config(wl):
 class DenseLayout:
     """The dense cache [B][Hkv][max_tokens]: kivi_decode_step / kivi_decode_attention."""
 
-    profile = "decode_attention_llama2-7b-mha.md"
+    profile_prefix = "decode_attention_"
     kernel = "kivi_decode_attention (decode_kernel + combine_kernel)"
 
     def __init__(self, wl, pre, dev, value_residual=False, bits=2):
@@ -332,7 +332,7 @@ class PagedLayout:
     """The paged pool: pages of P tokens scattered by a seeded permutation, lengths on
     the device: kivi_paged_decode_step / kivi_paged_decode_attention."""
 
-    profile = "decode_attention_paged_llama2-7b-mha.md"
+    profile_prefix = "decode_attention_paged_"
     kernel = "kivi_paged_decode_attention (paged decode_kernel + paged_combine_kernel)"
 
     def __init__(self, wl, pre, dev, page_tokens, graph=False, value_residual=False, bits=2):
@@ -482,7 +482,9 @@ def run_kivi(args, wl):
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
-    traffic = profiled_traffic(sha, lay.profile, wl.name,
+    # DRAM traffic from the committed ncu summary of this workload (named for it),
+    # when it was taken on the current decode sources; never for a changed batch
+    traffic = None if args.batch else profiled_traffic(sha, lay.profile_prefix + wl.name + ".md", wl.name,
                                f"bits={args.bits}, value_residual={int(bool(args.value_residual))}")
     del lay
 
@@ -715,6 +717,9 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt quantization (kivi_quantize_prefill) of the workload")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="run the workload's shape with this batch instead (for small profiling captures; "
+                         "the JSON line then names the batch in its config)")
     ap.add_argument("--workload", default="streaming",
                     help="workload name or unique prefix (tiny, llama2, mistral, streaming, long-gqa); "
                          "default: the streaming generation (B64, H32, 8192-token prompt, 512 steps), "
@@ -730,6 +735,10 @@ def main(argv=None):
     if len(hits) != 1:
         ap.error(f"--workload {args.workload!r}: choose one of {[w.name for w in synth.CONFIGS]}")
     wl = hits[0]
+    if args.batch:
+        import dataclasses
+
+        wl = dataclasses.replace(wl, B=args.batch)
     if args.compare_fp16:
         return run_compare(args)
     if args.impl == "reference":

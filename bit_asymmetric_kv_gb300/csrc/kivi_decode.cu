@@ -14,10 +14,13 @@
 //   * the codes enter as fp16 subnormals (exact, see unpack16);
 //   * the fp32 factors qs and p*s enter as an fp16 pair hi + lo (hi = fp16(x),
 //     lo = fp16(x - hi)), one per MMA column, which keeps ~22 significant bits;
-//     qs is first scaled by a power of two chosen per group so that its largest
-//     entry sits just below 2^14 (no fp16 overflow, full precision for any range).
+//     qs is scaled by a power of two per head, 2^(A - 15) with A putting the head's
+//     largest |q| just below 2^14: an fp16 scale is below 2^16, so every entry stays
+//     below 2^15 (no fp16 overflow) and the large entries keep full precision; an
+//     entry small enough for its lo part to fall among fp16 subnormals contributes
+//     at most 2^-25 absolute error in these units, negligible in the score.
 // Tokens are tiled by 16 (the MMA M dimension for q.K, the K dimension for P.V).
-// The 4 column pairs of an MMA carry (tile slot, query head): a softmax step covers
+// The 4 column pairs of an MMA carry (tile slot, query head): a round covers
 // T = 4/R tiles at once, so that for every R each lane owns the scores of one
 // (tile, head) pair: lane (g, tig) holds tokens g and g+8 of tile slot tig/R for
 // head tig%R.  For q.K the per-head factors are replicated over the slots and each
@@ -27,11 +30,22 @@
 // Work decomposition (persistent, balanced): a "unit" is 64 tokens of one (batch, KV
 // head) -- one or two key groups -- plus one unit for the fp16 residual keys when
 // n mod G > 0.  The grid holds exactly as many warps as fit on the GPU at once; warp
-// w takes the contiguous unit range [w*W/NW, (w+1)*W/NW), staging each unit (codes,
-// scales, zeros) in its shared memory with cp.async two units ahead, and runs an
-// online softmax over it.  At every head boundary the warp writes a partial (max,
-// sum, unnormalised output) to the workspace; the combine kernel merges a head's
-// partials (flash-decoding) and is launched as a programmatic dependent.
+// w takes the contiguous unit range [w*W/NW, (w+1)*W/NW).  At every head boundary
+// the warp writes a partial (max, sum, unnormalised output) to the workspace; the
+// combine kernel merges a head's partials (flash-decoding) and is launched as a
+// programmatic dependent.
+//
+// Staging: each warp owns a ring of stages in shared memory, filled one or two units
+// ahead of the one it computes.  One lane stages a unit with four linear bulk copies
+// (cp.async.bulk, executed by the TMA engine): key codes, value codes, value
+// {scale, zero} words and key-group {scale, zero} words, whose completion is counted
+// on the stage's mbarrier.  Every wait on an mbarrier is bounded: a warp whose copy
+// never completes records the fault, waits (bounded again) for its other copies and
+// stops; the combine then writes NaN outputs.
+//
+// One softmax update per unit for all R heads: the q.K MMAs of the unit's four
+// 16-token tiles come first (R rounds of T tiles), then the running maximum, the
+// probabilities and the P.V operand of every round, then the P.V MMAs.
 #include <math.h>
 
 #include <type_traits>
@@ -48,38 +62,45 @@ namespace kivi {
 
 namespace {
 
+// Set when a decode warp's wait for a staged unit ran out; the combine kernels then
+// write NaN outputs.  It stays set for the life of the process.
+__device__ int g_decode_fault = 0;
+
 constexpr int kWarps = kDecodeWarps;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
-// Units staged ahead of the one being computed (at most kStages - 1).
-#ifndef KIVI_DECODE_AHEAD
-#define KIVI_DECODE_AHEAD 2
-#endif
-constexpr int kAhead = KIVI_DECODE_AHEAD;
-static_assert(kAhead >= 1 && kAhead < kStages, "the ring must hold the computed unit and the staged ones");
-constexpr int kUnit = kDecodeUnit;                   // tokens per unit
-constexpr int kFragRowWords = 20;                    // 16 B-fragment words + 4 pad (bank spread)
+constexpr int kUnit = kDecodeUnit;  // tokens per unit
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+// Polls of a stage's mbarrier before a warp gives up on it.  Each poll may suspend
+// the warp for a short, hardware-chosen time, so this bound is far beyond the latency
+// of any copy.
+constexpr int kWaitPolls = 1 << 22;
 
-// Shared-memory layout of one warp's ring for BITS-bit codes.  4-bit rows are twice
-// as long, so their ring has two stages (one unit staged ahead) to keep two CTAs
-// per SM; 2-bit rows keep three.
+// Shared-memory layout of one warp: the ring of stages for BITS-bit codes, the q.K
+// B fragment of one key group, and one mbarrier per stage.  4-bit rows are twice as
+// long, so their ring has two stages (one unit staged ahead) to keep two CTAs per SM;
+// 2-bit rows keep three (two ahead).
 template <int R, int G, int BITS = 2>
 struct Layout {
   static constexpr int kRowBytes = 16 * BITS;                 // packed codes of one token row
-  static constexpr int kRowChunks = kRowBytes / 16;           // 16-byte copies per row
   static constexpr int kStages = BITS == 2 ? 3 : 2;
-  static constexpr int kAheadUnits = BITS == 2 ? kAhead : 1;  // units staged ahead of the computed one
+  static constexpr int kAhead = kStages - 1;                  // units staged ahead of the computed one
   static constexpr int kGroups = kUnit / G;                   // key groups per unit
   static constexpr int kKCodes = 0;                           // 64 rows
   static constexpr int kVCodes = kUnit * kRowBytes;           // 64 rows
   static constexpr int kVMeta = 2 * kUnit * kRowBytes;        // 64 x 4 B
   static constexpr int kKMeta = kVMeta + kUnit * 4;           // kGroups x 128 x 4 B
   static constexpr int kStageBytes = kKMeta + kGroups * kD * 4;
-  static constexpr int kFragGroupBytes = 8 * R * kFragRowWords * 4;  // rows 4*(2h+p)+tig
-  static constexpr int kWarpBytes = kStages * kStageBytes + kGroups * kFragGroupBytes;
+  // B fragment rows (2h + part) * 4 + tig of 16 words.  With fewer than four heads
+  // four lanes read each row, so rows are padded to 20 words to spread them over the
+  // shared-memory banks; with four heads every lane reads its own row.
+  static constexpr int kFragRowWords = R == 4 ? 16 : 20;
+  static constexpr int kFrag = kStages * kStageBytes;
+  static constexpr int kBars = kFrag + 8 * R * kFragRowWords * 4;
+  static constexpr int kWarpBytes = kBars + 32;               // kStages mbarriers of 8 bytes
   static constexpr int kSmem = kWarps * kWarpBytes;
-  static_assert(kAheadUnits >= 1 && kAheadUnits < kStages, "the ring holds the computed unit and the staged ones");
+  static_assert(kStages * 8 <= 32, "the barrier block holds every stage's mbarrier");
+  static_assert(kStageBytes % 16 == 0 && kFrag % 16 == 0 && kBars % 16 == 0, "16-byte aligned regions");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -92,6 +113,41 @@ __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) 
 
 __device__ __forceinline__ uint2 lds64(const unsigned char *p) { return *reinterpret_cast<const uint2 *>(p); }
 __device__ __forceinline__ uint32_t lds32(const unsigned char *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
+// ---- mbarriers and bulk copies (TMA engine), all on this CTA's shared memory ----------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(bar) : "memory");
+}
+
+// This thread's arrival on `bar`, with `bytes` more bytes expected in the phase.
+__device__ __forceinline__ void mbar_arm(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Linear global -> shared copy of `bytes` (a multiple of 16, both ends 16-byte
+// aligned); its completion is counted on `bar`.
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Wait until the phase of parity `parity` of `bar` has completed; false if it did not
+// within kWaitPolls polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kWaitPolls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
 
 __device__ __forceinline__ void load_frag(const unsigned char *row, uint32_t bf[16]) {
   const uint4 *p = reinterpret_cast<const uint4 *>(row);
@@ -106,7 +162,8 @@ __device__ __forceinline__ void load_frag(const unsigned char *row, uint32_t bf[
 }
 
 // q.K of one 16-token tile: A from the unpacked codes (or fp16 keys) of token g
-// (ra*) and g+8 (rb*), words 2tig (..0) and 2tig+1 (..1); accumulates into sc.
+// (ra*) and g+8 (rb*), words 2tig (..0) and 2tig+1 (..1); accumulates into sc.  The
+// two words accumulate in separate chains of four MMAs (shorter dependences).
 __device__ __forceinline__ void qk_tile(const uint32_t ra0[8], const uint32_t ra1[8], const uint32_t rb0[8],
                                         const uint32_t rb1[8], const uint32_t bf[16], float sc[4]) {
   float s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -150,11 +207,41 @@ __device__ __forceinline__ void pv_tile4(float acc[8][4], const uint2 v[4], uint
   for (int j = 0; j < 8; ++j) mma16816(acc[j], a01[0][j], a01[1][j], a23[0][j], a23[1][j], bw0, bw1);
 }
 
-// 32 fp16 keys (channels 32tig .. 32tig+31) of one residual token, paired (m, m+8)
-// like the unpacked codes.
+// P.V of one 16-token tile over fp16 values (the value residual): A is built from
+// the fp16 values of tokens tig, tig+4, tig+8, tig+12 of the tile (channels 16g + j
+// and 16g + 8 + j for MMA j) instead of unpacked codes.  `rows` points at the tile's
+// first token row; tokens at or beyond n_valid read as zero.
+__device__ __forceinline__ void pv_tile_f16(float acc[8][4], const uint16_t *rows, int n_valid, int g, int tig,
+                                            uint32_t b0, uint32_t b1) {
+  uint32_t w[4][8];  // token tig + 4k: channels 16g .. 16g+15 as 8 half2 words
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int tok = tig + 4 * k;
+    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+    if (tok < n_valid) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(rows + tok * kD + 16 * g);
+      lo = __ldg(src);
+      hi = __ldg(src + 1);
+    }
+    w[k][0] = lo.x; w[k][1] = lo.y; w[k][2] = lo.z; w[k][3] = lo.w;
+    w[k][4] = hi.x; w[k][5] = hi.y; w[k][6] = hi.z; w[k][7] = hi.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+    const int x = j >> 1, y = 4 + (j >> 1);  // words of channels 16g + j and 16g + 8 + j
+    mma16816(acc[j], prmt(w[0][x], w[1][x], sel), prmt(w[0][y], w[1][y], sel), prmt(w[2][x], w[3][x], sel),
+             prmt(w[2][y], w[3][y], sel), b0, b1);
+  }
+}
+
+// 32 fp16 keys (channels 32tig .. 32tig+31) of one residual token, paired like the
+// unpacked codes of the BITS-bit path: 2-bit r[i] = {channel i, i + 8} of each
+// 16-channel half, 4-bit r[4a + t] = {channel 8a + t, 8a + t + 4}.
+template <int BITS>
 __device__ __forceinline__ void residual_pairs(const uint16_t *row, bool valid, int tig, uint32_t r0[8],
                                                uint32_t r1[8]) {
-  uint32_t p[16];
+  uint32_t p[16];  // p[k]: channels 32tig + 2k (low half) and 32tig + 2k + 1
   if (valid) {
     const uint4 *src = reinterpret_cast<const uint4 *>(row + 32 * tig);
 #pragma unroll
@@ -171,23 +258,25 @@ __device__ __forceinline__ void residual_pairs(const uint16_t *row, bool valid, 
   }
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
+    int lo, hi;
+    if constexpr (BITS == 2) {
+      lo = m >> 1;
+      hi = (m >> 1) + 4;
+    } else {
+      lo = 4 * (m >> 2) + ((m & 3) >> 1);
+      hi = lo + 2;
+    }
     const uint32_t sel = (m & 1) ? 0x7632u : 0x5410u;
-    r0[m] = prmt(p[m >> 1], p[(m >> 1) + 4], sel);
-    r1[m] = prmt(p[8 + (m >> 1)], p[8 + (m >> 1) + 4], sel);
+    r0[m] = prmt(p[lo], p[hi], sel);
+    r1[m] = prmt(p[8 + lo], p[8 + hi], sel);
   }
 }
 
 // Index of the first warp whose unit range contains unit u.
 __device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t NW) { return ((u + 1) * NW - 1) / W; }
 
-// Per-lane constants of the fragment bookkeeping.
-struct LaneInfo {
-  int g, tig, slot_mine, pv_slot, src_a, src_b;
-  uint32_t pv_sel;
-};
-
-// Softmax state of the q.K side: running max (log2 domain, per head) and this
-// lane's shares of sum_t p_t and sum_t p_t z_t.
+// Softmax state of a head: running max (log2 domain) and this lane's shares of
+// sum_t p_t and sum_t p_t z_t.
 struct SoftState {
   float m, l, zs;
 };
@@ -199,102 +288,65 @@ __device__ __forceinline__ float head_max(float x) {
     // one head per warp: an order-preserving integer key and one warp reduction
     const int k = __float_as_int(x);
     const int key = k ^ ((k >> 31) & 0x7fffffff);
-    const int mk = __reduce_max_sync(0xffffffffu, key);
+    const int mk = __reduce_max_sync(kFull, key);
     return __int_as_float(mk ^ ((mk >> 31) & 0x7fffffff));
   } else {
 #pragma unroll
-    for (int off = R; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    for (int off = R; off < 32; off <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
     return x;
   }
 }
 
-// q.K side of one softmax step over T = 4/R tiles of 16 tokens.
-//   kfill(i, sc)  accumulates tile slot i's q.K MMA into sc[4];
-//   cq, beta      this lane's score scale and offset (log2 domain);
-//   n_valid       tokens of the step that exist (FULL: all 16*T);
-//   vmeta(tok)    {s, z} of step token tok.
-// Returns the P.V B operand of this lane (bw0, bw1) and the rescale factor alpha
-// that the P.V accumulators need before this step's contribution is added.
-template <int R, bool FULL, class KF, class VM>
-__device__ __forceinline__ void qk_step(SoftState &st, const LaneInfo &li, KF &&kfill, float cq, float beta,
-                                        int n_valid, VM &&vmeta, uint32_t &bw0, uint32_t &bw1, float &alpha) {
-  constexpr int T = 4 / R;
-  float S[T][4];
+// Warp sums of the q . z partials v[gi][h] (gi < NG key groups, h < R heads),
+// delivered where they are used: afterwards v[gi][0] holds, for every group, the sum
+// for this lane's head h = tig % R.  The heads are first scattered over lane bits
+// 0 .. log2(R) - 1 (each exchange sends the half of the heads that the partner keeps),
+// then the other lane bits are summed by a butterfly.  With one head and two groups
+// the group is scattered over lane bit 1 instead (lane tig reads tile slot tig, whose
+// group is tig >> 1), and v[0][0] = v[1][0] holds the lane's group's sum.
+template <int R, int NG>
+__device__ __forceinline__ void beta_reduce_heads(float (&v)[NG][R], int lane);
+
+template <int R, int NG>
+__device__ __forceinline__ void beta_reduce(float (&v)[NG][R], int lane) {
+  if constexpr (R == 1 && NG == 2) {
+    const bool up = (lane >> 1) & 1;
+    const float keep = up ? v[1][0] : v[0][0], send = up ? v[0][0] : v[1][0];
+    float s = keep + __shfl_xor_sync(kFull, send, 2);
+    s += __shfl_xor_sync(kFull, s, 1);
 #pragma unroll
-  for (int i = 0; i < T; ++i) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) S[i][k] = 0.f;
-    if (FULL || 16 * i < n_valid) kfill(i, S[i]);
+    for (int off = 4; off < 32; off <<= 1) s += __shfl_xor_sync(kFull, s, off);
+    v[0][0] = v[1][0] = s;
+  } else {
+    beta_reduce_heads<R, NG>(v, lane);
   }
-  float d[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) d[k] = S[0][k];
-#pragma unroll
-  for (int i = 1; i < T; ++i)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) d[k] = (li.slot_mine == i) ? S[i][k] : d[k];
-  const int ta = 16 * li.slot_mine + li.g, tb = ta + 8;  // this lane's tokens in the step
-  const bool va = FULL || ta < n_valid, vb = FULL || tb < n_valid;
-  const float sa = va ? fmaf(cq, d[0] + d[1], beta) : -INFINITY;
-  const float sb = vb ? fmaf(cq, d[2] + d[3], beta) : -INFINITY;
-  const float m_new = fmaxf(st.m, head_max<R>(fmaxf(sa, sb)));
-  alpha = ex2(st.m - m_new);  // st.m = -inf at the start of a head: alpha = 0
-  st.m = m_new;
-  const uint32_t vma = vmeta(va ? ta : 0), vmb = vmeta(vb ? tb : 0);
-  const float pa = va ? ex2(sa - m_new) : 0.f;
-  const float pb = vb ? ex2(sb - m_new) : 0.f;
-  const float2 fa = __half22float2(u2h2(vma)), fb = __half22float2(u2h2(vmb));  // {s, z}
-  const float sva = va ? fa.x : 0.f, zva = va ? fa.y : 0.f;
-  const float svb = vb ? fb.x : 0.f, zvb = vb ? fb.y : 0.f;
-  st.l = fmaf(st.l, alpha, pa + pb);
-  st.zs = fmaf(st.zs, alpha, fmaf(pa, zva, pb * zvb));
-  const float wa = pa * sva, wb = pb * svb;
-  // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
-  const __half2 hab = __floats2half2_rn(wa, wb);
-  const float2 fab = __half22float2(hab);
-  const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
-  const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
-  const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
-  // B of P.V for tile slot pv_slot, column g = (slot, head, part): K slots
-  // 2tig, 2tig+1, 2tig+8, 2tig+9 hold tokens tig, tig+4, tig+8, tig+12; token u's
-  // weight lives in lane 4*(u%8) + (g>>1) (first token if u < 8, else second)
-  const uint32_t a1 = __shfl_sync(0xffffffffu, q1, li.src_a);
-  const uint32_t b1 = __shfl_sync(0xffffffffu, q1, li.src_b);
-  const uint32_t a2 = __shfl_sync(0xffffffffu, q2, li.src_a);
-  const uint32_t b2 = __shfl_sync(0xffffffffu, q2, li.src_b);
-  bw0 = prmt(a1, b1, li.pv_sel);
-  bw1 = prmt(a2, b2, li.pv_sel);
 }
 
-// P.V side of one step: rescale the accumulators, then add the T tiles.
-//   vword(i, k)   word g of the value row of token tig + 4k of tile slot i.
-template <int R, int BITS, class VW>
-__device__ __forceinline__ void pv_step(float acc[8][4], const LaneInfo &li, int n_valid, uint32_t bw0, uint32_t bw1,
-                                        float alpha, VW &&vword) {
-  constexpr int T = 4 / R;
-  if (__any_sync(0xffffffffu, alpha != 1.f)) {
+template <int R, int NG>
+__device__ __forceinline__ void beta_reduce_heads(float (&v)[NG][R], int lane) {
+  if constexpr (R >= 2) {
+    const bool up = lane & 1;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int gi = 0; gi < NG; ++gi)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) acc[j][k] *= alpha;
-  }
-#pragma unroll
-  for (int i = 0; i < T; ++i) {
-    if (16 * i < n_valid) {
-      const bool mine = li.pv_slot == i;
-      if constexpr (BITS == 2) {
-        uint32_t v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
-        pv_tile(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
-      } else {
-        uint2 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = vword(i, k);
-        pv_tile4(acc, v, mine ? bw0 : 0u, mine ? bw1 : 0u);
+      for (int i = 0; i < R / 2; ++i) {
+        const float keep = up ? v[gi][2 * i + 1] : v[gi][2 * i];
+        const float send = up ? v[gi][2 * i] : v[gi][2 * i + 1];
+        v[gi][i] = keep + __shfl_xor_sync(kFull, send, 1);
       }
+  }
+  if constexpr (R == 4) {
+    const bool up = (lane >> 1) & 1;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const float keep = up ? v[gi][1] : v[gi][0], send = up ? v[gi][0] : v[gi][1];
+      v[gi][0] = keep + __shfl_xor_sync(kFull, send, 2);
     }
   }
+#pragma unroll
+  for (int off = R; off < 32; off <<= 1)
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) v[gi][0] += __shfl_xor_sync(kFull, v[gi][0], off);
 }
 
 // Position of a warp's cursor: head h = b * Hkv + kvh, unit uu of the head, and the
@@ -340,7 +392,7 @@ __device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
   int inc = loc;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    const int y = __shfl_up_sync(kFull, inc, off);
     if (lane >= off) inc += y;
   }
   if (lane == 31) s_tot[warp] = inc;
@@ -357,60 +409,19 @@ __device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
   __syncthreads();
 }
 
-// P.V of one step over fp16 values (the value residual): the same tile and column
-// layout as pv_step, with A built from the values of tokens tig, tig+4, tig+8,
-// tig+12 of each tile (channels 16g + j and 16g + 8 + j for MMA j) instead of
-// unpacked codes.  `rows` points at the step's first token row; tokens at or beyond
-// n_valid read as zero.  The accumulators must hold output units (no code factors).
-template <int R>
-__device__ __forceinline__ void pv_step_f16(float acc[8][4], const LaneInfo &li, int n_valid, uint32_t bw0,
-                                            uint32_t bw1, float alpha, const uint16_t *rows) {
-  constexpr int T = 4 / R;
-  if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[j][k] *= alpha;
-  }
-#pragma unroll
-  for (int i = 0; i < T; ++i) {
-    if (16 * i < n_valid) {
-      uint32_t w[4][8];  // token tig + 4k: channels 16g .. 16g+15 as 8 half2 words
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int tok = 16 * i + li.tig + 4 * k;
-        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-        if (tok < n_valid) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(rows + tok * kD + 16 * li.g);
-          lo = __ldg(src);
-          hi = __ldg(src + 1);
-        }
-        w[k][0] = lo.x; w[k][1] = lo.y; w[k][2] = lo.z; w[k][3] = lo.w;
-        w[k][4] = hi.x; w[k][5] = hi.y; w[k][6] = hi.z; w[k][7] = hi.w;
-      }
-      const bool mine = li.pv_slot == i;
-      const uint32_t b0 = mine ? bw0 : 0u, b1 = mine ? bw1 : 0u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-        const int x = j >> 1, y = 4 + (j >> 1);  // words of channels 16g + j and 16g + 8 + j
-        mma16816(acc[j], prmt(w[0][x], w[1][x], sel), prmt(w[0][y], w[1][y], sel), prmt(w[2][x], w[3][x], sel),
-                 prmt(w[2][y], w[3][y], sel), b0, b1);
-      }
-    }
-  }
-}
-
 template <int R, int G, bool PAGED, int BITS>
 __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   using L = Layout<R, G, BITS>;
   constexpr int WPR = words_per_row<BITS>();
-  constexpr int kStages = L::kStages;
-  constexpr int kAhead = L::kAheadUnits;
-  constexpr int T = 4 / R;           // tile slots per softmax step
-  constexpr int TPG = G / 16;        // tiles per key group
-  constexpr int NGU = L::kGroups;    // key groups per unit
+  constexpr int S = L::kStages;
+  constexpr int AH = L::kAhead;
+  constexpr int T = 4 / R;                 // tile slots per round
+  constexpr int TPG = G / 16;              // tiles per key group
+  constexpr int NGU = L::kGroups;          // key groups per unit
+  constexpr int FRW = L::kFragRowWords;
+  constexpr int SH = BITS == 2 ? 18 : 20;  // a q.K MMA product is code * qs * 2^(E - SH) for B scaled by 2^E
+  constexpr int PD = BITS == 2 ? 8 : 4;    // channel distance of the two codes of an unpacked register
   // the combine grid may launch now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -445,48 +456,72 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   const int n_my = (int)(u1 - u0);
 
   unsigned char *wbase = smem + warp * L::kWarpBytes;
-  unsigned char *frag = wbase + kStages * L::kStageBytes;
+  unsigned char *frag = wbase + L::kFrag;
+  const uint32_t bar0 = smem_addr(wbase + L::kBars);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
   const float c0 = a.softmax_scale * kLog2e;
 
-  LaneInfo li;
-  li.g = lane >> 2;
-  li.tig = lane & 3;
-  li.slot_mine = li.tig / R;
-  li.pv_slot = (li.g >> 1) / R;
-  li.src_a = 4 * li.tig + (li.g >> 1);
-  li.src_b = li.src_a + 16;
-  li.pv_sel = (li.g & 1) ? 0x7632u : 0x5410u;
-  const int g = li.g, tig = li.tig;
-  const int head_mine = tig % R;
+  // ---- lane roles in the MMAs
+  const int g = lane >> 2, tig = lane & 3;
+  const int head_mine = tig % R, slot_mine = tig / R;
+  const int pv_slot = (g >> 1) / R;
+  const int src_a = 4 * tig + (g >> 1), src_b = src_a + 16;
+  const uint32_t pv_sel = (g & 1) ? 0x7632u : 0x5410u;
   const int frag_row = 4 * (2 * ((g >> 1) % R) + (g & 1)) + tig;
-  // prep: channel c = lane + 32k lands in row 4*(2h+p) + k, half-word wh of the row
-  // (the same position for the channels lane + 32k of every k: the row differs).
-  // wh_pairs is the order of the fp16 residual keys (residual_pairs), which is also
-  // the order of the unpacked 2-bit codes: B half-word 2i + d of lane tig holds
-  // channel 32tig + 16(i >= 8) + (i mod 8) + 8d.
-  int wh_pairs;
-  {
-    const int i = lane & 15, i8 = i & 7;
-    const int j = 4 * (lane >> 4) + (i8 >> 1);
-    wh_pairs = (2 * j + (i8 & 1)) * 2 + (i >= 8 ? 1 : 0);
-  }
-  int wh;
-  float mult;
-  if constexpr (BITS == 2) {
-    wh = wh_pairs;
-    // codes of channel index i (mod 16) are unpacked with factor 4^(i mod 4);
-    // 4^(3 - i mod 4) brings every q.K product to code * qs * 64
-    mult = (float)(64 >> (2 * (lane & 3)));
-  } else {
-    // B half-word 2i + d holds channel 32tig + 16(i >= 8) + 8q + t + 4d, i = 8(i >= 8) + 4q + t
-    const int t = lane & 3, d = (lane >> 2) & 1, q = (lane >> 3) & 1, s16 = lane >> 4;
-    wh = 2 * (8 * s16 + 4 * q + t) + d;
-    // channel position t is unpacked with factor 16^(t mod 2); 16^(1 - t mod 2) brings
-    // every q.K product to code * qs * 16
-    mult = (t & 1) ? 1.f : 16.f;
-  }
+  // ---- lane roles in the factor preparation: B registers 8w + 2j and 8w + 2j + 1 of
+  // fragment row tig' (tig' = lane >> 3, w = bit 2, j = bits 0-1).  Like the unpacked
+  // codes they meet, register 8w + 2j pairs channels pc and pc + PD, register
+  // 8w + 2j + 1 channels pc + 1 and pc + PD + 1; fa and fb are the powers of two that
+  // bring each register's products to code * qs * 2^-SH (the codes' own factors are
+  // 4^(i mod 4) for 2-bit register i, 16^(i mod 2) for 4-bit register i).
+  const int pt = lane >> 3, pw = (lane >> 2) & 1, pj = lane & 3;
+  const int pc = BITS == 2 ? 32 * pt + 16 * pw + 2 * pj : 32 * pt + 16 * pw + 8 * (pj >> 1) + 2 * (pj & 1);
+  const int pword = 8 * pw + 2 * pj;
+  const float fa = BITS == 2 ? ((pj & 1) ? 4.f : 64.f) : 16.f;
+  const float fb = BITS == 2 ? ((pj & 1) ? 1.f : 16.f) : 1.f;
+  const float ifa = 1.f / fa, ifb = 1.f / fb;
 
-  // ---- cursors: ic stages unit u0 + kk (one ahead), cc computes it
+  // ---- the query heads of the current KV head: q of this lane's preparation
+  // channels (pc, pc + PD, pc + 1, pc + PD + 1) times fa / fb and 2^(A_h - 15), where
+  // A_h puts the head's largest |q * f| below 2^14; an fp16 scale lies below 2^16, so
+  // each B entry qa * s stays below 2^15
+  float qa[R][4];
+  float cqh = 0.f, cbh = 0.f;  // c0 * 2^(SH - A + 15) and c0 * 2^(15 - A) of this lane's head
+  auto q_row = [&](int64_t b, int64_t kvh) { return a.q + (b * a.Hq + kvh * R) * kD; };
+  auto load_q = [&](const uint16_t *qh) {
+#pragma unroll
+    for (int hh = 0; hh < R; ++hh) {
+      const uint32_t w01 = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc));
+      const uint32_t wd = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc + PD));
+      float x[4];
+      x[0] = h2f((uint16_t)(w01 & 0xffffu)) * fa;
+      x[1] = h2f((uint16_t)(wd & 0xffffu)) * fa;
+      x[2] = h2f((uint16_t)(w01 >> 16)) * fb;
+      x[3] = h2f((uint16_t)(wd >> 16)) * fb;
+      const float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(mx));
+      const int A = min(100, max(-90, 13 - ((int)(mb >> 23) - 127)));
+      const float sc = pow2i(A - 15);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) qa[hh][k] = x[k] * sc;
+      if (hh == head_mine) {
+        cqh = c0 * pow2i(SH - A + 15);
+        cbh = c0 * pow2i(15 - A);
+      }
+    }
+  };
+  // head of a dense cursor
+  auto head_bk = [&](int64_t h, int64_t &b, int64_t &kvh) {
+    b = h / a.Hkv;
+    kvh = h - b * a.Hkv;
+  };
+
+  // ---- cursors: ic stages unit u0 + kk (ahead), cc computes it
   Cursor ic;
   if constexpr (PAGED) {
     // the sequence holding unit u0: the last b with Hkv * cum[b] <= u0 (it has units)
@@ -525,6 +560,16 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       }
     }
   };
+  auto cursor_q = [&](const Cursor &c) {
+    int64_t b, kvh;
+    if constexpr (PAGED) {
+      b = c.b;
+      kvh = c.kvh;
+    } else {
+      head_bk(c.h, b, kvh);
+    }
+    return q_row(b, kvh);
+  };
   // page of token tok of sequence b (ids outside the pool are clamped into it: the
   // caller's block table is trusted for values, never for addresses)
   auto page_of = [&](int b, int tok) -> int64_t {
@@ -537,18 +582,20 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   }
 
   bool waited = false;
+  uint32_t armed = 0;  // stages with copies in flight (the same in every lane)
   auto issue = [&](int kk) {
+    if (kk >= n_my) return;
     // the last unit of a head holds the token a preceding append just wrote: when
     // this grid was launched as a programmatic dependent of that append, wait for it
-    if (a.wait_tail && !waited && kk < n_my && ic.uu == ic.U - 1) {
+    if (a.wait_tail && !waited && ic.uu == ic.U - 1) {
       asm volatile("griddepcontrol.wait;\n" ::: "memory");
+      asm volatile("fence.proxy.async;\n" ::: "memory");  // its writes, for the bulk copies too
       waited = true;
     }
-    if (kk < n_my && ic.uu < ic.ncu) {
+    if (ic.uu < ic.ncu) {
       const int g0 = ic.uu * NGU;
       const int ngr = min(NGU, ic.NG - g0);  // 1 or 2 groups (G = 32)
       const int rows = ngr * G;
-      unsigned char *stg = wbase + (kk % kStages) * L::kStageBytes;
       int64_t row0, grp0;
       if constexpr (PAGED) {
         const int64_t ph = pg_next * a.Hkv + ic.kvh;
@@ -559,29 +606,20 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         row0 = ic.h * a.max_tokens + (int64_t)g0 * G;
         grp0 = ic.h * (a.max_tokens / G) + g0;
       }
-      const unsigned char *kc = reinterpret_cast<const unsigned char *>(a.k_codes + row0 * WPR);
-      const unsigned char *vc = reinterpret_cast<const unsigned char *>(a.v_codes + row0 * WPR);
-      const unsigned char *vm = reinterpret_cast<const unsigned char *>(a.v_meta + row0);
-      const unsigned char *km = reinterpret_cast<const unsigned char *>(a.k_meta + grp0 * kD);
-      if (rows == kUnit) {
-#pragma unroll
-        for (int c = lane; c < kUnit * L::kRowChunks; c += 32) {
-          cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
-          cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
-        }
-        if (lane < kUnit / 4) cp_async16(stg + L::kVMeta + lane * 16, vm + lane * 16);
-#pragma unroll
-        for (int c = lane; c < NGU * 32; c += 32) cp_async16(stg + L::kKMeta + c * 16, km + c * 16);
-      } else {
-        for (int c = lane; c < rows * L::kRowChunks; c += 32) {
-          cp_async16(stg + L::kKCodes + c * 16, kc + c * 16);
-          cp_async16(stg + L::kVCodes + c * 16, vc + c * 16);
-        }
-        if (lane < rows / 4) cp_async16(stg + L::kVMeta + lane * 16, vm + lane * 16);
-        for (int c = lane; c < ngr * 32; c += 32) cp_async16(stg + L::kKMeta + c * 16, km + c * 16);
+      const int st = kk % S;
+      if (lane == 0) {
+        const uint32_t bar = bar0 + 8 * st;
+        const uint32_t dst = smem_addr(wbase + st * L::kStageBytes);
+        const uint32_t cb = (uint32_t)rows * L::kRowBytes;
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        mbar_arm(bar, 2 * cb + (uint32_t)rows * 4 + (uint32_t)ngr * kD * 4);
+        bulk_copy(dst + L::kKCodes, a.k_codes + row0 * WPR, cb, bar);
+        bulk_copy(dst + L::kVCodes, a.v_codes + row0 * WPR, cb, bar);
+        bulk_copy(dst + L::kVMeta, a.v_meta + row0, (uint32_t)rows * 4, bar);
+        bulk_copy(dst + L::kKMeta, a.k_meta + grp0 * kD, (uint32_t)ngr * kD * 4, bar);
       }
+      armed |= 1u << st;
     }
-    cp_async_commit();
     advance(ic);
     if constexpr (PAGED) {
       if (kk + 1 < n_my && ic.uu < ic.ncu) pg_next = page_of(ic.b, ic.uu * kUnit);
@@ -594,7 +632,6 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
-  float qv[R][4];
 
   // Write the partial of head h (this warp's share of it) from the P.V accumulators
   // and the softmax state (m, l, zs) that belongs to them.  acc_true: the
@@ -604,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     float l = fin.l, zs = fin.zs;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-      l += __shfl_xor_sync(0xffffffffu, l, off);
-      zs += __shfl_xor_sync(0xffffffffu, zs, off);
+      l += __shfl_xor_sync(kFull, l, off);
+      zs += __shfl_xor_sync(kFull, zs, off);
     }
     float o[16];
 #pragma unroll
@@ -616,12 +653,12 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     // sum the tile slots of the same head (tig bits above the head bits)
 #pragma unroll
     for (int off = R; off < 4; off <<= 1) {
-      l += __shfl_xor_sync(0xffffffffu, l, off);
-      zs += __shfl_xor_sync(0xffffffffu, zs, off);
+      l += __shfl_xor_sync(kFull, l, off);
+      zs += __shfl_xor_sync(kFull, zs, off);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) o[j] += __shfl_xor_sync(0xffffffffu, o[j], off);
+      for (int j = 0; j < 16; ++j) o[j] += __shfl_xor_sync(kFull, o[j], off);
     }
-    if (li.slot_mine == 0) {
+    if (slot_mine == 0) {
       float *dst;
       if constexpr (PAGED) {
         // pair index gw + h grows strictly along the unit order: unique per (warp, head)
@@ -633,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        // undo the code factor 4^(j mod 4) and the 2^-24 of the subnormal codes
+        // undo the code factor 4^(j mod 4) (16^(j mod 2)) and the 2^-24 of the subnormal codes
         const float un = acc_true ? 1.f : pow2i(BITS == 2 ? 24 - 2 * (j & 3) : 24 - 4 * (j & 1));
         dst[16 * g + j] = fmaf(o[j], un, zs);
         dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs);
@@ -649,220 +686,271 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       for (int k = 0; k < 4; ++k) acc[j][k] = 0.f;
     acc_true = false;
   };
-  auto load_q = [&](const Cursor &c) {
-    int64_t b, kvh;
-    if constexpr (PAGED) {
-      b = c.b;
-      kvh = c.kvh;
-    } else {
-      b = c.h / a.Hkv;
-      kvh = c.h - b * a.Hkv;
+
+  // One softmax update for a unit: sc[rho] holds the q.K accumulators of this lane's
+  // tile slot in round rho (tile rho*T + slot_mine, tokens g and g + 8, hi and lo
+  // columns); cq_of(rho), be_of(rho) are that tile's score scale and offset (log2
+  // domain), ntok the unit's valid tokens, vmeta(tok) the {s, z} word of its token tok.
+  // Builds the P.V B operand of every round (bw0, bw1) and returns the factor alpha
+  // that the P.V accumulators need before this unit's contribution is added.
+  auto update = [&](auto full_tag, const float (&sc)[R][4], auto &&cq_of, auto &&be_of, int ntok, auto &&vmeta,
+                    uint32_t (&bw0)[R], uint32_t (&bw1)[R]) -> float {
+    constexpr bool FULL = decltype(full_tag)::value;
+    float sv[R][2];
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho) {
+      const int ta = 16 * (rho * T + slot_mine) + g;
+      const bool va = FULL || ta < ntok, vb = FULL || ta + 8 < ntok;
+      const float cqv = cq_of(rho), bev = be_of(rho);
+      sv[rho][0] = va ? fmaf(cqv, sc[rho][0] + sc[rho][1], bev) : -INFINITY;
+      sv[rho][1] = vb ? fmaf(cqv, sc[rho][2] + sc[rho][3], bev) : -INFINITY;
+      mloc = fmaxf(mloc, fmaxf(sv[rho][0], sv[rho][1]));
     }
-    const uint16_t *qh = a.q + (b * a.Hq + kvh * R) * kD + lane;
+    const float m_new = fmaxf(ss.m, head_max<R>(mloc));
+    const float alpha = ex2(ss.m - m_new);  // ss.m = -inf at the start of a head: alpha = 0
+    ss.m = m_new;
+    float lsum = 0.f, zsum = 0.f;
 #pragma unroll
-    for (int hh = 0; hh < R; ++hh)
+    for (int rho = 0; rho < R; ++rho) {
+      const int ta = 16 * (rho * T + slot_mine) + g;
+      const bool va = FULL || ta < ntok, vb = FULL || ta + 8 < ntok;
+      const float pa = ex2(sv[rho][0] - m_new), pb = ex2(sv[rho][1] - m_new);
+      const float2 fva = __half22float2(u2h2(vmeta(va ? ta : 0)));
+      const float2 fvb = __half22float2(u2h2(vmeta(vb ? ta + 8 : 0)));
+      const float sva = va ? fva.x : 0.f, zva = va ? fva.y : 0.f;
+      const float svb = vb ? fvb.x : 0.f, zvb = vb ? fvb.y : 0.f;
+      lsum += pa + pb;
+      zsum = fmaf(pa, zva, fmaf(pb, zvb, zsum));
+      const float wa = pa * sva, wb = pb * svb;
+      // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
+      const __half2 hab = __floats2half2_rn(wa, wb);
+      const float2 fab = __half22float2(hab);
+      const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
+      const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
+      const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
+      // B of P.V, column g = (slot, head, part): K slots 2tig, 2tig+1, 2tig+8, 2tig+9
+      // hold tokens tig, tig+4, tig+8, tig+12; token u's weight lives in lane
+      // 4*(u%8) + (g>>1) (first token if u < 8, else second)
+      const uint32_t a1 = __shfl_sync(kFull, q1, src_a), b1 = __shfl_sync(kFull, q1, src_b);
+      const uint32_t a2 = __shfl_sync(kFull, q2, src_a), b2 = __shfl_sync(kFull, q2, src_b);
+      bw0[rho] = prmt(a1, b1, pv_sel);
+      bw1[rho] = prmt(a2, b2, pv_sel);
+    }
+    ss.l = fmaf(ss.l, alpha, lsum);
+    ss.zs = fmaf(ss.zs, alpha, zsum);
+    return alpha;
+  };
+  auto rescale = [&](float alpha) {
+    if (__any_sync(kFull, alpha != 1.f)) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) qv[hh][k] = h2f(qh[hh * kD + 32 * k]);
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[j][k] *= alpha;
+    }
+  };
+  // keep tile slot i's q.K accumulators in out if it is this lane's slot (slot 0
+  // initialises out)
+  auto keep_slot = [&](int i, const float (&s4)[4], float (&out)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out[k] = (i == 0 || slot_mine == i) ? s4[k] : out[k];
   };
 
-  load_q(cc);
+  // ---- a unit of quantized keys: ntok = 64 tokens, or 32 for a trailing single group
+  auto code_unit = [&](auto full_tag, const unsigned char *stg, int ntok) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const int ngr = FULL ? NGU : ntok / G;
+    // key codes, 2-bit: words 2tig, 2tig+1 of tokens g and g+8 (channels 32tig ..
+    // 32tig+31).  With one head all four tiles are in the first round; their codes are
+    // loaded before the factor preparation, so that the loads' latency overlaps it.
+    auto kcodes = [&](int t, uint2 (&kw)[2]) {
+      kw[0] = lds64(stg + L::kKCodes + (16 * t + g) * 32 + tig * 8);
+      kw[1] = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
+    };
+    uint2 kw0[T][2];
+    if constexpr (BITS == 2 && R == 1) {
 #pragma unroll
-  for (int kk = 0; kk < kAhead; ++kk) issue(kk);
-
-  for (int kk = 0; kk < n_my; ++kk) {
-    issue(kk + kAhead);
-    if constexpr (PAGED) {
-      // the warp that takes a head's first unit publishes where its partials go
-      if (cc.uu == 0 && lane == 0) {
-        const int64_t start = (int64_t)a.Hkv * s_cum[cc.b] + (int64_t)cc.kvh * cc.U;
-        const int64_t last = owner_warp(start + cc.U - 1, W, NW);
-        hdr[cc.h] = make_int2((int)(gw + cc.h), (int)(last - gw + 1));
-      }
+      for (int i = 0; i < T; ++i)
+        if (FULL || 16 * i < ntok) kcodes(i, kw0[i]);
     }
-    cp_async_wait<kAhead>();
-    __syncwarp();
-    const int stage = kk % kStages;
-    uint32_t nw0[R], nw1[R];
-    float nalpha[R];
+    // per key group: this lane's scales, the q . z partials of every head
+    float sp[NGU][4], bv[NGU][R];
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      nw0[j] = nw1[j] = 0u;
-      nalpha[j] = 1.f;
-    }
-    int n_kind, n_ntok;
-    int64_t n_res_row = 0;
-
-    if (cc.uu < cc.ncu) {
-      const unsigned char *stg = wbase + stage * L::kStageBytes;
-      const int ngr = min(NGU, cc.NG - cc.uu * NGU);
-      // ---- per group: qs = q * s scaled by 2^E * mult, split hi/lo into the
-      //      group's B fragment; this lane's score scale and beta = q . z
-      float cq_g[NGU], beta_g[NGU];
+    for (int gi = 0; gi < NGU; ++gi) {
+      if (FULL || gi < ngr) {
+        const unsigned char *km = stg + L::kKMeta + gi * kD * 4;
+        const uint2 m01 = lds64(km + pc * 4), md = lds64(km + (pc + PD) * 4);
+        const float2 v0 = __half22float2(u2h2(m01.x)), v1 = __half22float2(u2h2(md.x));
+        const float2 v2 = __half22float2(u2h2(m01.y)), v3 = __half22float2(u2h2(md.y));
+        sp[gi][0] = v0.x;
+        sp[gi][1] = v1.x;
+        sp[gi][2] = v2.x;
+        sp[gi][3] = v3.x;
+        const float z0 = v0.y * ifa, z1 = v1.y * ifa, z2 = v2.y * ifb, z3 = v3.y * ifb;
 #pragma unroll
-      for (int gi = 0; gi < NGU; ++gi) {
-        cq_g[gi] = 0.f;
-        beta_g[gi] = 0.f;
-        if (gi < ngr) {
-          uint16_t *fb = reinterpret_cast<uint16_t *>(frag + gi * L::kFragGroupBytes);
-          float x[R][4], beta[R];
-#pragma unroll
-          for (int hh = 0; hh < R; ++hh) beta[hh] = 0.f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t mt = lds32(stg + L::kKMeta + (gi * kD + lane + 32 * k) * 4);
-            const float2 sz = __half22float2(u2h2(mt));
-#pragma unroll
-            for (int hh = 0; hh < R; ++hh) {
-              x[hh][k] = qv[hh][k] * sz.x;
-              beta[hh] = fmaf(qv[hh][k], sz.y, beta[hh]);
-            }
-          }
-#pragma unroll
-          for (int hh = 0; hh < R; ++hh) {
-            const float mabs =
-                fmaxf(fmaxf(fabsf(x[hh][0]), fabsf(x[hh][1])), fmaxf(fabsf(x[hh][2]), fabsf(x[hh][3])));
-            const uint32_t mbits = __reduce_max_sync(0xffffffffu, __float_as_uint(mabs));
-            // largest |qs| in [2^e, 2^(e+1)): scale by 2^E, E = 7 - e, so |B| < 2^14
-            const int E = min(100, max(-100, 134 - (int)(mbits >> 23)));
-            const float sc = pow2i(E) * mult;
-#pragma unroll
-            for (int k = 0; k < 4; k += 2) {
-              const float y0 = x[hh][k] * sc, y1 = x[hh][k + 1] * sc;
-              const __half2 hi = __floats2half2_rn(y0, y1);
-              const float2 fh = __half22float2(hi);
-              const __half2 lo = __floats2half2_rn(y0 - fh.x, y1 - fh.y);
-              fb[(k + 8 * hh) * (kFragRowWords * 2) + wh] = __half_as_ushort(__low2half(hi));
-              fb[(k + 1 + 8 * hh) * (kFragRowWords * 2) + wh] = __half_as_ushort(__high2half(hi));
-              fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh] = __half_as_ushort(__low2half(lo));
-              fb[(k + 1 + 8 * hh + 4) * (kFragRowWords * 2) + wh] = __half_as_ushort(__high2half(lo));
-            }
-            float bsum = beta[hh];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, off);
-            if (head_mine == hh) {
-              // products are code * qs * 2^(E - 18) (2-bit) or 2^(E - 20) (4-bit)
-              cq_g[gi] = c0 * pow2i((BITS == 2 ? 18 : 20) - E);
-              beta_g[gi] = c0 * bsum;
-            }
-          }
-        }
-      }
-      __syncwarp();
-      // ---- R steps of T tiles cover the unit (a trailing single group: 32 tokens)
-      auto run = [&](auto full_tag, int n_tok) {
-        constexpr bool FULL = decltype(full_tag)::value;
-#pragma unroll
-        for (int s = 0; s < R; ++s) {
-          if (!FULL && 16 * T * s >= n_tok) break;
-          const int my_grp = (s * T + li.slot_mine) / TPG;
-          float cq = cq_g[0], beta = beta_g[0];
-          if (NGU > 1 && my_grp == 1) {
-            cq = cq_g[NGU - 1];
-            beta = beta_g[NGU - 1];
-          }
-          uint32_t bf[16];
-          auto kfill = [&](int i, float sc[4]) {
-            const int t = s * T + i;
-            // (re)load the B fragment at the first tile of each group in the step
-            if (i == 0 || t % TPG == 0)
-              load_frag(frag + (t / TPG) * L::kFragGroupBytes + frag_row * kFragRowWords * 4, bf);
-            uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-            if constexpr (BITS == 2) {
-              // words 2tig, 2tig+1 of tokens g and g+8: channels 32tig .. 32tig+31
-              const uint2 ka = lds64(stg + L::kKCodes + (16 * t + g) * 32 + tig * 8);
-              const uint2 kb = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
-              unpack16(ka.x, ra0);
-              unpack16(ka.y, ra1);
-              unpack16(kb.x, rb0);
-              unpack16(kb.y, rb1);
-            } else {
-              // words 4tig .. 4tig+3 of tokens g and g+8: channels 32tig .. 32tig+31
-              const uint4 ka = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g) * 64 + tig * 16);
-              const uint4 kb = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g + 8) * 64 + tig * 16);
-              unpack8(ka.x, ra0);
-              unpack8(ka.y, ra0 + 4);
-              unpack8(ka.z, ra1);
-              unpack8(ka.w, ra1 + 4);
-              unpack8(kb.x, rb0);
-              unpack8(kb.y, rb0 + 4);
-              unpack8(kb.z, rb1);
-              unpack8(kb.w, rb1 + 4);
-            }
-            qk_tile(ra0, ra1, rb0, rb1, bf, sc);
-          };
-          auto vmeta = [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + (16 * T * s + tok) * 4); };
-          qk_step<R, FULL>(ss, li, kfill, cq, beta, FULL ? 16 * T : n_tok - 16 * T * s, vmeta, nw0[s], nw1[s],
-                           nalpha[s]);
-        }
-      };
-      if (ngr == NGU)
-        run(std::true_type{}, kUnit);
-      else
-        run(std::false_type{}, ngr * G);
-      n_kind = 1;
-      n_ntok = ngr * G;
-    } else {
-      // ---- fp16 residual keys of the head: B = q itself (hi part, lo = 0), A = keys
-      uint16_t *fb = reinterpret_cast<uint16_t *>(frag);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-#pragma unroll
-        for (int hh = 0; hh < R; ++hh) {
-          fb[(k + 8 * hh) * (kFragRowWords * 2) + wh_pairs] = f2h(qv[hh][k]);
-          fb[(k + 8 * hh + 4) * (kFragRowWords * 2) + wh_pairs] = 0;
-        }
-      __syncwarp();
-      uint32_t bf[16];
-      load_frag(frag + frag_row * kFragRowWords * 4, bf);
-      const int r = cc.r;
-      const int64_t nq = (int64_t)cc.NG * G;
-      const uint16_t *res_head = a.k_res + cc.h * G * kD;
-      // value rows of the residual tokens nq .. nq + r - 1 (one page: pages hold whole groups)
-      if constexpr (PAGED) {
-        const int64_t ph = page_of(cc.b, (int)nq) * a.Hkv + cc.kvh;
-        n_res_row = ph * P + (nq & (P - 1));
+        for (int hh = 0; hh < R; ++hh)
+          bv[gi][hh] = fmaf(qa[hh][3], z3, fmaf(qa[hh][2], z2, fmaf(qa[hh][1], z1, qa[hh][0] * z0)));
       } else {
-        n_res_row = cc.h * a.max_tokens + nq;
-      }
-      const uint32_t *vm_head = a.v_meta + n_res_row;
 #pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int base = 16 * T * s;
-        if (base >= r) break;
-        auto kfill = [&](int i, float sc[4]) {
-          const int sa_slot = base + 16 * i + g, sb_slot = sa_slot + 8;
-          uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-          residual_pairs(res_head + sa_slot * kD, sa_slot < r, tig, ra0, ra1);
-          residual_pairs(res_head + sb_slot * kD, sb_slot < r, tig, rb0, rb1);
-          qk_tile(ra0, ra1, rb0, rb1, bf, sc);
-        };
-        // residual values are quantized ({s, z} of their row) or, with a value
-        // residual, fp16 themselves: weight p with s = 1, z = 0
-        auto vmeta = [&](int tok) -> uint32_t { return a.v_res ? 0x00003C00u : vm_head[base + tok]; };
-        qk_step<R, false>(ss, li, kfill, c0, 0.f, min(16 * T, r - base), vmeta, nw0[s], nw1[s], nalpha[s]);
+        for (int k = 0; k < 4; ++k) sp[gi][k] = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < R; ++hh) bv[gi][hh] = 0.f;
       }
-      n_kind = 2;
-      n_ntok = r;
     }
-
-    // ---- P.V of this unit: value codes from the stage, or (residual unit) from HBM
-    if (n_kind == 1) {
-      const unsigned char *stg = wbase + stage * L::kStageBytes;
+    beta_reduce<R, NGU>(bv, lane);
+    // B fragment of group gi: hi and lo rows of every head
+    auto write_frag = [&](int gi) {
+      uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
 #pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int nv = min(16 * T, n_ntok - 16 * T * s);
-        if (nv <= 0) break;
-        if constexpr (BITS == 2) {
-          pv_step<R, 2>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
-            return lds32(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 32 + g * 4);
-          });
-        } else {
-          pv_step<R, 4>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint2 {
-            return lds64(stg + L::kVCodes + (16 * (s * T + i) + tig + 4 * k) * 64 + g * 8);
-          });
+      for (int hh = 0; hh < R; ++hh) {
+        const float x0 = qa[hh][0] * sp[gi][0], x1 = qa[hh][1] * sp[gi][1];
+        const float x2 = qa[hh][2] * sp[gi][2], x3 = qa[hh][3] * sp[gi][3];
+        const __half2 hA = __floats2half2_rn(x0, x1), hB = __floats2half2_rn(x2, x3);
+        const float2 fA = __half22float2(hA), fB = __half22float2(hB);
+        const __half2 lA = __floats2half2_rn(x0 - fA.x, x1 - fA.y), lB = __floats2half2_rn(x2 - fB.x, x3 - fB.y);
+        *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) = make_uint2(h22u(hA), h22u(hB));
+        *reinterpret_cast<uint2 *>(fw + ((2 * hh + 1) * 4 + pt) * FRW + pword) = make_uint2(h22u(lA), h22u(lB));
+      }
+    };
+    write_frag(0);
+    __syncwarp();
+    uint32_t bf[16];
+    load_frag(frag + frag_row * FRW * 4, bf);
+    // ---- q.K: R rounds of T tiles, tiles in increasing order (group 1 from tile TPG on)
+    float sc[R][4];
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho) {
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        const int t = rho * T + i;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (FULL || 16 * t < ntok) {
+          if (NGU == 2 && t == TPG) {
+            __syncwarp();  // every lane has its copy of the first group's fragment
+            write_frag(1);
+            __syncwarp();
+            load_frag(frag + frag_row * FRW * 4, bf);
+          }
+          uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
+          if constexpr (BITS == 2) {
+            uint2 kw[2];
+            if (R == 1) {
+              kw[0] = kw0[i][0];
+              kw[1] = kw0[i][1];
+            } else {
+              kcodes(t, kw);
+            }
+            unpack16(kw[0].x, ra0);
+            unpack16(kw[0].y, ra1);
+            unpack16(kw[1].x, rb0);
+            unpack16(kw[1].y, rb1);
+          } else {
+            // words 4tig .. 4tig+3 of tokens g and g+8: channels 32tig .. 32tig+31
+            const uint4 ka = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g) * 64 + tig * 16);
+            const uint4 kb = *reinterpret_cast<const uint4 *>(stg + L::kKCodes + (16 * t + g + 8) * 64 + tig * 16);
+            unpack8(ka.x, ra0);
+            unpack8(ka.y, ra0 + 4);
+            unpack8(ka.z, ra1);
+            unpack8(ka.w, ra1 + 4);
+            unpack8(kb.x, rb0);
+            unpack8(kb.y, rb0 + 4);
+            unpack8(kb.z, rb1);
+            unpack8(kb.w, rb1 + 4);
+          }
+          qk_tile(ra0, ra1, rb0, rb1, bf, s4);
+        }
+        keep_slot(i, s4, sc[rho]);
+      }
+    }
+    // ---- softmax update of the unit
+    float be[NGU];
+#pragma unroll
+    for (int gi = 0; gi < NGU; ++gi) be[gi] = bv[gi][0] * cbh;
+    auto grp = [&](int rho) { return NGU == 1 ? 0 : (rho * T + slot_mine) / TPG; };
+    uint32_t bw0[R], bw1[R];
+    const float alpha = update(
+        full_tag, sc, [&](int) { return cqh; }, [&](int rho) { return grp(rho) ? be[NGU - 1] : be[0]; }, ntok,
+        [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + tok * 4); }, bw0, bw1);
+    // ---- P.V of the unit's tiles from the staged value codes
+    rescale(alpha);
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho)
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        const int t = rho * T + i;
+        if (FULL || 16 * t < ntok) {
+          const bool mine = pv_slot == i;
+          const uint32_t b0 = mine ? bw0[rho] : 0u, b1 = mine ? bw1[rho] : 0u;
+          if constexpr (BITS == 2) {
+            uint32_t v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = lds32(stg + L::kVCodes + (16 * t + tig + 4 * k) * 32 + g * 4);
+            pv_tile(acc, v, b0, b1);
+          } else {
+            uint2 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = lds64(stg + L::kVCodes + (16 * t + tig + 4 * k) * 64 + g * 8);
+            pv_tile4(acc, v, b0, b1);
+          }
         }
       }
-    } else if (a.v_res) {
+  };
+
+  // ---- the residual unit of a head: its r fp16 keys (read from the residual buffer)
+  // and their values (quantized rows nq .. nq + r - 1, or the fp16 value residual)
+  auto residual_unit = [&]() {
+    const int r = cc.r;
+    const int64_t nq = (int64_t)cc.NG * G;
+    const uint16_t *res_head = a.k_res + cc.h * G * kD;
+    int64_t vrow;  // value row of token nq (one page: pages hold whole groups)
+    if constexpr (PAGED) {
+      const int64_t ph = page_of(cc.b, (int)nq) * a.Hkv + cc.kvh;
+      vrow = ph * P + (nq & (P - 1));
+    } else {
+      vrow = cc.h * a.max_tokens + nq;
+    }
+    // B fragment: the fp16 query itself, in the pairing of the unpacked registers (the
+    // keys are fp16 themselves, so the products are exact and need no factor); lo rows 0
+    {
+      const uint16_t *qh = cursor_q(cc);
+      uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
+#pragma unroll
+      for (int hh = 0; hh < R; ++hh) {
+        const uint32_t w01 = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc));
+        const uint32_t wd = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc + PD));
+        *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) =
+            make_uint2(prmt(w01, wd, 0x5410u), prmt(w01, wd, 0x7632u));
+        *reinterpret_cast<uint2 *>(fw + ((2 * hh + 1) * 4 + pt) * FRW + pword) = make_uint2(0u, 0u);
+      }
+    }
+    __syncwarp();
+    uint32_t bf[16];
+    load_frag(frag + frag_row * FRW * 4, bf);
+    float sc[R][4];
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho) {
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        const int t = rho * T + i;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (16 * t < r) {
+          const int sa = 16 * t + g, sb = sa + 8;
+          uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
+          residual_pairs<BITS>(res_head + sa * kD, sa < r, tig, ra0, ra1);
+          residual_pairs<BITS>(res_head + sb * kD, sb < r, tig, rb0, rb1);
+          qk_tile(ra0, ra1, rb0, rb1, bf, s4);
+        }
+        keep_slot(i, s4, sc[rho]);
+      }
+    }
+    // residual values are quantized ({s, z} of their row) or, with a value residual,
+    // fp16 themselves: weight p with s = 1, z = 0
+    const uint32_t *vm_head = a.v_meta + vrow;
+    uint32_t bw0[R], bw1[R];
+    const float alpha = update(
+        std::false_type{}, sc, [&](int) { return c0; }, [&](int) { return 0.f; }, r,
+        [&](int tok) -> uint32_t { return a.v_res ? 0x00003C00u : __ldg(vm_head + tok); }, bw0, bw1);
+    if (a.v_res) {
       // fp16 residual values: this is the head's last unit, so the accumulators move
       // to output units here and the head's partial is written without code factors
 #pragma unroll
@@ -872,33 +960,90 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         for (int k = 0; k < 4; ++k) acc[j][k] *= un;
       }
       acc_true = true;
+      rescale(alpha);
       const uint16_t *vres_head = a.v_res + cc.h * G * kD;
 #pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int nv = min(16 * T, n_ntok - 16 * T * s);
-        if (nv <= 0) break;
-        pv_step_f16<R>(acc, li, nv, nw0[s], nw1[s], nalpha[s], vres_head + 16 * T * s * kD);
-      }
-    } else {
-      const uint32_t *vc_head = a.v_codes + n_res_row * WPR;
+      for (int rho = 0; rho < R; ++rho)
 #pragma unroll
-      for (int s = 0; s < R; ++s) {
-        const int nv = min(16 * T, n_ntok - 16 * T * s);
-        if (nv <= 0) break;
-        if constexpr (BITS == 2) {
-          pv_step<R, 2>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint32_t {
-            const int slot = 16 * (s * T + i) + tig + 4 * k;
-            return vc_head[(slot < n_ntok ? slot : 0) * WPR + g];
-          });
-        } else {
-          pv_step<R, 4>(acc, li, nv, nw0[s], nw1[s], nalpha[s], [&](int i, int k) -> uint2 {
-            const int slot = 16 * (s * T + i) + tig + 4 * k;
-            return *reinterpret_cast<const uint2 *>(vc_head + (slot < n_ntok ? slot : 0) * WPR + 2 * g);
-          });
+        for (int i = 0; i < T; ++i) {
+          const int t = rho * T + i;
+          if (16 * t < r) {
+            const bool mine = pv_slot == i;
+            pv_tile_f16(acc, vres_head + 16 * t * kD, r - 16 * t, g, tig, mine ? bw0[rho] : 0u,
+                        mine ? bw1[rho] : 0u);
+          }
         }
+    } else {
+      rescale(alpha);
+      const uint32_t *vc_head = a.v_codes + vrow * WPR;
+#pragma unroll
+      for (int rho = 0; rho < R; ++rho)
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+          const int t = rho * T + i;
+          if (16 * t < r) {
+            const bool mine = pv_slot == i;
+            const uint32_t b0 = mine ? bw0[rho] : 0u, b1 = mine ? bw1[rho] : 0u;
+            if constexpr (BITS == 2) {
+              uint32_t v[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int slot = 16 * t + tig + 4 * k;
+                v[k] = vc_head[(slot < r ? slot : 0) * WPR + g];
+              }
+              pv_tile(acc, v, b0, b1);
+            } else {
+              uint2 v[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int slot = 16 * t + tig + 4 * k;
+                v[k] = *reinterpret_cast<const uint2 *>(vc_head + (slot < r ? slot : 0) * WPR + 2 * g);
+              }
+              pv_tile4(acc, v, b0, b1);
+            }
+          }
+        }
+    }
+  };
+
+  // ---- the warp's units
+  load_q(cursor_q(cc));
+#pragma unroll
+  for (int kk = 0; kk < AH; ++kk) issue(kk);
+  uint32_t phase = 0;  // parity of each stage's next phase
+  bool fault = false;
+  for (int kk = 0; kk < n_my; ++kk) {
+    issue(kk + AH);  // into the stage of unit kk - 1, which every lane has finished reading
+    if constexpr (PAGED) {
+      // the warp that takes a head's first unit publishes where its partials go
+      if (cc.uu == 0 && lane == 0) {
+        const int64_t start = (int64_t)a.Hkv * s_cum[cc.b] + (int64_t)cc.kvh * cc.U;
+        const int64_t last = owner_warp(start + cc.U - 1, W, NW);
+        hdr[cc.h] = make_int2((int)(gw + cc.h), (int)(last - gw + 1));
       }
     }
-    __syncwarp();  // this unit's stage may be refilled from now on
+    if (cc.uu < cc.ncu) {
+      const int st = kk % S;
+      if (!mbar_wait(bar0 + 8 * st, (phase >> st) & 1u)) {
+        fault = true;
+        break;
+      }
+      phase ^= 1u << st;
+      armed &= ~(1u << st);
+      const unsigned char *stg = wbase + st * L::kStageBytes;
+      if constexpr (NGU == 1) {
+        code_unit(std::true_type{}, stg, kUnit);
+      } else {
+        const int ngr = min(NGU, cc.NG - cc.uu * NGU);  // a trailing single group: 32 tokens
+        if (ngr == NGU)
+          code_unit(std::true_type{}, stg, kUnit);
+        else
+          code_unit(std::false_type{}, stg, ngr * G);
+      }
+    } else {
+      residual_unit();
+    }
+    __syncwarp();  // this unit's stage and the fragment may be rewritten from now on
     if (kk + 1 < n_my) {
       if (cc.uu + 1 == cc.U) {  // the next unit starts a new head
         emit(cc.h, ss);
@@ -906,21 +1051,29 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
         ss.l = 0.f;
         ss.zs = 0.f;
         advance(cc);
-        load_q(cc);
+        load_q(cursor_q(cc));
       } else {
         advance(cc);
       }
     }
   }
+  if (fault) {
+    // a staged copy never completed: record it, wait (bounded) for this warp's other
+    // copies in flight, and stop without writing partials
+    if (lane == 0) atomicExch(&g_decode_fault, 1);
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+      if ((armed >> s) & 1u) mbar_wait(bar0 + 8 * s, (phase >> s) & 1u);
+    return;
+  }
   emit(cc.h, ss);
-  cp_async_wait<0>();
 }
-
 // Merge np partials (max, sum, unnormalised output; `stride` floats apart) of one
 // (batch, query head) into out_row with one warp: lane l owns channels 2l, 2l+1,
 // 64+2l, 64+2l+1.  Every partial's loads are issued before any is used (the
 // partials sit in L2), then an online max-rescaled sum merges them.  np == 0 (no
-// tokens) writes zeros.  Partial rows are 8-byte aligned (stride 130 floats).
+// tokens) writes zeros; after a decode fault (g_decode_fault) the row is NaN.
+// Partial rows are 8-byte aligned (stride 130 floats).
 __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
                                             uint16_t *__restrict__ out_row, int lane) {
   constexpr int kBatch = 16;
@@ -951,7 +1104,9 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np,
       }
     }
   }
-  const float inv = np > 0 ? 1.f / L : 0.f;
+  float inv = np > 0 ? 1.f / L : 0.f;
+  // a decode warp that gave up on a staged copy left partials unwritten: say so
+  if (*reinterpret_cast<volatile int *>(&g_decode_fault)) inv = __int_as_float(0x7fc00000);
   uint32_t *dst = reinterpret_cast<uint32_t *>(out_row);
   dst[lane] = h22u(__floats2half2_rn(o0 * inv, o1 * inv));
   dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
