@@ -19,13 +19,16 @@ outside the timed events.  With no flags the timed steps cover one schedule:
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kivi|reference]
                   [--workload NAME] [--layout dense|paged [--page-tokens P] [--graph]]
-                  [--value-residual] [--bits 2|4] [--compare-fp16] [--prefill-only]
+                  [--value-residual] [--bits 2|4] [--compare-fp16] [--prefill-only] [--prefill-fused]
 
 --layout paged runs the same workload through the paged cache (pages of P tokens
 from one pool, scattered by a seeded permutation; lengths on the device); with
 --graph each step is replayed from a CUDA graph captured once per input set.
 
---prefill-only times the prompt quantization alone (a separate JSON line).
+--prefill-only times the prompt quantization alone (a separate JSON line);
+--prefill-fused the fused prefill (the prompt's causal attention with the cache
+quantized in the same kernel) against the attention alone and the separate
+quantization pass (one JSON object).
 
 --impl reference times the CPU oracle (plain C, the host's cores) on a bounded
 sample of the same workload.  Under torchrun every rank runs an independent
@@ -596,6 +599,65 @@ def run_prefill(args, wl):
     return 0
 
 
+def run_prefill_fused(args, wl):
+    """--prefill-fused: the prompt's causal attention with the cache quantized in the
+    same kernel (kivi_prefill_attention), next to the same attention without the cache
+    and the separate quantization pass (kivi_quantize_prefill), L2 flushed before each
+    call; prints one JSON object."""
+    import torch
+
+    from bit_asymmetric_kv_gb300 import kivi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kivi.lib()
+    pre = synth.make_prefill(wl)
+    q = synth.make_prompt_queries(wl).to(dev)
+    k, v = pre.k.to(dev), pre.v.to(dev)
+    out = torch.empty_like(q)
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_residual=args.value_residual,
+                                bits=args.bits)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                ts.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in ts)
+        return ms[len(ms) // 2]
+
+    fused = timed(lambda: kivi.kivi_prefill_attention(cache, q, k, v, 1.0, out=out, stream=stream))
+    alone = timed(lambda: kivi.kivi_prefill_attention(None, q, k, v, 1.0, out=out, dims=cache.dims, stream=stream))
+    quant = timed(lambda: kivi.kivi_quantize_prefill(cache, k, v, stream=stream))
+    n = wl.n
+    kv_bytes = 2 * wl.B * wl.Hkv * n * wl.D * 2
+    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, n, args.value_residual, args.bits)
+    flops = 4.0 * wl.D * (n * (n + 1) / 2) * wl.B * wl.Hq  # q.K and P.V over the causal triangle
+    peak, src = measured_peak()
+    extra = fused - alone
+    print(json.dumps({
+        "mode": "fused prefill", "workload": wl.name, "steps": args.steps, "warmup": args.warmup, "bits": args.bits,
+        "value_residual": bool(args.value_residual), "l2": "flushed by a 256 MiB write before every call",
+        "fused_ms": fused, "attention_alone_ms": alone, "separate_quantize_ms": quant,
+        "quantization_cost_in_fused_ms": extra,
+        "separate_path_ms": alone + quant, "fused_saving_ms": alone + quant - fused,
+        "attention_tflops": flops / (alone / 1e3) / 1e12, "fused_attention_tflops": flops / (fused / 1e3) / 1e12,
+        "separate_quantize_GBps": moved / quant / 1e6, "separate_quantize_frac_of_peak": moved / quant / 1e6 / peak,
+        "quantize_bytes": moved, "prompt_kv_bytes": kv_bytes,
+        "note": "the fused kernel quantizes the key/value tiles it already holds in shared memory: its quantization "
+                "cost is fused_ms - attention_alone_ms against separate_quantize_ms for the second read of the prompt",
+        "peak_GBps": peak, "peak_source": src}))
+    return 0
+
+
 def cycle_workspace(cache, wl, n0, dev):
     """A zero-filled decode workspace large enough for every context of a cycle."""
     import torch
@@ -717,6 +779,9 @@ def main(argv=None):
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt quantization (kivi_quantize_prefill) of the workload")
+    ap.add_argument("--prefill-fused", action="store_true",
+                    help="time the fused prefill (causal prompt attention + cache quantization in one kernel) "
+                         "against the attention alone and the separate quantization pass")
     ap.add_argument("--batch", type=int, default=0,
                     help="run the workload's shape with this batch instead (for small profiling captures; "
                          "the JSON line then names the batch in its config)")
@@ -745,6 +810,8 @@ def main(argv=None):
         return run_reference(args, wl)
     if args.prefill_only:
         return run_prefill(args, wl)
+    if args.prefill_fused:
+        return run_prefill_fused(args, wl)
     return run_kivi(args, wl)
 
 

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(OUT_DIR, "libkivi.so")
 OBJ_DIR = os.path.join(HERE, "_build")
-SOURCES = ["kivi_quant.cu", "kivi_decode.cu", "kivi_decode_host.cu", "kivi_fp16.cu", "kivi_api.cu", "kivi_noalloc.cu"]
+SOURCES = ["kivi_quant.cu", "kivi_decode.cu", "kivi_decode_host.cu", "kivi_fp16.cu", "kivi_prefill.cu", "kivi_api.cu",
+           "kivi_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

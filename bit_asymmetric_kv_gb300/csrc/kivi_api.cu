@@ -295,6 +295,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.pmax = g.pmax;
+  a.small = g.small ? 1 : 0;
   a.wait_tail = 0;
   a.softmax_scale = softmax_scale;
   return cuda_status(kivi::launch_decode(a, st));
@@ -343,6 +344,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.pmax = g.pmax;
+  a.small = g.small ? 1 : 0;
   a.wait_tail = 1;
   a.softmax_scale = softmax_scale;
   if ((s = cuda_status(kivi::launch_decode(a, st))) != KIVI_OK) return s;
@@ -360,6 +362,42 @@ int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out,
   return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta, vres(d, c),
                                           (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->bits, d->max_tokens, k_out, v_out,
                                           st));
+}
+
+int kivi_prefill_attention(const kivi_dims *d, kivi_cache *c, const uint16_t *q, int32_t Hq, const uint16_t *k,
+                           const uint16_t *v, int64_t n, float softmax_scale, uint16_t *out, cudaStream_t st) {
+  int s = check_dims(d);
+  if (s != KIVI_OK) return s;
+  if (c && (s = check_cache(d, c)) != KIVI_OK) return s;
+  if ((s = check_heads(d, Hq)) != KIVI_OK) return s;
+  if (n <= 0 || !q || !k || !v || !out) return KIVI_ERR_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return KIVI_ERR_ALIGN;
+  if ((int64_t)d->B * Hq > 65535) return KIVI_ERR_UNSUPPORTED;  // grid.y of the launch
+  if (c && n > d->max_tokens) return KIVI_ERR_CAPACITY;
+  kivi::PrefillArgs a = {};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  if (c) {
+    a.k_codes = c->k_codes;
+    a.k_meta = c->k_meta;
+    a.v_codes = c->v_codes;
+    a.v_meta = c->v_meta;
+    a.k_res = c->k_res;
+    a.v_res = vres(d, c);
+  }
+  a.n = n;
+  a.max_tokens = d->max_tokens;
+  a.B = d->B;
+  a.Hkv = d->Hkv;
+  a.Hq = Hq;
+  a.G = d->G;
+  a.bits = d->bits;
+  a.softmax_scale = softmax_scale;
+  if ((s = cuda_status(kivi::launch_prefill_attention(a, st))) != KIVI_OK) return s;
+  if (c) c->n_tokens = n;
+  return KIVI_OK;
 }
 
 static int fp16_sizes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int64_t n, int *splits, int64_t *tps) {

@@ -14,11 +14,10 @@
 //   * the codes enter as fp16 subnormals (exact, see unpack16);
 //   * the fp32 factors qs and p*s enter as an fp16 pair hi + lo (hi = fp16(x),
 //     lo = fp16(x - hi)), one per MMA column, which keeps ~22 significant bits;
-//     qs is scaled by a power of two per head, 2^(A - 15) with A putting the head's
-//     largest |q| just below 2^14: an fp16 scale is below 2^16, so every entry stays
-//     below 2^15 (no fp16 overflow) and the large entries keep full precision; an
-//     entry small enough for its lo part to fall among fp16 subnormals contributes
-//     at most 2^-25 absolute error in these units, negligible in the score.
+//     qs is scaled by a power of two per (head, group) chosen from a bound on its
+//     entries (the largest |q| of the head times the largest scale of the group), so
+//     that every entry stays below 2^15 (no fp16 overflow) and the large entries keep
+//     their lo parts out of the fp16 subnormals (full precision for any range).
 // Tokens are tiled by 16 (the MMA M dimension for q.K, the K dimension for P.V).
 // The 4 column pairs of an MMA carry (tile slot, query head): a round covers
 // T = 4/R tiles at once, so that for every R each lane owns the scores of one
@@ -235,43 +234,6 @@ __device__ __forceinline__ void pv_tile_f16(float acc[8][4], const uint16_t *row
   }
 }
 
-// 32 fp16 keys (channels 32tig .. 32tig+31) of one residual token, paired like the
-// unpacked codes of the BITS-bit path: 2-bit r[i] = {channel i, i + 8} of each
-// 16-channel half, 4-bit r[4a + t] = {channel 8a + t, 8a + t + 4}.
-template <int BITS>
-__device__ __forceinline__ void residual_pairs(const uint16_t *row, bool valid, int tig, uint32_t r0[8],
-                                               uint32_t r1[8]) {
-  uint32_t p[16];  // p[k]: channels 32tig + 2k (low half) and 32tig + 2k + 1
-  if (valid) {
-    const uint4 *src = reinterpret_cast<const uint4 *>(row + 32 * tig);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 uu = __ldg(src + k);
-      p[4 * k] = uu.x;
-      p[4 * k + 1] = uu.y;
-      p[4 * k + 2] = uu.z;
-      p[4 * k + 3] = uu.w;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 16; ++k) p[k] = 0u;
-  }
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    int lo, hi;
-    if constexpr (BITS == 2) {
-      lo = m >> 1;
-      hi = (m >> 1) + 4;
-    } else {
-      lo = 4 * (m >> 2) + ((m & 3) >> 1);
-      hi = lo + 2;
-    }
-    const uint32_t sel = (m & 1) ? 0x7632u : 0x5410u;
-    r0[m] = prmt(p[lo], p[hi], sel);
-    r1[m] = prmt(p[8 + lo], p[8 + hi], sel);
-  }
-}
-
 // Index of the first warp whose unit range contains unit u.
 __device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t NW) { return ((u + 1) * NW - 1) / W; }
 
@@ -409,8 +371,88 @@ __device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
   __syncthreads();
 }
 
-template <int R, int G, bool PAGED, int BITS>
-__global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
+// Merge np partials (max, sum, unnormalised output; `stride` floats apart) of one
+// (batch, query head) into out_row with one warp: lane l owns channels 2l, 2l+1,
+// 64+2l, 64+2l+1.  Every partial's loads are issued before any is used (the
+// partials sit in L2, or in shared memory with SHARED), then an online max-rescaled
+// sum merges them.  np == 0 (no
+// tokens) writes zeros; after a decode fault (g_decode_fault) the row is NaN.
+// Partial rows are 8-byte aligned (stride 130 floats).
+template <bool SHARED>
+__device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
+                                            uint16_t *__restrict__ out_row, int lane) {
+  constexpr int kBatch = 16;
+  float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  for (int j0 = 0; j0 < np; j0 += kBatch) {
+    float2 ml[kBatch], lo[kBatch], hi[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (j0 + k < np) {
+        const float *r = p + (int64_t)(j0 + k) * stride;
+        if constexpr (SHARED) {
+          ml[k] = *reinterpret_cast<const float2 *>(r + kD);
+          lo[k] = *reinterpret_cast<const float2 *>(r + 2 * lane);
+          hi[k] = *reinterpret_cast<const float2 *>(r + 64 + 2 * lane);
+        } else {
+          ml[k] = __ldcg(reinterpret_cast<const float2 *>(r + kD));
+          lo[k] = __ldcg(reinterpret_cast<const float2 *>(r + 2 * lane));
+          hi[k] = __ldcg(reinterpret_cast<const float2 *>(r + 64 + 2 * lane));
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (j0 + k < np && ml[k].x != -INFINITY) {
+        const float m = fmaxf(M, ml[k].x);
+        const float a = ex2(M - m);  // M = -inf on the first partial: a = 0
+        const float w = ex2(ml[k].x - m);
+        L = fmaf(L, a, w * ml[k].y);
+        o0 = fmaf(o0, a, w * lo[k].x);
+        o1 = fmaf(o1, a, w * lo[k].y);
+        o2 = fmaf(o2, a, w * hi[k].x);
+        o3 = fmaf(o3, a, w * hi[k].y);
+        M = m;
+      }
+    }
+  }
+  float inv = np > 0 ? 1.f / L : 0.f;
+  // a decode warp that gave up on a staged copy left partials unwritten: say so
+  if (*reinterpret_cast<volatile int *>(&g_decode_fault)) inv = __int_as_float(0x7fc00000);
+  uint32_t *dst = reinterpret_cast<uint32_t *>(out_row);
+  dst[lane] = h22u(__floats2half2_rn(o0 * inv, o1 * inv));
+  dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
+}
+
+
+// The small path's merge: once every warp of the CTA has written its partials, warp r
+// merges query head r's partials of the CTA's (batch, KV head) into the output.
+template <int R>
+__device__ __forceinline__ void small_merge(const DecodeArgs &a, const float *s_part, int64_t NW, int warp,
+                                            int lane) {
+  __syncthreads();
+  if (warp < R) {
+    const int64_t h = blockIdx.x, b = h / a.Hkv, kvh = h - b * a.Hkv;
+    combine_row<true>(s_part + warp * (kD + 2), (int)NW, (int64_t)R * (kD + 2),
+                      a.out + (b * a.Hq + kvh * R + warp) * kD, lane);
+  }
+}
+
+// Launch modes of the decode body: the persistent grid over a dense or a paged cache,
+// and the small-context path (one CTA of kSmallWarps warps per (batch, KV head) of a
+// dense cache, its warps' partials merged in shared memory: no workspace round trip
+// and no combine launch).
+constexpr int kModeDense = 0, kModePaged = 1, kModeSmall = 2;
+constexpr int kSmallWarps = kDecodeSmallWarps;
+
+// Partials of the small path's CTA: [warp][R] rows of kD + 2 floats after the warps'
+// rings.
+template <int R>
+__host__ __device__ constexpr int small_part_bytes() { return kSmallWarps * R * (kD + 2) * 4; }
+
+template <int R, int G, int MODE, int BITS, int NWARPS>
+__device__ __forceinline__ void decode_body(const DecodeArgs &a) {
+  constexpr bool PAGED = MODE == kModePaged;
+  constexpr bool SMALL = MODE == kModeSmall;
   extern __shared__ __align__(16) unsigned char smem[];
   using L = Layout<R, G, BITS>;
   constexpr int WPR = words_per_row<BITS>();
@@ -425,9 +467,10 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   // the combine grid may launch now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t gw = SMALL ? warp : (int64_t)blockIdx.x * NWARPS + warp;
   int64_t NW = a.n_warps;
   int64_t W;
+  float *s_part = reinterpret_cast<float *>(smem + NWARPS * L::kWarpBytes);  // small path only
   int *s_len = nullptr, *s_cum = nullptr;
   int2 *hdr = nullptr;
   float *part = a.ws;
@@ -447,12 +490,25 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     // fewer units than warps: use one warp per unit, so that no warp between a
     // head's first and last owner is left without units (every partial is written)
     if (W < NW) NW = W;
+  } else if constexpr (SMALL) {
+    W = a.units_per_head;  // the units of head blockIdx.x
+    NW = W < NWARPS ? W : NWARPS;
   } else {
     W = a.total_units;
   }
-  if (gw >= NW) return;
-  const int64_t u0 = gw * W / NW, u1 = (gw + 1) * W / NW;
-  if (u0 >= u1) return;
+  int64_t u0 = 0, u1 = 0;
+  if (gw < NW) {
+    u0 = gw * W / NW;
+    u1 = (gw + 1) * W / NW;
+  }
+  if constexpr (SMALL) {
+    u0 += (int64_t)blockIdx.x * W;
+    u1 += (int64_t)blockIdx.x * W;
+  }
+  if (u0 >= u1) {
+    if constexpr (SMALL) small_merge<R>(a, s_part, NW, warp, lane);
+    return;
+  }
   const int n_my = (int)(u1 - u0);
 
   unsigned char *wbase = smem + warp * L::kWarpBytes;
@@ -487,11 +543,11 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
   const float ifa = 1.f / fa, ifb = 1.f / fb;
 
   // ---- the query heads of the current KV head: q of this lane's preparation
-  // channels (pc, pc + PD, pc + 1, pc + PD + 1) times fa / fb and 2^(A_h - 15), where
-  // A_h puts the head's largest |q * f| below 2^14; an fp16 scale lies below 2^16, so
-  // each B entry qa * s stays below 2^15
+  // channels (pc, pc + PD, pc + 1, pc + PD + 1) times fa / fb and 2^A_h, where A_h puts
+  // the head's largest |q * f| below 2^14; with every scale of a group below
+  // 2^(es + 1) and scaled by 2^-es, each B entry stays below 2^15
   float qa[R][4];
-  float cqh = 0.f, cbh = 0.f;  // c0 * 2^(SH - A + 15) and c0 * 2^(15 - A) of this lane's head
+  float cqh = 0.f, cbh = 0.f;  // c0 * 2^(SH - A) and c0 * 2^-A of this lane's head
   auto q_row = [&](int64_t b, int64_t kvh) { return a.q + (b * a.Hq + kvh * R) * kD; };
   auto load_q = [&](const uint16_t *qh) {
 #pragma unroll
@@ -505,13 +561,13 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       x[3] = h2f((uint16_t)(wd >> 16)) * fb;
       const float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
       const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(mx));
-      const int A = min(100, max(-90, 13 - ((int)(mb >> 23) - 127)));
-      const float sc = pow2i(A - 15);
+      const int A = min(100, max(-100, 13 - ((int)(mb >> 23) - 127)));
+      const float sc = pow2i(A);
 #pragma unroll
       for (int k = 0; k < 4; ++k) qa[hh][k] = x[k] * sc;
       if (hh == head_mine) {
-        cqh = c0 * pow2i(SH - A + 15);
-        cbh = c0 * pow2i(15 - A);
+        cqh = c0 * pow2i(SH - A);
+        cbh = c0 * pow2i(-A);
       }
     }
   };
@@ -660,7 +716,9 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     }
     if (slot_mine == 0) {
       float *dst;
-      if constexpr (PAGED) {
+      if constexpr (SMALL) {
+        dst = s_part + (gw * R + head_mine) * (kD + 2);
+      } else if constexpr (PAGED) {
         // pair index gw + h grows strictly along the unit order: unique per (warp, head)
         dst = part + ((gw + h) * R + head_mine) * (kD + 2);
       } else {
@@ -768,46 +826,67 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
       kw[1] = lds64(stg + L::kKCodes + (16 * t + g + 8) * 32 + tig * 8);
     };
     uint2 kw0[T][2];
+    (void)kw0;
     if constexpr (BITS == 2 && R == 1) {
 #pragma unroll
       for (int i = 0; i < T; ++i)
         if (FULL || 16 * i < ntok) kcodes(i, kw0[i]);
     }
-    // per key group: this lane's scales, the q . z partials of every head
-    float sp[NGU][4], bv[NGU][R];
+    // per key group: this lane's scales scaled by 2^-es (every scale of the group lies
+    // below 2^(es + 1)), the q . z partials of every head, and the score scale
+    float sp[NGU][4], bv[NGU][R], cq[NGU];
 #pragma unroll
     for (int gi = 0; gi < NGU; ++gi) {
       if (FULL || gi < ngr) {
         const unsigned char *km = stg + L::kKMeta + gi * kD * 4;
         const uint2 m01 = lds64(km + pc * 4), md = lds64(km + (pc + PD) * 4);
+        // non-negative fp16 scales order like their bit patterns
+        uint32_t smx = max(max(m01.x & 0xffffu, m01.y & 0xffffu), max(md.x & 0xffffu, md.y & 0xffffu));
+        smx = __reduce_max_sync(kFull, smx);
+        const int es = (int)(smx >> 10) - 15;
+        const float ps = pow2i(-es);
         const float2 v0 = __half22float2(u2h2(m01.x)), v1 = __half22float2(u2h2(md.x));
         const float2 v2 = __half22float2(u2h2(m01.y)), v3 = __half22float2(u2h2(md.y));
-        sp[gi][0] = v0.x;
-        sp[gi][1] = v1.x;
-        sp[gi][2] = v2.x;
-        sp[gi][3] = v3.x;
+        sp[gi][0] = v0.x * ps;
+        sp[gi][1] = v1.x * ps;
+        sp[gi][2] = v2.x * ps;
+        sp[gi][3] = v3.x * ps;
         const float z0 = v0.y * ifa, z1 = v1.y * ifa, z2 = v2.y * ifb, z3 = v3.y * ifb;
 #pragma unroll
         for (int hh = 0; hh < R; ++hh)
           bv[gi][hh] = fmaf(qa[hh][3], z3, fmaf(qa[hh][2], z2, fmaf(qa[hh][1], z1, qa[hh][0] * z0)));
+        cq[gi] = cqh * pow2i(es);
       } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) sp[gi][k] = 0.f;
 #pragma unroll
         for (int hh = 0; hh < R; ++hh) bv[gi][hh] = 0.f;
+        cq[gi] = 0.f;
       }
     }
     beta_reduce<R, NGU>(bv, lane);
     // B fragment of group gi: hi and lo rows of every head
+    // The hi parts lie on a grid: the tensor cores add the 16 products of an MMA
+    // k-step keeping only about 15 bits below the largest of them, so hi is rounded
+    // to a multiple of u = 2^(e - 7), e = floor(log2 max |y|) over the group's channels,
+    // y = x / f the entry without its code factor.  Every hi product is then
+    // code * 64 * 2^-24 * (a multiple of u), at most 3 * 2^8 units, and the MMA adds
+    // them exactly; lo = x - hi (below u/2) carries the rest in fp16, and its own
+    // sums lose at most about 2^-23 of the largest entry.
     auto write_frag = [&](int gi) {
       uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
 #pragma unroll
       for (int hh = 0; hh < R; ++hh) {
         const float x0 = qa[hh][0] * sp[gi][0], x1 = qa[hh][1] * sp[gi][1];
         const float x2 = qa[hh][2] * sp[gi][2], x3 = qa[hh][3] * sp[gi][3];
-        const __half2 hA = __floats2half2_rn(x0, x1), hB = __floats2half2_rn(x2, x3);
-        const float2 fA = __half22float2(hA), fB = __half22float2(hB);
-        const __half2 lA = __floats2half2_rn(x0 - fA.x, x1 - fA.y), lB = __floats2half2_rn(x2 - fB.x, x3 - fB.y);
+        const float ym = fmaxf(fmaxf(fabsf(x0), fabsf(x1)) * ifa, fmaxf(fabsf(x2), fabsf(x3)) * ifb);
+        const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(ym));
+        const int ge = min(120, max(-126, (int)(mb >> 23) - 127 - 7));
+        const float ca = pow2i(-ge) * ifa, da = pow2i(ge) * fa, cb = pow2i(-ge) * ifb, db = pow2i(ge) * fb;
+        const float h0 = rintf(x0 * ca) * da, h1 = rintf(x1 * ca) * da;
+        const float h2 = rintf(x2 * cb) * db, h3 = rintf(x3 * cb) * db;
+        const __half2 hA = __floats2half2_rn(h0, h1), hB = __floats2half2_rn(h2, h3);
+        const __half2 lA = __floats2half2_rn(x0 - h0, x1 - h1), lB = __floats2half2_rn(x2 - h2, x3 - h3);
         *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) = make_uint2(h22u(hA), h22u(hB));
         *reinterpret_cast<uint2 *>(fw + ((2 * hh + 1) * 4 + pt) * FRW + pword) = make_uint2(h22u(lA), h22u(lB));
       }
@@ -869,7 +948,8 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     auto grp = [&](int rho) { return NGU == 1 ? 0 : (rho * T + slot_mine) / TPG; };
     uint32_t bw0[R], bw1[R];
     const float alpha = update(
-        full_tag, sc, [&](int) { return cqh; }, [&](int rho) { return grp(rho) ? be[NGU - 1] : be[0]; }, ntok,
+        full_tag, sc, [&](int rho) { return grp(rho) ? cq[NGU - 1] : cq[0]; },
+        [&](int rho) { return grp(rho) ? be[NGU - 1] : be[0]; }, ntok,
         [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + tok * 4); }, bw0, bw1);
     // ---- P.V of the unit's tiles from the staged value codes
     rescale(alpha);
@@ -909,39 +989,36 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     } else {
       vrow = cc.h * a.max_tokens + nq;
     }
-    // B fragment: the fp16 query itself, in the pairing of the unpacked registers (the
-    // keys are fp16 themselves, so the products are exact and need no factor); lo rows 0
-    {
-      const uint16_t *qh = cursor_q(cc);
-      uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
+    // q.K of the fp16 residual keys on the CUDA cores in fp32 (full products and
+    // fp32 sums; the tensor cores' narrow addition window would cost precision on keys
+    // with outlier channels): lane (g, tig) scores tokens 16t + g and 16t + g + 8 of
+    // its tile slot t of every round, for its head.  The hi/lo column pair of the MMA
+    // layout becomes (score, 0).
+    const uint16_t *qh_row = cursor_q(cc) + head_mine * kD;
+    auto dot = [&](const uint16_t *krow) {
+      const uint4 *qp = reinterpret_cast<const uint4 *>(qh_row), *kp = reinterpret_cast<const uint4 *>(krow);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < kD / 8; ++c) {
+        const uint4 qq = __ldg(qp + c), kk = __ldg(kp + c);
+        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w}, kw4[4] = {kk.x, kk.y, kk.z, kk.w};
 #pragma unroll
-      for (int hh = 0; hh < R; ++hh) {
-        const uint32_t w01 = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc));
-        const uint32_t wd = __ldg(reinterpret_cast<const unsigned int *>(qh + hh * kD + pc + PD));
-        *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) =
-            make_uint2(prmt(w01, wd, 0x5410u), prmt(w01, wd, 0x7632u));
-        *reinterpret_cast<uint2 *>(fw + ((2 * hh + 1) * 4 + pt) * FRW + pword) = make_uint2(0u, 0u);
+        for (int i = 0; i < 4; ++i) {
+          const float2 a = __half22float2(u2h2(qw[i])), b = __half22float2(u2h2(kw4[i]));
+          s0 = fmaf(a.x, b.x, s0);
+          s1 = fmaf(a.y, b.y, s1);
+        }
       }
-    }
-    __syncwarp();
-    uint32_t bf[16];
-    load_frag(frag + frag_row * FRW * 4, bf);
+      return s0 + s1;
+    };
     float sc[R][4];
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) {
-#pragma unroll
-      for (int i = 0; i < T; ++i) {
-        const int t = rho * T + i;
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-        if (16 * t < r) {
-          const int sa = 16 * t + g, sb = sa + 8;
-          uint32_t ra0[8], ra1[8], rb0[8], rb1[8];
-          residual_pairs<BITS>(res_head + sa * kD, sa < r, tig, ra0, ra1);
-          residual_pairs<BITS>(res_head + sb * kD, sb < r, tig, rb0, rb1);
-          qk_tile(ra0, ra1, rb0, rb1, bf, s4);
-        }
-        keep_slot(i, s4, sc[rho]);
-      }
+      const int sa = 16 * (rho * T + slot_mine) + g, sb = sa + 8;
+      sc[rho][0] = sa < r ? dot(res_head + sa * kD) : 0.f;
+      sc[rho][1] = 0.f;
+      sc[rho][2] = sb < r ? dot(res_head + sb * kD) : 0.f;
+      sc[rho][3] = 0.f;
     }
     // residual values are quantized ({s, z} of their row) or, with a value residual,
     // fp16 themselves: weight p with s = 1, z = 0
@@ -1006,10 +1083,11 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
     }
   };
 
-  // ---- the warp's units
-  load_q(cursor_q(cc));
+  // ---- the warp's units (the first copies go out before the query is loaded, so
+  // that the two latencies overlap)
 #pragma unroll
   for (int kk = 0; kk < AH; ++kk) issue(kk);
+  load_q(cursor_q(cc));
   uint32_t phase = 0;  // parity of each stage's next phase
   bool fault = false;
   for (int kk = 0; kk < n_my; ++kk) {
@@ -1064,54 +1142,21 @@ __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(
 #pragma unroll
     for (int s = 0; s < S; ++s)
       if ((armed >> s) & 1u) mbar_wait(bar0 + 8 * s, (phase >> s) & 1u);
-    return;
+  } else {
+    emit(cc.h, ss);
   }
-  emit(cc.h, ss);
-}
-// Merge np partials (max, sum, unnormalised output; `stride` floats apart) of one
-// (batch, query head) into out_row with one warp: lane l owns channels 2l, 2l+1,
-// 64+2l, 64+2l+1.  Every partial's loads are issued before any is used (the
-// partials sit in L2), then an online max-rescaled sum merges them.  np == 0 (no
-// tokens) writes zeros; after a decode fault (g_decode_fault) the row is NaN.
-// Partial rows are 8-byte aligned (stride 130 floats).
-__device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
-                                            uint16_t *__restrict__ out_row, int lane) {
-  constexpr int kBatch = 16;
-  float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  for (int j0 = 0; j0 < np; j0 += kBatch) {
-    float2 ml[kBatch], lo[kBatch], hi[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      if (j0 + k < np) {
-        const float *r = p + (int64_t)(j0 + k) * stride;
-        ml[k] = __ldcg(reinterpret_cast<const float2 *>(r + kD));
-        lo[k] = __ldcg(reinterpret_cast<const float2 *>(r + 2 * lane));
-        hi[k] = __ldcg(reinterpret_cast<const float2 *>(r + 64 + 2 * lane));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      if (j0 + k < np && ml[k].x != -INFINITY) {
-        const float m = fmaxf(M, ml[k].x);
-        const float a = ex2(M - m);  // M = -inf on the first partial: a = 0
-        const float w = ex2(ml[k].x - m);
-        L = fmaf(L, a, w * ml[k].y);
-        o0 = fmaf(o0, a, w * lo[k].x);
-        o1 = fmaf(o1, a, w * lo[k].y);
-        o2 = fmaf(o2, a, w * hi[k].x);
-        o3 = fmaf(o3, a, w * hi[k].y);
-        M = m;
-      }
-    }
-  }
-  float inv = np > 0 ? 1.f / L : 0.f;
-  // a decode warp that gave up on a staged copy left partials unwritten: say so
-  if (*reinterpret_cast<volatile int *>(&g_decode_fault)) inv = __int_as_float(0x7fc00000);
-  uint32_t *dst = reinterpret_cast<uint32_t *>(out_row);
-  dst[lane] = h22u(__floats2half2_rn(o0 * inv, o1 * inv));
-  dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
+  if constexpr (SMALL) small_merge<R>(a, s_part, NW, warp, lane);
 }
 
+template <int R, int G, bool PAGED, int BITS>
+__global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
+  decode_body<R, G, PAGED ? kModePaged : kModeDense, BITS, kWarps>(a);
+}
+
+template <int R, int G, int BITS>
+__global__ void __launch_bounds__(kSmallWarps * 32, 1) decode_small_kernel(const DecodeArgs a) {
+  decode_body<R, G, kModeSmall, BITS, kSmallWarps>(a);
+}
 // Dense layout: the partials of (batch, query head) `row` sit at slots 0 .. np-1 of
 // the row's pmax slots; np follows from the unit split.
 __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(const float *__restrict__ ws, int64_t pmax,
@@ -1124,7 +1169,7 @@ __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(const float 
   const int64_t b = row / Hq, hq = row - b * Hq;
   const int64_t head = b * Hkv + hq / (Hq / Hkv);
   const int64_t first = owner_warp(head * U, W, NW), last = owner_warp(head * U + U - 1, W, NW);
-  combine_row(ws + row * pmax * (kD + 2), (int)(last - first + 1), kD + 2, out + row * kD, threadIdx.x & 31);
+  combine_row<false>(ws + row * pmax * (kD + 2), (int)(last - first + 1), kD + 2, out + row * kD, threadIdx.x & 31);
 }
 
 // Paged layout: the decode grid wrote, per (batch, KV head), the index of its first
@@ -1143,7 +1188,7 @@ __global__ void __launch_bounds__(32 * kCombineRows) paged_combine_kernel(const 
   const int64_t head = b * Hkv + hq / R;
   const int2 hd = __ldcg(reinterpret_cast<const int2 *>(ws) + head);
   const float *part = ws + 2 * (int64_t)B * Hkv;
-  combine_row(part + ((int64_t)hd.x * R + hq % R) * (kD + 2), hd.y, (int64_t)R * (kD + 2), out + row * kD, lane);
+  combine_row<false>(part + ((int64_t)hd.x * R + hq % R) * (kD + 2), hd.y, (int64_t)R * (kD + 2), out + row * kD, lane);
   if (advance && hq == 0 && lane == 0) {
     const int32_t len = advance[b];
     advance[b] = len < cap ? len + 1 : cap;
@@ -1162,6 +1207,28 @@ const void *select_kernel(int R, int G) {
            : R == 2 ? kernel_ptr<2, 32, PAGED, BITS>()
                     : kernel_ptr<4, 32, PAGED, BITS>();
   return R == 1 ? kernel_ptr<1, 64, PAGED, BITS>() : R == 2 ? kernel_ptr<2, 64, PAGED, BITS>() : kernel_ptr<4, 64, PAGED, BITS>();
+}
+
+template <int R, int G, int BITS>
+const void *small_ptr() {
+  return reinterpret_cast<const void *>(&decode_small_kernel<R, G, BITS>);
+}
+
+template <int BITS>
+const void *select_small(int R, int G) {
+  if (G == 32) return R == 1 ? small_ptr<1, 32, BITS>() : R == 2 ? small_ptr<2, 32, BITS>() : small_ptr<4, 32, BITS>();
+  return R == 1 ? small_ptr<1, 64, BITS>() : R == 2 ? small_ptr<2, 64, BITS>() : small_ptr<4, 64, BITS>();
+}
+
+template <int BITS>
+int small_smem_bytes(int R, int G) {
+  if (G == 32)
+    return R == 1   ? kSmallWarps * Layout<1, 32, BITS>::kWarpBytes + small_part_bytes<1>()
+           : R == 2 ? kSmallWarps * Layout<2, 32, BITS>::kWarpBytes + small_part_bytes<2>()
+                    : kSmallWarps * Layout<4, 32, BITS>::kWarpBytes + small_part_bytes<4>();
+  return R == 1   ? kSmallWarps * Layout<1, 64, BITS>::kWarpBytes + small_part_bytes<1>()
+         : R == 2 ? kSmallWarps * Layout<2, 64, BITS>::kWarpBytes + small_part_bytes<2>()
+                  : kSmallWarps * Layout<4, 64, BITS>::kWarpBytes + small_part_bytes<4>();
 }
 
 template <int BITS>
@@ -1184,10 +1251,14 @@ DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B) {
     k.smem = base + paged_extra(B);
     k.smem_limit = base + paged_extra(kPagedMaxBatch);
     k.combine = reinterpret_cast<const void *>(&paged_combine_kernel);
+    k.small = nullptr;
+    k.small_smem = 0;
   } else {
     k.decode = bits == 2 ? select_kernel<false, 2>(R, G) : select_kernel<false, 4>(R, G);
     k.smem = k.smem_limit = base;
     k.combine = reinterpret_cast<const void *>(&combine_kernel);
+    k.small = bits == 2 ? select_small<2>(R, G) : select_small<4>(R, G);
+    k.small_smem = bits == 2 ? small_smem_bytes<2>(R, G) : small_smem_bytes<4>(R, G);
   }
   return k;
 }

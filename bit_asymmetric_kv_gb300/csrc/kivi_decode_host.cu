@@ -25,13 +25,14 @@ struct WarpsEntry {
   const void *fn;
   int smem;
   int n_warps;
+  int sms;
 };
 constexpr int kWarpsCache = 256;
 WarpsEntry g_warps[kWarpsCache];
 int g_warps_used = 0;
 std::mutex g_warps_lock;
 
-cudaError_t warps_on_device(const DecodeKernels &k, int *n_warps) {
+cudaError_t warps_on_device(const DecodeKernels &k, int *n_warps, int *n_sms = nullptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -40,19 +41,25 @@ cudaError_t warps_on_device(const DecodeKernels &k, int *n_warps) {
     for (int i = 0; i < g_warps_used; ++i)
       if (g_warps[i].dev == dev && g_warps[i].fn == k.decode && g_warps[i].smem == k.smem) {
         *n_warps = g_warps[i].n_warps;
+        if (n_sms) *n_sms = g_warps[i].sms;
         return cudaSuccess;
       }
   }
   e = cudaFuncSetAttribute(k.decode, cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem_limit);
   if (e != cudaSuccess) return e;
+  if (k.small) {  // the small-context kernel of the same shapes: one CTA per SM at most
+    e = cudaFuncSetAttribute(k.small, cudaFuncAttributeMaxDynamicSharedMemorySize, k.small_smem);
+    if (e != cudaSuccess) return e;
+  }
   int sms = 0, per_sm = 0;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.decode, 32 * kDecodeWarps, k.smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   *n_warps = sms * per_sm * kDecodeWarps;
+  if (n_sms) *n_sms = sms;
   std::lock_guard<std::mutex> guard(g_warps_lock);
-  if (g_warps_used < kWarpsCache) g_warps[g_warps_used++] = WarpsEntry{dev, k.decode, k.smem, *n_warps};
+  if (g_warps_used < kWarpsCache) g_warps[g_warps_used++] = WarpsEntry{dev, k.decode, k.smem, *n_warps, sms};
   return cudaSuccess;
 }
 
@@ -87,8 +94,8 @@ cudaError_t launch_pair(const DecodeKernels &k, const DecodeArgs &a, void **comb
 
 cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out) {
   const int R = Hq / Hkv;
-  int nw = 0;
-  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, false, B), &nw);
+  int nw = 0, sms = 0;
+  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, false, B), &nw, &sms);
   if (e != cudaSuccess) return e;
   const int64_t heads = (int64_t)B * Hkv;
   const int64_t ng = n / G;
@@ -102,6 +109,10 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, 
   out->n_warps = (int)NW;
   out->grid = (int)((NW + kDecodeWarps - 1) / kDecodeWarps);
   out->pmax = (int)((U + q - 1) / q + 1);
+  // small contexts: at most one CTA per SM, and at most two units per warp of it.
+  // There the persistent grid's fixed cost (the workspace round trip and the combine
+  // launch) outweighs its wider split.
+  out->small = heads <= sms && U <= 2 * kDecodeSmallWarps;
   return cudaSuccess;
 }
 
@@ -120,6 +131,22 @@ cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, int bits, Paged
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
   const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, a.bits, false, a.B);
+  if (a.small) {
+    // one CTA per (batch, KV head); a programmatic dependent of a preceding append when
+    // asked (the same tail wait as the persistent grid)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)a.B * a.Hkv));
+    cfg.blockDim = dim3(32 * kDecodeSmallWarps);
+    cfg.dynamicSmemBytes = (size_t)k.small_smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.wait_tail ? 1 : 0;
+    void *args[] = {const_cast<DecodeArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, k.small, args);
+  }
   const float *ws = a.ws;
   int64_t pmax = a.pmax, W = a.total_units, NW = a.n_warps, U = a.units_per_head;
   int Hkv = a.Hkv, Hq = a.Hq;

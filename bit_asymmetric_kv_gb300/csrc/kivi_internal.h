@@ -74,6 +74,7 @@ struct DecodeArgs {
   int grid;                // CTAs (4 warps each)
   int pmax;                // partial slots per query head in the workspace
   int wait_tail;           // launched as a dependent of an append: wait before each head's last unit
+  int small;               // dense: the small-context path (decode_geometry's choice)
   float softmax_scale;
   // paged layout only: per-sequence lengths on the device, rows found through the
   // block table; the partials are addressed by (warp + head) and a per-head header
@@ -91,6 +92,7 @@ struct DecodeArgs {
 // (kivi_decode_host.cu) sizes the grid from the occupancy of `decode` with `smem`
 // bytes of dynamic shared memory; `smem_limit` is the most any launch of it uses.
 constexpr int kDecodeWarps = 4;   // warps per decode CTA
+constexpr int kDecodeSmallWarps = 8;  // warps per CTA of the small-context path
 constexpr int kDecodeUnit = 64;   // tokens per unit of work
 constexpr int kCombineRows = 4;   // (batch, query head) rows per combine CTA, one warp each
 struct DecodeKernels {
@@ -99,6 +101,8 @@ struct DecodeKernels {
   int smem_limit;
   const void *combine;  // dense: (ws, pmax, W, NW, U, Hkv, Hq, rows, out);
                         // paged: (ws, Hkv, Hq, B, advance, cap, out)
+  const void *small;    // dense only: one CTA of kDecodeSmallWarps warps per (batch, KV head)
+  int small_smem;
 };
 DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B);
 
@@ -109,6 +113,7 @@ struct DecodeGeom {
   int n_warps;
   int grid;
   int pmax;
+  bool small;  // the small-context path: one CTA per (batch, KV head), no workspace, no combine
 };
 cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
@@ -124,6 +129,21 @@ struct PagedGeom {
 constexpr int kPagedMaxBatch = 512;
 cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, int bits, PagedGeom *out);
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t st);
+
+// Fused prefill (kivi_prefill.cu): causal attention over the fp16 prompt and, when
+// k_codes is not null, the cache quantized from the same tiles.
+struct PrefillArgs {
+  const uint16_t *q;  // [B][Hq][n][128]
+  const uint16_t *k;  // [B][Hkv][n][128]
+  const uint16_t *v;
+  uint16_t *out;      // [B][Hq][n][128]
+  uint32_t *k_codes, *k_meta, *v_codes, *v_meta;  // the cache (null: attention only)
+  uint16_t *k_res, *v_res;                        // v_res null without a value residual
+  int64_t n, max_tokens;
+  int B, Hkv, Hq, G, bits;
+  float softmax_scale;
+};
+cudaError_t launch_prefill_attention(const PrefillArgs &a, cudaStream_t st);
 
 // Decode attention over an unquantized fp16 cache (the comparison kernel).
 struct Fp16Args {

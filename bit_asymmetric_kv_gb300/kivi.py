@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.kivi_buffer_bytes.argtypes = [D, ctypes.POINTER(sz)]
         L.kivi_quantize_prefill.argtypes = [D, C, P, P, i64, P]
         L.kivi_append_token.argtypes = [D, C, P, P, P]
+        L.kivi_prefill_attention.argtypes = [D, C, P, i32, P, P, i64, ctypes.c_float, P, P]
+        L.kivi_prefill_attention.restype = ctypes.c_int
         L.kivi_decode_splits.argtypes = [D, i32, i64]
         L.kivi_decode_workspace_bytes.argtypes = [D, i32, i64]
         L.kivi_decode_workspace_bytes.restype = sz
@@ -174,6 +176,28 @@ def kivi_quantize_prefill(cache: Cache, k: torch.Tensor, v: torch.Tensor, stream
     n = k.shape[2]
     _check(lib().kivi_quantize_prefill(ctypes.byref(cache.dims), ctypes.byref(cache.c), _ptr(k), _ptr(v), n,
                                        _stream(stream)), "kivi_quantize_prefill")
+
+
+def kivi_prefill_attention(cache: Cache | None, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                           softmax_scale: float, out: torch.Tensor | None = None, dims: kivi_dims | None = None,
+                           stream=None) -> torch.Tensor:
+    """Causal prompt attention (q fp16 [B, Hq, n, D], k, v fp16 [B, Hkv, n, D] on the
+    device) with the cache quantized from the same k, v in the same kernel; with
+    cache=None (and the cache geometry in `dims`) the attention alone."""
+    _f16(q, "q"), _f16(k, "k"), _f16(v, "v")
+    if out is None:
+        out = torch.empty_like(q)
+    _f16(out, "out")
+    B, Hq, n, D = q.shape
+    if cache is not None:
+        d, c = ctypes.byref(cache.dims), ctypes.byref(cache.c)
+    else:
+        if dims is None:
+            raise ValueError("attention alone needs the geometry in `dims`")
+        d, c = ctypes.byref(dims), None
+    _check(lib().kivi_prefill_attention(d, c, _ptr(q), Hq, _ptr(k), _ptr(v), n, float(softmax_scale), _ptr(out),
+                                        _stream(stream)), "kivi_prefill_attention")
+    return out
 
 
 def kivi_append_token(cache: Cache, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:

@@ -116,6 +116,22 @@ def make_step(wl: Workload, pre: Prefill, step: int):
     return k, v, q
 
 
+def make_prompt_queries(wl: Workload, n: int | None = None) -> torch.Tensor:
+    """fp16 [B, Hq, n, D]: the prompt's own queries, N(0,1)/sqrt(D) like the decode
+    queries, drawn from a generator of their own (the prompt's K and V draws are
+    unchanged)."""
+    n = wl.n if n is None else n
+    gen = _gen(wl.seed * 1_000_003 + 999_983)
+    out = torch.empty((wl.B, wl.Hq, n, wl.D), dtype=torch.float16)
+    flat = out.view(-1, wl.D)
+    rows = 1 << 22
+    for r0 in range(0, flat.shape[0], rows):
+        r1 = min(flat.shape[0], r0 + rows)
+        flat[r0:r1] = (torch.randn((r1 - r0, wl.D), generator=gen, dtype=torch.float32) / math.sqrt(wl.D)).to(
+            torch.float16)
+    return out
+
+
 def small(name: str, B: int, Hq: int, Hkv: int, G: int, n: int, seed: int, steps: int = 0,
           factor_lo: float = 50.0, factor_hi: float = 50.0, outliers: int = 2) -> Workload:
     """A reduced workload with the same distributions, for oracle-sized parity cases."""

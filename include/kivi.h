@@ -190,6 +190,26 @@ KIVI_API int kivi_decode_step(const kivi_dims *dims, kivi_cache *cache, const ui
                               uint16_t *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Fused prefill: the prompt's causal attention over its full-precision keys and
+ * values, with the cache quantized from the same key and value tiles while they are
+ * on chip (section "Kod ve Entegrasyon Haritasi": FlashAttention runs the prefill,
+ * KIVI quantizes the cache; headline paragraph and section "Iddia ve Gerceklik",
+ * paragraphs 2-3, for the cache).  For every batch b, query head h and prompt
+ * position i:
+ *   out[b][h][i] = sum_{j <= i} softmax_j(softmax_scale * q[b][h][i] . k[b][h / (Hq/Hkv)][j])
+ *                  v[b][h / (Hq/Hkv)][j].
+ * q, out: fp16 [B][Hq][n][D]; k, v: fp16 [B][Hkv][n][D]; all device, 16-byte aligned.
+ * With a cache, it is written exactly as kivi_quantize_prefill(k, v, n) writes it
+ * (codes, scales and zeros bit for bit; the residual; n_tokens = n); cache == NULL
+ * computes the attention alone.  The probabilities enter the P.V contraction as an
+ * fp16 pair hi + lo.  n <= 0: KIVI_ERR_ARG; with a cache, n > max_tokens:
+ * KIVI_ERR_CAPACITY; B * Hq > 65535: KIVI_ERR_UNSUPPORTED.  Nothing is allocated.
+ */
+KIVI_API int kivi_prefill_attention(const kivi_dims *dims, kivi_cache *cache, const uint16_t *q, int32_t Hq,
+                                    const uint16_t *k, const uint16_t *v, int64_t n, float softmax_scale,
+                                    uint16_t *out, cudaStream_t stream);
+
+/*
  * Test aid: write the dequantized cache as fp32 [B][Hkv][n_tokens][D] to k_out and
  * v_out (device, caller-owned).  Quantized entries are fp32(z) + code * fp32(s)
  * (exact product, one rounding); residual keys are copied exactly.

@@ -83,6 +83,8 @@ def lib():
             L.oracle_prefill_attention_head.restype = i32
             L.oracle_prefill_attention.argtypes = [i32, i32, i32, i32, i64, P, P, P, f64, P]
             L.oracle_prefill_attention.restype = i32
+            L.oracle_prefill_attention_rows.argtypes = [i32, i64, i64, P, P, P, P, f64, P]
+            L.oracle_prefill_attention_rows.restype = i32
             _lib = L
         return _lib
 
@@ -312,4 +314,17 @@ def prefill_attention(q, k, v, sigma: float) -> np.ndarray:
     out = np.zeros((B, Hq, n, D), np.float64)
     if lib().oracle_prefill_attention(B, Hq, Hkv, D, n, _ptr(qb), _ptr(kb), _ptr(vb), float(sigma), _ptr(out)) != 0:
         raise ValueError("oracle prefill attention: empty prompt or Hq % Hkv != 0")
+    return out
+
+
+def prefill_attention_rows(q, k, v, rows, sigma: float) -> np.ndarray:
+    """R12 at selected positions of one head: q, k, v fp16 [n, D], rows int [nr] ->
+    out [nr, D] fp64 (the rows of prefill_attention for this head)."""
+    qb, kb, vb = _f16_bits(q), _f16_bits(k), _f16_bits(v)
+    n, D = qb.shape
+    r = np.ascontiguousarray(np.asarray(rows, np.int64))
+    out = np.zeros((len(r), D), np.float64)
+    if lib().oracle_prefill_attention_rows(D, n, len(r), _ptr(r), _ptr(qb), _ptr(kb), _ptr(vb), float(sigma),
+                                           _ptr(out)) != 0:
+        raise ValueError("oracle prefill attention rows: empty prompt or a position outside it")
     return out

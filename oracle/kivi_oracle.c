@@ -410,30 +410,48 @@ int oracle_attention_raw_head(int D, int64_t n, const uint16_t *k, const uint16_
  *   out_i = sum_{j <= i} p_ij v_j,  p_i = softmax_j (sigma * q_i . k_j) over j <= i.
  * Returns 0, or -1 when n <= 0.
  */
+/* One row of R12: position i's query q_i [D] over keys and values 0 .. i; score is
+ * scratch space of i + 1 doubles. */
+static void prefill_attention_row(int D, int64_t i, const uint16_t *q_i, const uint16_t *k, const uint16_t *v,
+                                  double sigma, double *score, double *o) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j <= i; ++j) {
+    double acc = 0.0;
+    for (int c = 0; c < D; ++c) acc += (double)h2f(q_i[c]) * (double)h2f(k[(size_t)j * D + c]);
+    score[j] = sigma * acc;
+    if (score[j] > m) m = score[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    score[j] = exp(score[j] - m);
+    l += score[j];
+  }
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    double p = score[j] / l;
+    for (int c = 0; c < D; ++c) o[c] += p * (double)h2f(v[(size_t)j * D + c]);
+  }
+}
+
 int oracle_prefill_attention_head(int D, int64_t n, const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                   double sigma, double *out) {
   if (n <= 0) return -1;
   double *score = (double *)malloc((size_t)n * sizeof(double));
-  for (int64_t i = 0; i < n; ++i) {
-    double m = -INFINITY;
-    for (int64_t j = 0; j <= i; ++j) {
-      double acc = 0.0;
-      for (int c = 0; c < D; ++c) acc += (double)h2f(q[(size_t)i * D + c]) * (double)h2f(k[(size_t)j * D + c]);
-      score[j] = sigma * acc;
-      if (score[j] > m) m = score[j];
-    }
-    double l = 0.0;
-    for (int64_t j = 0; j <= i; ++j) {
-      score[j] = exp(score[j] - m);
-      l += score[j];
-    }
-    double *o = out + (size_t)i * D;
-    for (int c = 0; c < D; ++c) o[c] = 0.0;
-    for (int64_t j = 0; j <= i; ++j) {
-      double p = score[j] / l;
-      for (int c = 0; c < D; ++c) o[c] += p * (double)h2f(v[(size_t)j * D + c]);
-    }
-  }
+  for (int64_t i = 0; i < n; ++i) prefill_attention_row(D, i, q + (size_t)i * D, k, v, sigma, score, out + (size_t)i * D);
+  free(score);
+  return 0;
+}
+
+/* R12 at selected positions of one head: rows[r] in [0, n), q [n][D] the head's queries,
+ * out [nr][D] fp64.  Returns 0, or -1 on an empty prompt or a position outside it. */
+int oracle_prefill_attention_rows(int D, int64_t n, int64_t nr, const int64_t *rows, const uint16_t *q,
+                                  const uint16_t *k, const uint16_t *v, double sigma, double *out) {
+  if (n <= 0) return -1;
+  for (int64_t r = 0; r < nr; ++r)
+    if (rows[r] < 0 || rows[r] >= n) return -1;
+  double *score = (double *)malloc((size_t)n * sizeof(double));
+  for (int64_t r = 0; r < nr; ++r)
+    prefill_attention_row(D, rows[r], q + (size_t)rows[r] * D, k, v, sigma, score, out + (size_t)r * D);
   free(score);
   return 0;
 }

@@ -103,3 +103,19 @@ def test_empty_prompt_and_bad_heads_are_errors():
     kv = np.zeros((1, 2, 4, D), np.float16)
     with pytest.raises(ValueError):
         oracle.prefill_attention(q, kv, kv, 1.0)
+
+
+def test_selected_rows_are_the_rows_of_the_whole_prompt():
+    """The selected-rows entry (used where the whole prompt is too long for the
+    oracle) gives, bit for bit, the rows of the whole-prompt attention, which the
+    closed forms above pin; positions outside the prompt are errors."""
+    rng = np.random.default_rng(21)
+    n = 150
+    q, k, v = _rand(rng, 1, 1, n, D, scale=0.2), _rand(rng, 1, 1, n, D), _rand(rng, 1, 1, n, D)
+    full = oracle.prefill_attention(q, k, v, 0.8)[0, 0]
+    rows = [0, 1, 63, 64, 65, 149, 7]
+    got = oracle.prefill_attention_rows(q[0, 0], k[0, 0], v[0, 0], rows, 0.8)
+    assert np.array_equal(got, full[rows])
+    assert np.array_equal(oracle.prefill_attention_rows(q[0, 0], k[0, 0], v[0, 0], [0], 0.8)[0], v[0, 0, 0])
+    with pytest.raises(ValueError):
+        oracle.prefill_attention_rows(q[0, 0], k[0, 0], v[0, 0], [n], 0.8)
