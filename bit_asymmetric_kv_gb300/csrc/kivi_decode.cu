@@ -547,6 +547,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   // the head's largest |q * f| below 2^14; with every scale of a group below
   // 2^(es + 1) and scaled by 2^-es, each B entry stays below 2^15
   float qa[R][4];
+  // 1.5 * 2^23 * u_h: adding and subtracting it times f rounds an entry x to the grid
+  // u_h * f of the hi parts (see write_frag); u_h = 2^(E_h - 8), E_h = floor(log2 of the
+  // head's largest |q| * 2^A), so that every |x| / (u_h * f) stays below 2^10
+  float gu[R];
   float cqh = 0.f, cbh = 0.f;  // c0 * 2^(SH - A) and c0 * 2^-A of this lane's head
   auto q_row = [&](int64_t b, int64_t kvh) { return a.q + (b * a.Hq + kvh * R) * kD; };
   auto load_q = [&](const uint16_t *qh) {
@@ -560,11 +564,14 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
       x[2] = h2f((uint16_t)(w01 >> 16)) * fb;
       x[3] = h2f((uint16_t)(wd >> 16)) * fb;
       const float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+      const float my = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])) * ifa, fmaxf(fabsf(x[2]), fabsf(x[3])) * ifb);
       const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(mx));
+      const uint32_t yb = __reduce_max_sync(kFull, __float_as_uint(my));
       const int A = min(100, max(-100, 13 - ((int)(mb >> 23) - 127)));
       const float sc = pow2i(A);
 #pragma unroll
       for (int k = 0; k < 4; ++k) qa[hh][k] = x[k] * sc;
+      gu[hh] = 1.5f * pow2i(min(100, max(-100, (int)(yb >> 23) - 127 + A + 15)));
       if (hh == head_mine) {
         cqh = c0 * pow2i(SH - A);
         cbh = c0 * pow2i(-A);
@@ -868,23 +875,22 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     // B fragment of group gi: hi and lo rows of every head
     // The hi parts lie on a grid: the tensor cores add the 16 products of an MMA
     // k-step keeping only about 15 bits below the largest of them, so hi is rounded
-    // to a multiple of u = 2^(e - 7), e = floor(log2 max |y|) over the group's channels,
-    // y = x / f the entry without its code factor.  Every hi product is then
-    // code * 64 * 2^-24 * (a multiple of u), at most 3 * 2^8 units, and the MMA adds
-    // them exactly; lo = x - hi (below u/2) carries the rest in fp16, and its own
-    // sums lose at most about 2^-23 of the largest entry.
+    // to a multiple of u_h * f.  Every scaled scale of a group is below 2, so every
+    // |x| / f is below 2^(E_h + 2) = 2^10 u_h, every hi product is code * 64 * 2^-24 *
+    // (a multiple of u_h) of at most 3 * 2^10 units, and the MMA adds them exactly;
+    // lo = x - hi (at most u_h * f / 2) carries the rest in fp16, and its own sums lose
+    // at most about 2^-23 of the head's largest entry.
     auto write_frag = [&](int gi) {
       uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
 #pragma unroll
       for (int hh = 0; hh < R; ++hh) {
         const float x0 = qa[hh][0] * sp[gi][0], x1 = qa[hh][1] * sp[gi][1];
         const float x2 = qa[hh][2] * sp[gi][2], x3 = qa[hh][3] * sp[gi][3];
-        const float ym = fmaxf(fmaxf(fabsf(x0), fabsf(x1)) * ifa, fmaxf(fabsf(x2), fabsf(x3)) * ifb);
-        const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(ym));
-        const int ge = min(120, max(-126, (int)(mb >> 23) - 127 - 7));
-        const float ca = pow2i(-ge) * ifa, da = pow2i(ge) * fa, cb = pow2i(-ge) * ifb, db = pow2i(ge) * fb;
-        const float h0 = rintf(x0 * ca) * da, h1 = rintf(x1 * ca) * da;
-        const float h2 = rintf(x2 * cb) * db, h3 = rintf(x3 * cb) * db;
+        // fp32 round to nearest even onto the grid: |x| / (u_h f) < 2^10, far inside
+        // the 2^22 that adding and subtracting 1.5 * 2^23 * u_h * f needs
+        const float ma = gu[hh] * fa, mbg = gu[hh] * fb;
+        const float h0 = __fsub_rn(__fadd_rn(x0, ma), ma), h1 = __fsub_rn(__fadd_rn(x1, ma), ma);
+        const float h2 = __fsub_rn(__fadd_rn(x2, mbg), mbg), h3 = __fsub_rn(__fadd_rn(x3, mbg), mbg);
         const __half2 hA = __floats2half2_rn(h0, h1), hB = __floats2half2_rn(h2, h3);
         const __half2 lA = __floats2half2_rn(x0 - h0, x1 - h1), lB = __floats2half2_rn(x2 - h2, x3 - h3);
         *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) = make_uint2(h22u(hA), h22u(hB));
@@ -994,30 +1000,35 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     // with outlier channels): lane (g, tig) scores tokens 16t + g and 16t + g + 8 of
     // its tile slot t of every round, for its head.  The hi/lo column pair of the MMA
     // layout becomes (score, 0).
-    const uint16_t *qh_row = cursor_q(cc) + head_mine * kD;
-    auto dot = [&](const uint16_t *krow) {
-      const uint4 *qp = reinterpret_cast<const uint4 *>(qh_row), *kp = reinterpret_cast<const uint4 *>(krow);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < kD / 8; ++c) {
-        const uint4 qq = __ldg(qp + c), kk = __ldg(kp + c);
-        const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w}, kw4[4] = {kk.x, kk.y, kk.z, kk.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 a = __half22float2(u2h2(qw[i])), b = __half22float2(u2h2(kw4[i]));
-          s0 = fmaf(a.x, b.x, s0);
-          s1 = fmaf(a.y, b.y, s1);
-        }
-      }
-      return s0 + s1;
-    };
+    const uint4 *qp = reinterpret_cast<const uint4 *>(cursor_q(cc) + head_mine * kD);
     float sc[R][4];
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) {
       const int sa = 16 * (rho * T + slot_mine) + g, sb = sa + 8;
-      sc[rho][0] = sa < r ? dot(res_head + sa * kD) : 0.f;
+      const bool va = sa < r, vb = sb < r;
+      const uint4 *ka = reinterpret_cast<const uint4 *>(res_head + (va ? sa : 0) * kD);
+      const uint4 *kb = reinterpret_cast<const uint4 *>(res_head + (vb ? sb : 0) * kD);
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+      if (va || vb) {  // the two keys of the lane share each query load
+#pragma unroll 4
+        for (int c = 0; c < kD / 8; ++c) {
+          const uint4 qq = __ldg(qp + c), xa = __ldg(ka + c), xb = __ldg(kb + c);
+          const uint32_t qw[4] = {qq.x, qq.y, qq.z, qq.w}, wa[4] = {xa.x, xa.y, xa.z, xa.w};
+          const uint32_t wb[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 fq = __half22float2(u2h2(qw[i]));
+            const float2 fa2 = __half22float2(u2h2(wa[i])), fb2 = __half22float2(u2h2(wb[i]));
+            a0 = fmaf(fq.x, fa2.x, a0);
+            a1 = fmaf(fq.y, fa2.y, a1);
+            b0 = fmaf(fq.x, fb2.x, b0);
+            b1 = fmaf(fq.y, fb2.y, b1);
+          }
+        }
+      }
+      sc[rho][0] = va ? a0 + a1 : 0.f;
       sc[rho][1] = 0.f;
-      sc[rho][2] = sb < r ? dot(res_head + sb * kD) : 0.f;
+      sc[rho][2] = vb ? b0 + b1 : 0.f;
       sc[rho][3] = 0.f;
     }
     // residual values are quantized ({s, z} of their row) or, with a value residual,
