@@ -23,9 +23,10 @@
 // and the last one it loads, after its attention.  Key groups of G tokens per channel
 // (a 64-token tile holds 64/G whole groups), value rows per token, the last n mod G
 // keys (and values, with a value residual) copied to the residual buffers.  The
-// rounding rule is the library's: make_qparams and quant_code of kivi_device.cuh
-// (fp32 RNE, the comparison form for 2-bit codes, an IEEE division for 4-bit codes),
-// so the cache is bit for bit the one kivi_quantize_prefill writes.
+// rounding rule is the library's (kivi_device.cuh: make_qparams, the proven fp16
+// thresholds of 2-bit codes with the fp32 comparison form as the fallback, the
+// reciprocal product of 4-bit codes), so the cache is bit for bit the one
+// kivi_quantize_prefill writes.
 #include <math.h>
 
 #include "kivi_device.cuh"
@@ -73,87 +74,191 @@ __device__ __forceinline__ void pcp_async16(void *smem, const void *gmem, bool v
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) { return h22u(__floats2half2_rn(lo, hi)); }
 
-// Quantize key/value tile qt of one (batch, KV head), staged in shared memory as 64
-// rows of kPRow bytes (rows past the prompt hold zeros and are not written).  All
-// threads of the CTA take part; `scratch` holds 64/G x 128 parameter sets.
+// Pieces of LPW lanes x LPW rows transposed across the lanes.  Before, lane j holds
+// its piece of row i at bits [PB*i, PB*i + PB); after, lane j holds row j, with lane
+// i's piece at bits [PB*i, PB*i + PB).  Stage d swaps the off-diagonal blocks of
+// size d between lanes j and j ^ d (d = LPW/2 .. 1): log2(LPW) shuffles for LPW rows.
+template <int LPW, int PB>
+__device__ __forceinline__ uint32_t transpose_pieces(uint32_t A, int j) {
+#pragma unroll
+  for (int d = LPW / 2; d >= 1; d >>= 1) {
+    uint32_t lo = 0;  // the pieces whose index has bit d clear
+#pragma unroll
+    for (int i = 0; i < 32 / PB; ++i)
+      if (!(i & d)) lo |= ((1u << PB) - 1u) << (PB * i);
+    const bool up = (j & d) != 0;
+    const uint32_t send = up ? (A & lo) << (PB * d) : (A & ~lo) >> (PB * d);
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, d);
+    A = (up ? (A & ~lo) : (A & lo)) | recv;
+  }
+  return A;
+}
+
+// Quantize key/value tile t0 / 64 of one (batch, KV head), staged in shared memory as
+// 64 rows of kPRow bytes (rows past the prompt hold zeros and are not written).  All
+// threads of the CTA take part; `scratch` holds 1 KB.
+// Keys: thread (rh, cp) = (tid / 64, tid % 64) holds channels 2cp, 2cp+1 of rows
+// 32rh .. 32rh+31 in registers (one whole group for G = 32; with G = 64 the two row
+// halves merge their min/max through `scratch`), derives both channels' parameters
+// and codes each row, two codes per lane; a transpose across the LPW lanes of a word
+// then gives each lane one packed word of one row.  Values: 4 lanes per row, lane
+// (q, r8) = (lane / 8, lane % 8) holding channels 32q .. 32q+31 of row r8 of its
+// 8-row step, so that the 8 lanes of a shared-memory phase read 8 different rows.
+// 2-bit codes come from fp16 thresholds (the per-element fp32 form when a warp holds
+// a threshold that is not proven), 4-bit codes from the reciprocal product: the rule
+// and its fast forms are those of the standalone quantizers, bit for bit.
 template <int BITS>
 __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, const unsigned char *ks,
-                              const unsigned char *vs, QParams *scratch) {
+                              const unsigned char *vs, unsigned char *scratch) {
   constexpr int WPR = words_per_row<BITS>();
-  constexpr int CPW = 32 / BITS;  // channels (codes) per packed word
+  constexpr int PB = 2 * BITS;   // bits of one lane's two codes
+  constexpr int LPW = 32 / PB;   // lanes (channel pairs) per packed word
   const int G = a.G;
   const int64_t n = a.n, nq = (n / G) * G;
   const int64_t t_end = min(n, t0 + kPTile);
-  const int tid = threadIdx.x;
-  // ---- key groups: thread c derives channel c's parameters for each whole group
-  const int ngroups = kPTile / G;
-  for (int gi = 0; gi < ngroups; ++gi) {
-    const int64_t g0 = t0 + (int64_t)gi * G;
-    if (g0 + G > nq) break;  // not a whole quantized group (the residual, or past the prompt)
-    const int c = tid;
-    __half mn = __ushort_as_half(*reinterpret_cast<const uint16_t *>(ks + (gi * G) * kPRow + 2 * c));
-    __half mx = mn;
-    for (int r = 1; r < G; ++r) {
-      const __half x = __ushort_as_half(*reinterpret_cast<const uint16_t *>(ks + (gi * G + r) * kPRow + 2 * c));
-      mn = __hmin(mn, x);
-      mx = __hmax(mx, x);
-    }
-    const QParams p = make_qparams<BITS>(__half2float(mn), __half2float(mx));
-    scratch[gi * kD + c] = p;
-    a.k_meta[(bh * (a.max_tokens / G) + g0 / G) * kD + c] = p.meta;
-  }
-  __syncthreads();
-  // codes: item = (token row r of a whole group, word w)
-  for (int it = tid; it < kPTile * WPR; it += kPThreads) {
-    const int r = it / WPR, w = it - r * WPR;
-    const int64_t t = t0 + r;
-    if (t >= nq) continue;
-    const QParams *pp = scratch + (r / G) * kD + w * CPW;
-    const uint16_t *x = reinterpret_cast<const uint16_t *>(ks + r * kPRow) + w * CPW;
-    uint32_t bits = 0;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  // ---- key groups
+  const int cp = tid & 63, rh = tid >> 6;
+  uint32_t x[32];
 #pragma unroll
-    for (int i = 0; i < CPW; ++i) bits |= quant_code<BITS>(h2f(x[i]), pp[i]) << (BITS * i);
-    a.k_codes[(bh * a.max_tokens + t) * WPR + w] = bits;
+  for (int r = 0; r < 32; ++r) x[r] = *reinterpret_cast<const uint32_t *>(ks + (32 * rh + r) * kPRow + 4 * cp);
+  __half2 mn = u2h2(x[0]), mx = mn;
+#pragma unroll
+  for (int r = 1; r < 32; ++r) {
+    mn = __hmin2(mn, u2h2(x[r]));
+    mx = __hmax2(mx, u2h2(x[r]));
   }
-  // the residual keys: positions nq .. n - 1 that lie in this tile
+  if (G == 64) {  // uniform over the CTA
+    uint2 *s_mm = reinterpret_cast<uint2 *>(scratch);
+    s_mm[tid] = make_uint2(h22u(mn), h22u(mx));
+    __syncthreads();
+    const uint2 o = s_mm[tid ^ 64];
+    mn = __hmin2(mn, u2h2(o.x));
+    mx = __hmax2(mx, u2h2(o.y));
+  }
+  const int64_t g0 = G == 32 ? t0 + 32 * rh : t0;  // first token of this thread's group
+  const bool whole = g0 + G <= nq;                  // a quantized group (not the residual)
+  const QParams p0 = make_qparams<BITS>(__low2float(mn), __low2float(mx));
+  const QParams p1 = make_qparams<BITS>(__high2float(mn), __high2float(mx));
+  if (whole && (G == 32 || rh == 0))
+    *reinterpret_cast<uint2 *>(a.k_meta + (bh * (a.max_tokens / G) + g0 / G) * kD + 2 * cp) =
+        make_uint2(p0.meta, p1.meta);
+  uint32_t T1 = 0, T2 = 0, T3 = 0;
+  bool fast = true;
+  float rs0 = 0.f, rs1 = 0.f;
+  if constexpr (BITS == 2) {
+    uint32_t a1, a2, a3, b1, b2, b3;
+    bool oa, ob;
+    fp16_thresholds(p0, a1, a2, a3, oa);
+    fp16_thresholds(p1, b1, b2, b3, ob);
+    T1 = a1 | (b1 << 16);
+    T2 = a2 | (b2 << 16);
+    T3 = a3 | (b3 << 16);
+    fast = __all_sync(0xffffffffu, oa && ob);
+  } else {
+    rs0 = __frcp_rn(p0.s);
+    rs1 = __frcp_rn(p1.s);
+  }
+#pragma unroll
+  for (int blk = 0; blk < 32 / LPW; ++blk) {
+    uint32_t A = 0;
+#pragma unroll
+    for (int i = 0; i < LPW; ++i) {
+      const uint32_t v = x[blk * LPW + i];
+      uint32_t pc;
+      if constexpr (BITS == 2) {
+        if (fast) {
+          const __half2 h = u2h2(v);
+          const uint32_t m1 = __hgt2_mask(h, u2h2(T1)), m2 = __hgt2_mask(h, u2h2(T2));
+          const uint32_t m3 = __hgt2_mask(h, u2h2(T3));
+          // nested masks: the code's low bit is their parity, its high bit the middle one
+          const uint32_t c = ((m1 ^ m2 ^ m3) & 0x00010001u) | (m2 & 0x00020002u);
+          pc = (c | (c >> 14)) & 0xFu;
+        } else {
+          pc = quant_code<2>(h2f((uint16_t)(v & 0xffffu)), p0) | (quant_code<2>(h2f((uint16_t)(v >> 16)), p1) << 2);
+        }
+      } else {
+        pc = code4(h2f((uint16_t)(v & 0xffffu)), p0.mn, p0.s, rs0) |
+             (code4(h2f((uint16_t)(v >> 16)), p1.mn, p1.s, rs1) << 4);
+      }
+      A |= pc << (PB * i);
+    }
+    const int j = lane % LPW;
+    const uint32_t word = transpose_pieces<LPW, PB>(A, j);
+    if (whole) a.k_codes[(bh * a.max_tokens + t0 + 32 * rh + blk * LPW + j) * WPR + cp / LPW] = word;
+  }
+  // the residual keys (and values): positions nq .. n - 1 that lie in this tile
   for (int it = tid; it < kPTile * (kD / 8); it += kPThreads) {
     const int r = it / (kD / 8), ch = it - r * (kD / 8);
     const int64_t t = t0 + r;
     if (t < nq || t >= t_end) continue;
-    const uint4 x = *reinterpret_cast<const uint4 *>(ks + r * kPRow + 16 * ch);
-    *reinterpret_cast<uint4 *>(a.k_res + (bh * G + (t - nq)) * kD + 8 * ch) = x;
+    const uint4 xk = *reinterpret_cast<const uint4 *>(ks + r * kPRow + 16 * ch);
+    *reinterpret_cast<uint4 *>(a.k_res + (bh * G + (t - nq)) * kD + 8 * ch) = xk;
     if (a.v_res) {
       const uint4 y = *reinterpret_cast<const uint4 *>(vs + r * kPRow + 16 * ch);
       *reinterpret_cast<uint4 *>(a.v_res + (bh * G + (t - nq)) * kD + 8 * ch) = y;
     }
   }
-  // ---- value rows: one warp per row, lane l holds channels 4l .. 4l+3
-  const int warp = tid >> 5, lane = tid & 31;
+  // ---- value rows
   const int64_t nv = a.v_res ? nq : n;  // values quantized per token
-  for (int r = warp; r < kPTile; r += kPWarps) {
+  const int vq = lane >> 3, vr = lane & 7, warp = tid >> 5;
+  for (int r0 = 8 * warp; r0 < kPTile; r0 += 8 * kPWarps) {
+    const int r = r0 + vr;
     const int64_t t = t0 + r;
-    if (t >= nv) break;
-    const uint2 xw = *reinterpret_cast<const uint2 *>(vs + r * kPRow + 8 * lane);
-    const __half2 x01 = u2h2(xw.x), x23 = u2h2(xw.y);
-    __half2 mn2 = __hmin2(x01, x23), mx2 = __hmax2(x01, x23);
-    __half mn = __hmin(__low2half(mn2), __high2half(mn2)), mx = __hmax(__low2half(mx2), __high2half(mx2));
+    const bool ok_row = t < nv;
+    uint32_t xv[4][4];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      mn = __hmin(mn, __ushort_as_half((uint16_t)__shfl_xor_sync(0xffffffffu, __half_as_ushort(mn), off)));
-      mx = __hmax(mx, __ushort_as_half((uint16_t)__shfl_xor_sync(0xffffffffu, __half_as_ushort(mx), off)));
+    for (int k = 0; k < 4; ++k) {
+      const uint4 c = *reinterpret_cast<const uint4 *>(vs + r * kPRow + 16 * (4 * vq + k));
+      xv[k][0] = c.x;
+      xv[k][1] = c.y;
+      xv[k][2] = c.z;
+      xv[k][3] = c.w;
     }
-    const QParams p = make_qparams<BITS>(__half2float(mn), __half2float(mx));
-    uint32_t bits = quant_code<BITS>(__low2float(x01), p) | (quant_code<BITS>(__high2float(x01), p) << BITS) |
-                    (quant_code<BITS>(__low2float(x23), p) << (2 * BITS)) |
-                    (quant_code<BITS>(__high2float(x23), p) << (3 * BITS));
-    // lane l's 4 codes are channels 4l .. 4l+3: bits [4 BITS (l mod CPW/4), ...) of word l / (CPW/4)
-    constexpr int LPW = CPW / 4;  // lanes per word: 4 (2-bit) or 2 (4-bit)
-    bits <<= 4 * BITS * (lane % LPW);
+    __half2 mn2 = u2h2(xv[0][0]), mx2 = mn2;
 #pragma unroll
-    for (int off = 1; off < LPW; off <<= 1) bits |= __shfl_xor_sync(0xffffffffu, bits, off);
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int e = (k == 0 ? 1 : 0); e < 4; ++e) {
+        mn2 = __hmin2(mn2, u2h2(xv[k][e]));
+        mx2 = __hmax2(mx2, u2h2(xv[k][e]));
+      }
+    // (min, -max) so that one __hmin2 reduces both over the row's 4 lanes
+    __half2 red = __halves2half2(__hmin(__low2half(mn2), __high2half(mn2)),
+                                 __hneg(__hmax(__low2half(mx2), __high2half(mx2))));
+    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 8)));
+    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 16)));
+    const QParams p = make_qparams<BITS>(__low2float(red), -__high2float(red));
     uint32_t *row = a.v_codes + (bh * a.max_tokens + t) * WPR;
-    if (lane % LPW == 0) row[lane / LPW] = bits;
-    if (lane == 0) a.v_meta[bh * a.max_tokens + t] = p.meta;
+    if constexpr (BITS == 2) {
+      // lane q < 3 of the row proves threshold q + 1 (X2 is the strict one: d >= t2)
+      bool ok = true;
+      uint32_t xq = 0x7c00u;
+      if (p.s != 0.f && vq < 3) xq = fp16_threshold(p.mn, vq == 0 ? p.t1 : (vq == 1 ? p.t2 : p.t3), vq == 1, ok);
+      const uint32_t x1 = __shfl_sync(0xffffffffu, xq, vr), x2 = __shfl_sync(0xffffffffu, xq, vr + 8),
+                     x3 = __shfl_sync(0xffffffffu, xq, vr + 16);
+      uint32_t c[4];
+      if (__all_sync(0xffffffffu, ok)) {
+        const uint32_t p1 = x1 | (x1 << 16), p2 = x2 | (x2 << 16), p3 = x3 | (x3 << 16);
+        const uint32_t X1[4] = {p1, p1, p1, p1}, X2[4] = {p2, p2, p2, p2}, X3[4] = {p3, p3, p3, p3};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = codes2_chunk8(xv[k], X1, X2, X3);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) c[k] = quant_chunk8<2>(make_uint4(xv[k][0], xv[k][1], xv[k][2], xv[k][3]), p);
+      }
+      // chunks 4q .. 4q+3 are words 2q (chunks 4q, 4q+1) and 2q+1
+      if (ok_row)
+        *reinterpret_cast<uint2 *>(row + 2 * vq) =
+            make_uint2((c[0] & 0xffffu) | (c[1] << 16), (c[2] & 0xffffu) | (c[3] << 16));
+    } else {
+      uint32_t c[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) c[k] = qchunk8<4>(make_uint4(xv[k][0], xv[k][1], xv[k][2], xv[k][3]), p);
+      if (ok_row) *reinterpret_cast<uint4 *>(row + 4 * vq) = make_uint4(c[0], c[1], c[2], c[3]);
+    }
+    if (ok_row && vq == 0) a.v_meta[bh * a.max_tokens + t] = p.meta;
   }
 }
 
@@ -321,7 +426,7 @@ __global__ void __launch_bounds__(kPThreads) prefill_kernel(const PrefillArgs a)
   // still staged in shared memory (the last tile it loaded)
   if (a.k_codes && h % R == 0) {
     const unsigned char *ks = smem + (qt & 1) * kPStage;
-    QParams *scratch = reinterpret_cast<QParams *>(smem + ((qt + 1) & 1) * kPStage);
+    unsigned char *scratch = smem + ((qt + 1) & 1) * kPStage;
     quantize_tile<BITS>(a, bh, qt * kPTile, ks, ks + kPTileBytes, scratch);
   }
 }

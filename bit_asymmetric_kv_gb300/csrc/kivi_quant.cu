@@ -13,123 +13,6 @@
 
 namespace kivi {
 
-// ---- 2-bit codes by fp16 comparisons -------------------------------------------------
-// The 2-bit code [d > t1] + [d >= t2] + [d > t3] of d = fl32(x - mn) never decreases as
-// the fp16 input x grows (fp32 subtraction rounds monotonically), so each of its three
-// terms is [x > X] for one fp16 threshold X: the largest fp16 x for which the term is
-// 0.  fp16_threshold finds it from the estimate c = fp16 round-down of fl32(mn + t) and
-// proves it with two evaluations of the term itself: X = c when the term is 0 at c and
-// 1 at the next fp16 above c, X = the fp16 below c when the term is 1 at c and 0 there.
-// Anything else clears `ok` and the caller takes the per-element fp32 path: that needs
-// fp16 steps near mn + t finer than the fp32 rounding of d, i.e. mn + t close to zero
-// next to a large t (a minimum far below zero).  With s = 0 every term is 0: X = +inf.
-
-// Order-preserving key of fp16 bits (finite or infinite, not NaN): -0 and +0 share 0x8000.
-__device__ __forceinline__ uint32_t h16_key(uint32_t b) {
-  return (b & 0x8000u) ? 0x8000u - (b & 0x7fffu) : 0x8000u + b;
-}
-__device__ __forceinline__ uint32_t h16_from_key(uint32_t k) {
-  return k >= 0x8000u ? k - 0x8000u : (0x8000u | (0x8000u - k));
-}
-
-// strict: the term is [d >= t] (X = the largest x with d < t); else [d > t].
-__device__ __forceinline__ uint32_t fp16_threshold(float mn, float t, bool strict, bool &ok) {
-  const uint32_t c = __half_as_ushort(__float2half_rd(__fadd_rn(mn, t)));
-  const float dc = __fsub_rn(h2f((uint16_t)c), mn);
-  const bool below_c = strict ? (dc < t) : (dc <= t);  // the term is 0 at c
-  const uint32_t kc = h16_key(c);
-  const uint32_t nb = h16_from_key(below_c ? kc + 1u : kc - 1u);  // the neighbour to test
-  const float dn = __fsub_rn(h2f((uint16_t)nb), mn);
-  const bool below_n = strict ? (dn < t) : (dn <= t);
-  ok = below_c ? !below_n : below_n;
-  return below_c ? c : nb;
-}
-
-// Thresholds (X1, X2, X3) of one set of 2-bit parameters; ok as above.
-__device__ __forceinline__ void fp16_thresholds(const QParams &p, uint32_t &x1, uint32_t &x2, uint32_t &x3,
-                                                bool &ok) {
-  if (p.s == 0.f) {
-    x1 = x2 = x3 = 0x7c00u;  // +inf: every code is 0
-    ok = true;
-    return;
-  }
-  bool o1, o2, o3;
-  x1 = fp16_threshold(p.mn, p.t1, false, o1);
-  x2 = fp16_threshold(p.mn, p.t2, true, o2);
-  x3 = fp16_threshold(p.mn, p.t3, false, o3);
-  ok = o1 && o2 && o3;
-}
-
-// 2-bit codes of the 8 channels of a 16-byte chunk from fp16 thresholds: pair j of the
-// chunk (channels 2j, 2j+1) is compared with the half2 thresholds X1[j], X2[j], X3[j]
-// (one threshold per channel).  The three masks are nested, so the code's low bit is
-// their parity and its high bit the middle mask.  Channel i of the chunk lands at bits
-// [2i, 2i+1] of the low 16 bits of the result (the high 16 bits are left over).
-__device__ __forceinline__ uint32_t codes2_chunk8(const uint32_t x[4], const uint32_t X1[4], const uint32_t X2[4],
-                                                  const uint32_t X3[4]) {
-  uint32_t r = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const __half2 v = u2h2(x[j]);
-    const uint32_t m1 = __hgt2_mask(v, u2h2(X1[j]));
-    const uint32_t m2 = __hgt2_mask(v, u2h2(X2[j]));
-    const uint32_t m3 = __hgt2_mask(v, u2h2(X3[j]));
-    const uint32_t odd = m1 ^ m2 ^ m3;
-    // channel 2j at bits 4j, 4j+1 (low half); channel 2j+1 at bits 16 + 4j+2, +3
-    const uint32_t k0 = (1u << (4 * j)) | (1u << (18 + 4 * j));
-    r |= (odd & k0) | (m2 & (k0 << 1));
-  }
-  return r | (r >> 16);
-}
-
-// ---- 4-bit codes without a division per element -------------------------------------
-// The 4-bit code is clamp(rint(fl32(d / s)), 0, 15) with d = fl32(x - mn) >= 0 and the
-// fp16 scale s > 0.  With rs = 1/s rounded to nearest, q = fl32(d * rs) lies within
-// Q * 2^-23 of the quotient Q = d / s, and the correctly rounded quotient within
-// Q * 2^-24 of Q; below 64 both are under 2^-16.  So when q is more than 2^-15 from
-// every half-integer, the division rounds to the same integer as q; only there
-// does the division itself run.  q >= 64 means Q > 63: the code is 15.
-__device__ __forceinline__ uint32_t code4(float x, float mn, float s, float rs) {
-  if (s == 0.f) return 0u;
-  const float d = __fsub_rn(x, mn);
-  const float q = __fmul_rn(d, rs);
-  if (q >= 64.f) return 15u;
-  float c = rintf(q);                                   // half to even, like the division's rounding
-  if (fabsf(q - c) > 0.5f - 0x1p-15f) c = rintf(__fdiv_rn(d, s));  // q - c is exact
-  const int ci = (int)c;
-  return (uint32_t)(ci > 15 ? 15 : ci);
-}
-
-// One code of either width; rs = 1/s (used by 4-bit codes only).
-template <int BITS>
-__device__ __forceinline__ uint32_t qcode(float x, const QParams &p, float rs) {
-  if constexpr (BITS == 2) {
-    return quant_code<2>(x, p);
-  } else {
-    return code4(x, p.mn, p.s, rs);
-  }
-}
-
-// Codes of the 8 channels of a 16-byte chunk under one set of parameters (channel j at
-// bits [BITS*j, BITS*j + BITS - 1]).
-template <int BITS>
-__device__ __forceinline__ uint32_t qchunk8(const uint4 &c, const QParams &p) {
-  if constexpr (BITS == 2) {
-    return quant_chunk8<2>(c, p);
-  } else {
-    const float rs = __frcp_rn(p.s);
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t bits = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      bits |= code4(h2f((uint16_t)(w[k] & 0xffffu)), p.mn, p.s, rs) << (8 * k);
-      bits |= code4(h2f((uint16_t)(w[k] >> 16)), p.mn, p.s, rs) << (8 * k + 4);
-    }
-    return bits;
-  }
-}
-
-
 // Row of token t of head bh in a paged pool (false: the block table gives no page
 // of the pool for it, and the row is skipped).
 __device__ __forceinline__ bool paged_row(const PageMap &pm, int64_t bh, int64_t t, int64_t *row) {

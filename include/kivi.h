@@ -166,6 +166,12 @@ KIVI_API size_t kivi_decode_workspace_bytes(const kivi_dims *dims, int32_t Hq, i
  * the last n mod G tokens, and V'_t = z_t + code * s_t.  q, out: fp16 [B][Hq][D]
  * device.  ws: device workspace of at least kivi_decode_workspace_bytes() bytes,
  * caller-owned, contents overwritten.  n_tokens == 0 returns KIVI_ERR_ARG.
+ * Small contexts (at most 16 units per (batch, KV head), a unit being 64 quantized
+ * tokens or the residual, and no more (batch, KV head) pairs than SMs) run on one
+ * CTA per pair, which leaves ws unused.
+ * Device faults: every wait of the kernel for its own staged copies is bounded; a
+ * wait that runs out (a copy that never completes) makes every later output of the
+ * decode attention calls in this process NaN instead of hanging the GPU.
  */
 KIVI_API int kivi_decode_attention(const kivi_dims *dims, const kivi_cache *cache, const uint16_t *q,
                           int32_t Hq, float softmax_scale, uint16_t *out, void *ws,

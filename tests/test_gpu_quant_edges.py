@@ -19,7 +19,7 @@ import torch
 import oracle
 from bit_asymmetric_kv_gb300 import build as kbuild
 from bit_asymmetric_kv_gb300 import kivi
-from helpers import assert_cache_equal
+from helpers import assert_cache_equal, u16, u32
 
 pytestmark = pytest.mark.gpu
 
@@ -173,3 +173,28 @@ def test_adversarial_inputs_reach_the_fallback_and_the_ties():
         ties, far = _ties_and_far_thresholds(k, n, G)
     assert ties >= 20, ties
     assert far >= 1, far
+
+
+@pytest.mark.parametrize("bits,vr", [(2, 0), (4, 0), (2, 1)])
+@pytest.mark.parametrize("G,n", [(32, 32 * 12 + 7), (64, 64 * 6 + 33)])
+def test_adversarial_fused_prefill_bit_exact(G, n, bits, vr):
+    """The fused prefill (kivi_prefill_attention) quantizes its key and value tiles in
+    shared memory with the same rule and fast forms: the same adversarial prompts give
+    the oracle's cache bit for bit (GQA 2, so that one CTA per KV head quantizes)."""
+    k, v = _adversarial(2, 2, n, G, seed=300 + G + bits + vr)
+    T = ((n + G) // G) * G
+    q = torch.from_numpy((np.random.default_rng(7).standard_normal((2, 4, n, 128)) * 0.05).astype(np.float16))
+    orc = oracle.prefill(k, v, G, T, bits=bits, value_residual=bool(vr))
+    gpu = kivi.Cache.allocate(2, 2, G, T, bits=bits, value_residual=bool(vr))
+    kivi.kivi_prefill_attention(gpu, q.cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 1.0)
+    torch.cuda.synchronize()
+    assert gpu.n_tokens == n
+    if not vr:
+        assert_cache_equal(gpu, orc)
+        return
+    # with a value residual: values of whole groups quantized, the last n mod G in fp16
+    ng, nq = n // G, (n // G) * G
+    for got, ref, m in [(u32(gpu.k_codes), orc.k_codes, nq), (u32(gpu.k_meta), orc.k_meta, ng),
+                        (u16(gpu.k_res), orc.k_res, n - nq), (u32(gpu.v_codes), orc.v_codes, nq),
+                        (u32(gpu.v_meta), orc.v_meta, nq), (u16(gpu.v_res), orc.v_res, n - nq)]:
+        assert np.array_equal(got[:, :, :m], ref[:, :, :m])
