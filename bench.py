@@ -65,28 +65,32 @@ def cycle_of(wl) -> int:
     return wl.steps if wl.steps else SHORT_CYCLE
 
 
-def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2) -> int:
+def algorithmic_bytes(B: int, Hq: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2,
+                      value_group: int = 0) -> int:
     """Bytes one decode-attention launch must move at context n (D = 128, c = 16*bits
-    bytes of codes per token row): per (batch, KV head) nq*(c + 512/G) + r*256 +
-    n*(c + 4), plus q and out; with a value residual the last r values are fp16:
-    nq*(c + 4) + r*256 instead of n*(c + 4)."""
+    bytes of codes per token row, e = 4 * 128/vg bytes of value {s, z} per token):
+    per (batch, KV head) nq*(c + 512/G) + r*256 + n*(c + e), plus q and out; with a
+    value residual the last r values are fp16: nq*(c + e) + r*256 instead of n*(c + e)."""
     c = 16 * bits
+    e = 4 * (128 // (value_group or 128))
     nq = (n // G) * G
     r = n - nq
-    values = nq * (c + 4) + r * 256 if value_residual else n * (c + 4)
+    values = nq * (c + e) + r * 256 if value_residual else n * (c + e)
     per_head = nq * c + (nq // G) * 512 + r * 256 + values
     return B * Hkv * per_head + 2 * B * Hq * 128 * 2
 
 
-def prefill_bytes(B: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2) -> int:
+def prefill_bytes(B: int, Hkv: int, G: int, n: int, value_residual: bool = False, bits: int = 2,
+                  value_group: int = 0) -> int:
     """Bytes one prompt quantization must move (D = 128, c = 16*bits bytes of codes per
-    token row): fp16 K and V read once (2 * n * 256 per (batch, KV head)), then written
-    nq*(c + 512/G) + r*256 for the keys and n*(c + 4) for the values (with a value
-    residual nq*(c + 4) + r*256)."""
+    token row, e = 4 * 128/vg bytes of value {s, z}): fp16 K and V read once
+    (2 * n * 256 per (batch, KV head)), then written nq*(c + 512/G) + r*256 for the
+    keys and n*(c + e) for the values (with a value residual nq*(c + e) + r*256)."""
     c = 16 * bits
+    e = 4 * (128 // (value_group or 128))
     nq = (n // G) * G
     r = n - nq
-    values = nq * (c + 4) + r * 256 if value_residual else n * (c + 4)
+    values = nq * (c + e) + r * 256 if value_residual else n * (c + e)
     return B * Hkv * (2 * n * 256 + nq * c + (nq // G) * 512 + r * 256 + values)
 
 
@@ -210,7 +214,7 @@ def dist_env():
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
 def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False,
-                  bits: int = 2):
+                  bits: int = 2, value_group: int = 0):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
     cache) on `sample_heads` of the workload's KV heads; scale to the whole batch.
     Like the GPU loop, the cache is rolled back to the prompt every cycle_of(wl)
@@ -225,7 +229,8 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
     T = wl.capacity(extra=cycle + 64)
     k = np.stack([pre.k[b, h].numpy() for b, h in heads])[None]
     v = np.stack([pre.v[b, h].numpy() for b, h in heads])[None]
-    c0 = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits)  # untimed, like the GPU's prefill
+    c0 = oracle.prefill(k, v, wl.G, T, value_residual=value_residual, bits=bits,
+                        value_group=value_group or None)  # untimed, like the GPU's prefill
     R = wl.Hq // wl.Hkv
     t_total, done = 0.0, 0
     c = c0
@@ -258,7 +263,7 @@ def run_reference(args, wl):
     pre = synth.make_prefill(wl)
     for w in range(args.warmup):  # untimed warm-up: the first call builds the oracle
         oracle_timing(wl, pre, 1, 4, 0.0)
-    cb = oracle_timing(wl, pre, args.steps, 32, 60.0, args.value_residual, args.bits)
+    cb = oracle_timing(wl, pre, args.steps, 32, 60.0, args.value_residual, args.bits, args.value_group)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B / cb["value"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -297,12 +302,12 @@ class DenseLayout:
     profile_prefix = "decode_attention_"
     kernel = "kivi_decode_attention (decode_kernel + combine_kernel)"
 
-    def __init__(self, wl, pre, dev, value_residual=False, bits=2):
+    def __init__(self, wl, pre, dev, value_residual=False, bits=2, value_group=0):
         from bit_asymmetric_kv_gb300 import kivi
 
         self.wl, self.kivi = wl, kivi
         self.cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(extra=cycle_of(wl) + 64), device=dev,
-                                         value_residual=value_residual, bits=bits)
+                                         value_residual=value_residual, bits=bits, value_group=value_group)
         kivi.kivi_quantize_prefill(self.cache, pre.k.to(dev), pre.v.to(dev))
         self.n0 = self.cache.n_tokens
         self.res0 = self.cache.k_res.clone()
@@ -396,7 +401,7 @@ def make_layout(args, wl, pre, dev):
     if args.layout == "paged":
         return PagedLayout(wl, pre, dev, args.page_tokens, graph=args.graph, value_residual=args.value_residual,
                            bits=args.bits)
-    return DenseLayout(wl, pre, dev, value_residual=args.value_residual, bits=args.bits)
+    return DenseLayout(wl, pre, dev, value_residual=args.value_residual, bits=args.bits, value_group=args.value_group)
 
 
 # ----------------------------------------------------------------------------------------
@@ -481,14 +486,15 @@ def run_kivi(args, wl):
             attn_ms.append((e0, e1))
     torch.cuda.synchronize()
     attn_avg_ms = sum(a0.elapsed_time(a1) for a0, a1 in attn_ms) / len(attn_ms)
-    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0, args.value_residual, args.bits)
+    bytes_attn = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, n0, args.value_residual, args.bits, args.value_group)
     achieved = bytes_attn / (attn_avg_ms / 1e3) / 1e9
     peak, peak_src = measured_peak()
     sha = kernel_source_sha()
     # DRAM traffic from the committed ncu summary of this workload (named for it),
     # when it was taken on the current decode sources; never for a changed batch
     traffic = None if args.batch else profiled_traffic(sha, lay.profile_prefix + wl.name + ".md", wl.name,
-                               f"bits={args.bits}, value_residual={int(bool(args.value_residual))}")
+                               f"bits={args.bits}, value_residual={int(bool(args.value_residual))}"
+                               + (f", value_group={args.value_group}" if args.value_group else ""))
     del lay
 
     prefill = prefill_timing(args, wl, pre, dev, stream, flush)
@@ -502,7 +508,8 @@ def run_kivi(args, wl):
 
             dist.destroy_process_group()
         return 0
-    cb = oracle_timing(wl, pre, 100000, 32, 10.0, args.value_residual, args.bits) if world == 1 else None
+    cb = (oracle_timing(wl, pre, 100000, 32, 10.0, args.value_residual, args.bits, args.value_group)
+          if world == 1 else None)
     lay_cfg = make_layout_config(args)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -539,6 +546,8 @@ def make_layout_config(args):
                "api": api}
     cfg["value_residual"] = bool(args.value_residual)
     cfg["bits"] = args.bits
+    if args.value_group:
+        cfg["value_group"] = args.value_group
     return cfg
 
 
@@ -550,7 +559,8 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int
 
     from bit_asymmetric_kv_gb300 import kivi
 
-    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_residual=args.value_residual,
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_group=args.value_group,
+                                value_residual=args.value_residual,
                                 bits=args.bits)
     k, v = pre.k.to(dev), pre.v.to(dev)
     assert k.shape[2] == wl.n, (k.shape, wl.n)
@@ -564,7 +574,7 @@ def prefill_timing(args, wl, pre, dev, stream, flush, reps: int = 5, warmup: int
         torch.cuda.synchronize()
         if i >= warmup:
             ms.append(e0.elapsed_time(e1))
-    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, wl.n, args.value_residual, args.bits)
+    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, wl.n, args.value_residual, args.bits, args.value_group)
     best = min(ms)
     peak, _ = measured_peak()
     return {"ms": best, "ms_mean": sum(ms) / len(ms), "bytes": moved, "GBps": moved / best / 1e6,
@@ -615,7 +625,8 @@ def run_prefill_fused(args, wl):
     q = synth.make_prompt_queries(wl).to(dev)
     k, v = pre.k.to(dev), pre.v.to(dev)
     out = torch.empty_like(q)
-    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_residual=args.value_residual,
+    cache = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, wl.capacity(), device=dev, value_group=args.value_group,
+                                value_residual=args.value_residual,
                                 bits=args.bits)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -639,7 +650,7 @@ def run_prefill_fused(args, wl):
     quant = timed(lambda: kivi.kivi_quantize_prefill(cache, k, v, stream=stream))
     n = wl.n
     kv_bytes = 2 * wl.B * wl.Hkv * n * wl.D * 2
-    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, n, args.value_residual, args.bits)
+    moved = prefill_bytes(wl.B, wl.Hkv, wl.G, n, args.value_residual, args.bits, args.value_group)
     flops = 4.0 * wl.D * (n * (n + 1) / 2) * wl.B * wl.Hq  # q.K and P.V over the causal triangle
     peak, src = measured_peak()
     extra = fused - alone
@@ -777,6 +788,9 @@ def main(argv=None):
     ap.add_argument("--value-residual", action="store_true",
                     help="keep the last n mod G values in fp16 beside the key residual (the variant cache)")
     ap.add_argument("--bits", type=int, choices=[2, 4], default=2, help="code width of the cache (default 2)")
+    ap.add_argument("--value-group", type=int, choices=[0, 32, 64], default=0,
+                    help="channels per value scale: 0 (one per token, default) or value channel groups of 32 / 64 "
+                         "(dense 2-bit cache without a value residual)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prompt quantization (kivi_quantize_prefill) of the workload")
     ap.add_argument("--prefill-fused", action="store_true",
@@ -792,6 +806,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.value_group and (args.layout != "dense" or args.bits != 2 or args.value_residual):
+        ap.error("--value-group needs the dense 2-bit cache without --value-residual")
     if args.graph and args.layout != "paged":
         ap.error("--graph needs --layout paged (the dense step takes its token count from the host)")
     from bit_asymmetric_kv_gb300 import synth

@@ -20,6 +20,11 @@ int check_dims(const kivi_dims *d) {
   if (d->D != 128 || (d->bits != 2 && d->bits != 4) || (d->G != 32 && d->G != 64)) return KIVI_ERR_UNSUPPORTED;
   if (d->max_tokens % d->G != 0) return KIVI_ERR_ARG;
   if (d->value_residual != 0 && d->value_residual != 1) return KIVI_ERR_ARG;
+  if (d->value_group < 0) return KIVI_ERR_ARG;
+  if (d->value_group != 0 && d->value_group != 32 && d->value_group != 64 && d->value_group != 128)
+    return KIVI_ERR_UNSUPPORTED;
+  // value channel groups: built for 2-bit codes without a value residual
+  if (d->value_group != 0 && d->value_group != 128 && (d->bits != 2 || d->value_residual)) return KIVI_ERR_UNSUPPORTED;
   // token rows are indexed with int64 and buffer sizes in size_t: keep far from both
   const uint64_t heads = (uint64_t)d->B * (uint64_t)d->Hkv;  // below 2^62
   if (heads > kMaxRows || (uint64_t)d->max_tokens > kMaxRows / heads) return KIVI_ERR_UNSUPPORTED;
@@ -38,13 +43,16 @@ int check_cache(const kivi_dims *d, const kivi_cache *c) {
 // The value residual buffer the kernels use: null without the variant.
 uint16_t *vres(const kivi_dims *d, const kivi_cache *c) { return d->value_residual ? c->v_res : nullptr; }
 
+// Channels per value {s, z}: D (one per token) unless value channel groups are set.
+int vgroup(const kivi_dims *d) { return d->value_group ? d->value_group : d->D; }
+
 // Append token n of every (batch, KV head); when that fills the residual, quantize
 // it as group n / G (keys per channel; with a value residual, values per token).
 cudaError_t append_and_flush(const kivi_dims *d, const kivi_cache *c, const uint16_t *k_new,
                              const uint16_t *v_new, int64_t n, cudaStream_t st) {
   const int64_t heads = (int64_t)d->B * d->Hkv;
   cudaError_t e = kivi::launch_append(k_new, v_new, heads, n, d->G, d->bits, c->k_res, c->v_codes, c->v_meta,
-                                      d->max_tokens, vres(d, c), st);
+                                      d->max_tokens, vres(d, c), st, vgroup(d));
   if (e == cudaSuccess && (n % d->G) + 1 == d->G) {
     e = kivi::launch_key_groups(c->k_res, (int64_t)d->G * 128, heads, 1, n / d->G, d->G, d->bits, c->k_codes,
                                 c->k_meta, d->max_tokens, st);
@@ -200,7 +208,7 @@ int kivi_buffer_bytes(const kivi_dims *d, size_t out[6]) {
   out[1] = heads * (T / d->G) * d->D * sizeof(uint32_t);
   out[2] = heads * (size_t)d->G * d->D * sizeof(uint16_t);
   out[3] = heads * T * wpr * sizeof(uint32_t);
-  out[4] = heads * T * sizeof(uint32_t);
+  out[4] = heads * T * (size_t)(d->D / vgroup(d)) * sizeof(uint32_t);
   out[5] = d->value_residual ? out[2] : 0;
   return KIVI_OK;
 }
@@ -223,7 +231,7 @@ int kivi_quantize_prefill(const kivi_dims *d, kivi_cache *c, const uint16_t *k, 
     // values: all n quantized, or with a value residual the first nq and the rest kept
     const int64_t nv = d->value_residual ? nq : n;
     if (e == cudaSuccess)
-      e = kivi::launch_value_rows(v, heads, nv, n, 0, d->bits, c->v_codes, c->v_meta, d->max_tokens, st);
+      e = kivi::launch_value_rows(v, heads, nv, n, 0, d->bits, c->v_codes, c->v_meta, d->max_tokens, st, vgroup(d));
     if (e == cudaSuccess && d->value_residual) e = kivi::launch_residual_copy(v, heads, n, nq, d->G, c->v_res, st);
     if ((s = cuda_status(e)) != KIVI_OK) return s;
   }
@@ -249,7 +257,7 @@ int kivi_append_token(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, 
 int kivi_decode_splits(const kivi_dims *d, int32_t Hq, int64_t n) {
   if (check_dims(d) != KIVI_OK || check_heads(d, Hq) != KIVI_OK || n <= 0) return 0;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n, &g) != cudaSuccess) return 0;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n, &g, vgroup(d)) != cudaSuccess) return 0;
   return g.pmax;
 }
 
@@ -269,7 +277,8 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   if (!aligned16(q) || !aligned16(out)) return KIVI_ERR_ALIGN;
   if (c->n_tokens <= 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, c->n_tokens, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, c->n_tokens, &g, vgroup(d)) != cudaSuccess)
+    return KIVI_ERR_CUDA;
   const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
@@ -296,6 +305,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.grid = g.grid;
   a.pmax = g.pmax;
   a.small = g.small ? 1 : 0;
+  a.vg = vgroup(d);
   a.wait_tail = 0;
   a.softmax_scale = softmax_scale;
   return cuda_status(kivi::launch_decode(a, st));
@@ -314,7 +324,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   if (n < 0) return KIVI_ERR_ARG;
   if (n >= d->max_tokens) return KIVI_ERR_CAPACITY;
   kivi::DecodeGeom g;
-  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n + 1, &g) != cudaSuccess) return KIVI_ERR_CUDA;
+  if (kivi::decode_geometry(d->B, d->Hkv, Hq, d->G, d->bits, n + 1, &g, vgroup(d)) != cudaSuccess) return KIVI_ERR_CUDA;
   const size_t need = (size_t)d->B * (size_t)Hq * (size_t)g.pmax * (size_t)(d->D + 2) * sizeof(float);
   if (!ws || ws_bytes < need) return KIVI_ERR_WORKSPACE;
   if (!aligned16(ws)) return KIVI_ERR_ALIGN;
@@ -345,6 +355,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   a.grid = g.grid;
   a.pmax = g.pmax;
   a.small = g.small ? 1 : 0;
+  a.vg = vgroup(d);
   a.wait_tail = 1;
   a.softmax_scale = softmax_scale;
   if ((s = cuda_status(kivi::launch_decode(a, st))) != KIVI_OK) return s;
@@ -361,7 +372,7 @@ int kivi_dequantize_debug(const kivi_dims *d, const kivi_cache *c, float *k_out,
   if (c->n_tokens < 0 || c->n_tokens > d->max_tokens) return KIVI_ERR_ARG;
   return cuda_status(kivi::launch_dequant(c->k_codes, c->k_meta, c->k_res, c->v_codes, c->v_meta, vres(d, c),
                                           (int64_t)d->B * d->Hkv, c->n_tokens, d->G, d->bits, d->max_tokens, k_out, v_out,
-                                          st));
+                                          st, vgroup(d)));
 }
 
 int kivi_prefill_attention(const kivi_dims *d, kivi_cache *c, const uint16_t *q, int32_t Hq, const uint16_t *k,
@@ -394,6 +405,7 @@ int kivi_prefill_attention(const kivi_dims *d, kivi_cache *c, const uint16_t *q,
   a.Hq = Hq;
   a.G = d->G;
   a.bits = d->bits;
+  a.vg = vgroup(d);
   a.softmax_scale = softmax_scale;
   if ((s = cuda_status(kivi::launch_prefill_attention(a, st))) != KIVI_OK) return s;
   if (c) c->n_tokens = n;

@@ -78,17 +78,19 @@ constexpr int kWaitPolls = 1 << 22;
 // Shared-memory layout of one warp: the ring of stages for BITS-bit codes, the q.K
 // B fragment of one key group, and one mbarrier per stage.  4-bit rows are twice as
 // long, so their ring has two stages (one unit staged ahead) to keep two CTAs per SM;
-// 2-bit rows keep three (two ahead).
-template <int R, int G, int BITS = 2>
+// 2-bit rows keep three (two ahead).  VG < 128: each value token carries 128 / VG
+// {s, z} words (value channel groups of VG channels).
+template <int R, int G, int BITS = 2, int VG = kD>
 struct Layout {
+  static constexpr int kNV = kD / VG;                         // {s, z} words per value token
   static constexpr int kRowBytes = 16 * BITS;                 // packed codes of one token row
   static constexpr int kStages = BITS == 2 ? 3 : 2;
   static constexpr int kAhead = kStages - 1;                  // units staged ahead of the computed one
   static constexpr int kGroups = kUnit / G;                   // key groups per unit
   static constexpr int kKCodes = 0;                           // 64 rows
   static constexpr int kVCodes = kUnit * kRowBytes;           // 64 rows
-  static constexpr int kVMeta = 2 * kUnit * kRowBytes;        // 64 x 4 B
-  static constexpr int kKMeta = kVMeta + kUnit * 4;           // kGroups x 128 x 4 B
+  static constexpr int kVMeta = 2 * kUnit * kRowBytes;        // 64 x kNV x 4 B
+  static constexpr int kKMeta = kVMeta + kUnit * kNV * 4;     // kGroups x 128 x 4 B
   static constexpr int kStageBytes = kKMeta + kGroups * kD * 4;
   // B fragment rows (2h + part) * 4 + tig of 16 words.  With fewer than four heads
   // four lanes read each row, so rows are padded to 20 words to spread them over the
@@ -239,8 +241,11 @@ __device__ __forceinline__ int64_t owner_warp(int64_t u, int64_t W, int64_t NW) 
 
 // Softmax state of a head: running max (log2 domain) and this lane's shares of
 // sum_t p_t and sum_t p_t z_t.
+// Running softmax state of a head: max m and sum l of the weights (log2 domain), and
+// zs[m] = sum of weight * z over the tokens, one per value channel group.
+template <int NV>
 struct SoftState {
-  float m, l, zs;
+  float m, l, zs[NV];
 };
 
 // Max over the lanes that share this lane's query head.
@@ -449,12 +454,17 @@ constexpr int kSmallWarps = kDecodeSmallWarps;
 template <int R>
 __host__ __device__ constexpr int small_part_bytes() { return kSmallWarps * R * (kD + 2) * 4; }
 
-template <int R, int G, int MODE, int BITS, int NWARPS>
+template <int R, int G, int MODE, int BITS, int NWARPS, int VG = kD>
 __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   constexpr bool PAGED = MODE == kModePaged;
   constexpr bool SMALL = MODE == kModeSmall;
   extern __shared__ __align__(16) unsigned char smem[];
-  using L = Layout<R, G, BITS>;
+  using L = Layout<R, G, BITS, VG>;
+  // value channel groups (VG < 128): NV {s, z} words per value token, group m over
+  // channels VG*m .. VG*m + VG - 1, i.e. code words WG*m .. WG*m + WG - 1 of a row
+  constexpr int NV = L::kNV;
+  constexpr int WG = VG / 16;
+  static_assert(NV == 1 || (BITS == 2 && MODE == kModeDense), "value groups: dense 2-bit caches");
   constexpr int WPR = words_per_row<BITS>();
   constexpr int S = L::kStages;
   constexpr int AH = L::kAhead;
@@ -675,10 +685,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
         const uint32_t dst = smem_addr(wbase + st * L::kStageBytes);
         const uint32_t cb = (uint32_t)rows * L::kRowBytes;
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        mbar_arm(bar, 2 * cb + (uint32_t)rows * 4 + (uint32_t)ngr * kD * 4);
+        mbar_arm(bar, 2 * cb + (uint32_t)rows * NV * 4 + (uint32_t)ngr * kD * 4);
         bulk_copy(dst + L::kKCodes, a.k_codes + row0 * WPR, cb, bar);
         bulk_copy(dst + L::kVCodes, a.v_codes + row0 * WPR, cb, bar);
-        bulk_copy(dst + L::kVMeta, a.v_meta + row0, (uint32_t)rows * 4, bar);
+        bulk_copy(dst + L::kVMeta, a.v_meta + row0 * NV, (uint32_t)rows * NV * 4, bar);
         bulk_copy(dst + L::kKMeta, a.k_meta + grp0 * kD, (uint32_t)ngr * kD * 4, bar);
       }
       armed |= 1u << st;
@@ -689,7 +699,14 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     }
   };
 
-  SoftState ss = {-INFINITY, 0.f, 0.f};
+  SoftState<NV> ss;
+  auto reset_state = [&]() {
+    ss.m = -INFINITY;
+    ss.l = 0.f;
+#pragma unroll
+    for (int m = 0; m < NV; ++m) ss.zs[m] = 0.f;
+  };
+  reset_state();
   float acc[8][4];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
@@ -700,12 +717,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   // and the softmax state (m, l, zs) that belongs to them.  acc_true: the
   // accumulators already hold output units (a value residual was added to them).
   bool acc_true = false;
-  auto emit = [&](int64_t h, const SoftState &fin) {
-    float l = fin.l, zs = fin.zs;
+  auto emit = [&](int64_t h, const SoftState<NV> &fin) {
+    float l = fin.l, zs[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) zs[m] = fin.zs[m];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l += __shfl_xor_sync(kFull, l, off);
-      zs += __shfl_xor_sync(kFull, zs, off);
+#pragma unroll
+      for (int m = 0; m < NV; ++m) zs[m] += __shfl_xor_sync(kFull, zs[m], off);
     }
     float o[16];
 #pragma unroll
@@ -717,7 +737,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
 #pragma unroll
     for (int off = R; off < 4; off <<= 1) {
       l += __shfl_xor_sync(kFull, l, off);
-      zs += __shfl_xor_sync(kFull, zs, off);
+#pragma unroll
+      for (int m = 0; m < NV; ++m) zs[m] += __shfl_xor_sync(kFull, zs[m], off);
 #pragma unroll
       for (int j = 0; j < 16; ++j) o[j] += __shfl_xor_sync(kFull, o[j], off);
     }
@@ -733,12 +754,23 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
         const int64_t slot = gw - owner_warp(h * a.units_per_head, W, NW);
         dst = a.ws + ((b * a.Hq + kvh * R + head_mine) * a.pmax + slot) * (kD + 2);
       }
+      if constexpr (NV == 1) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        // undo the code factor 4^(j mod 4) (16^(j mod 2)) and the 2^-24 of the subnormal codes
-        const float un = acc_true ? 1.f : pow2i(BITS == 2 ? 24 - 2 * (j & 3) : 24 - 4 * (j & 1));
-        dst[16 * g + j] = fmaf(o[j], un, zs);
-        dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs);
+        for (int j = 0; j < 8; ++j) {
+          // undo the code factor 4^(j mod 4) (16^(j mod 2)) and the 2^-24 of the subnormal codes
+          const float un = acc_true ? 1.f : pow2i(BITS == 2 ? 24 - 2 * (j & 3) : 24 - 4 * (j & 1));
+          dst[16 * g + j] = fmaf(o[j], un, zs[0]);
+          dst[16 * g + 8 + j] = fmaf(o[8 + j], un, zs[0]);
+        }
+      } else {
+        // accumulator w holds channels 16w + g and 16w + 8 + g (code word w), both with
+        // the code factor 4^(g mod 4); word w lies in value group w / WG
+        const float un = pow2i(24 - 2 * (g & 3));
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          dst[16 * w + g] = fmaf(o[w], un, zs[w / WG]);
+          dst[16 * w + 8 + g] = fmaf(o[8 + w], un, zs[w / WG]);
+        }
       }
       if (g == 0) {
         dst[kD] = fin.m;
@@ -752,14 +784,35 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     acc_true = false;
   };
 
+  // The P.V B operand of one round from the weights wa, wb of this lane's two tokens
+  // (tokens g and g + 8 of its tile slot): each weight split hi/lo and moved to the
+  // lanes whose B registers hold it.
+  auto to_b = [&](float wa, float wb, uint32_t &b0, uint32_t &b1) {
+    // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
+    const __half2 hab = __floats2half2_rn(wa, wb);
+    const float2 fab = __half22float2(hab);
+    const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
+    const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
+    const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
+    // B of P.V, column g = (slot, head, part): K slots 2tig, 2tig+1, 2tig+8, 2tig+9
+    // hold tokens tig, tig+4, tig+8, tig+12; token u's weight lives in lane
+    // 4*(u%8) + (g>>1) (first token if u < 8, else second)
+    const uint32_t a1 = __shfl_sync(kFull, q1, src_a), b1v = __shfl_sync(kFull, q1, src_b);
+    const uint32_t a2 = __shfl_sync(kFull, q2, src_a), b2v = __shfl_sync(kFull, q2, src_b);
+    b0 = prmt(a1, b1v, pv_sel);
+    b1 = prmt(a2, b2v, pv_sel);
+  };
+
   // One softmax update for a unit: sc[rho] holds the q.K accumulators of this lane's
   // tile slot in round rho (tile rho*T + slot_mine, tokens g and g + 8, hi and lo
   // columns); cq_of(rho), be_of(rho) are that tile's score scale and offset (log2
-  // domain), ntok the unit's valid tokens, vmeta(tok) the {s, z} word of its token tok.
-  // Builds the P.V B operand of every round (bw0, bw1) and returns the factor alpha
-  // that the P.V accumulators need before this unit's contribution is added.
+  // domain), ntok the unit's valid tokens, vmeta(tok, m) the {s, z} word of value
+  // group m of its token tok.  With one value group it builds the P.V B operand of
+  // every round (bw0, bw1); with several it keeps the weights (pp) for the per-group
+  // operands.  Returns the factor alpha that the P.V accumulators need before this
+  // unit's contribution is added.
   auto update = [&](auto full_tag, const float (&sc)[R][4], auto &&cq_of, auto &&be_of, int ntok, auto &&vmeta,
-                    uint32_t (&bw0)[R], uint32_t (&bw1)[R]) -> float {
+                    uint32_t (&bw0)[R], uint32_t (&bw1)[R], float (&pp)[R][2]) -> float {
     constexpr bool FULL = decltype(full_tag)::value;
     float sv[R][2];
     float mloc = -INFINITY;
@@ -775,36 +828,80 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     const float m_new = fmaxf(ss.m, head_max<R>(mloc));
     const float alpha = ex2(ss.m - m_new);  // ss.m = -inf at the start of a head: alpha = 0
     ss.m = m_new;
-    float lsum = 0.f, zsum = 0.f;
+    float lsum = 0.f, zsum[NV];
+#pragma unroll
+    for (int m = 0; m < NV; ++m) zsum[m] = 0.f;
 #pragma unroll
     for (int rho = 0; rho < R; ++rho) {
       const int ta = 16 * (rho * T + slot_mine) + g;
       const bool va = FULL || ta < ntok, vb = FULL || ta + 8 < ntok;
       const float pa = ex2(sv[rho][0] - m_new), pb = ex2(sv[rho][1] - m_new);
-      const float2 fva = __half22float2(u2h2(vmeta(va ? ta : 0)));
-      const float2 fvb = __half22float2(u2h2(vmeta(vb ? ta + 8 : 0)));
-      const float sva = va ? fva.x : 0.f, zva = va ? fva.y : 0.f;
-      const float svb = vb ? fvb.x : 0.f, zvb = vb ? fvb.y : 0.f;
       lsum += pa + pb;
-      zsum = fmaf(pa, zva, fmaf(pb, zvb, zsum));
-      const float wa = pa * sva, wb = pb * svb;
-      // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
-      const __half2 hab = __floats2half2_rn(wa, wb);
-      const float2 fab = __half22float2(hab);
-      const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
-      const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
-      const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
-      // B of P.V, column g = (slot, head, part): K slots 2tig, 2tig+1, 2tig+8, 2tig+9
-      // hold tokens tig, tig+4, tig+8, tig+12; token u's weight lives in lane
-      // 4*(u%8) + (g>>1) (first token if u < 8, else second)
-      const uint32_t a1 = __shfl_sync(kFull, q1, src_a), b1 = __shfl_sync(kFull, q1, src_b);
-      const uint32_t a2 = __shfl_sync(kFull, q2, src_a), b2 = __shfl_sync(kFull, q2, src_b);
-      bw0[rho] = prmt(a1, b1, pv_sel);
-      bw1[rho] = prmt(a2, b2, pv_sel);
+      if constexpr (NV == 1) {
+        const float2 fva = __half22float2(u2h2(vmeta(va ? ta : 0, 0)));
+        const float2 fvb = __half22float2(u2h2(vmeta(vb ? ta + 8 : 0, 0)));
+        const float sva = va ? fva.x : 0.f, zva = va ? fva.y : 0.f;
+        const float svb = vb ? fvb.x : 0.f, zvb = vb ? fvb.y : 0.f;
+        zsum[0] = fmaf(pa, zva, fmaf(pb, zvb, zsum[0]));
+        to_b(pa * sva, pb * svb, bw0[rho], bw1[rho]);
+      } else {
+        pp[rho][0] = va ? pa : 0.f;
+        pp[rho][1] = vb ? pb : 0.f;
+#pragma unroll
+        for (int m = 0; m < NV; ++m) {
+          const float zva = va ? __high2float(u2h2(vmeta(ta, m))) : 0.f;
+          const float zvb = vb ? __high2float(u2h2(vmeta(ta + 8, m))) : 0.f;
+          zsum[m] = fmaf(pp[rho][0], zva, fmaf(pp[rho][1], zvb, zsum[m]));
+        }
+      }
     }
     ss.l = fmaf(ss.l, alpha, lsum);
-    ss.zs = fmaf(ss.zs, alpha, zsum);
+#pragma unroll
+    for (int m = 0; m < NV; ++m) ss.zs[m] = fmaf(ss.zs[m], alpha, zsum[m]);
     return alpha;
+  };
+  // P.V of a unit with value channel groups: the MMA of code word w takes channels
+  // 16w + g (row g, the low half of the word) and 16w + 8 + g (row g + 8, the high
+  // half) of the lane's four tokens; so one MMA stays inside one value group, and its
+  // B operand is p * s of that group.  One prmt pairs two tokens' halves; for g >= 4
+  // it takes the upper byte of each half, so that the code lands at bits
+  // [2(g mod 4), 2(g mod 4) + 1] of each fp16 half (bits 8 and up are the exponent
+  // and sign), and the mask leaves the subnormal code * 4^(g mod 4) * 2^-24.
+  // word(tok, w) loads code word w of the unit's token tok, vmeta(tok, m) the {s, z}
+  // word of group m.
+  auto pv_groups = [&](auto full_tag, int ntok, auto &&word, auto &&vmeta, const float (&pp)[R][2]) {
+    constexpr bool FULL = decltype(full_tag)::value;
+    const uint32_t M = 0x00030003u << (2 * (g & 3));
+    const uint32_t sel_lo = (g & 4) ? 0x5511u : 0x5410u, sel_hi = (g & 4) ? 0x7733u : 0x7632u;
+#pragma unroll
+    for (int rho = 0; rho < R; ++rho) {
+      const int ta = 16 * (rho * T + slot_mine) + g;
+      const bool va = FULL || ta < ntok, vb = FULL || ta + 8 < ntok;
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        const float sa = va ? __low2float(u2h2(vmeta(ta, m))) : 0.f;
+        const float sb = vb ? __low2float(u2h2(vmeta(ta + 8, m))) : 0.f;
+        uint32_t bm0, bm1;
+        to_b(pp[rho][0] * sa, pp[rho][1] * sb, bm0, bm1);
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+          const int t = rho * T + i;
+          if (FULL || 16 * t < ntok) {
+            const bool mine = pv_slot == i;
+            const uint32_t b0 = mine ? bm0 : 0u, b1 = mine ? bm1 : 0u;
+#pragma unroll
+            for (int ww = 0; ww < WG; ++ww) {
+              const int w = WG * m + ww;
+              uint32_t v[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) v[k] = word(16 * t + tig + 4 * k, w);
+              mma16816(acc[w], prmt(v[0], v[1], sel_lo) & M, prmt(v[0], v[1], sel_hi) & M,
+                       prmt(v[2], v[3], sel_lo) & M, prmt(v[2], v[3], sel_hi) & M, b0, b1);
+            }
+          }
+        }
+      }
+    }
   };
   auto rescale = [&](float alpha) {
     if (__any_sync(kFull, alpha != 1.f)) {
@@ -953,33 +1050,39 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     for (int gi = 0; gi < NGU; ++gi) be[gi] = bv[gi][0] * cbh;
     auto grp = [&](int rho) { return NGU == 1 ? 0 : (rho * T + slot_mine) / TPG; };
     uint32_t bw0[R], bw1[R];
+    float pp[R][2];
+    auto vmeta = [&](int tok, int m) -> uint32_t { return lds32(stg + L::kVMeta + (tok * NV + m) * 4); };
     const float alpha = update(
         full_tag, sc, [&](int rho) { return grp(rho) ? cq[NGU - 1] : cq[0]; },
-        [&](int rho) { return grp(rho) ? be[NGU - 1] : be[0]; }, ntok,
-        [&](int tok) -> uint32_t { return lds32(stg + L::kVMeta + tok * 4); }, bw0, bw1);
+        [&](int rho) { return grp(rho) ? be[NGU - 1] : be[0]; }, ntok, vmeta, bw0, bw1, pp);
     // ---- P.V of the unit's tiles from the staged value codes
     rescale(alpha);
+    if constexpr (NV > 1) {
+      pv_groups(full_tag, ntok, [&](int tok, int w) { return lds32(stg + L::kVCodes + tok * 32 + w * 4); }, vmeta,
+                pp);
+    } else {
 #pragma unroll
-    for (int rho = 0; rho < R; ++rho)
+      for (int rho = 0; rho < R; ++rho)
 #pragma unroll
-      for (int i = 0; i < T; ++i) {
-        const int t = rho * T + i;
-        if (FULL || 16 * t < ntok) {
-          const bool mine = pv_slot == i;
-          const uint32_t b0 = mine ? bw0[rho] : 0u, b1 = mine ? bw1[rho] : 0u;
-          if constexpr (BITS == 2) {
-            uint32_t v[4];
+        for (int i = 0; i < T; ++i) {
+          const int t = rho * T + i;
+          if (FULL || 16 * t < ntok) {
+            const bool mine = pv_slot == i;
+            const uint32_t b0 = mine ? bw0[rho] : 0u, b1 = mine ? bw1[rho] : 0u;
+            if constexpr (BITS == 2) {
+              uint32_t v[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = lds32(stg + L::kVCodes + (16 * t + tig + 4 * k) * 32 + g * 4);
-            pv_tile(acc, v, b0, b1);
-          } else {
-            uint2 v[4];
+              for (int k = 0; k < 4; ++k) v[k] = lds32(stg + L::kVCodes + (16 * t + tig + 4 * k) * 32 + g * 4);
+              pv_tile(acc, v, b0, b1);
+            } else {
+              uint2 v[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = lds64(stg + L::kVCodes + (16 * t + tig + 4 * k) * 64 + g * 8);
-            pv_tile4(acc, v, b0, b1);
+              for (int k = 0; k < 4; ++k) v[k] = lds64(stg + L::kVCodes + (16 * t + tig + 4 * k) * 64 + g * 8);
+              pv_tile4(acc, v, b0, b1);
+            }
           }
         }
-      }
+    }
   };
 
   // ---- the residual unit of a head: its r fp16 keys (read from the residual buffer)
@@ -1033,12 +1136,19 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     }
     // residual values are quantized ({s, z} of their row) or, with a value residual,
     // fp16 themselves: weight p with s = 1, z = 0
-    const uint32_t *vm_head = a.v_meta + vrow;
+    const uint32_t *vm_head = a.v_meta + vrow * NV;
     uint32_t bw0[R], bw1[R];
+    float pp[R][2];
+    auto vmeta = [&](int tok, int m) -> uint32_t { return a.v_res ? 0x00003C00u : __ldg(vm_head + tok * NV + m); };
     const float alpha = update(
-        std::false_type{}, sc, [&](int) { return c0; }, [&](int) { return 0.f; }, r,
-        [&](int tok) -> uint32_t { return a.v_res ? 0x00003C00u : __ldg(vm_head + tok); }, bw0, bw1);
-    if (a.v_res) {
+        std::false_type{}, sc, [&](int) { return c0; }, [&](int) { return 0.f; }, r, vmeta, bw0, bw1, pp);
+    if constexpr (NV > 1) {
+      // (value channel groups come without a value residual)
+      rescale(alpha);
+      const uint32_t *vc_head = a.v_codes + vrow * WPR;
+      pv_groups(std::false_type{}, r, [&](int tok, int w) { return __ldg(vc_head + (tok < r ? tok : 0) * WPR + w); },
+                vmeta, pp);
+    } else if (a.v_res) {
       // fp16 residual values: this is the head's last unit, so the accumulators move
       // to output units here and the head's partial is written without code factors
 #pragma unroll
@@ -1136,9 +1246,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     if (kk + 1 < n_my) {
       if (cc.uu + 1 == cc.U) {  // the next unit starts a new head
         emit(cc.h, ss);
-        ss.m = -INFINITY;
-        ss.l = 0.f;
-        ss.zs = 0.f;
+        reset_state();
         advance(cc);
         load_q(cursor_q(cc));
       } else {
@@ -1159,9 +1267,9 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   if constexpr (SMALL) small_merge<R>(a, s_part, NW, warp, lane);
 }
 
-template <int R, int G, bool PAGED, int BITS>
+template <int R, int G, bool PAGED, int BITS, int VG = kD>
 __global__ void __launch_bounds__(kThreads, KIVI_DECODE_MIN_CTAS) decode_kernel(const DecodeArgs a) {
-  decode_body<R, G, PAGED ? kModePaged : kModeDense, BITS, kWarps>(a);
+  decode_body<R, G, PAGED ? kModePaged : kModeDense, BITS, kWarps, VG>(a);
 }
 
 template <int R, int G, int BITS>
@@ -1211,6 +1319,25 @@ const void *kernel_ptr() {
   return reinterpret_cast<const void *>(&decode_kernel<R, G, PAGED, BITS>);
 }
 
+// Dense 2-bit kernels with value channel groups of VG channels (persistent grid only).
+template <int VG>
+const void *select_vg_kernel(int R, int G) {
+  if (G == 32)
+    return R == 1   ? reinterpret_cast<const void *>(&decode_kernel<1, 32, false, 2, VG>)
+           : R == 2 ? reinterpret_cast<const void *>(&decode_kernel<2, 32, false, 2, VG>)
+                    : reinterpret_cast<const void *>(&decode_kernel<4, 32, false, 2, VG>);
+  return R == 1   ? reinterpret_cast<const void *>(&decode_kernel<1, 64, false, 2, VG>)
+         : R == 2 ? reinterpret_cast<const void *>(&decode_kernel<2, 64, false, 2, VG>)
+                  : reinterpret_cast<const void *>(&decode_kernel<4, 64, false, 2, VG>);
+}
+
+template <int VG>
+int vg_smem_bytes(int R, int G) {
+  if (G == 32)
+    return R == 1 ? Layout<1, 32, 2, VG>::kSmem : R == 2 ? Layout<2, 32, 2, VG>::kSmem : Layout<4, 32, 2, VG>::kSmem;
+  return R == 1 ? Layout<1, 64, 2, VG>::kSmem : R == 2 ? Layout<2, 64, 2, VG>::kSmem : Layout<4, 64, 2, VG>::kSmem;
+}
+
 template <bool PAGED, int BITS>
 const void *select_kernel(int R, int G) {
   if (G == 32)
@@ -1254,8 +1381,16 @@ constexpr int paged_extra(int B) { return (4 * (2 * B + 5) + 15) & ~15; }
 
 }  // namespace
 
-DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B) {
+DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B, int vg) {
   DecodeKernels k;
+  if (vg != kD) {  // value channel groups: dense 2-bit caches, persistent grid
+    k.decode = vg == 64 ? select_vg_kernel<64>(R, G) : select_vg_kernel<32>(R, G);
+    k.smem = k.smem_limit = vg == 64 ? vg_smem_bytes<64>(R, G) : vg_smem_bytes<32>(R, G);
+    k.combine = reinterpret_cast<const void *>(&combine_kernel);
+    k.small = nullptr;
+    k.small_smem = 0;
+    return k;
+  }
   const int base = bits == 2 ? smem_bytes<2>(R, G) : smem_bytes<4>(R, G);
   if (paged) {
     k.decode = bits == 2 ? select_kernel<true, 2>(R, G) : select_kernel<true, 4>(R, G);

@@ -92,10 +92,10 @@ cudaError_t launch_pair(const DecodeKernels &k, const DecodeArgs &a, void **comb
 
 }  // namespace
 
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out) {
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out, int vg) {
   const int R = Hq / Hkv;
   int nw = 0, sms = 0;
-  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, false, B), &nw, &sms);
+  cudaError_t e = warps_on_device(decode_kernels(R, G, bits, false, B, vg), &nw, &sms);
   if (e != cudaSuccess) return e;
   const int64_t heads = (int64_t)B * Hkv;
   const int64_t ng = n / G;
@@ -112,7 +112,7 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, 
   // small contexts: at most one CTA per SM, and at most two units per warp of it.
   // There the persistent grid's fixed cost (the workspace round trip and the combine
   // launch) outweighs its wider split.
-  out->small = heads <= sms && U <= 2 * kDecodeSmallWarps;
+  out->small = vg == kD && heads <= sms && U <= 2 * kDecodeSmallWarps;
   return cudaSuccess;
 }
 
@@ -130,7 +130,7 @@ cudaError_t paged_decode_geometry(int B, int Hkv, int Hq, int G, int bits, Paged
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st) {
-  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, a.bits, false, a.B);
+  const DecodeKernels k = decode_kernels(a.Hq / a.Hkv, a.G, a.bits, false, a.B, a.vg ? a.vg : kD);
   if (a.small) {
     // one CTA per (batch, KV head); a programmatic dependent of a preceding append when
     // asked (the same tail wait as the persistent grid)

@@ -10,12 +10,14 @@ namespace kivi {
 cudaError_t launch_key_groups(const uint16_t *in, int64_t in_head_stride, int64_t heads, int64_t groups_per_head,
                               int64_t g0, int G, int bits, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens,
                               cudaStream_t st);
+// vg: channels per value {s, z} (128: one per token; 64 or 32: value channel groups,
+// 2-bit codes, v_meta rows of 128 / vg words).
 cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
                               int64_t t0, int bits, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens,
-                              cudaStream_t st);
+                              cudaStream_t st, int vg = 128);
 cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G, int bits,
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
-                          cudaStream_t st);
+                          cudaStream_t st, int vg = 128);
 cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, int64_t nq, int G, uint16_t *k_res,
                                  cudaStream_t st);
 // Paged destinations of a prefill: the block-table row of one sequence.
@@ -52,7 +54,7 @@ cudaError_t launch_advance_lens(int32_t *seq_lens, int B, int32_t cap, cudaStrea
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                            const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
                            int64_t n, int G, int bits, int64_t max_tokens, float *k_out, float *v_out,
-                           cudaStream_t st);
+                           cudaStream_t st, int vg = 128);
 
 struct DecodeArgs {
   const uint32_t *k_codes;
@@ -75,6 +77,7 @@ struct DecodeArgs {
   int pmax;                // partial slots per query head in the workspace
   int wait_tail;           // launched as a dependent of an append: wait before each head's last unit
   int small;               // dense: the small-context path (decode_geometry's choice)
+  int vg;                  // channels per value {s, z}: 128 (per token), 64 or 32 (value channel groups)
   float softmax_scale;
   // paged layout only: per-sequence lengths on the device, rows found through the
   // block table; the partials are addressed by (warp + head) and a per-head header
@@ -104,7 +107,9 @@ struct DecodeKernels {
   const void *small;    // dense only: one CTA of kDecodeSmallWarps warps per (batch, KV head)
   int small_smem;
 };
-DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B);
+// vg: channels per value scale (128, or 64 / 32 for value channel groups: dense
+// 2-bit caches only, no small-context kernel).
+DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B, int vg = 128);
 
 // Geometry of one decode call on the current device (deterministic for given sizes).
 struct DecodeGeom {
@@ -115,7 +120,7 @@ struct DecodeGeom {
   int pmax;
   bool small;  // the small-context path: one CTA per (batch, KV head), no workspace, no combine
 };
-cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out);
+cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out, int vg = 128);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
 // Paged decode: the grid fills the GPU whatever the lengths; n_warps and grid come
@@ -141,6 +146,7 @@ struct PrefillArgs {
   uint16_t *k_res, *v_res;                        // v_res null without a value residual
   int64_t n, max_tokens;
   int B, Hkv, Hq, G, bits;
+  int vg;             // channels per value {s, z}: 128, 64 or 32
   float softmax_scale;
 };
 cudaError_t launch_prefill_attention(const PrefillArgs &a, cudaStream_t st);

@@ -103,7 +103,8 @@ __device__ __forceinline__ uint32_t transpose_pieces(uint32_t A, int j) {
 // and codes each row, two codes per lane; a transpose across the LPW lanes of a word
 // then gives each lane one packed word of one row.  Values: 4 lanes per row, lane
 // (q, r8) = (lane / 8, lane % 8) holding channels 32q .. 32q+31 of row r8 of its
-// 8-row step, so that the 8 lanes of a shared-memory phase read 8 different rows.
+// 8-row step, so that the 8 lanes of a shared-memory phase read 8 different rows; a
+// value channel group of 32 (64) channels is one lane's (two lanes') channels.
 // 2-bit codes come from fp16 thresholds (the per-element fp32 form when a warp holds
 // a threshold that is not proven), 4-bit codes from the reciprocal product: the rule
 // and its fast forms are those of the standalone quantizers, bit for bit.
@@ -202,6 +203,7 @@ __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, cons
   }
   // ---- value rows
   const int64_t nv = a.v_res ? nq : n;  // values quantized per token
+  const int vg = a.vg;                  // channels per value {s, z}: 128, 64 or 32 (2-bit codes)
   const int vq = lane >> 3, vr = lane & 7, warp = tid >> 5;
   for (int r0 = 8 * warp; r0 < kPTile; r0 += 8 * kPWarps) {
     const int r = r0 + vr;
@@ -227,17 +229,26 @@ __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, cons
     // (min, -max) so that one __hmin2 reduces both over the row's 4 lanes
     __half2 red = __halves2half2(__hmin(__low2half(mn2), __high2half(mn2)),
                                  __hneg(__hmax(__low2half(mx2), __high2half(mx2))));
-    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 8)));
-    red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 16)));
+    // over the lanes of the row's value group: all 4 lanes (vg = 128), lanes q and
+    // q ^ 1 (vg = 64), this lane alone (vg = 32)
+    if (vg >= 64) red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 8)));
+    if (vg == kD) red = __hmin2(red, u2h2(__shfl_xor_sync(0xffffffffu, h22u(red), 16)));
     const QParams p = make_qparams<BITS>(__low2float(red), -__high2float(red));
     uint32_t *row = a.v_codes + (bh * a.max_tokens + t) * WPR;
     if constexpr (BITS == 2) {
-      // lane q < 3 of the row proves threshold q + 1 (X2 is the strict one: d >= t2)
+      // one set of parameters per row: lane q < 3 of the row proves threshold q + 1 (X2
+      // is the strict one: d >= t2); per value group: each lane proves its group's three
       bool ok = true;
-      uint32_t xq = 0x7c00u;
-      if (p.s != 0.f && vq < 3) xq = fp16_threshold(p.mn, vq == 0 ? p.t1 : (vq == 1 ? p.t2 : p.t3), vq == 1, ok);
-      const uint32_t x1 = __shfl_sync(0xffffffffu, xq, vr), x2 = __shfl_sync(0xffffffffu, xq, vr + 8),
-                     x3 = __shfl_sync(0xffffffffu, xq, vr + 16);
+      uint32_t x1, x2, x3;
+      if (vg == kD) {
+        uint32_t xq = 0x7c00u;
+        if (p.s != 0.f && vq < 3) xq = fp16_threshold(p.mn, vq == 0 ? p.t1 : (vq == 1 ? p.t2 : p.t3), vq == 1, ok);
+        x1 = __shfl_sync(0xffffffffu, xq, vr);
+        x2 = __shfl_sync(0xffffffffu, xq, vr + 8);
+        x3 = __shfl_sync(0xffffffffu, xq, vr + 16);
+      } else {
+        fp16_thresholds(p, x1, x2, x3, ok);
+      }
       uint32_t c[4];
       if (__all_sync(0xffffffffu, ok)) {
         const uint32_t p1 = x1 | (x1 << 16), p2 = x2 | (x2 << 16), p3 = x3 | (x3 << 16);
@@ -258,7 +269,7 @@ __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, cons
       for (int k = 0; k < 4; ++k) c[k] = qchunk8<4>(make_uint4(xv[k][0], xv[k][1], xv[k][2], xv[k][3]), p);
       if (ok_row) *reinterpret_cast<uint4 *>(row + 4 * vq) = make_uint4(c[0], c[1], c[2], c[3]);
     }
-    if (ok_row && vq == 0) a.v_meta[bh * a.max_tokens + t] = p.meta;
+    if (ok_row && vq % (vg / 32) == 0) a.v_meta[(bh * a.max_tokens + t) * (kD / vg) + vq / (vg / 32)] = p.meta;
   }
 }
 

@@ -179,9 +179,11 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
 // Value tokens at append: 16 lanes per token row (one 16-byte chunk of 8 channels each).
 // quantize_value_row works on one half-warp; `lane16` is the lane within it.
 // -------------------------------------------------------------------------------------
+// With value channel groups, lanes 8m/vg .. share group m: the min/max reduction runs
+// over vg_lanes = vg / 8 lanes, and the group's first lane writes meta_out[group].
 template <int BITS>
 __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, uint32_t half_mask,
-                                                   uint32_t *codes_row, uint32_t *meta_out) {
+                                                   uint32_t *codes_row, uint32_t *meta_out, int vg_lanes = 16) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
   __half2 mn = __hmin2(__hmin2(u2h2(w[0]), u2h2(w[1])), __hmin2(u2h2(w[2]), u2h2(w[3])));
   __half2 mx = __hmax2(__hmax2(u2h2(w[0]), u2h2(w[1])), __hmax2(u2h2(w[2]), u2h2(w[3])));
@@ -189,7 +191,8 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   __half2 red = __halves2half2(__hmin(__low2half(mn), __high2half(mn)),
                                __hneg(__hmax(__low2half(mx), __high2half(mx))));
 #pragma unroll
-  for (int off = 1; off < 16; off <<= 1) red = __hmin2(red, u2h2(__shfl_xor_sync(half_mask, h22u(red), off)));
+  for (int off = 1; off < 16; off <<= 1)
+    if (off < vg_lanes) red = __hmin2(red, u2h2(__shfl_xor_sync(half_mask, h22u(red), off)));
   const float fmn = __low2float(red);
   const float fmx = -__high2float(red);
   const QParams p = make_qparams<BITS>(fmn, fmx);
@@ -200,7 +203,7 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
   } else {
     codes_row[lane16] = bits;  // chunk lane16 = channels 8*lane16 .. +7 = word lane16
   }
-  if (lane16 == 0) *meta_out = p.meta;
+  if (lane16 % vg_lanes == 0) meta_out[lane16 / vg_lanes] = p.meta;
 }
 
 // Value rows, 4 lanes per row and 8 rows per warp: lane q of a row holds the 16-byte
@@ -212,7 +215,10 @@ __device__ __forceinline__ void quantize_value_row(const uint4 x, int lane16, ui
 // chunk c of a row is code word c.
 // rows = heads * tokens_per_head; row r -> head r / tokens_per_head, token t0 + r % tokens_per_head,
 // read from input row (head * in_rows_per_head + r % tokens_per_head)
-template <bool PAGED, int BITS>
+// VG < 128 (value channel groups, dense 2-bit caches): lane q's chunk q + 4k lies in
+// group k / (VG / 32); each group's min/max is reduced over the row's 4 lanes, and its
+// codes take the fp32 comparison form; the row's meta holds 128 / VG {s, z} words.
+template <bool PAGED, int BITS, int VG = kD>
 __global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__restrict__ v, int64_t rows,
                                                           int64_t tokens_per_head, int64_t in_rows_per_head,
                                                           int64_t t0, uint32_t *__restrict__ v_codes,
@@ -241,6 +247,43 @@ __global__ void __launch_bounds__(256) value_rows2_kernel(const uint16_t *__rest
       x[k][1] = c.y;
       x[k][2] = c.z;
       x[k][3] = c.w;
+    }
+    if constexpr (VG < kD) {
+      static_assert(BITS == 2 && !PAGED, "value channel groups: dense 2-bit caches");
+      constexpr int NV = kD / VG, KPG = VG / 32;  // groups per row, chunks of a lane per group
+      QParams pg[NV];
+#pragma unroll
+      for (int m = 0; m < NV; ++m) {
+        __half2 gmn = u2h2(x[m * KPG][0]), gmx = gmn;
+#pragma unroll
+        for (int k = m * KPG; k < (m + 1) * KPG; ++k)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            gmn = __hmin2(gmn, u2h2(x[k][j]));
+            gmx = __hmax2(gmx, u2h2(x[k][j]));
+          }
+        __half2 gred = __halves2half2(__hmin(__low2half(gmn), __high2half(gmn)),
+                                      __hneg(__hmax(__low2half(gmx), __high2half(gmx))));
+        gred = __hmin2(gred, u2h2(__shfl_xor_sync(0xffffffffu, h22u(gred), 1)));
+        gred = __hmin2(gred, u2h2(__shfl_xor_sync(0xffffffffu, h22u(gred), 2)));
+        pg[m] = make_qparams<2>(__low2float(gred), -__high2float(gred));
+      }
+      uint32_t r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) r[k] = quant_chunk8<2>(make_uint4(x[k][0], x[k][1], x[k][2], x[k][3]), pg[k / KPG]);
+      const uint32_t A = __byte_perm(r[0], r[1], 0x5410), B = __byte_perm(r[2], r[3], 0x5410);
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, (q & 1) ? A : B, 1);
+      const uint32_t lo = (q & 1) ? recv : A, hi = (q & 1) ? B : recv;
+      if (ok_row) {
+        uint32_t *codes_row = v_codes + dst * 8;
+        const int w = (q >> 1) + ((q & 1) ? 4 : 0);
+        codes_row[w] = __byte_perm(lo, hi, 0x5410);
+        codes_row[w + 2] = __byte_perm(lo, hi, 0x7632);
+#pragma unroll
+        for (int m = 0; m < NV; ++m)
+          if (q == m) v_meta[dst * NV + m] = pg[m].meta;
+      }
+      continue;
     }
     __half2 mn = u2h2(x[0][0]), mx = mn;
 #pragma unroll
@@ -307,7 +350,7 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
                                                      int64_t n, int G, uint16_t *__restrict__ k_res,
                                                      uint32_t *__restrict__ v_codes,
                                                      uint32_t *__restrict__ v_meta, int64_t max_tokens,
-                                                     uint16_t *__restrict__ v_res) {
+                                                     uint16_t *__restrict__ v_res, int vg) {
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int64_t bh = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -320,7 +363,7 @@ __global__ void __launch_bounds__(128) append_kernel(const uint16_t *__restrict_
       reinterpret_cast<uint4 *>(v_res + (bh * G + n % G) * kD)[lane16] = x;
     else
       quantize_value_row<BITS>(x, lane16, 0x0000ffffu, v_codes + (bh * max_tokens + n) * words_per_row<BITS>(),
-                               v_meta + bh * max_tokens + n);
+                               v_meta + (bh * max_tokens + n) * (kD / vg), vg / 8);
   } else {
     const int64_t r = n % G;
     const uint4 x = __ldg(reinterpret_cast<const uint4 *>(k_new + bh * kD) + lane16);
@@ -446,7 +489,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
                                                       const uint32_t *__restrict__ v_meta, int64_t heads, int64_t n,
                                                       int G, int64_t max_tokens, float *__restrict__ k_out,
                                                       float *__restrict__ v_out,
-                                                      const uint16_t *__restrict__ v_res) {
+                                                      const uint16_t *__restrict__ v_res, int vg) {
   const int64_t total = heads * n * (kD / 8);
   const int64_t nq = (n / G) * G;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -477,7 +520,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint32_t *__restrict
       for (int j = 0; j < 8; ++j) vo[j] = h2f(res[j]);
       continue;
     }
-    const uint32_t vm = v_meta[bh * max_tokens + t];
+    const uint32_t vm = v_meta[(bh * max_tokens + t) * (kD / vg) + c0 / vg];  // the chunk's value group
     const float s = h2f((uint16_t)(vm & 0xffffu)), z = h2f((uint16_t)(vm >> 16));
     const uint32_t word = v_codes[(bh * max_tokens + t) * words_per_row<BITS>() + (c0 * BITS) / 32] >>
                           ((c0 * BITS) % 32);
@@ -532,11 +575,17 @@ cudaError_t launch_key_groups_paged(const uint16_t *in, int64_t in_head_stride, 
 
 cudaError_t launch_value_rows(const uint16_t *v, int64_t heads, int64_t tokens_per_head, int64_t in_rows_per_head,
                               int64_t t0, int bits, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens,
-                              cudaStream_t st) {
+                              cudaStream_t st, int vg) {
   const int64_t rows = heads * tokens_per_head;
   if (rows == 0) return cudaSuccess;
   const int grid = grid_cap((rows + 63) / 64);  // 64 rows per CTA and pass
-  if (bits == 2)
+  if (vg == 32)
+    value_rows2_kernel<false, 2, 32><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes,
+                                                            v_meta, max_tokens, PageMap{});
+  else if (vg == 64)
+    value_rows2_kernel<false, 2, 64><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes,
+                                                            v_meta, max_tokens, PageMap{});
+  else if (bits == 2)
     value_rows2_kernel<false, 2><<<grid, 256, 0, st>>>(v, rows, tokens_per_head, in_rows_per_head, t0, v_codes,
                                                         v_meta, max_tokens, PageMap{});
   else
@@ -562,12 +611,12 @@ cudaError_t launch_value_rows_paged(const uint16_t *v, int64_t heads, int64_t to
 
 cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, int64_t heads, int64_t n, int G, int bits,
                           uint16_t *k_res, uint32_t *v_codes, uint32_t *v_meta, int64_t max_tokens, uint16_t *v_res,
-                          cudaStream_t st) {
+                          cudaStream_t st, int vg) {
   const unsigned grid = (unsigned)((heads + 3) / 4);
   if (bits == 2)
-    append_kernel<2><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res);
+    append_kernel<2><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res, vg);
   else
-    append_kernel<4><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res);
+    append_kernel<4><<<grid, 128, 0, st>>>(k_new, v_new, heads, n, G, k_res, v_codes, v_meta, max_tokens, v_res, vg);
   return cudaGetLastError();
 }
 
@@ -601,16 +650,16 @@ cudaError_t launch_residual_copy(const uint16_t *k, int64_t heads, int64_t n, in
 cudaError_t launch_dequant(const uint32_t *k_codes, const uint32_t *k_meta, const uint16_t *k_res,
                            const uint32_t *v_codes, const uint32_t *v_meta, const uint16_t *v_res, int64_t heads,
                            int64_t n, int G, int bits, int64_t max_tokens, float *k_out, float *v_out,
-                           cudaStream_t st) {
+                           cudaStream_t st, int vg) {
   const int64_t total = heads * n * (kD / 8);
   if (total == 0) return cudaSuccess;
   const int grid = grid_cap((total + 255) / 256);
   if (bits == 2)
     dequant_kernel<2><<<grid, 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G, max_tokens, k_out,
-                                            v_out, v_res);
+                                            v_out, v_res, vg);
   else
     dequant_kernel<4><<<grid, 256, 0, st>>>(k_codes, k_meta, k_res, v_codes, v_meta, heads, n, G, max_tokens, k_out,
-                                            v_out, v_res);
+                                            v_out, v_res, vg);
   return cudaGetLastError();
 }
 

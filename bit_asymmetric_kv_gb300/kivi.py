@@ -30,7 +30,8 @@ class KiviError(RuntimeError):
 
 class kivi_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("G", ctypes.c_int32),
-                ("bits", ctypes.c_int32), ("value_residual", ctypes.c_int32), ("max_tokens", ctypes.c_int64)]
+                ("bits", ctypes.c_int32), ("value_residual", ctypes.c_int32), ("value_group", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int64)]
 
 
 class kivi_cache(ctypes.Structure):
@@ -125,8 +126,8 @@ def _f16(t: torch.Tensor, name: str) -> torch.Tensor:
 
 
 def make_dims(B: int, Hkv: int, G: int, max_tokens: int, D: int = 128, bits: int = 2,
-              value_residual: bool = False) -> kivi_dims:
-    return kivi_dims(B, Hkv, D, G, bits, int(value_residual), max_tokens)
+              value_residual: bool = False, value_group: int = 0) -> kivi_dims:
+    return kivi_dims(B, Hkv, D, G, bits, int(value_residual), int(value_group), max_tokens)
 
 
 def kivi_buffer_bytes(dims: kivi_dims) -> list[int]:
@@ -144,7 +145,7 @@ class Cache:
     k_meta: torch.Tensor   # int32 [B, Hkv, T/G, D]    ({s, z} fp16 pairs)
     k_res: torch.Tensor    # fp16  [B, Hkv, G, D]
     v_codes: torch.Tensor  # int32 [B, Hkv, T, D*bits/32]
-    v_meta: torch.Tensor   # int32 [B, Hkv, T]
+    v_meta: torch.Tensor   # int32 [B, Hkv, T], or [B, Hkv, T, D/vg] with value channel groups
     c: kivi_cache
     v_res: torch.Tensor | None = None  # fp16 [B, Hkv, G, D] with a value residual
 
@@ -154,8 +155,9 @@ class Cache:
 
     @classmethod
     def allocate(cls, B: int, Hkv: int, G: int, max_tokens: int, device="cuda", D: int = 128,
-                 value_residual: bool = False, bits: int = 2) -> "Cache":
-        dims = make_dims(B, Hkv, G, max_tokens, D, bits=bits, value_residual=value_residual)
+                 value_residual: bool = False, bits: int = 2, value_group: int = 0) -> "Cache":
+        dims = make_dims(B, Hkv, G, max_tokens, D, bits=bits, value_residual=value_residual,
+                         value_group=value_group)
         kivi_buffer_bytes(dims)  # validates the geometry
         T = max_tokens
         W = D * bits // 32  # words of a packed token row
@@ -163,7 +165,8 @@ class Cache:
         km = torch.empty((B, Hkv, T // G, D), dtype=torch.int32, device=device)
         kr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device)
         vc = torch.empty((B, Hkv, T, W), dtype=torch.int32, device=device)
-        vm = torch.empty((B, Hkv, T), dtype=torch.int32, device=device)
+        vg = value_group or D
+        vm = torch.empty((B, Hkv, T) if vg == D else (B, Hkv, T, D // vg), dtype=torch.int32, device=device)
         vr = torch.empty((B, Hkv, G, D), dtype=torch.float16, device=device) if value_residual else None
         c = kivi_cache(kc.data_ptr(), km.data_ptr(), kr.data_ptr(), vc.data_ptr(), vm.data_ptr(),
                        0 if vr is None else vr.data_ptr(), 0)

@@ -19,6 +19,9 @@
  *     operations IEEE round-to-nearest-even, computed with the stored fp16 scale;
  *     a group whose fp16 scale is 0 gets all-zero codes; a zero of -0 is stored +0;
  *   - one (scale, zero) pair per value token per KV head over all D channels;
+ *   - variant (value_group = vg < D): a value token is quantized in D / vg groups of
+ *     vg consecutive channels (group g = channels g*vg .. g*vg + vg - 1), each by the
+ *     rule above, its D / vg {s, z} words stored in group order;
  *   - only keys have a residual; a key group is quantized ("flushed") as soon as it
  *     holds G tokens, so the residual holds n mod G tokens;
  *   - variant (value_residual = 1): the values keep the same residual as the keys,
@@ -36,7 +39,9 @@
  *   k_meta   uint32 [B][Hkv][max_tokens/G][D]   per (group, channel) {s, z}
  *   k_res    fp16   [B][Hkv][G][D]              residual keys, slot j = token nq + j
  *   v_codes  uint32 [B][Hkv][max_tokens][D/16]  token rows of packed value codes
- *   v_meta   uint32 [B][Hkv][max_tokens]        per token {s, z}
+ *   v_meta   uint32 [B][Hkv][max_tokens][D/vg]  per token {s, z} of each value channel
+ *                                               group (vg = dims.value_group, D when 0:
+ *                                               one word per token)
  *   v_res    fp16   [B][Hkv][G][D]              residual values (value_residual = 1
  *                                               only; NULL otherwise)
  * A {s, z} word holds the fp16 scale in bits 0-15 and the fp16 zero in bits 16-31.
@@ -92,7 +97,8 @@ typedef enum {
   KIVI_ERR_ARG = 1,          /* null pointer, non-positive size, n > max_tokens ... */
   KIVI_ERR_ALIGN = 2,        /* a buffer is not 16-byte aligned */
   KIVI_ERR_UNSUPPORTED = 3,  /* D != 128, bits not 2 or 4, G not in {32, 64}, Hq/Hkv not in {1,2,4},
-                                sizes beyond the supported range */
+                                value_group not in {0, 32, 64, 128}, or below 128 with 4-bit
+                                codes or a value residual; sizes beyond the supported range */
   KIVI_ERR_CAPACITY = 4,     /* append on a full cache, prefill longer than max_tokens */
   KIVI_ERR_WORKSPACE = 5,    /* workspace missing or smaller than required */
   KIVI_ERR_CUDA = 6          /* a CUDA runtime call or launch failed */
@@ -107,6 +113,9 @@ typedef struct {
   int32_t G;         /* key group size, 32 or 64 */
   int32_t bits;      /* code width, 2 or 4 */
   int32_t value_residual; /* 1: values keep an fp16 residual beside the keys'; 0: none */
+  int32_t value_group;    /* channels per value {s, z}: 0 or D (one per token), or the
+                             variant 32 / 64 (value channel groups; 2-bit codes without a
+                             value residual only, else KIVI_ERR_UNSUPPORTED) */
   int64_t max_tokens;
 } kivi_dims;
 

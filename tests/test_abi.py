@@ -43,9 +43,10 @@ def test_status_strings(L):
 
 
 def _dims(**kw):
-    d = dict(B=2, Hkv=4, D=128, G=32, bits=2, value_residual=0, max_tokens=256)
+    d = dict(B=2, Hkv=4, D=128, G=32, bits=2, value_residual=0, value_group=0, max_tokens=256)
     d.update(kw)
-    return kivi.kivi_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["value_residual"], d["max_tokens"])
+    return kivi.kivi_dims(d["B"], d["Hkv"], d["D"], d["G"], d["bits"], d["value_residual"], d["value_group"],
+                          d["max_tokens"])
 
 
 FAKE = 1 << 20  # an aligned, never dereferenced address
@@ -63,6 +64,10 @@ def test_buffer_bytes(L):
     assert out[5] == heads * 64 * 128 * 2
     out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640, bits=4))
     assert out[0] == out[3] == heads * 640 * 64 and out[1] == heads * 10 * 128 * 4
+    # value channel groups: 128 / vg {s, z} words per value token
+    for vg, words in ((0, 1), (128, 1), (64, 2), (32, 4)):
+        out = kivi.kivi_buffer_bytes(_dims(B=3, Hkv=5, G=64, max_tokens=640, value_group=vg))
+        assert out[4] == heads * 640 * 4 * words and out[3] == heads * 640 * 32
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -73,6 +78,12 @@ def test_buffer_bytes(L):
     (dict(B=0), kivi.KIVI_ERR_ARG),
     (dict(max_tokens=100), kivi.KIVI_ERR_ARG),   # not a multiple of G
     (dict(value_residual=2), kivi.KIVI_ERR_ARG),
+    (dict(value_group=-32), kivi.KIVI_ERR_ARG),
+    (dict(value_group=16), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(value_group=48), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(value_group=256), kivi.KIVI_ERR_UNSUPPORTED),
+    (dict(value_group=32, bits=4), kivi.KIVI_ERR_UNSUPPORTED),        # groups: 2-bit codes only
+    (dict(value_group=64, value_residual=1), kivi.KIVI_ERR_UNSUPPORTED),  # groups: no value residual
     (dict(max_tokens=1 << 62), kivi.KIVI_ERR_UNSUPPORTED),                    # beyond 2^40 token rows
     (dict(B=1 << 20, Hkv=1 << 10, max_tokens=1 << 12), kivi.KIVI_ERR_UNSUPPORTED),  # 2^42 rows
     (dict(B=2147483647, Hkv=2147483647, max_tokens=32), kivi.KIVI_ERR_UNSUPPORTED),  # no overflow

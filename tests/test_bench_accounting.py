@@ -42,3 +42,19 @@ def test_byte_formulas_match_the_cache_layout(B, Hkv, G, n, vres, bits):
         q_out = 2 * B * Hq * 128 * 2
         assert bench.algorithmic_bytes(B, Hq, Hkv, G, n, vres, bits) == cache + q_out
     assert bench.prefill_bytes(B, Hkv, G, n, vres, bits) == cache + k.nbytes + v.nbytes
+
+
+@pytest.mark.parametrize("vg", [32, 64])
+@pytest.mark.parametrize("B,Hkv,G,n", CASES)
+def test_byte_formulas_with_value_channel_groups(B, Hkv, G, n, vg):
+    """With value channel groups each value token carries 128 / vg {s, z} words."""
+    rng = np.random.default_rng(n + G + vg)
+    k = rng.standard_normal((B, Hkv, n, 128)).astype(np.float16)
+    v = rng.standard_normal((B, Hkv, n, 128)).astype(np.float16)
+    c = oracle.prefill(k, v, G, ((n + G) // G) * G, value_group=vg)
+    assert c.v_meta.shape[-1] == 128 // vg
+    cache = _defined_bytes(c)
+    for R in (1, 2, 4):
+        Hq = R * Hkv
+        assert bench.algorithmic_bytes(B, Hq, Hkv, G, n, value_group=vg) == cache + 2 * B * Hq * 128 * 2
+    assert bench.prefill_bytes(B, Hkv, G, n, value_group=vg) == cache + k.nbytes + v.nbytes

@@ -198,3 +198,29 @@ def test_adversarial_fused_prefill_bit_exact(G, n, bits, vr):
                         (u16(gpu.k_res), orc.k_res, n - nq), (u32(gpu.v_codes), orc.v_codes, nq),
                         (u32(gpu.v_meta), orc.v_meta, nq), (u16(gpu.v_res), orc.v_res, n - nq)]:
         assert np.array_equal(got[:, :, :m], ref[:, :, :m])
+
+
+@pytest.mark.parametrize("vg", [32, 64])
+def test_adversarial_value_groups_bit_exact(vg):
+    """Value channel groups (2-bit, the fp32 comparison form per group) on the same
+    adversarial rows, through the prefill, token-by-token appends and the fused
+    prefill: the oracle's codes and per-group {s, z} bit for bit."""
+    G, n = 32, 32 * 4 + 9
+    k, v = _adversarial(1, 2, n, G, seed=400 + vg)
+    T = 192
+    orc = oracle.prefill(k, v, G, T, value_group=vg)
+    gpu = kivi.Cache.allocate(1, 2, G, T, value_group=vg)
+    kivi.kivi_quantize_prefill(gpu, torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda())
+    torch.cuda.synchronize()
+    assert_cache_equal(gpu, orc)
+    app = kivi.Cache.allocate(1, 2, G, T, value_group=vg)
+    for t in range(n):
+        kivi.kivi_append_token(app, torch.from_numpy(np.ascontiguousarray(k[:, :, t])).cuda(),
+                               torch.from_numpy(np.ascontiguousarray(v[:, :, t])).cuda())
+    torch.cuda.synchronize()
+    assert_cache_equal(app, orc)
+    fused = kivi.Cache.allocate(1, 2, G, T, value_group=vg)
+    q = torch.from_numpy((np.random.default_rng(9).standard_normal((1, 2, n, 128)) * 0.05).astype(np.float16))
+    kivi.kivi_prefill_attention(fused, q.cuda(), torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(), 1.0)
+    torch.cuda.synchronize()
+    assert_cache_equal(fused, orc)
