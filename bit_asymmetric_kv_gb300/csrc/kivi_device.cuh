@@ -262,6 +262,92 @@ __device__ __forceinline__ uint32_t qchunk8(const uint4 &c, const QParams &p) {
   }
 }
 
+// Pieces of LPW lanes x LPW rows transposed across the lanes.  Before, lane j holds
+// its piece of row i at bits [PB*i, PB*i + PB); after, lane j holds row j, with lane
+// i's piece at bits [PB*i, PB*i + PB).  Stage d swaps the off-diagonal blocks of
+// size d between lanes j and j ^ d (d = LPW/2 .. 1): log2(LPW) shuffles for LPW rows.
+template <int LPW, int PB>
+__device__ __forceinline__ uint32_t transpose_pieces(uint32_t A, int j) {
+#pragma unroll
+  for (int d = LPW / 2; d >= 1; d >>= 1) {
+    uint32_t lo = 0;  // the pieces whose index has bit d clear
+#pragma unroll
+    for (int i = 0; i < 32 / PB; ++i)
+      if (!(i & d)) lo |= ((1u << PB) - 1u) << (PB * i);
+    const bool up = (j & d) != 0;
+    const uint32_t send = up ? (A & lo) << (PB * d) : (A & ~lo) >> (PB * d);
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, d);
+    A = (up ? (A & ~lo) : (A & lo)) | recv;
+  }
+  return A;
+}
+
+// Key codes of one channel pair over 32 token rows of one key group, held by one
+// lane: x[r] = the fp16 pair (channels 2cp, 2cp+1) of row r, mn / mx their min and max
+// over the whole group.  The lane derives both channels' parameters, writes their
+// {s, z} words to meta_dst[0..1] when `write_meta`, codes its rows (2-bit: fp16
+// comparisons with proven thresholds, the fp32 comparison form when a threshold of
+// the warp is not proven; 4-bit: the reciprocal product), and the transpose above
+// packs the LPW lanes of a code word: lane j of them stores word cp / LPW of row
+// blk * LPW + j at codes_dst[(blk * LPW + j) * WPR], codes_dst pointing at that word
+// of row 0.  Nothing is stored unless `whole` (a quantized group, not the residual).
+// Every lane of the warp must call it (shuffles), the 32 lanes holding consecutive
+// channel pairs.
+template <int BITS>
+__device__ __forceinline__ void key_pair_codes(const uint32_t (&x)[32], __half2 mn, __half2 mx, int lane, bool whole,
+                                               bool write_meta, uint32_t *meta_dst, uint32_t *codes_dst) {
+  constexpr int WPR = words_per_row<BITS>();
+  constexpr int PB = 2 * BITS;   // bits of one lane's two codes
+  constexpr int LPW = 32 / PB;   // lanes (channel pairs) per packed word
+  const QParams p0 = make_qparams<BITS>(__low2float(mn), __low2float(mx));
+  const QParams p1 = make_qparams<BITS>(__high2float(mn), __high2float(mx));
+  if (whole && write_meta) *reinterpret_cast<uint2 *>(meta_dst) = make_uint2(p0.meta, p1.meta);
+  uint32_t T1 = 0, T2 = 0, T3 = 0;
+  bool fast = true;
+  float rs0 = 0.f, rs1 = 0.f;
+  if constexpr (BITS == 2) {
+    uint32_t a1, a2, a3, b1, b2, b3;
+    bool oa, ob;
+    fp16_thresholds(p0, a1, a2, a3, oa);
+    fp16_thresholds(p1, b1, b2, b3, ob);
+    T1 = a1 | (b1 << 16);
+    T2 = a2 | (b2 << 16);
+    T3 = a3 | (b3 << 16);
+    fast = __all_sync(0xffffffffu, oa && ob);
+  } else {
+    rs0 = __frcp_rn(p0.s);
+    rs1 = __frcp_rn(p1.s);
+  }
+#pragma unroll
+  for (int blk = 0; blk < 32 / LPW; ++blk) {
+    uint32_t A = 0;
+#pragma unroll
+    for (int i = 0; i < LPW; ++i) {
+      const uint32_t v = x[blk * LPW + i];
+      uint32_t pc;
+      if constexpr (BITS == 2) {
+        if (fast) {
+          const __half2 hv = u2h2(v);
+          const uint32_t m1 = __hgt2_mask(hv, u2h2(T1)), m2 = __hgt2_mask(hv, u2h2(T2));
+          const uint32_t m3 = __hgt2_mask(hv, u2h2(T3));
+          // nested masks: the code's low bit is their parity, its high bit the middle one
+          const uint32_t c = ((m1 ^ m2 ^ m3) & 0x00010001u) | (m2 & 0x00020002u);
+          pc = (c | (c >> 14)) & 0xFu;
+        } else {
+          pc = quant_code<2>(h2f((uint16_t)(v & 0xffffu)), p0) | (quant_code<2>(h2f((uint16_t)(v >> 16)), p1) << 2);
+        }
+      } else {
+        pc = code4(h2f((uint16_t)(v & 0xffffu)), p0.mn, p0.s, rs0) |
+             (code4(h2f((uint16_t)(v >> 16)), p1.mn, p1.s, rs1) << 4);
+      }
+      A |= pc << (PB * i);
+    }
+    const int j = lane % LPW;
+    const uint32_t word = transpose_pieces<LPW, PB>(A, j);
+    if (whole) codes_dst[(blk * LPW + j) * WPR] = word;
+  }
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
 
 }  // namespace kivi

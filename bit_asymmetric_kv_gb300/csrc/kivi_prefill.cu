@@ -74,26 +74,6 @@ __device__ __forceinline__ void pcp_async16(void *smem, const void *gmem, bool v
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) { return h22u(__floats2half2_rn(lo, hi)); }
 
-// Pieces of LPW lanes x LPW rows transposed across the lanes.  Before, lane j holds
-// its piece of row i at bits [PB*i, PB*i + PB); after, lane j holds row j, with lane
-// i's piece at bits [PB*i, PB*i + PB).  Stage d swaps the off-diagonal blocks of
-// size d between lanes j and j ^ d (d = LPW/2 .. 1): log2(LPW) shuffles for LPW rows.
-template <int LPW, int PB>
-__device__ __forceinline__ uint32_t transpose_pieces(uint32_t A, int j) {
-#pragma unroll
-  for (int d = LPW / 2; d >= 1; d >>= 1) {
-    uint32_t lo = 0;  // the pieces whose index has bit d clear
-#pragma unroll
-    for (int i = 0; i < 32 / PB; ++i)
-      if (!(i & d)) lo |= ((1u << PB) - 1u) << (PB * i);
-    const bool up = (j & d) != 0;
-    const uint32_t send = up ? (A & lo) << (PB * d) : (A & ~lo) >> (PB * d);
-    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, d);
-    A = (up ? (A & ~lo) : (A & lo)) | recv;
-  }
-  return A;
-}
-
 // Quantize key/value tile t0 / 64 of one (batch, KV head), staged in shared memory as
 // 64 rows of kPRow bytes (rows past the prompt hold zeros and are not written).  All
 // threads of the CTA take part; `scratch` holds 1 KB.
@@ -112,8 +92,7 @@ template <int BITS>
 __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, const unsigned char *ks,
                               const unsigned char *vs, unsigned char *scratch) {
   constexpr int WPR = words_per_row<BITS>();
-  constexpr int PB = 2 * BITS;   // bits of one lane's two codes
-  constexpr int LPW = 32 / PB;   // lanes (channel pairs) per packed word
+  constexpr int LPW = 16 / BITS;  // channel pairs per packed word
   const int G = a.G;
   const int64_t n = a.n, nq = (n / G) * G;
   const int64_t t_end = min(n, t0 + kPTile);
@@ -140,55 +119,9 @@ __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, cons
   }
   const int64_t g0 = G == 32 ? t0 + 32 * rh : t0;  // first token of this thread's group
   const bool whole = g0 + G <= nq;                  // a quantized group (not the residual)
-  const QParams p0 = make_qparams<BITS>(__low2float(mn), __low2float(mx));
-  const QParams p1 = make_qparams<BITS>(__high2float(mn), __high2float(mx));
-  if (whole && (G == 32 || rh == 0))
-    *reinterpret_cast<uint2 *>(a.k_meta + (bh * (a.max_tokens / G) + g0 / G) * kD + 2 * cp) =
-        make_uint2(p0.meta, p1.meta);
-  uint32_t T1 = 0, T2 = 0, T3 = 0;
-  bool fast = true;
-  float rs0 = 0.f, rs1 = 0.f;
-  if constexpr (BITS == 2) {
-    uint32_t a1, a2, a3, b1, b2, b3;
-    bool oa, ob;
-    fp16_thresholds(p0, a1, a2, a3, oa);
-    fp16_thresholds(p1, b1, b2, b3, ob);
-    T1 = a1 | (b1 << 16);
-    T2 = a2 | (b2 << 16);
-    T3 = a3 | (b3 << 16);
-    fast = __all_sync(0xffffffffu, oa && ob);
-  } else {
-    rs0 = __frcp_rn(p0.s);
-    rs1 = __frcp_rn(p1.s);
-  }
-#pragma unroll
-  for (int blk = 0; blk < 32 / LPW; ++blk) {
-    uint32_t A = 0;
-#pragma unroll
-    for (int i = 0; i < LPW; ++i) {
-      const uint32_t v = x[blk * LPW + i];
-      uint32_t pc;
-      if constexpr (BITS == 2) {
-        if (fast) {
-          const __half2 h = u2h2(v);
-          const uint32_t m1 = __hgt2_mask(h, u2h2(T1)), m2 = __hgt2_mask(h, u2h2(T2));
-          const uint32_t m3 = __hgt2_mask(h, u2h2(T3));
-          // nested masks: the code's low bit is their parity, its high bit the middle one
-          const uint32_t c = ((m1 ^ m2 ^ m3) & 0x00010001u) | (m2 & 0x00020002u);
-          pc = (c | (c >> 14)) & 0xFu;
-        } else {
-          pc = quant_code<2>(h2f((uint16_t)(v & 0xffffu)), p0) | (quant_code<2>(h2f((uint16_t)(v >> 16)), p1) << 2);
-        }
-      } else {
-        pc = code4(h2f((uint16_t)(v & 0xffffu)), p0.mn, p0.s, rs0) |
-             (code4(h2f((uint16_t)(v >> 16)), p1.mn, p1.s, rs1) << 4);
-      }
-      A |= pc << (PB * i);
-    }
-    const int j = lane % LPW;
-    const uint32_t word = transpose_pieces<LPW, PB>(A, j);
-    if (whole) a.k_codes[(bh * a.max_tokens + t0 + 32 * rh + blk * LPW + j) * WPR + cp / LPW] = word;
-  }
+  key_pair_codes<BITS>(x, mn, mx, lane, whole, (G == 32 || rh == 0),
+                       a.k_meta + (bh * (a.max_tokens / G) + g0 / G) * kD + 2 * cp,
+                       a.k_codes + (bh * a.max_tokens + t0 + 32 * rh) * WPR + cp / LPW);
   // the residual keys (and values): positions nq .. n - 1 that lie in this tile
   for (int it = tid; it < kPTile * (kD / 8); it += kPThreads) {
     const int r = it / (kD / 8), ch = it - r * (kD / 8);
