@@ -176,6 +176,134 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
 }
 
 // -------------------------------------------------------------------------------------
+// 2-bit key groups of G = 32 tokens, two groups per CTA: warp w takes group w / 2 of
+// the pair and channels 64 (w % 2) .. 64 (w % 2) + 63.  Lane = 8 * t4 + c8 loads the
+// 16-byte chunk c8 (8 channels) of tokens t4, t4 + 4, .. t4 + 28, so that each lane
+// holds 64 elements, as the G = 64 kernel's lanes do: the per-channel min/max then
+// needs two shuffle rounds over the 4 token lanes, and lane (t4, c8) derives the
+// parameters and proves the thresholds of channel pair t4 of its chunk.
+// -------------------------------------------------------------------------------------
+template <bool PAGED>
+__global__ void __launch_bounds__(128) key_pairs32_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
+                                                          int64_t groups_per_head, int64_t pairs_per_head,
+                                                          int64_t g0, uint32_t *__restrict__ k_codes,
+                                                          uint32_t *__restrict__ k_meta, int64_t max_tokens,
+                                                          const PageMap pm) {
+  // a decode launched as a programmatic dependent may start its independent work now
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  constexpr int G = 32, WPR = 8;
+  __shared__ __align__(16) uint32_t s_codes[2 * G * WPR];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = warp >> 1, ch = warp & 1, t4 = lane >> 3, c8 = lane & 7;
+  const int64_t bh = (int64_t)blockIdx.x / pairs_per_head;
+  const int64_t gi0 = ((int64_t)blockIdx.x - bh * pairs_per_head) * 2;  // first group of the pair (source)
+  const int ngrp = (int)min((int64_t)2, groups_per_head - gi0);          // 1 or 2
+  const int64_t g = g0 + gi0;                                             // destination group
+  int64_t row0, grp;
+  if constexpr (PAGED) {
+    if (!paged_row(pm, bh, g * G, &row0)) return;  // the whole CTA: both groups lie in one page
+    grp = row0 / G;
+  } else {
+    row0 = bh * max_tokens + g * G;
+    grp = bh * (max_tokens / G) + g;
+  }
+  if (gq < ngrp) {
+    const uint16_t *src = in + bh * in_head_stride + (gi0 + gq) * (int64_t)G * kD + 64 * ch + 8 * c8;
+    uint32_t x[8][4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(src + (int64_t)(t4 + 4 * k) * kD));
+      x[k][0] = c.x;
+      x[k][1] = c.y;
+      x[k][2] = c.z;
+      x[k][3] = c.w;
+    }
+    __half2 mn[4], mx[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mn[j] = mx[j] = u2h2(x[0][j]);
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mn[j] = __hmin2(mn[j], u2h2(x[k][j]));
+        mx[j] = __hmax2(mx[j], u2h2(x[k][j]));
+      }
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mn[j] = __hmin2(mn[j], u2h2(__shfl_xor_sync(0xffffffffu, h22u(mn[j]), off)));
+        mx[j] = __hmax2(mx[j], u2h2(__shfl_xor_sync(0xffffffffu, h22u(mx[j]), off)));
+      }
+    // this lane's channel pair: t4 of the chunk (channels 8 c8 + 2 t4, + 1)
+    __half2 pmn = mn[0], pmx = mx[0];
+#pragma unroll
+    for (int j = 1; j < 4; ++j)
+      if (t4 == j) {
+        pmn = mn[j];
+        pmx = mx[j];
+      }
+    const QParams p0 = make_qparams<2>(__low2float(pmn), __low2float(pmx));
+    const QParams p1 = make_qparams<2>(__high2float(pmn), __high2float(pmx));
+    *reinterpret_cast<uint2 *>(k_meta + (grp + gq) * kD + 64 * ch + 8 * c8 + 2 * t4) = make_uint2(p0.meta, p1.meta);
+    uint32_t a1, a2, a3, b1, b2, b3;
+    bool oa, ob;
+    fp16_thresholds(p0, a1, a2, a3, oa);
+    fp16_thresholds(p1, b1, b2, b3, ob);
+    uint32_t r[8];
+    if (__all_sync(0xffffffffu, oa && ob)) {
+      const uint32_t P1 = a1 | (b1 << 16), P2 = a2 | (b2 << 16), P3 = a3 | (b3 << 16);
+      uint32_t T1[4], T2[4], T3[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // pair j of the chunk lives in lane 8 j + c8
+        T1[j] = __shfl_sync(0xffffffffu, P1, 8 * j + c8);
+        T2[j] = __shfl_sync(0xffffffffu, P2, 8 * j + c8);
+        T3[j] = __shfl_sync(0xffffffffu, P3, 8 * j + c8);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) r[k] = codes2_chunk8(x[k], T1, T2, T3);
+    } else {
+      // the fp32 comparison form with every channel's parameters of the chunk
+      QParams q[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int sl = 8 * j + c8;
+        q[2 * j].mn = __shfl_sync(0xffffffffu, p0.mn, sl);
+        q[2 * j].t1 = __shfl_sync(0xffffffffu, p0.t1, sl);
+        q[2 * j].t2 = __shfl_sync(0xffffffffu, p0.t2, sl);
+        q[2 * j].t3 = __shfl_sync(0xffffffffu, p0.t3, sl);
+        q[2 * j + 1].mn = __shfl_sync(0xffffffffu, p1.mn, sl);
+        q[2 * j + 1].t1 = __shfl_sync(0xffffffffu, p1.t1, sl);
+        q[2 * j + 1].t2 = __shfl_sync(0xffffffffu, p1.t2, sl);
+        q[2 * j + 1].t3 = __shfl_sync(0xffffffffu, p1.t3, sl);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          bits |= quant_code<2>(h2f((uint16_t)(x[k][j] & 0xffffu)), q[2 * j]) << (4 * j);
+          bits |= quant_code<2>(h2f((uint16_t)(x[k][j] >> 16)), q[2 * j + 1]) << (4 * j + 2);
+        }
+        r[k] = bits;
+      }
+    }
+    // chunks 2m and 2m+1 (lanes c8 and c8 ^ 1) form word 4 ch + m of a token row
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, r[k], 1);
+      if ((c8 & 1) == 0)
+        s_codes[(gq * G + t4 + 4 * k) * WPR + 4 * ch + (c8 >> 1)] = (r[k] & 0xffffu) | (other << 16);
+    }
+  }
+  __syncthreads();
+  // coalesced write of the pair's packed token rows (contiguous: one page holds both)
+  uint4 *dst = reinterpret_cast<uint4 *>(k_codes + row0 * WPR);
+  const uint4 *s4 = reinterpret_cast<const uint4 *>(s_codes);
+  for (int i = threadIdx.x; i < ngrp * G * WPR / 4; i += blockDim.x) dst[i] = s4[i];
+}
+
+// -------------------------------------------------------------------------------------
 // Value tokens at append: 16 lanes per token row (one 16-byte chunk of 8 channels each).
 // quantize_value_row works on one half-warp; `lane16` is the lane within it.
 // -------------------------------------------------------------------------------------
@@ -538,7 +666,11 @@ static int grid_cap(int64_t want) {
 template <bool PAGED, int BITS>
 void key_groups(const uint16_t *in, int64_t in_head_stride, int64_t blocks, int64_t groups_per_head, int64_t g0,
                 int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens, const PageMap &pm, cudaStream_t st) {
-  if (G == 32)
+  if (G == 32 && BITS == 2) {  // two groups per CTA
+    const int64_t heads = blocks / groups_per_head, pairs = (groups_per_head + 1) / 2;
+    key_pairs32_kernel<PAGED><<<(unsigned)(heads * pairs), 128, 0, st>>>(in, in_head_stride, groups_per_head, pairs,
+                                                                         g0, k_codes, k_meta, max_tokens, pm);
+  } else if (G == 32)
     key_group_kernel<32, PAGED, BITS><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0,
                                                                         k_codes, k_meta, max_tokens, pm);
   else
