@@ -109,10 +109,11 @@ cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, 
   out->n_warps = (int)NW;
   out->grid = (int)((NW + kDecodeWarps - 1) / kDecodeWarps);
   out->pmax = (int)((U + q - 1) / q + 1);
-  // small contexts: at most one CTA per SM, and at most two units per warp of it.
-  // There the persistent grid's fixed cost (the workspace round trip and the combine
-  // launch) outweighs its wider split.
-  out->small = vg == kD && heads <= sms && U <= 2 * kDecodeSmallWarps;
+  // small contexts: at most one CTA per SM, and one unit per warp of it.  There the
+  // persistent grid's fixed cost (the workspace round trip and the combine launch)
+  // outweighs its wider split; with two units per warp the second unit's compute,
+  // serial in each warp, costs more than the combine saves (measured).
+  out->small = vg == kD && heads <= sms && U <= kDecodeSmallWarps;
   return cudaSuccess;
 }
 

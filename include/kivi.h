@@ -175,7 +175,7 @@ KIVI_API size_t kivi_decode_workspace_bytes(const kivi_dims *dims, int32_t Hq, i
  * the last n mod G tokens, and V'_t = z_t + code * s_t.  q, out: fp16 [B][Hq][D]
  * device.  ws: device workspace of at least kivi_decode_workspace_bytes() bytes,
  * caller-owned, contents overwritten.  n_tokens == 0 returns KIVI_ERR_ARG.
- * Small contexts (at most 16 units per (batch, KV head), a unit being 64 quantized
+ * Small contexts (at most 8 units per (batch, KV head), a unit being 64 quantized
  * tokens or the residual, and no more (batch, KV head) pairs than SMs) run on one
  * CTA per pair, which leaves ws unused.
  * Device faults: every wait of the kernel for its own staged copies is bounded; a

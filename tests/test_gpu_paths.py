@@ -1,7 +1,7 @@
 """Both launch paths of the dense decode attention against the CPU oracle.
 
-Small contexts (at most one CTA per SM, at most 16 units of 64 tokens per (batch, KV
-head)) run on one CTA per (batch, KV head) whose warps merge their partials in shared
+Small contexts (at most one CTA per SM, at most 8 units of 64 tokens per (batch, KV
+head): one unit per warp) run on one CTA per (batch, KV head) whose warps merge their partials in shared
 memory; larger ones on the persistent grid with the workspace and the combine
 kernel.  The same shapes just below and just above that boundary, with tails and
 residual keys, for every GQA ratio and both group sizes, through
@@ -33,12 +33,12 @@ def units(n, G):
     return (ng * G + 63) // 64 + (1 if n % G else 0)
 
 
-# (B, Hq, Hkv, G, n): 16 units (small path) and 17 or more (persistent grid)
+# (B, Hq, Hkv, G, n): 8 units (small path) and 9 (persistent grid)
 SHAPES = [
-    (2, 2, 2, 32, 64 * 15 + 17), (2, 2, 2, 32, 64 * 16 + 17),
-    (1, 4, 2, 64, 64 * 15 + 40), (1, 4, 2, 64, 64 * 16 + 40),
-    (3, 8, 2, 32, 64 * 16), (3, 8, 2, 32, 64 * 17),
-    (2, 4, 1, 32, 64 * 14 + 32 + 5), (2, 4, 1, 32, 64 * 15 + 32 + 5),
+    (2, 2, 2, 32, 64 * 7 + 17), (2, 2, 2, 32, 64 * 8 + 17),
+    (1, 4, 2, 64, 64 * 7 + 40), (1, 4, 2, 64, 64 * 8 + 40),
+    (3, 8, 2, 32, 64 * 8), (3, 8, 2, 32, 64 * 9),
+    (2, 4, 1, 32, 64 * 6 + 32 + 5), (2, 4, 1, 32, 64 * 7 + 32 + 5),
 ]
 
 
@@ -55,10 +55,10 @@ def test_decode_attention_on_both_paths(B, Hq, Hkv, G, n):
         assert_close(out, oracle.attention(orc, pre.q.numpy(), sigma))
 
 
-@pytest.mark.parametrize("Hq,Hkv,G,n0", [(2, 2, 32, 64 * 15 + 20), (8, 2, 64, 64 * 15 + 50), (4, 1, 32, 64 * 15 + 10)])
+@pytest.mark.parametrize("Hq,Hkv,G,n0", [(2, 2, 32, 64 * 7 + 20), (8, 2, 64, 64 * 7 + 50), (4, 1, 32, 64 * 7 + 10)])
 def test_decode_step_across_the_boundary(Hq, Hkv, G, n0):
     """A stream that starts on the small path and grows onto the persistent grid
-    (the unit count passes 16 as the context grows), with key-group flushes."""
+    (the unit count passes 8 as the context grows), with key-group flushes."""
     steps = G + 40
     wl = synth.small("paths-step", 2, Hq, Hkv, G, n0, seed=67, steps=steps, factor_lo=30, factor_hi=100)
     pre = synth.make_prefill(wl)
@@ -69,7 +69,7 @@ def test_decode_step_across_the_boundary(Hq, Hkv, G, n0):
     seen = set()
     for step in range(steps):
         k_new, v_new, q = synth.make_step(wl, pre, step)
-        seen.add(units(n0 + step + 1, G) <= 16)
+        seen.add(units(n0 + step + 1, G) <= 8)
         out = kivi.kivi_decode_step(gpu, k_new.cuda(), v_new.cuda(), q.cuda(), 1.0, ws=ws)
         oracle.append(orc, k_new.numpy(), v_new.numpy())
         assert_close(out, oracle.attention(orc, q.numpy(), 1.0))
