@@ -680,10 +680,17 @@ def cycle_workspace(cache, wl, n0, dev):
 
 
 def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
-    """Same metric through the public API with host inputs: every step copies its
-    new k, v, q from pinned host memory (one buffer, one copy), runs append + decode
-    attention and copies the output back; the copies are inside the timed events.
-    steps_in: the host inputs (k, v, q) of the steps of one rollback cycle."""
+    """Same metric through the public API with host inputs: every step copies its new
+    k, v, q from pinned host memory (one buffer, one copy), runs append + decode
+    attention and copies the output back; every copy is inside the timed region.
+    steps_in: the host inputs (k, v, q) of the steps of one rollback cycle.
+
+    Workloads whose steps read more than the 256 MiB L2 flush (each step's own reads
+    then evict the L2) run as a serving loop would: the inputs of step i+1 are copied
+    on a second stream while step i computes, the output of step i is copied back on
+    it, and the whole loop of K steps is timed (no flush).  Smaller workloads, and
+    graph replay (whose captured steps read fixed buffers), time each step with its
+    copies in order on one stream, the L2 flushed before each step outside the events."""
     import torch
 
     total = args.warmup + args.steps
@@ -693,31 +700,87 @@ def e2e_run(args, wl, pre, steps_in, dev, stream, flush):
     shapes = [t.shape for t in steps_in[0]]
     sizes = [t.numel() for t in steps_in[0]]
     host = [torch.cat([t.reshape(-1) for t in kvq]).pin_memory() for kvq in steps_in]
-    dbuf = host[0].to(dev)
-    dk, dv, dq = (p.view(sh) for p, sh in zip(torch.split(dbuf, sizes), shapes))
-    out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    lay.prepare([(dk, dv, dq)], out)
-    times = []
-    for i in range(total):
-        if i % cycle == 0:
-            lay.rollback()
-        flush.fill_(i & 0xFF)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        dbuf.copy_(host[i % cycle], non_blocking=True)
-        lay.step(dk, dv, dq, out, stream)
-        out_h.copy_(out, non_blocking=True)
-        e1.record(stream)
-        if i >= args.warmup:
-            times.append((e0, e1))
-    torch.cuda.synchronize()
-    ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     h2d = host[0].numel() * host[0].element_size()
-    d2h = out.numel() * out.element_size()
+    d2h = wl.B * wl.Hq * wl.D * 2
+    step_bytes = algorithmic_bytes(wl.B, wl.Hq, wl.Hkv, wl.G, wl.n, args.value_residual, args.bits, args.value_group)
+    pipelined = step_bytes > L2_FLUSH_BYTES and not getattr(lay, "graph", False)
+    if not pipelined:
+        dbuf = host[0].to(dev)
+        dk, dv, dq = (p.view(sh) for p, sh in zip(torch.split(dbuf, sizes), shapes))
+        out = torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev)
+        out_h = torch.empty_like(out, device="cpu").pin_memory()
+        lay.prepare([(dk, dv, dq)], out)
+        times = []
+        for i in range(total):
+            if i % cycle == 0:
+                lay.rollback()
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dbuf.copy_(host[i % cycle], non_blocking=True)
+            lay.step(dk, dv, dq, out, stream)
+            out_h.copy_(out, non_blocking=True)
+            e1.record(stream)
+            if i >= args.warmup:
+                times.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in times) / len(times)
+        return {"value": wl.B * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "method": "per step on one stream: H2D copy, step, D2H copy, CUDA events around the three; "
+                          "L2 flushed before each step (outside the events)"}
+
+    # serving loop: two input and output buffers, copies on a second stream
+    copy = torch.cuda.Stream(dev)
+    dbufs = [host[0].to(dev) for _ in range(2)]
+    views = [[p.view(sh) for p, sh in zip(torch.split(d, sizes), shapes)] for d in dbufs]
+    outs = [torch.empty((wl.B, wl.Hq, wl.D), dtype=torch.float16, device=dev) for _ in range(2)]
+    outs_h = [torch.empty_like(outs[0], device="cpu").pin_memory() for _ in range(2)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    lay.prepare([tuple(views[0])], outs[0])
+
+    def run(i0, i1):
+        copy.wait_stream(stream)
+        with torch.cuda.stream(copy):
+            dbufs[i0 % 2].copy_(host[i0 % cycle], non_blocking=True)
+            ev_in[i0 % 2].record(copy)
+        for i in range(i0, i1):
+            b, nb = i % 2, (i + 1) % 2
+            if i % cycle == 0:
+                lay.rollback()
+            stream.wait_event(ev_in[b])
+            if i - i0 >= 2:
+                stream.wait_event(ev_out[b])  # outs[b] has been copied back (step i - 2)
+            dk, dv, dq = views[b]
+            lay.step(dk, dv, dq, outs[b], stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(copy):
+                if i + 1 < i1:
+                    if i > i0:
+                        copy.wait_event(ev_done[nb])  # step i - 1 has read dbufs[nb]
+                    dbufs[nb].copy_(host[(i + 1) % cycle], non_blocking=True)
+                    ev_in[nb].record(copy)
+                copy.wait_event(ev_done[b])
+                outs_h[b].copy_(outs[b], non_blocking=True)
+                ev_out[b].record(copy)
+        stream.wait_stream(copy)
+
+    run(0, args.warmup)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    run(args.warmup, total)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
     return {"value": wl.B * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "method": "serving loop: the H2D copy of step i+1 and the D2H copy of step i on a second stream "
+                      "while step i computes; CUDA events around the whole loop of K steps, every copy inside",
+            "l2": f"no flush: each step reads {step_bytes / 1e9:.2f} GB, more than the 256 MiB flush and "
+                  "twice the 129 MB L2"}
 
 
 def run_compare(args):
