@@ -214,7 +214,7 @@ def dist_env():
 # CPU oracle timing (cpu_baseline leg and --impl reference)
 # ----------------------------------------------------------------------------------------
 def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value_residual: bool = False,
-                  bits: int = 2, value_group: int = 0):
+                  bits: int = 2, value_group: int = 0, single_thread: bool = True):
     """Time the oracle's decode step (append + fp64 attention over the dequantized
     cache) on `sample_heads` of the workload's KV heads; scale to the whole batch.
     Like the GPU loop, the cache is rolled back to the prompt every cycle_of(wl)
@@ -224,6 +224,7 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
     import oracle
     from bit_asymmetric_kv_gb300 import synth
 
+    sample_heads = min(sample_heads, wl.B * wl.Hkv)
     heads = [(i % wl.B, (i * 7) % wl.Hkv) for i in range(sample_heads)]
     cycle = cycle_of(wl)
     T = wl.capacity(extra=cycle + 64)
@@ -249,9 +250,20 @@ def oracle_timing(wl, pre, steps: int, sample_heads: int, budget_s: float, value
         if t_total > budget_s:
             break
     per_step = t_total / done * (wl.B * wl.Hkv / sample_heads)
-    return {"value": wl.B / per_step, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+    line = {"value": wl.B / per_step, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
             "sample": f"{sample_heads} of {wl.B * wl.Hkv} KV heads x {done} decode steps (append + fp64 attention), "
                       f"scaled to the full batch", "seconds": round(t_total, 3)}
+    if single_thread and wl.B * wl.Hkv <= 256:
+        # the same steps on one host thread, for the small workloads (a few seconds)
+        cores = oracle.max_threads()
+        oracle.set_threads(1)
+        try:
+            one = oracle_timing(wl, pre, steps, sample_heads, min(budget_s, 3.0), value_residual, bits, value_group,
+                                single_thread=False)
+        finally:
+            oracle.set_threads(cores)
+        line["single_thread"] = {"value": one["value"], "unit": UNIT, "sample": one["sample"]}
+    return line
 
 
 def run_reference(args, wl):

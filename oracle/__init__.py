@@ -60,6 +60,7 @@ def lib():
             L.oracle_h2f.argtypes, L.oracle_h2f.restype = [ctypes.c_uint16], ctypes.c_float
             L.oracle_f2h.argtypes, L.oracle_f2h.restype = [ctypes.c_float], ctypes.c_uint16
             L.oracle_max_threads.restype = i32
+            L.oracle_set_threads.argtypes, L.oracle_set_threads.restype = [i32], None
             L.oracle_quantize_group.argtypes = [P, i64, i64, i32, P, P, P]
             L.oracle_pack_row.argtypes = [P, i32, i32, P]
             L.oracle_prefill_head.argtypes = [i32, i32, i32, i32, i64, P, P, P, P, P, P, P, P]
@@ -91,6 +92,11 @@ def lib():
 
 def max_threads() -> int:
     return int(lib().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the OpenMP loops over (batch, head); results do not depend on it."""
+    lib().oracle_set_threads(int(n))
 
 
 def _ptr(a: np.ndarray):

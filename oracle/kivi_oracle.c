@@ -92,6 +92,16 @@ int oracle_max_threads(void) {
 #endif
 }
 
+/* Threads of the batch entry points' OpenMP loops (timing only; results do not
+ * depend on it: each (batch, head) is computed by one thread). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  omp_set_num_threads(n > 0 ? n : 1);
+#else
+  (void)n;
+#endif
+}
+
 /*
  * Quantize one group of `count` fp16 values x[i * stride] (R1-R4).
  * A key group is one channel of G consecutive tokens; a value group is one token
