@@ -10,7 +10,7 @@ import torch
 import oracle
 from bit_asymmetric_kv_gb300 import build as kbuild
 from bit_asymmetric_kv_gb300 import kivi, synth
-from helpers import assert_close, u16, u32
+from helpers import assert_cache_equal, assert_close, u16, u32
 
 pytestmark = pytest.mark.gpu
 
@@ -62,30 +62,31 @@ def test_full_size_decode(idx):
 
 
 def test_full_size_streaming():
-    """Prefill 8192 tokens (G=32) for 64 x 32 heads, then 512 append + decode steps."""
+    """Prefill 8192 tokens (G=32) for 64 x 32 heads, then 512 append + decode steps:
+    every (batch, head) against the oracle's own stream at steps 0, 1, 30, 31, 32
+    (around the first key-group flush), 255 and 511, and the whole final cache bit
+    for bit (the oracle's batch entry points run over all 2048 heads)."""
     wl = synth.STREAMING
     pre = synth.make_prefill(wl)
     T = wl.capacity()
     gpu = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T)
     kivi.kivi_quantize_prefill(gpu, pre.k.cuda(), pre.v.cuda())
-    heads = sample_heads(wl, k=3, seed=3)
-    orcs = {h: oracle.prefill_head(pre.k[h[0], h[1]].numpy(), pre.v[h[0], h[1]].numpy(), wl.G, T) for h in heads}
+    orc = oracle.prefill(pre.k.numpy(), pre.v.numpy(), wl.G, T)
     check_steps = {0, 1, 30, 31, 32, 255, wl.steps - 1}
     ws = kivi.workspace(gpu, wl.Hq, n_tokens=wl.n + wl.steps)
+    checked = 0
     for step in range(wl.steps):
         k_new, v_new, q = synth.make_step(wl, pre, step)
         kivi.kivi_append_token(gpu, k_new.cuda(), v_new.cuda())
-        for (b, kvh), orc in orcs.items():
-            oracle.append(orc, k_new[b, kvh][None, None].numpy().copy(), v_new[b, kvh][None, None].numpy().copy())
+        oracle.append(orc, k_new.numpy(), v_new.numpy())
         if step in check_steps:
             out = kivi.kivi_decode_attention(gpu, q.cuda(), 1.0, ws=ws)
             torch.cuda.synchronize()
-            for (b, kvh), orc in orcs.items():
-                ref = oracle.attention_head(orc, 0, 0, q[b, kvh].numpy(), 1.0)
-                assert_close(out[b, kvh:kvh + 1], ref[None])
+            assert_close(out, oracle.attention(orc, q.numpy(), 1.0))
+            checked += 1
     torch.cuda.synchronize()
-    for (b, kvh), orc in orcs.items():
-        check_head(gpu, orc, b, kvh)
+    assert checked == len(check_steps)
+    assert_cache_equal(gpu, orc)
 
 
 def flush_neighbourhood(n0: int, G: int, steps: int, cycles: int = 2) -> set:

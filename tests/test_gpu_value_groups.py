@@ -122,7 +122,7 @@ def test_workload_shape_sampled_heads():
     """The Llama-2-7B decode shape (B8, H32, n = 4113, G32) with 32-channel value
     groups: the persistent grid over every head, the cache of sampled KV heads bit for
     bit against a per-head oracle, their query heads within 2e-3."""
-    wl = synth.CONFIGS[1]
+    wl = synth.LLAMA2_7B_MHA
     pre = synth.make_prefill(wl)
     T = wl.capacity()
     gpu = kivi.Cache.allocate(wl.B, wl.Hkv, wl.G, T, value_group=32)
