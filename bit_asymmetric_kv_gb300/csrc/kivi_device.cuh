@@ -233,6 +233,26 @@ __device__ __forceinline__ uint32_t code4(float x, float mn, float s, float rs) 
   return (uint32_t)(ci > 15 ? 15 : ci);
 }
 
+// Two 4-bit codes at once (channel pair or two elements of one row): x, mn, s and
+// rs = 1/s (0 when s = 0: every code is then 0) per element.  d = fl(x - mn) and
+// q = fl(d * rs) by paired fp32 operations, each element rounded to nearest like the
+// scalar operations of code4.  rint(q) comes from adding and subtracting 1.5 * 2^23
+// (round half to even for 0 <= q < 2^22; q stays below 32 here), its integer from the
+// sum's bit pattern, and q - rint(q) is exact; within 2^-15 of a half-integer the
+// division decides, as in code4.  Returns c0 | c1 << 4.
+__device__ __forceinline__ uint32_t code4x2(float2 x, float2 mn, float2 s, float2 rs) {
+  constexpr float kM = 12582912.f;  // 1.5 * 2^23
+  const float2 d = __fadd2_rn(x, make_float2(-mn.x, -mn.y));
+  const float2 q = __fmul2_rn(d, rs);
+  const float2 t = __fadd2_rn(q, make_float2(kM, kM));
+  const float2 r = __fadd2_rn(t, make_float2(-kM, -kM));
+  const float2 e = __fadd2_rn(q, make_float2(-r.x, -r.y));
+  int c0 = __float_as_int(t.x) - __float_as_int(kM), c1 = __float_as_int(t.y) - __float_as_int(kM);
+  if (fabsf(e.x) > 0.5f - 0x1p-15f) c0 = (int)rintf(__fdiv_rn(d.x, s.x));
+  if (fabsf(e.y) > 0.5f - 0x1p-15f) c1 = (int)rintf(__fdiv_rn(d.y, s.y));
+  return (uint32_t)min(c0, 15) | ((uint32_t)min(c1, 15) << 4);
+}
+
 // One code of either width; rs = 1/s (used by 4-bit codes only).
 template <int BITS>
 __device__ __forceinline__ uint32_t qcode(float x, const QParams &p, float rs) {
@@ -250,14 +270,12 @@ __device__ __forceinline__ uint32_t qchunk8(const uint4 &c, const QParams &p) {
   if constexpr (BITS == 2) {
     return quant_chunk8<2>(c, p);
   } else {
-    const float rs = __frcp_rn(p.s);
+    const float rs = p.s == 0.f ? 0.f : __frcp_rn(p.s);
+    const float2 mn2 = make_float2(p.mn, p.mn), s2 = make_float2(p.s, p.s), rs2 = make_float2(rs, rs);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
     uint32_t bits = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      bits |= code4(h2f((uint16_t)(w[k] & 0xffffu)), p.mn, p.s, rs) << (8 * k);
-      bits |= code4(h2f((uint16_t)(w[k] >> 16)), p.mn, p.s, rs) << (8 * k + 4);
-    }
+    for (int k = 0; k < 4; ++k) bits |= code4x2(__half22float2(u2h2(w[k])), mn2, s2, rs2) << (8 * k);
     return bits;
   }
 }
@@ -315,8 +333,8 @@ __device__ __forceinline__ void key_pair_codes(const uint32_t (&x)[32], __half2 
     T3 = a3 | (b3 << 16);
     fast = __all_sync(0xffffffffu, oa && ob);
   } else {
-    rs0 = __frcp_rn(p0.s);
-    rs1 = __frcp_rn(p1.s);
+    rs0 = p0.s == 0.f ? 0.f : __frcp_rn(p0.s);
+    rs1 = p1.s == 0.f ? 0.f : __frcp_rn(p1.s);
   }
 #pragma unroll
   for (int blk = 0; blk < 32 / LPW; ++blk) {
@@ -337,8 +355,8 @@ __device__ __forceinline__ void key_pair_codes(const uint32_t (&x)[32], __half2 
           pc = quant_code<2>(h2f((uint16_t)(v & 0xffffu)), p0) | (quant_code<2>(h2f((uint16_t)(v >> 16)), p1) << 2);
         }
       } else {
-        pc = code4(h2f((uint16_t)(v & 0xffffu)), p0.mn, p0.s, rs0) |
-             (code4(h2f((uint16_t)(v >> 16)), p1.mn, p1.s, rs1) << 4);
+        pc = code4x2(__half22float2(u2h2(v)), make_float2(p0.mn, p1.mn), make_float2(p0.s, p1.s),
+                     make_float2(rs0, rs1));
       }
       A |= pc << (PB * i);
     }

@@ -135,28 +135,35 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
   }
   if (!fast) {
     QParams p[8];
+    float rs[8];  // 4-bit: 1/s, 0 where s = 0 (code4x2 then gives 0), one reciprocal per lane
+    const float rs_mine = BITS == 4 && mine.s != 0.f ? __frcp_rn(mine.s) : 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int src_lane = 4 * j + c4;
       p[j].mn = __shfl_sync(0xffffffffu, mine.mn, src_lane);
+      rs[j] = 0.f;
       if constexpr (BITS == 2) {
         p[j].t1 = __shfl_sync(0xffffffffu, mine.t1, src_lane);
         p[j].t2 = __shfl_sync(0xffffffffu, mine.t2, src_lane);
         p[j].t3 = __shfl_sync(0xffffffffu, mine.t3, src_lane);
       } else {
         p[j].s = __shfl_sync(0xffffffffu, mine.s, src_lane);
+        rs[j] = __shfl_sync(0xffffffffu, rs_mine, src_lane);
       }
     }
-    float rs[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) rs[j] = BITS == 4 ? __frcp_rn(p[j].s) : 0.f;
 #pragma unroll
     for (int k = 0; k < TPL; ++k) {
       uint32_t bits = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j], rs[2 * j]) << (2 * BITS * j);
-        bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1], rs[2 * j + 1]) << (2 * BITS * j + BITS);
+        if constexpr (BITS == 4) {
+          bits |= code4x2(__half22float2(u2h2(x[k][j])), make_float2(p[2 * j].mn, p[2 * j + 1].mn),
+                          make_float2(p[2 * j].s, p[2 * j + 1].s), make_float2(rs[2 * j], rs[2 * j + 1]))
+                  << (8 * j);
+        } else {
+          bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] & 0xffffu)), p[2 * j], rs[2 * j]) << (2 * BITS * j);
+          bits |= qcode<BITS>(h2f((uint16_t)(x[k][j] >> 16)), p[2 * j + 1], rs[2 * j + 1]) << (2 * BITS * j + BITS);
+        }
       }
       if constexpr (BITS == 2) {
         // chunks 2m and 2m+1 form word 2*warp + m of the token row
@@ -176,14 +183,16 @@ __global__ void __launch_bounds__(128) key_group_kernel(const uint16_t *__restri
 }
 
 // -------------------------------------------------------------------------------------
-// 2-bit key groups of G = 32 tokens, two groups per CTA: warp w takes group w / 2 of
+// Key groups of G = 32 tokens, two groups per CTA: warp w takes group w / 2 of
 // the pair and channels 64 (w % 2) .. 64 (w % 2) + 63.  Lane = 8 * t4 + c8 loads the
 // 16-byte chunk c8 (8 channels) of tokens t4, t4 + 4, .. t4 + 28, so that each lane
 // holds 64 elements, as the G = 64 kernel's lanes do: the per-channel min/max then
 // needs two shuffle rounds over the 4 token lanes, and lane (t4, c8) derives the
-// parameters and proves the thresholds of channel pair t4 of its chunk.
+// parameters (and, for 2-bit codes, proves the thresholds) of channel pair t4 of its
+// chunk.  4-bit codes: the chunk's parameters are broadcast to its lanes, and each
+// token's chunk is one packed word, coded by pairs (code4x2).
 // -------------------------------------------------------------------------------------
-template <bool PAGED>
+template <bool PAGED, int BITS>
 __global__ void __launch_bounds__(128) key_pairs32_kernel(const uint16_t *__restrict__ in, int64_t in_head_stride,
                                                           int64_t groups_per_head, int64_t pairs_per_head,
                                                           int64_t g0, uint32_t *__restrict__ k_codes,
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(128) key_pairs32_kernel(const uint16_t *__rest
                                                           const PageMap pm) {
   // a decode launched as a programmatic dependent may start its independent work now
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  constexpr int G = 32, WPR = 8;
+  constexpr int G = 32, WPR = words_per_row<BITS>();
   __shared__ __align__(16) uint32_t s_codes[2 * G * WPR];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = warp >> 1, ch = warp & 1, t4 = lane >> 3, c8 = lane & 7;
@@ -243,9 +252,29 @@ __global__ void __launch_bounds__(128) key_pairs32_kernel(const uint16_t *__rest
         pmn = mn[j];
         pmx = mx[j];
       }
-    const QParams p0 = make_qparams<2>(__low2float(pmn), __low2float(pmx));
-    const QParams p1 = make_qparams<2>(__high2float(pmn), __high2float(pmx));
+    const QParams p0 = make_qparams<BITS>(__low2float(pmn), __low2float(pmx));
+    const QParams p1 = make_qparams<BITS>(__high2float(pmn), __high2float(pmx));
     *reinterpret_cast<uint2 *>(k_meta + (grp + gq) * kD + 64 * ch + 8 * c8 + 2 * t4) = make_uint2(p0.meta, p1.meta);
+    if constexpr (BITS == 4) {
+      // every channel of the chunk: pair j from lane 8 j + c8 (1/s, 0 where s = 0)
+      const float rs0 = p0.s == 0.f ? 0.f : __frcp_rn(p0.s), rs1 = p1.s == 0.f ? 0.f : __frcp_rn(p1.s);
+      float2 cmn[4], cs[4], crs[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int sl = 8 * j + c8;
+        cmn[j] = make_float2(__shfl_sync(0xffffffffu, p0.mn, sl), __shfl_sync(0xffffffffu, p1.mn, sl));
+        cs[j] = make_float2(__shfl_sync(0xffffffffu, p0.s, sl), __shfl_sync(0xffffffffu, p1.s, sl));
+        crs[j] = make_float2(__shfl_sync(0xffffffffu, rs0, sl), __shfl_sync(0xffffffffu, rs1, sl));
+      }
+      // chunk c8 of channel half ch is word 8 ch + c8 of a token row
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) word |= code4x2(__half22float2(u2h2(x[k][j])), cmn[j], cs[j], crs[j]) << (8 * j);
+        s_codes[(gq * G + t4 + 4 * k) * WPR + 8 * ch + c8] = word;
+      }
+    } else {
     uint32_t a1, a2, a3, b1, b2, b3;
     bool oa, ob;
     fp16_thresholds(p0, a1, a2, a3, oa);
@@ -294,6 +323,7 @@ __global__ void __launch_bounds__(128) key_pairs32_kernel(const uint16_t *__rest
       const uint32_t other = __shfl_xor_sync(0xffffffffu, r[k], 1);
       if ((c8 & 1) == 0)
         s_codes[(gq * G + t4 + 4 * k) * WPR + 4 * ch + (c8 >> 1)] = (r[k] & 0xffffu) | (other << 16);
+    }
     }
   }
   __syncthreads();
@@ -666,14 +696,11 @@ static int grid_cap(int64_t want) {
 template <bool PAGED, int BITS>
 void key_groups(const uint16_t *in, int64_t in_head_stride, int64_t blocks, int64_t groups_per_head, int64_t g0,
                 int G, uint32_t *k_codes, uint32_t *k_meta, int64_t max_tokens, const PageMap &pm, cudaStream_t st) {
-  if (G == 32 && BITS == 2) {  // two groups per CTA
+  if (G == 32) {  // two groups per CTA
     const int64_t heads = blocks / groups_per_head, pairs = (groups_per_head + 1) / 2;
-    key_pairs32_kernel<PAGED><<<(unsigned)(heads * pairs), 128, 0, st>>>(in, in_head_stride, groups_per_head, pairs,
-                                                                         g0, k_codes, k_meta, max_tokens, pm);
-  } else if (G == 32)
-    key_group_kernel<32, PAGED, BITS><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0,
-                                                                        k_codes, k_meta, max_tokens, pm);
-  else
+    key_pairs32_kernel<PAGED, BITS><<<(unsigned)(heads * pairs), 128, 0, st>>>(
+        in, in_head_stride, groups_per_head, pairs, g0, k_codes, k_meta, max_tokens, pm);
+  } else
     key_group_kernel<64, PAGED, BITS><<<(unsigned)blocks, 128, 0, st>>>(in, in_head_stride, groups_per_head, g0,
                                                                         k_codes, k_meta, max_tokens, pm);
 }

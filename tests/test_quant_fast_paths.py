@@ -121,3 +121,62 @@ def test_reciprocal_product_rounds_like_the_division_outside_the_margin():
     # from 64 up the code clamps to 15 either way
     big = q >= 64
     assert np.all(np.rint(div[big]) >= 15)
+
+
+def _code4x2_emulated(d: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """The paired 4-bit coder's steps in numpy float32: q = fl(d * rs) (rs = fl(1/s),
+    0 where s = 0), rint(q) as fl(fl(q + 1.5 * 2^23) - 1.5 * 2^23) and its integer from
+    the sum's bit pattern, the division within 2^-15 of a half-integer, a clamp to 15."""
+    M = np.float32(12582912.0)
+    with np.errstate(divide="ignore"):
+        rs = np.where(s == 0, np.float32(0), (np.float32(1.0) / s).astype(np.float32)).astype(np.float32)
+    q = (d * rs).astype(np.float32)
+    t = (q + M).astype(np.float32)
+    r = (t - M).astype(np.float32)
+    e = (q - r).astype(np.float32)
+    c = t.view(np.int32) - np.array([M], np.float32).view(np.int32)[0]
+    near = np.abs(e) > np.float32(0.5) - np.float32(2.0 ** -15)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        div = np.rint((d / s).astype(np.float32))
+    c = np.where(near, div, c)
+    return np.minimum(c, 15)
+
+
+def test_magic_constant_rounding_is_round_half_even():
+    """fl(fl(q + 1.5 * 2^23) - 1.5 * 2^23) == rint(q) (half to even), and the sum's
+    bit pattern minus the constant's is that integer, for every q the 4-bit
+    quantizer can produce (0 <= q < 32): all float32 values near each half-integer
+    and a million random ones."""
+    M = np.float32(12582912.0)
+    halves = np.arange(0, 32, dtype=np.float64) + 0.5
+    near = np.concatenate([np.atleast_1d(np.nextafter(np.float32(h), np.float32(np.inf))) for h in halves] +
+                          [np.atleast_1d(np.nextafter(np.float32(h), np.float32(-np.inf))) for h in halves] +
+                          [np.float32(h) + np.arange(-600, 601, dtype=np.float32) * np.float32(2.0 ** -18) for h in halves])
+    rng = np.random.default_rng(5)
+    q = np.concatenate([near.astype(np.float32), halves.astype(np.float32), np.arange(32, dtype=np.float32),
+                        rng.uniform(0, 32, 1_000_000).astype(np.float32)])
+    q = q[(q >= 0) & (q < 32)]
+    t = (q + M).astype(np.float32)
+    r = (t - M).astype(np.float32)
+    assert np.array_equal(r, np.rint(q))
+    assert np.array_equal(t.view(np.int32) - np.array([M], np.float32).view(np.int32)[0], np.rint(q).astype(np.int32))
+    assert np.array_equal((q - r).astype(np.float64), q.astype(np.float64) - r.astype(np.float64))  # exact
+
+
+def test_paired_4bit_coder_equals_the_division():
+    """The paired coder's codes equal clamp(rint(fl(d / s)), 0, 15) on the quotients of
+    the reciprocal test (a third within a few ulps of a half-integer) and on s = 0."""
+    rng = np.random.default_rng(12)
+    n = 1_000_000
+    s = rng.integers(1, 0x7C00, size=n).astype(np.uint16).view(np.float16).astype(np.float32)
+    Q = rng.uniform(0, 20, size=n)
+    near = rng.random(n) < 0.35
+    Q[near] = np.floor(Q[near]) + 0.5 + rng.integers(-40, 41, size=int(near.sum())) * 2.0 ** -21
+    with np.errstate(over="ignore"):
+        d = (Q * s.astype(np.float64)).astype(np.float32)
+    keep = np.isfinite(d) & (d >= 0)
+    d, s = d[keep], s[keep]
+    ref = np.clip(np.rint((d / s).astype(np.float32)), 0, 15)
+    assert np.array_equal(_code4x2_emulated(d, s), ref)
+    z = np.zeros(1000, np.float32)
+    assert np.array_equal(_code4x2_emulated(rng.uniform(0, 5, 1000).astype(np.float32) * 0, z), np.zeros(1000))
