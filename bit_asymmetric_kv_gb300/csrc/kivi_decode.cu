@@ -791,7 +791,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     // hi/lo split of the two weights: q1 = {hi_a, lo_a}, q2 = {hi_b, lo_b}
     const __half2 hab = __floats2half2_rn(wa, wb);
     const float2 fab = __half22float2(hab);
-    const __half2 lab = __floats2half2_rn(wa - fab.x, wb - fab.y);
+    const float2 lo = __fadd2_rn(make_float2(wa, wb), make_float2(-fab.x, -fab.y));
+    const __half2 lab = __floats2half2_rn(lo.x, lo.y);
     const uint32_t q1 = prmt(h22u(hab), h22u(lab), 0x5410u);
     const uint32_t q2 = prmt(h22u(hab), h22u(lab), 0x7632u);
     // B of P.V, column g = (slot, head, part): K slots 2tig, 2tig+1, 2tig+8, 2tig+9
@@ -821,8 +822,10 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
       const int ta = 16 * (rho * T + slot_mine) + g;
       const bool va = FULL || ta < ntok, vb = FULL || ta + 8 < ntok;
       const float cqv = cq_of(rho), bev = be_of(rho);
-      sv[rho][0] = va ? fmaf(cqv, sc[rho][0] + sc[rho][1], bev) : -INFINITY;
-      sv[rho][1] = vb ? fmaf(cqv, sc[rho][2] + sc[rho][3], bev) : -INFINITY;
+      const float2 t = __fadd2_rn(make_float2(sc[rho][0], sc[rho][2]), make_float2(sc[rho][1], sc[rho][3]));
+      const float2 sab = __ffma2_rn(make_float2(cqv, cqv), t, make_float2(bev, bev));
+      sv[rho][0] = va ? sab.x : -INFINITY;
+      sv[rho][1] = vb ? sab.y : -INFINITY;
       mloc = fmaxf(mloc, fmaxf(sv[rho][0], sv[rho][1]));
     }
     const float m_new = fmaxf(ss.m, head_max<R>(mloc));
@@ -843,7 +846,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
         const float sva = va ? fva.x : 0.f, zva = va ? fva.y : 0.f;
         const float svb = vb ? fvb.x : 0.f, zvb = vb ? fvb.y : 0.f;
         zsum[0] = fmaf(pa, zva, fmaf(pb, zvb, zsum[0]));
-        to_b(pa * sva, pb * svb, bw0[rho], bw1[rho]);
+        const float2 w = __fmul2_rn(make_float2(pa, pb), make_float2(sva, svb));
+        to_b(w.x, w.y, bw0[rho], bw1[rho]);
       } else {
         pp[rho][0] = va ? pa : 0.f;
         pp[rho][1] = vb ? pb : 0.f;
@@ -951,11 +955,15 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
         const float ps = pow2i(-es);
         const float2 v0 = __half22float2(u2h2(m01.x)), v1 = __half22float2(u2h2(md.x));
         const float2 v2 = __half22float2(u2h2(m01.y)), v3 = __half22float2(u2h2(md.y));
-        sp[gi][0] = v0.x * ps;
-        sp[gi][1] = v1.x * ps;
-        sp[gi][2] = v2.x * ps;
-        sp[gi][3] = v3.x * ps;
-        const float z0 = v0.y * ifa, z1 = v1.y * ifa, z2 = v2.y * ifb, z3 = v3.y * ifb;
+        const float2 s01 = __fmul2_rn(make_float2(v0.x, v1.x), make_float2(ps, ps));
+        const float2 s23 = __fmul2_rn(make_float2(v2.x, v3.x), make_float2(ps, ps));
+        sp[gi][0] = s01.x;
+        sp[gi][1] = s01.y;
+        sp[gi][2] = s23.x;
+        sp[gi][3] = s23.y;
+        const float2 z01 = __fmul2_rn(make_float2(v0.y, v1.y), make_float2(ifa, ifa));
+        const float2 z23 = __fmul2_rn(make_float2(v2.y, v3.y), make_float2(ifb, ifb));
+        const float z0 = z01.x, z1 = z01.y, z2 = z23.x, z3 = z23.y;
 #pragma unroll
         for (int hh = 0; hh < R; ++hh)
           bv[gi][hh] = fmaf(qa[hh][3], z3, fmaf(qa[hh][2], z2, fmaf(qa[hh][1], z1, qa[hh][0] * z0)));
@@ -981,15 +989,18 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
       uint32_t *fw = reinterpret_cast<uint32_t *>(frag);
 #pragma unroll
       for (int hh = 0; hh < R; ++hh) {
-        const float x0 = qa[hh][0] * sp[gi][0], x1 = qa[hh][1] * sp[gi][1];
-        const float x2 = qa[hh][2] * sp[gi][2], x3 = qa[hh][3] * sp[gi][3];
+        // paired fp32 operations (each element rounded to nearest, like the scalar ones)
+        const float2 xa = __fmul2_rn(make_float2(qa[hh][0], qa[hh][1]), make_float2(sp[gi][0], sp[gi][1]));
+        const float2 xb = __fmul2_rn(make_float2(qa[hh][2], qa[hh][3]), make_float2(sp[gi][2], sp[gi][3]));
         // fp32 round to nearest even onto the grid: |x| / (u_h f) < 2^10, far inside
         // the 2^22 that adding and subtracting 1.5 * 2^23 * u_h * f needs
-        const float ma = gu[hh] * fa, mbg = gu[hh] * fb;
-        const float h0 = __fsub_rn(__fadd_rn(x0, ma), ma), h1 = __fsub_rn(__fadd_rn(x1, ma), ma);
-        const float h2 = __fsub_rn(__fadd_rn(x2, mbg), mbg), h3 = __fsub_rn(__fadd_rn(x3, mbg), mbg);
-        const __half2 hA = __floats2half2_rn(h0, h1), hB = __floats2half2_rn(h2, h3);
-        const __half2 lA = __floats2half2_rn(x0 - h0, x1 - h1), lB = __floats2half2_rn(x2 - h2, x3 - h3);
+        const float2 m = __fmul2_rn(make_float2(gu[hh], gu[hh]), make_float2(fa, fb));
+        const float2 ma = make_float2(m.x, m.x), mb = make_float2(m.y, m.y);
+        const float2 ha = __fadd2_rn(__fadd2_rn(xa, ma), make_float2(-ma.x, -ma.y));
+        const float2 hb = __fadd2_rn(__fadd2_rn(xb, mb), make_float2(-mb.x, -mb.y));
+        const float2 la = __fadd2_rn(xa, make_float2(-ha.x, -ha.y)), lb = __fadd2_rn(xb, make_float2(-hb.x, -hb.y));
+        const __half2 hA = __floats2half2_rn(ha.x, ha.y), hB = __floats2half2_rn(hb.x, hb.y);
+        const __half2 lA = __floats2half2_rn(la.x, la.y), lB = __floats2half2_rn(lb.x, lb.y);
         *reinterpret_cast<uint2 *>(fw + ((2 * hh) * 4 + pt) * FRW + pword) = make_uint2(h22u(hA), h22u(hB));
         *reinterpret_cast<uint2 *>(fw + ((2 * hh + 1) * 4 + pt) * FRW + pword) = make_uint2(h22u(lA), h22u(lB));
       }
