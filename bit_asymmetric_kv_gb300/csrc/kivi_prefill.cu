@@ -206,8 +206,10 @@ __device__ void quantize_tile(const PrefillArgs &a, int64_t bh, int64_t t0, cons
   }
 }
 
+// Three CTAs (12 warps) per SM: 168 registers, a few spilled in the 2-bit kernels, are
+// 1.7% faster on the Llama-2 prompt than 177 registers at two CTAs per SM (measured).
 template <int R, int BITS>
-__global__ void __launch_bounds__(kPThreads) prefill_kernel(const PrefillArgs a) {
+__global__ void __launch_bounds__(kPThreads, 3) prefill_kernel(const PrefillArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
