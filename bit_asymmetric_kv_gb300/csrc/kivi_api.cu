@@ -304,7 +304,7 @@ int kivi_decode_attention(const kivi_dims *d, const kivi_cache *c, const uint16_
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.pmax = g.pmax;
-  a.small = g.small ? 1 : 0;
+  a.small = g.small;
   a.vg = vgroup(d);
   a.wait_tail = 0;
   a.softmax_scale = softmax_scale;
@@ -354,7 +354,7 @@ int kivi_decode_step(const kivi_dims *d, kivi_cache *c, const uint16_t *k_new, c
   a.n_warps = g.n_warps;
   a.grid = g.grid;
   a.pmax = g.pmax;
-  a.small = g.small ? 1 : 0;
+  a.small = g.small;
   a.vg = vgroup(d);
   a.wait_tail = 1;
   a.softmax_scale = softmax_scale;

@@ -383,9 +383,9 @@ __device__ void paged_prefix(const DecodeArgs &a, int *s_len, int *s_cum) {
 // sum merges them.  np == 0 (no
 // tokens) writes zeros; after a decode fault (g_decode_fault) the row is NaN.
 // Partial rows are 8-byte aligned (stride 130 floats).
-template <bool SHARED>
-__device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
-                                            uint16_t *__restrict__ out_row, int lane) {
+// Partial j starts at row(j).
+template <bool SHARED, typename RowFn>
+__device__ __forceinline__ void combine_rows(RowFn row, int np, uint16_t *__restrict__ out_row, int lane) {
   constexpr int kBatch = 16;
   float M = -INFINITY, L = 0.f, o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
   for (int j0 = 0; j0 < np; j0 += kBatch) {
@@ -393,7 +393,7 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np,
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) {
       if (j0 + k < np) {
-        const float *r = p + (int64_t)(j0 + k) * stride;
+        const float *r = row(j0 + k);
         if constexpr (SHARED) {
           ml[k] = *reinterpret_cast<const float2 *>(r + kD);
           lo[k] = *reinterpret_cast<const float2 *>(r + 2 * lane);
@@ -428,36 +428,78 @@ __device__ __forceinline__ void combine_row(const float *__restrict__ p, int np,
   dst[32 + lane] = h22u(__floats2half2_rn(o2 * inv, o3 * inv));
 }
 
+// Partial j at p + j * stride.
+template <bool SHARED>
+__device__ __forceinline__ void combine_row(const float *__restrict__ p, int np, int64_t stride,
+                                            uint16_t *__restrict__ out_row, int lane) {
+  combine_rows<SHARED>([&](int j) { return p + (int64_t)j * stride; }, np, out_row, lane);
+}
 
-// The small path's merge: once every warp of the CTA has written its partials, warp r
-// merges query head r's partials of the CTA's (batch, KV head) into the output.
-template <int R>
+
+// Thread-block cluster barrier halves and the shared-memory window of a cluster peer.
+// Threads that have exited count as arrived, and no kernel here waits on a cluster
+// barrier inside a loop, so every wait ends once each CTA of the cluster gets there.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;\n" ::: "memory"); }
+__device__ __forceinline__ int cluster_rank() {
+  int r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// Generic address of `p` (this CTA's shared memory) in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ const float *cluster_peer(const float *p, int rank) {
+  const float *q;
+  asm volatile("mapa.u64 %0, %1, %2;\n" : "=l"(q) : "l"(p), "r"(rank));
+  return q;
+}
+
+// The small path's merge: once every warp of the CTA (CL = 1), or of every CTA of the
+// cluster (CL > 1), has written its partials into its own CTA's shared memory, warp r
+// of the first CTA merges query head r's partials of the (batch, KV head) into the
+// output.  A cluster's first CTA reads the other CTAs' partials in their shared memory
+// (coalesced 8-byte loads; scattered 4-byte stores into its own memory from the other
+// CTAs were slower), and they stay resident until it has.
+template <int R, int CL, int NWARPS>
 __device__ __forceinline__ void small_merge(const DecodeArgs &a, const float *s_part, int64_t NW, int warp,
                                             int lane) {
-  __syncthreads();
-  if (warp < R) {
-    const int64_t h = blockIdx.x, b = h / a.Hkv, kvh = h - b * a.Hkv;
-    combine_row<true>(s_part + warp * (kD + 2), (int)NW, (int64_t)R * (kD + 2),
-                      a.out + (b * a.Hq + kvh * R + warp) * kD, lane);
+  const int64_t h = blockIdx.x / CL, b = h / a.Hkv, kvh = h - b * a.Hkv;
+  uint16_t *out_row = a.out + (b * a.Hq + kvh * R + warp) * kD;
+  if constexpr (CL == 1) {
+    __syncthreads();
+    if (warp < R) combine_row<true>(s_part + warp * (kD + 2), (int)NW, (int64_t)R * (kD + 2), out_row, lane);
+  } else {
+    cluster_arrive();  // release: this CTA's partials
+    cluster_wait();    // acquire: every CTA's
+    if (warp < R && cluster_rank() == 0) {
+      // partial j: warp j mod NWARPS of cluster CTA j / NWARPS
+      const float *mine = s_part + warp * (kD + 2);
+      combine_rows<true>(
+          [&](int j) { return cluster_peer(mine + (j % NWARPS) * R * (kD + 2), j / NWARPS); }, (int)NW, out_row,
+          lane);
+    }
+    cluster_arrive();  // the first CTA has read every partial
+    cluster_wait();
   }
 }
 
 // Launch modes of the decode body: the persistent grid over a dense or a paged cache,
 // and the small-context path (one CTA of kSmallWarps warps per (batch, KV head) of a
 // dense cache, its warps' partials merged in shared memory: no workspace round trip
-// and no combine launch).
+// and no combine launch).  With CL > 1 the small path runs on a cluster of CL CTAs
+// per (batch, KV head), whose first CTA merges the partials of all of them.
 constexpr int kModeDense = 0, kModePaged = 1, kModeSmall = 2;
 constexpr int kSmallWarps = kDecodeSmallWarps;
 
-// Partials of the small path's CTA: [warp][R] rows of kD + 2 floats after the warps'
-// rings.
-template <int R>
-__host__ __device__ constexpr int small_part_bytes() { return kSmallWarps * R * (kD + 2) * 4; }
+// Partials of the small path: [warp][R] rows of kD + 2 floats after the warps' rings
+// (each CTA of a cluster holds its own warps').
+template <int R, int NW = kSmallWarps>
+__host__ __device__ constexpr int small_part_bytes() { return NW * R * (kD + 2) * 4; }
 
-template <int R, int G, int MODE, int BITS, int NWARPS, int VG = kD>
+template <int R, int G, int MODE, int BITS, int NWARPS, int VG = kD, int CL = 1>
 __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   constexpr bool PAGED = MODE == kModePaged;
   constexpr bool SMALL = MODE == kModeSmall;
+  static_assert(CL == 1 || SMALL, "clusters: the small path only");
   extern __shared__ __align__(16) unsigned char smem[];
   using L = Layout<R, G, BITS, VG>;
   // value channel groups (VG < 128): NV {s, z} words per value token, group m over
@@ -477,7 +519,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   // the combine grid may launch now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gw = SMALL ? warp : (int64_t)blockIdx.x * NWARPS + warp;
+  const int rank = CL > 1 ? cluster_rank() : 0;
+  const int64_t gw = SMALL ? (int64_t)rank * NWARPS + warp : (int64_t)blockIdx.x * NWARPS + warp;
   int64_t NW = a.n_warps;
   int64_t W;
   float *s_part = reinterpret_cast<float *>(smem + NWARPS * L::kWarpBytes);  // small path only
@@ -501,8 +544,8 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     // head's first and last owner is left without units (every partial is written)
     if (W < NW) NW = W;
   } else if constexpr (SMALL) {
-    W = a.units_per_head;  // the units of head blockIdx.x
-    NW = W < NWARPS ? W : NWARPS;
+    W = a.units_per_head;  // the units of head blockIdx.x / CL
+    NW = W < CL * NWARPS ? W : CL * NWARPS;
   } else {
     W = a.total_units;
   }
@@ -512,11 +555,11 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     u1 = (gw + 1) * W / NW;
   }
   if constexpr (SMALL) {
-    u0 += (int64_t)blockIdx.x * W;
-    u1 += (int64_t)blockIdx.x * W;
+    u0 += (int64_t)(blockIdx.x / CL) * W;
+    u1 += (int64_t)(blockIdx.x / CL) * W;
   }
   if (u0 >= u1) {
-    if constexpr (SMALL) small_merge<R>(a, s_part, NW, warp, lane);
+    if constexpr (SMALL) small_merge<R, CL, NWARPS>(a, s_part, NW, warp, lane);
     return;
   }
   const int n_my = (int)(u1 - u0);
@@ -745,7 +788,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
     if (slot_mine == 0) {
       float *dst;
       if constexpr (SMALL) {
-        dst = s_part + (gw * R + head_mine) * (kD + 2);
+        dst = s_part + (warp * R + head_mine) * (kD + 2);
       } else if constexpr (PAGED) {
         // pair index gw + h grows strictly along the unit order: unique per (warp, head)
         dst = part + ((gw + h) * R + head_mine) * (kD + 2);
@@ -1275,7 +1318,7 @@ __device__ __forceinline__ void decode_body(const DecodeArgs &a) {
   } else {
     emit(cc.h, ss);
   }
-  if constexpr (SMALL) small_merge<R>(a, s_part, NW, warp, lane);
+  if constexpr (SMALL) small_merge<R, CL, NWARPS>(a, s_part, NW, warp, lane);
 }
 
 template <int R, int G, bool PAGED, int BITS, int VG = kD>
@@ -1287,6 +1330,14 @@ template <int R, int G, int BITS>
 __global__ void __launch_bounds__(kSmallWarps * 32, 1) decode_small_kernel(const DecodeArgs a) {
   decode_body<R, G, kModeSmall, BITS, kSmallWarps>(a);
 }
+
+// The small path on clusters: CTAs CL * h .. CL * h + CL - 1 of NW warps each form the
+// cluster of (batch, KV head) h.
+template <int R, int G, int BITS, int CL, int NW>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NW * 32, 1) decode_cluster_kernel(const DecodeArgs a) {
+  decode_body<R, G, kModeSmall, BITS, NW, kD, CL>(a);
+}
+
 // Dense layout: the partials of (batch, query head) `row` sit at slots 0 .. np-1 of
 // the row's pmax slots; np follows from the unit split.
 __global__ void __launch_bounds__(32 * kCombineRows) combine_kernel(const float *__restrict__ ws, int64_t pmax,
@@ -1369,6 +1420,40 @@ const void *select_small(int R, int G) {
   return R == 1 ? small_ptr<1, 64, BITS>() : R == 2 ? small_ptr<2, 64, BITS>() : small_ptr<4, 64, BITS>();
 }
 
+template <int R, int G, int BITS, int CL, int NW>
+const void *cluster_ptr() {
+  return reinterpret_cast<const void *>(&decode_cluster_kernel<R, G, BITS, CL, NW>);
+}
+
+template <int BITS, int CL, int NW>
+const void *select_cluster(int R, int G) {
+  if (G == 32)
+    return R == 1   ? cluster_ptr<1, 32, BITS, CL, NW>()
+           : R == 2 ? cluster_ptr<2, 32, BITS, CL, NW>()
+                    : cluster_ptr<4, 32, BITS, CL, NW>();
+  return R == 1 ? cluster_ptr<1, 64, BITS, CL, NW>() : R == 2 ? cluster_ptr<2, 64, BITS, CL, NW>() : cluster_ptr<4, 64, BITS, CL, NW>();
+}
+
+// Shared memory of a cluster kernel's CTA: its warps' rings and partials.  A CTA of
+// fewer than 8 warps claims more than half of an SM's 228 KB, so that every CTA of a
+// cluster has an SM to itself (8 warps of two CTAs on one SM take each unit's compute
+// longer).
+constexpr int kOwnSmSmem = 116 * 1024;
+template <int R, int G, int BITS, int CL, int NW>
+constexpr int cluster_smem() {
+  constexpr int b = NW * Layout<R, G, BITS>::kWarpBytes + small_part_bytes<R, NW>();
+  return NW < 8 && b < kOwnSmSmem ? kOwnSmSmem : b;
+}
+
+template <int BITS, int CL, int NW>
+int cluster_smem_bytes(int R, int G) {
+  if (G == 32)
+    return R == 1   ? cluster_smem<1, 32, BITS, CL, NW>()
+           : R == 2 ? cluster_smem<2, 32, BITS, CL, NW>()
+                    : cluster_smem<4, 32, BITS, CL, NW>();
+  return R == 1 ? cluster_smem<1, 64, BITS, CL, NW>() : R == 2 ? cluster_smem<2, 64, BITS, CL, NW>() : cluster_smem<4, 64, BITS, CL, NW>();
+}
+
 template <int BITS>
 int small_smem_bytes(int R, int G) {
   if (G == 32)
@@ -1398,8 +1483,8 @@ DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B, int vg) 
     k.decode = vg == 64 ? select_vg_kernel<64>(R, G) : select_vg_kernel<32>(R, G);
     k.smem = k.smem_limit = vg == 64 ? vg_smem_bytes<64>(R, G) : vg_smem_bytes<32>(R, G);
     k.combine = reinterpret_cast<const void *>(&combine_kernel);
-    k.small = nullptr;
-    k.small_smem = 0;
+    k.small = k.pair = k.quad = nullptr;
+    k.small_smem = k.pair_smem = k.quad_smem = 0;
     return k;
   }
   const int base = bits == 2 ? smem_bytes<2>(R, G) : smem_bytes<4>(R, G);
@@ -1408,14 +1493,19 @@ DecodeKernels decode_kernels(int R, int G, int bits, bool paged, int B, int vg) 
     k.smem = base + paged_extra(B);
     k.smem_limit = base + paged_extra(kPagedMaxBatch);
     k.combine = reinterpret_cast<const void *>(&paged_combine_kernel);
-    k.small = nullptr;
-    k.small_smem = 0;
+    k.small = k.pair = k.quad = nullptr;
+    k.small_smem = k.pair_smem = k.quad_smem = 0;
   } else {
     k.decode = bits == 2 ? select_kernel<false, 2>(R, G) : select_kernel<false, 4>(R, G);
     k.smem = k.smem_limit = base;
     k.combine = reinterpret_cast<const void *>(&combine_kernel);
     k.small = bits == 2 ? select_small<2>(R, G) : select_small<4>(R, G);
     k.small_smem = bits == 2 ? small_smem_bytes<2>(R, G) : small_smem_bytes<4>(R, G);
+    constexpr int PC = kDecodePairCtas, PW = kDecodePairWarps, QC = kDecodeQuadCtas, QW = kDecodeQuadWarps;
+    k.pair = bits == 2 ? select_cluster<2, PC, PW>(R, G) : select_cluster<4, PC, PW>(R, G);
+    k.pair_smem = bits == 2 ? cluster_smem_bytes<2, PC, PW>(R, G) : cluster_smem_bytes<4, PC, PW>(R, G);
+    k.quad = bits == 2 ? select_cluster<2, QC, QW>(R, G) : select_cluster<4, QC, QW>(R, G);
+    k.quad_smem = bits == 2 ? cluster_smem_bytes<2, QC, QW>(R, G) : cluster_smem_bytes<4, QC, QW>(R, G);
   }
   return k;
 }

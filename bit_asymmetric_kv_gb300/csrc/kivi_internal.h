@@ -76,7 +76,8 @@ struct DecodeArgs {
   int grid;                // CTAs (4 warps each)
   int pmax;                // partial slots per query head in the workspace
   int wait_tail;           // launched as a dependent of an append: wait before each head's last unit
-  int small;               // dense: the small-context path (decode_geometry's choice)
+  int small;               // dense: CTAs per (batch, KV head) of the small-context path, 0 for the
+                           // persistent grid (decode_geometry's choice)
   int vg;                  // channels per value {s, z}: 128 (per token), 64 or 32 (value channel groups)
   float softmax_scale;
   // paged layout only: per-sequence lengths on the device, rows found through the
@@ -96,6 +97,10 @@ struct DecodeArgs {
 // bytes of dynamic shared memory; `smem_limit` is the most any launch of it uses.
 constexpr int kDecodeWarps = 4;   // warps per decode CTA
 constexpr int kDecodeSmallWarps = 8;  // warps per CTA of the small-context path
+// Its clusters for 9 to 16 units: 4 CTAs of 4 warps while that many clusters fit at
+// once, else 2 CTAs of 8 warps.
+constexpr int kDecodeQuadCtas = 4, kDecodeQuadWarps = 4;
+constexpr int kDecodePairCtas = 2, kDecodePairWarps = 8;
 constexpr int kDecodeUnit = 64;   // tokens per unit of work
 constexpr int kCombineRows = 4;   // (batch, query head) rows per combine CTA, one warp each
 struct DecodeKernels {
@@ -106,6 +111,10 @@ struct DecodeKernels {
                         // paged: (ws, Hkv, Hq, B, advance, cap, out)
   const void *small;    // dense only: one CTA of kDecodeSmallWarps warps per (batch, KV head)
   int small_smem;
+  const void *pair;     // dense only: a cluster of kDecodePairCtas CTAs per (batch, KV head)
+  int pair_smem;
+  const void *quad;     // dense only: a cluster of kDecodeQuadCtas CTAs per (batch, KV head)
+  int quad_smem;
 };
 // vg: channels per value scale (128, or 64 / 32 for value channel groups: dense
 // 2-bit caches only, no small-context kernel).
@@ -118,7 +127,8 @@ struct DecodeGeom {
   int n_warps;
   int grid;
   int pmax;
-  bool small;  // the small-context path: one CTA per (batch, KV head), no workspace, no combine
+  int small;  // the small-context path, no workspace and no combine: CTAs per (batch, KV
+              // head), 1, kDecodePairCtas or kDecodeQuadCtas; 0 for the persistent grid
 };
 cudaError_t decode_geometry(int B, int Hkv, int Hq, int G, int bits, int64_t n, DecodeGeom *out, int vg = 128);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);

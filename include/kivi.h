@@ -175,9 +175,10 @@ KIVI_API size_t kivi_decode_workspace_bytes(const kivi_dims *dims, int32_t Hq, i
  * the last n mod G tokens, and V'_t = z_t + code * s_t.  q, out: fp16 [B][Hq][D]
  * device.  ws: device workspace of at least kivi_decode_workspace_bytes() bytes,
  * caller-owned, contents overwritten.  n_tokens == 0 returns KIVI_ERR_ARG.
- * Small contexts (at most 8 units per (batch, KV head), a unit being 64 quantized
- * tokens or the residual, and no more (batch, KV head) pairs than SMs) run on one
- * CTA per pair, which leaves ws unused.
+ * Small contexts (a unit being 64 quantized tokens or the residual) leave ws
+ * unused: at most 8 units per (batch, KV head), with no more (batch, KV head) pairs
+ * than SMs, run on one CTA per pair; 9 to 16 units, with no more pairs than
+ * two-CTA clusters fit on the device at once, on a cluster of two CTAs per pair.
  * Device faults: every wait of the kernel for its own staged copies is bounded; a
  * wait that runs out (a copy that never completes) makes every later output of the
  * decode attention calls in this process NaN instead of hanging the GPU.
