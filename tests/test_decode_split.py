@@ -58,3 +58,48 @@ def test_workload_shapes():
     shapes = [(1, 16), (256, 65 + 1), (128, 513 + 1), (2048, 129 + 1), (32, 4097 + 1), (1, 2001), (4, 11)]
     for heads, U in shapes:
         walk(heads, U, nw)
+
+
+# ---- the small-context path: one CTA, or a cluster of CL CTAs, per (batch, KV head)
+
+def walk_small(U, CL, NWARPS, R, kD=128):
+    """The small path's split and merge addressing for one (batch, KV head) of U units
+    on CL CTAs of NWARPS warps: warp `warp` of cluster CTA `rank` is gw = rank * NWARPS
+    + warp and takes units [gw*U/NW, (gw+1)*U/NW), NW = min(U, CL * NWARPS).  It writes
+    its partial of query head r into its own CTA's region, row warp * R + r of kD + 2
+    floats (NWARPS * R rows); the first CTA's warp r reads partial j of head r from CTA
+    j // NWARPS, row (j % NWARPS) * R + r.  Every unit is taken exactly once, every
+    warp gw < NW takes one (at most 16 units: exactly one), no row leaves its CTA's
+    region, and the merge reads exactly the rows the warps wrote."""
+    NW = min(U, CL * NWARPS)
+    region = NWARPS * R * (kD + 2)
+    taken, written = [], set()
+    for rank in range(CL):
+        for warp in range(NWARPS):
+            gw = rank * NWARPS + warp
+            if gw >= NW:
+                continue
+            u0, u1 = gw * U // NW, (gw + 1) * U // NW
+            assert u0 < u1, (U, CL, NWARPS, gw)
+            if U <= CL * NWARPS:
+                assert u1 - u0 == 1
+            taken.extend(range(u0, u1))
+            for r in range(R):
+                off = (warp * R + r) * (kD + 2)
+                assert 0 <= off and off + kD + 2 <= region
+                written.add((rank, off))
+    assert taken == list(range(U))
+    for r in range(R):
+        read = {(j // NWARPS, ((j % NWARPS) * R + r) * (kD + 2)) for j in range(NW)}
+        assert read <= written and len(read) == NW
+    return NW
+
+
+@pytest.mark.parametrize("R", [1, 2, 4])
+def test_small_and_cluster_paths(R):
+    # one CTA of 8 warps up to 8 units; clusters of 4 x 4 and 2 x 8 warps for 9 to 16
+    for U in range(1, 9):
+        walk_small(U, 1, 8, R)
+    for U in range(9, 17):
+        walk_small(U, 4, 4, R)
+        walk_small(U, 2, 8, R)
