@@ -59,8 +59,9 @@
  *
  * Process-wide tables: the decode calls size their grids from the occupancy of
  * their kernels on the current device.  The first decode call for a given (device,
- * kernel, shared-memory size) asks the CUDA runtime (it raises the kernel's
- * dynamic shared-memory limit and queries the occupancy calculator) and records the
+ * kernel, shared-memory size) asks the CUDA runtime (it raises the kernels'
+ * dynamic shared-memory limits and queries the occupancy calculator, for CTAs and
+ * for the small-context path's thread-block clusters) and records the
  * answer in a table inside the library, guarded by a mutex; later calls only read
  * it, so they make no runtime query but cudaGetDevice and can be captured in a CUDA
  * graph.  Make a first decode call (or a kivi_decode_workspace_bytes /
